@@ -1,0 +1,228 @@
+/*
+ * kvq.h — C ABI of libkvq: attention over an INT8-quantised, paged K/V cache,
+ * hand-written CUDA for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the method (cited by page title and section):
+ *   [DCU]   "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" (INT8 KV and INT8
+ *           MMAC attention on a gfx936 DCU), sections 1.1-1.3, 2.1-2.3, 3.2-3.3, 5.4.
+ *   [DOT4]  "dot4-flash-attention" README (INT8 DOT4 FlashAttention for llama.cpp HIP):
+ *           route table, "Tile Inner Loop (pseudocode)", split-K stage 1 + stage 2.
+ *   [QSA]   "#3381 [Engine] STRATA_PROMPT_ATTN_RDNA2=1 ... prompt QSA attention without
+ *           the decode kernel's split and merge": sections "Problem and result", "Approach".
+ *   [RDNA4] "ROCm/RDNA4 (gfx1201) vLLM: native HIP kernels ...": "Segments, split-K and
+ *           tile shape", "The reduce is not free".
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument named as "device" is device memory of the current CUDA
+ *     device, owned by the caller.  The library allocates nothing, keeps no per-call
+ *     state and never synchronises, except kvq_device_status().
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - bf16 tensors are passed as raw 16-bit patterns (const void*).
+ *   - Outputs of the attention calls are fp32 (a bf16 output would add up to 2^-9
+ *     relative rounding error by itself).
+ *   - Return value: a kvq_status.  Host-side checks run before any launch; on an error
+ *     nothing is launched and no output is touched.  Problems that only the device can
+ *     see (a block-table entry out of range, a cell index out of range, a bounded wait
+ *     that ran out) set bits in the device status word (KVQ_DEV_*), the offending unit
+ *     is skipped (its output is left as zeros where the call writes one), and the
+ *     kernel never traps.  Read and clear those bits with kvq_device_status().
+ *
+ * Cache layout in HBM (one layer; KVQ_BLOCK_SIZE = 16 tokens per page).  Token at
+ * logical position p of sequence s lives in physical page
+ * block_table[s * max_blocks_per_seq + p / 16], slot p % 16.  The K and V layouts are
+ * the ones printed in [DCU] §2.3: K in 16-element head-dimension chunks with the
+ * tokens of a chunk adjacent, V token-contiguous per head dimension.  Scales are
+ * stored head-major ([page][head][slot]) rather than [page][slot][head] so that the
+ * 16 scales of one (page, head) are one contiguous 64-byte run.
+ *     k       int8  [num_blocks][n_kv_heads][head_dim/16][16 slots][16]
+ *     v       int8  [num_blocks][n_kv_heads][head_dim][16 slots]
+ *     k_scale fp32  [num_blocks][n_kv_heads][16 slots]
+ *     v_scale fp32  [num_blocks][n_kv_heads][16 slots]
+ * One (page, head) of K or V is head_dim*16 contiguous bytes (4096 B at head_dim 256).
+ * Per token and layer this is 2*Hkv*D + 2*Hkv*4 bytes: 2080 B at 4 KV heads x 256
+ * against 4096 B for bf16 K/V ([DCU] §1.1).
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_ABI_VERSION 1
+#define KVQ_BLOCK_SIZE 16          /* tokens per cache page */
+#define KVQ_PV_TILE 128            /* keys per P re-quantisation tile in prefill */
+#define KVQ_DEFAULT_SPLIT_ROWS 512 /* keys per split in the split-K decode route */
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0, ... */
+  KVQ_ERR_UNSUPPORTED = 2, /* head_dim not in {128, 256}, block_size != 16, ... */
+  KVQ_ERR_MISALIGNED = 3,  /* a device pointer is not 16-byte aligned */
+  KVQ_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the *_workspace_bytes size */
+  KVQ_ERR_CUDA = 5         /* a launch failed (cudaGetLastError after the launch) */
+} kvq_status;
+
+/* Device status bits (sticky until read by kvq_device_status). */
+#define KVQ_DEV_BAD_BLOCK 0x1u /* a block-table entry is outside [0, num_blocks) */
+#define KVQ_DEV_BAD_POS 0x2u   /* a position / length exceeds what the block table maps */
+#define KVQ_DEV_TIMEOUT 0x4u   /* a bounded mbarrier wait ran out; the CTA returned early */
+#define KVQ_DEV_BAD_CELL 0x8u  /* a sparse cell index is negative or past the mapped range */
+#define KVQ_DEV_BAD_SEQ 0x10u  /* a seq_idx is outside [0, num_seqs) */
+
+typedef struct kvq_cache {
+  int8_t* k;          /* device, layout above */
+  int8_t* v;          /* device, layout above */
+  float* k_scale;     /* device, layout above */
+  float* v_scale;     /* device, layout above */
+  int32_t num_blocks; /* physical pages */
+  int32_t block_size; /* must be KVQ_BLOCK_SIZE */
+  int32_t n_kv_heads;
+  int32_t head_dim;   /* 128 or 256 */
+} kvq_cache;
+
+/*
+ * kvq_quant_write — fused per-(token, KV head) absmax quantisation of new K and V rows
+ * into the paged int8 cache, codes and scales in one kernel ([DCU] §2.1 rule, §2.2
+ * fused producer, §2.3 layout).  For every row x (head_dim values of one token and one
+ * KV head, K and V separately):
+ *     amax = max |x|;  scale = amax / 127 (fp32, IEEE round-to-nearest);
+ *     code = clamp(rint(x / scale), -127, 127) (fp32 IEEE division, ties to even);
+ *     amax == 0 gives scale 0 and all-zero codes.
+ *   k_new, v_new : device bf16 [n_tokens][n_kv_heads][head_dim]
+ *   seq_idx, pos : device int32 [n_tokens]; token i goes to sequence seq_idx[i],
+ *                  logical position pos[i]
+ *   block_table  : device int32 [num_seqs][max_blocks_per_seq]
+ * A token whose seq_idx, position or page is out of range is skipped and sets
+ * KVQ_DEV_BAD_SEQ / KVQ_DEV_BAD_POS / KVQ_DEV_BAD_BLOCK.  Tokens must target distinct
+ * slots (two tokens writing one slot race).
+ */
+int kvq_quant_write(const kvq_cache* cache, const void* k_new, const void* v_new,
+                    int32_t n_tokens, const int32_t* seq_idx, const int32_t* pos,
+                    const int32_t* block_table, int32_t num_seqs,
+                    int32_t max_blocks_per_seq, void* stream);
+
+/* Options of kvq_attn_decode_int8kv (pass NULL for the defaults). */
+typedef struct kvq_decode_opts {
+  int32_t split_rows;      /* keys per split in the split route; 0 -> 512; multiple of 16 */
+  int32_t route_threshold; /* max_ctx <= threshold -> single-CTA route; 0 -> 2048 ([DOT4] route table) */
+  int32_t force_route;     /* 0 auto, 1 single CTA per (sequence, KV head), 2 split-K */
+} kvq_decode_opts;
+
+/* Workspace (bytes) the split route of kvq_attn_decode_int8kv needs; 0 when the call
+ * will take the single-CTA route. */
+size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_ctx,
+                                  int32_t head_dim, const kvq_decode_opts* opts);
+
+/*
+ * kvq_attn_decode_int8kv — one query per sequence over its int8 paged K/V
+ * ([DCU] §3.3 decode data flow; [DOT4] route table and split-K stage 1 + stage 2).
+ *   out[b][h][:] = sum_t softmax_t(s) * v^[t],   s[t] = softmax_scale * q[b][h] . k^[t],
+ *   k^[t] = k_code[t] * k_scale[t] (per token and KV head), same for v^, t < ctx_lens[b],
+ *   KV head of query head h = h / (n_q_heads / n_kv_heads) (GQA).
+ * The int8 codes are consumed directly; no dequantised copy is written.  Route: when
+ * max_ctx <= route_threshold one CTA per (sequence, KV head) walks all keys; otherwise
+ * stage 1 runs one CTA per (split_rows-key split, KV head, sequence) and writes a
+ * partial (max, sum, acc[head_dim]) per query head, and stage 2 merges the partials
+ * with the log-sum-exp rule.
+ *   q          : device bf16 [batch][n_q_heads][head_dim]
+ *   block_table: device int32 [batch][max_blocks_per_seq]
+ *   ctx_lens   : device int32 [batch], each in [0, max_ctx]; ctx 0 gives zeros
+ *   max_ctx    : host upper bound of ctx_lens (sizes the grid and the workspace)
+ *   out        : device fp32 [batch][n_q_heads][head_dim]
+ *   workspace  : device, >= kvq_decode_workspace_bytes(...), 16-byte aligned; its
+ *                contents on entry do not matter
+ */
+int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
+                           int32_t n_q_heads, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens,
+                           int32_t max_ctx, float softmax_scale, float* out,
+                           void* workspace, size_t workspace_bytes,
+                           const kvq_decode_opts* opts, void* stream);
+
+/* Workspace (bytes) of kvq_attn_prefill_int8: the int8 Q codes and their fp32 scales. */
+size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t head_dim);
+
+/*
+ * kvq_attn_prefill_int8 — a chunk of n_tokens causal queries of one sequence against
+ * its history plus the chunk itself, all from the int8 cache, in one online softmax
+ * ([DCU] §3.2 non-first prefill chunk; §1.3 and §3.3 INT8 QK / INT8 PV).
+ *   Query i sits at position history_len + i and sees keys t <= history_len + i.
+ *   Q is quantised per (token, query head) by the kvq_quant_write rule.
+ *   S[i][t] = sum_d q_code[i][d] * k_code[t][d]  (exact integer),
+ *   score = S * q_scale[i] * k_scale[t] * softmax_scale,
+ *   p = exp(score - m) (online max m), l = sum of p (unquantised),
+ *   w = p * v_scale[t]; per (query row, KVQ_PV_TILE keys at absolute multiples of 128):
+ *   ps = max w / 127, c = rint(w / ps) in [0, 127];
+ *   out = (sum over tiles of ps * sum_t c * v_code[t]) / l.
+ * The integer contractions run on the tensor cores with int8 codes widened to
+ * integer-valued fp16 (exact: every partial sum is an integer below 2^24).  The chunk's
+ * own K/V must already be in the cache (kvq_quant_write).
+ *   q              : device bf16 [n_tokens][n_q_heads][head_dim]
+ *   block_table_row: device int32 [n_blocks_row], covering history_len + n_tokens keys
+ *   out            : device fp32 [n_tokens][n_q_heads][head_dim]
+ *   workspace      : device, >= kvq_prefill_workspace_bytes(...), 16-byte aligned
+ */
+int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_tokens,
+                          int32_t n_q_heads, int32_t history_len,
+                          const int32_t* block_table_row, int32_t n_blocks_row,
+                          float softmax_scale, float* out, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/*
+ * kvq_attn_sparse_int8kv — sparse prompt attention ([QSA] "Problem and result",
+ * "Approach"): one CTA per (query, KV head) walks the query's list of selected cells
+ * in 64-cell chunks with an online softmax; each chunk's sums start from zero and are
+ * folded into the running sums with one fma, so no scratch and no merge pass.
+ *   out[i][h] = sum_{t in cells(i)} softmax_t(s) * v^[t], s as in decode.
+ *   q           : device bf16 [n_queries][n_q_heads][head_dim]
+ *   cell_offsets: device int32 [n_queries + 1]; cells of query i are
+ *                 cells[cell_offsets[i] .. cell_offsets[i+1]), logical positions, sorted
+ *                 ascending (the order only changes fp32 rounding); an empty list gives zeros
+ *   block_table_row: device int32 [n_blocks_row] mapping logical positions to pages
+ *   out         : device fp32 [n_queries][n_q_heads][head_dim]
+ */
+int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_queries,
+                           int32_t n_q_heads, const int32_t* cell_offsets,
+                           const int32_t* cells, const int32_t* block_table_row,
+                           int32_t n_blocks_row, float softmax_scale, float* out,
+                           void* stream);
+
+/*
+ * Test entry points of the prefill path (same device code as kvq_attn_prefill_int8).
+ * kvq_debug_prefill_q_codes: the per-(token, query head) Q quantisation step alone.
+ *   q: device bf16 [n_tokens][n_q_heads][head_dim]; q_codes: device int8, same shape;
+ *   q_scales: device fp32 [n_tokens][n_q_heads].
+ * kvq_debug_prefill_qk_int32: the tensor-core QK tile alone, no mask: for query rows
+ *   q0 .. q0+127 of query head q_head and keys k0 .. k0+nk-1 (k0 and nk multiples of
+ *   128) writes the exact integer S[row][key] to s_out (device int32 [128][nk]); rows
+ *   at or past n_tokens are written as 0.
+ *   q_codes: device int8 [n_tokens][n_q_heads][head_dim] (from kvq_debug_prefill_q_codes).
+ */
+int kvq_debug_prefill_q_codes(const void* q, int32_t n_tokens, int32_t n_q_heads,
+                              int32_t head_dim, int8_t* q_codes, float* q_scales,
+                              void* stream);
+int kvq_debug_prefill_qk_int32(const kvq_cache* cache, const int8_t* q_codes,
+                               int32_t n_tokens, int32_t n_q_heads,
+                               const int32_t* block_table_row, int32_t n_blocks_row,
+                               int32_t q_head, int32_t q0, int32_t k0, int32_t nk,
+                               int32_t* s_out, void* stream);
+
+/* Synchronises `stream`, then returns the device status bits of the current device in
+ * *flags_out and clears them.  Returns KVQ_ERR_CUDA if the stream reports an error. */
+int kvq_device_status(uint32_t* flags_out, void* stream);
+
+/* Static text for a kvq_status value. */
+const char* kvq_status_string(int status);
+
+/* KVQ_ABI_VERSION of the loaded library. */
+int kvq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */
