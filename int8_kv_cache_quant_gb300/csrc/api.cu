@@ -1,0 +1,321 @@
+// api.cu — the C ABI of libkvq (include/kvq.h): host-side validation, routing and launch.
+// Every entry point checks its arguments before launching anything, allocates nothing and
+// never synchronises (except kvq_device_status).
+#include <cstdint>
+#include <mutex>
+
+#include "kvq.h"
+#include "kvq_launch.h"
+
+namespace {
+
+// Device status word (KVQ_DEV_* bits), one per device that loads the library.
+__device__ unsigned int g_kvq_status = 0;
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_status_mu;
+
+// Device address of the status word on the current device, looked up once per device.
+unsigned int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kvq_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int check_cache(const kvq_cache* c) {
+  if (!c || !c->k || !c->v || !c->k_scale || !c->v_scale) return KVQ_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->n_kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  if (c->block_size != KVQ_BLOCK_SIZE) return KVQ_ERR_UNSUPPORTED;
+  if (c->head_dim != 128 && c->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(c->k) || !aligned16(c->v) || !aligned16(c->k_scale) || !aligned16(c->v_scale))
+    return KVQ_ERR_MISALIGNED;
+  return KVQ_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+kvq_decode_opts decode_defaults(const kvq_decode_opts* o) {
+  kvq_decode_opts r = {KVQ_DEFAULT_SPLIT_ROWS, 2048, 0};
+  if (o) {
+    if (o->split_rows > 0) r.split_rows = o->split_rows;
+    if (o->route_threshold > 0) r.route_threshold = o->route_threshold;
+    r.force_route = o->force_route;
+  }
+  return r;
+}
+
+constexpr int kMaxSplits = 16384;
+
+}  // namespace
+
+extern "C" {
+
+int kvq_version(void) { return KVQ_ABI_VERSION; }
+
+const char* kvq_status_string(int s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case KVQ_ERR_MISALIGNED: return "device pointer not 16-byte aligned";
+    case KVQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KVQ_ERR_CUDA: return "CUDA launch or runtime error";
+    default: return "unknown status";
+  }
+}
+
+int kvq_device_status(uint32_t* flags_out, void* stream) {
+  if (!flags_out) return KVQ_ERR_INVALID_ARG;
+  *flags_out = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_kvq_status, sizeof v) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_kvq_status, &zero, sizeof zero) != cudaSuccess) return KVQ_ERR_CUDA;
+  *flags_out = v;
+  return KVQ_OK;
+}
+
+int kvq_quant_write(const kvq_cache* cache, const void* k_new, const void* v_new, int32_t n_tokens,
+                    const int32_t* seq_idx, const int32_t* pos, const int32_t* block_table,
+                    int32_t num_seqs, int32_t max_blocks_per_seq, void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_tokens < 0 || num_seqs <= 0 || max_blocks_per_seq <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KVQ_OK;
+  if (!k_new || !v_new || !seq_idx || !pos || !block_table) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return KVQ_ERR_MISALIGNED;
+  if (!aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table)) return KVQ_ERR_MISALIGNED;
+  kvq::QuantWriteArgs a{};
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.n_tokens = n_tokens;
+  a.seq_idx = seq_idx;
+  a.pos = pos;
+  a.block_table = block_table;
+  a.num_seqs = num_seqs;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.status = status_ptr();
+  return cuda_status(kvq::launch_quant_write(a, static_cast<cudaStream_t>(stream)));
+}
+
+static bool decode_split_route(const kvq_decode_opts& o, int32_t max_ctx) {
+  if (o.force_route == 1) return false;
+  if (o.force_route == 2) return true;
+  return max_ctx > o.route_threshold;
+}
+
+size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_ctx,
+                                  int32_t head_dim, const kvq_decode_opts* opts) {
+  const kvq_decode_opts o = decode_defaults(opts);
+  if (batch <= 0 || n_q_heads <= 0 || max_ctx <= 0 || head_dim <= 0 || o.split_rows <= 0) return 0;
+  if (!decode_split_route(o, max_ctx)) return 0;
+  return kvq::decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, o.split_rows);
+}
+
+int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_q_heads,
+                           const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
+                           void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
+                           void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q || !block_table || !ctx_lens || !out) return KVQ_ERR_INVALID_ARG;
+  if (batch <= 0 || n_q_heads <= 0 || max_blocks_per_seq <= 0 || max_ctx < 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  const int G = n_q_heads / cache->n_kv_heads;
+  if (G > 8) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
+  if (!aligned4(block_table) || !aligned4(ctx_lens)) return KVQ_ERR_MISALIGNED;
+  const kvq_decode_opts o = decode_defaults(opts);
+  if (o.split_rows % KVQ_BLOCK_SIZE != 0 || o.force_route < 0 || o.force_route > 2) return KVQ_ERR_INVALID_ARG;
+  const int mc = max_ctx > 0 ? max_ctx : 1;
+  const bool split = decode_split_route(o, mc);
+  kvq::DecodeArgs a{};
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.q = q;
+  a.batch = batch;
+  a.n_q_heads = n_q_heads;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.ctx_lens = ctx_lens;
+  a.max_ctx = mc;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.split_rows = o.split_rows;
+  a.status = status_ptr();
+  if (split) {
+    const long long n_split = (static_cast<long long>(mc) + o.split_rows - 1) / o.split_rows;
+    if (n_split > kMaxSplits) return KVQ_ERR_UNSUPPORTED;
+    const size_t need = kvq::decode_workspace_bytes(batch, n_q_heads, mc, cache->head_dim, o.split_rows);
+    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
+    a.n_split = static_cast<int>(n_split);
+    const long long units = static_cast<long long>(batch) * n_q_heads * n_split;
+    const long long acc_bytes = ((units * cache->head_dim * 4 + 255) / 256) * 256;
+    a.part_acc = static_cast<float*>(workspace);
+    a.part_stats = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
+    return cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSplit, static_cast<cudaStream_t>(stream)));
+  }
+  a.n_split = 1;
+  return cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSingle, static_cast<cudaStream_t>(stream)));
+}
+
+size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t head_dim) {
+  if (n_tokens <= 0 || n_q_heads <= 0 || head_dim <= 0) return 0;
+  return kvq::prefill_workspace_bytes(n_tokens, n_q_heads, head_dim);
+}
+
+static kvq::PrefillArgs prefill_args(const kvq_cache* cache, const void* q, int32_t n_tokens,
+                                     int32_t n_q_heads, int32_t history_len,
+                                     const int32_t* block_table_row, int32_t n_blocks_row,
+                                     float softmax_scale, float* out, void* workspace) {
+  kvq::PrefillArgs a{};
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.q = q;
+  a.n_tokens = n_tokens;
+  a.n_q_heads = n_q_heads;
+  a.history_len = history_len;
+  a.block_table_row = block_table_row;
+  a.n_blocks_row = n_blocks_row;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  const long long codes = static_cast<long long>(n_tokens) * n_q_heads * cache->head_dim;
+  a.q_codes = static_cast<int8_t*>(workspace);
+  a.q_scales = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((codes + 255) / 256) * 256);
+  a.status = status_ptr();
+  return a;
+}
+
+int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_tokens, int32_t n_q_heads,
+                          int32_t history_len, const int32_t* block_table_row, int32_t n_blocks_row,
+                          float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q || !block_table_row || !out) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(history_len) + n_tokens > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || !aligned4(block_table_row)) return KVQ_ERR_MISALIGNED;
+  const size_t need = kvq::prefill_workspace_bytes(n_tokens, n_q_heads, cache->head_dim);
+  if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
+  kvq::PrefillArgs a = prefill_args(cache, q, n_tokens, n_q_heads, history_len, block_table_row,
+                                    n_blocks_row, softmax_scale, out, workspace);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = kvq::launch_prefill_q_quant(a, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_CUDA;
+  e = kvq::launch_prefill(a, s);
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_queries, int32_t n_q_heads,
+                           const int32_t* cell_offsets, const int32_t* cells,
+                           const int32_t* block_table_row, int32_t n_blocks_row, float softmax_scale,
+                           float* out, void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q || !cell_offsets || !cells || !block_table_row || !out) return KVQ_ERR_INVALID_ARG;
+  if (n_queries <= 0 || n_q_heads <= 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  const int G = n_q_heads / cache->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 6 && G != 8 && G != 12) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
+  if (!aligned4(cell_offsets) || !aligned4(cells) || !aligned4(block_table_row)) return KVQ_ERR_MISALIGNED;
+  kvq::SparseArgs a{};
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.q = q;
+  a.n_queries = n_queries;
+  a.n_q_heads = n_q_heads;
+  a.cell_offsets = cell_offsets;
+  a.cells = cells;
+  a.block_table_row = block_table_row;
+  a.n_blocks_row = n_blocks_row;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.status = status_ptr();
+  return cuda_status(kvq::launch_sparse(a, static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_debug_prefill_q_codes(const void* q, int32_t n_tokens, int32_t n_q_heads, int32_t head_dim,
+                              int8_t* q_codes, float* q_scales, void* stream) {
+  if (!q || !q_codes || !q_scales || n_tokens <= 0 || n_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  if (head_dim != 128 && head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(q_codes) || !aligned4(q_scales)) return KVQ_ERR_MISALIGNED;
+  kvq::PrefillArgs a{};
+  a.head_dim = head_dim;
+  a.q = q;
+  a.n_tokens = n_tokens;
+  a.n_q_heads = n_q_heads;
+  a.q_codes = q_codes;
+  a.q_scales = q_scales;
+  a.status = status_ptr();
+  return cuda_status(kvq::launch_prefill_q_quant(a, static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_debug_prefill_qk_int32(const kvq_cache* cache, const int8_t* q_codes, int32_t n_tokens,
+                               int32_t n_q_heads, const int32_t* block_table_row, int32_t n_blocks_row,
+                               int32_t q_head, int32_t q0, int32_t k0, int32_t nk, int32_t* s_out,
+                               void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q_codes || !block_table_row || !s_out) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens <= 0 || n_q_heads <= 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (q_head < 0 || q_head >= n_q_heads || q0 < 0 || q0 >= n_tokens) return KVQ_ERR_INVALID_ARG;
+  if (k0 < 0 || nk <= 0 || k0 % 128 != 0 || nk % 128 != 0) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(k0) + nk > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned16(s_out) || !aligned4(block_table_row)) return KVQ_ERR_MISALIGNED;
+  kvq::PrefillArgs a = prefill_args(cache, nullptr, n_tokens, n_q_heads, 0, block_table_row, n_blocks_row,
+                                    1.0f, nullptr, nullptr);
+  a.q_codes = const_cast<int8_t*>(q_codes);
+  a.q_scales = nullptr;
+  a.dbg_q_head = q_head;
+  a.dbg_q0 = q0;
+  a.dbg_k0 = k0;
+  a.dbg_nk = nk;
+  a.dbg_s_out = s_out;
+  cudaError_t e = kvq::launch_prefill_qk_debug(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return e == cudaErrorNotSupported ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_CUDA;
+  return KVQ_OK;
+}
+
+}  // extern "C"

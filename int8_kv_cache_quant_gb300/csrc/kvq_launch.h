@@ -1,0 +1,99 @@
+// kvq_launch.h — internal launcher interface between the C ABI (api.cu) and the kernels.
+// Host-side validation happens in api.cu; the launchers assume valid arguments.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+struct QuantWriteArgs {
+  int8_t* k;
+  int8_t* v;
+  float* k_scale;
+  float* v_scale;
+  int num_blocks, n_kv_heads, head_dim;
+  const void* k_new;
+  const void* v_new;
+  int n_tokens;
+  const int32_t* seq_idx;
+  const int32_t* pos;
+  const int32_t* block_table;
+  int num_seqs, max_blocks_per_seq;
+  unsigned int* status;
+};
+cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream);
+
+// Decode: one query per sequence.  Stage 1 (both routes) walks a key range of one
+// (sequence, KV head); the single-CTA route writes `out` directly, the split route writes
+// partials that stage 2 merges.
+struct DecodeArgs {
+  const int8_t* k;
+  const int8_t* v;
+  const float* k_scale;
+  const float* v_scale;
+  int num_blocks, n_kv_heads, head_dim;
+  const void* q;  // bf16 [B][Hq][D]
+  int batch, n_q_heads;
+  const int32_t* block_table;
+  int max_blocks_per_seq;
+  const int32_t* ctx_lens;
+  int max_ctx;
+  float softmax_scale;
+  float* out;          // fp32 [B][Hq][D]
+  float* part_acc;     // fp32 [B][Hq][n_split][D]      (split route)
+  float* part_stats;   // fp32 [B][Hq][n_split][4]       (split route: m_s, m_z, l, unused)
+  int split_rows;      // keys per split (split route); ignored by the single route
+  int n_split;         // splits per sequence in the grid (split route)
+  unsigned int* status;
+};
+enum class DecodeRoute { kSingle = 1, kSplit = 2 };
+size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_dim, int split_rows);
+cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream);
+
+struct SparseArgs {
+  const int8_t* k;
+  const int8_t* v;
+  const float* k_scale;
+  const float* v_scale;
+  int num_blocks, n_kv_heads, head_dim;
+  const void* q;  // bf16 [N][Hq][D]
+  int n_queries, n_q_heads;
+  const int32_t* cell_offsets;
+  const int32_t* cells;
+  const int32_t* block_table_row;
+  int n_blocks_row;
+  float softmax_scale;
+  float* out;
+  unsigned int* status;
+};
+cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
+
+struct PrefillArgs {
+  const int8_t* k;
+  const int8_t* v;
+  const float* k_scale;
+  const float* v_scale;
+  int num_blocks, n_kv_heads, head_dim;
+  const void* q;  // bf16 [T][Hq][D]
+  int n_tokens, n_q_heads, history_len;
+  const int32_t* block_table_row;
+  int n_blocks_row;
+  float softmax_scale;
+  float* out;        // fp32 [T][Hq][D]
+  int8_t* q_codes;   // workspace int8 [T][Hq][D]
+  float* q_scales;   // workspace fp32 [T][Hq]
+  unsigned int* status;
+  // debug QK tile (kvq_debug_prefill_qk_int32)
+  int dbg_q_head, dbg_q0, dbg_k0, dbg_nk;
+  int32_t* dbg_s_out;
+};
+size_t prefill_workspace_bytes(int n_tokens, int n_q_heads, int head_dim);
+cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_prefill_qk_debug(const PrefillArgs& a, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,128 @@
+// quant_write.cu — fused per-(token, KV head) absmax int8 quantisation of new K/V rows
+// into the paged cache: codes and fp32 scale in one kernel.
+//
+// Method: "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §2.1 (quantisation rule:
+// amax = max|x|, scale = amax / 127, q = clamp(round(x / scale), -127, 127)), §2.2 (one
+// producer kernel: quantise and write the paged cache and the scale, no bf16 write-back),
+// §2.3 (K in 16-element head-dimension chunks with the tokens of a chunk adjacent, V
+// token-contiguous per dimension).
+//
+// Mapping: one warp per (token, KV head, K|V) row.  The row (head_dim bf16 values) is read
+// with one vector load per lane, amax is a warp-shuffle max, every division is IEEE fp32
+// (__fdiv_rn) and rounding is to nearest even, so the codes and scales are bit-identical
+// to the reference rule.  K codes go out as 8- or 4-byte stores into the [chunk][slot][16]
+// rows; V codes are one byte per dimension into [dim][slot].
+#include "kvq_dev.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+
+template <int D>
+__global__ void __launch_bounds__(256) quant_write_kernel(QuantWriteArgs a) {
+  constexpr int kPerLane = D / 32;  // 8 (D = 256) or 4 (D = 128) values per lane
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int H = a.n_kv_heads;
+  const long long n_rows = static_cast<long long>(a.n_tokens) * H * 2;
+  if (row >= n_rows) return;
+  const int is_v = static_cast<int>(row & 1);
+  const long long th = row >> 1;
+  const int tok = static_cast<int>(th / H);
+  const int h = static_cast<int>(th % H);
+
+  const int seq = a.seq_idx[tok];
+  const int pos = a.pos[tok];
+  if (seq < 0 || seq >= a.num_seqs) {
+    if (lane == 0) set_status(a.status, KVQ_DEV_BAD_SEQ);
+    return;
+  }
+  if (pos < 0 || pos / KVQ_BLOCK_SIZE >= a.max_blocks_per_seq) {
+    if (lane == 0) set_status(a.status, KVQ_DEV_BAD_POS);
+    return;
+  }
+  const int page = a.block_table[static_cast<long long>(seq) * a.max_blocks_per_seq + pos / KVQ_BLOCK_SIZE];
+  if (page < 0 || page >= a.num_blocks) {
+    if (lane == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
+    return;
+  }
+  const int slot = pos % KVQ_BLOCK_SIZE;
+
+  const uint16_t* src = static_cast<const uint16_t*>(is_v ? a.v_new : a.k_new) +
+                        (static_cast<long long>(tok) * H + h) * D + lane * kPerLane;
+  float x[kPerLane];
+  if constexpr (kPerLane == 8) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(src));
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = __fdiv_rn(amax, 127.0f);
+
+  int8_t q[kPerLane];
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    float c = 0.0f;
+    if (amax != 0.0f) {
+      c = rintf(__fdiv_rn(x[i], scale));
+      c = fminf(fmaxf(c, -127.0f), 127.0f);
+    }
+    q[i] = static_cast<int8_t>(static_cast<int>(c));
+  }
+
+  const long long ph = static_cast<long long>(page) * H + h;
+  if (!is_v) {
+    // K: [page][head][d/16][slot][16]; this lane's dims lane*kPerLane .. +kPerLane-1 lie in
+    // chunk (lane*kPerLane)/16 at byte offset (lane*kPerLane)%16 of the 16-byte row.
+    const int d0 = lane * kPerLane;
+    int8_t* dst = a.k + ((ph * (D / 16) + d0 / 16) * KVQ_BLOCK_SIZE + slot) * 16 + (d0 % 16);
+    if constexpr (kPerLane == 8) {
+      uint2 v;
+      v.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) |
+            ((uint32_t)(uint8_t)q[3] << 24);
+      v.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) | ((uint32_t)(uint8_t)q[6] << 16) |
+            ((uint32_t)(uint8_t)q[7] << 24);
+      *reinterpret_cast<uint2*>(dst) = v;
+    } else {
+      uint32_t v = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
+                   ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
+      *reinterpret_cast<uint32_t*>(dst) = v;
+    }
+    if (lane == 0) a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
+  } else {
+    // V: [page][head][d][slot]
+    int8_t* dst = a.v + (ph * D + lane * kPerLane) * KVQ_BLOCK_SIZE + slot;
+#pragma unroll
+    for (int i = 0; i < kPerLane; ++i) dst[i * KVQ_BLOCK_SIZE] = q[i];
+    if (lane == 0) a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
+  }
+}
+
+cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.n_tokens) * a.n_kv_heads * 2;
+  const int warps_per_block = 8;
+  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  if (a.head_dim == 256)
+    quant_write_kernel<256><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  else
+    quant_write_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

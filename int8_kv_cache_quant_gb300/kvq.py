@@ -1,0 +1,214 @@
+"""Python binding of libkvq (include/kvq.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls.  torch supplies device
+memory and the current stream; all arithmetic runs in libkvq's CUDA kernels.  There is no
+CPU fallback: if libkvq.so is missing or the call fails, an exception is raised.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+BLOCK_SIZE = 16
+PV_TILE = 128
+DEFAULT_SPLIT_ROWS = 512
+
+_STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or option",
+           3: "device pointer not 16-byte aligned", 4: "workspace missing or too small",
+           5: "CUDA launch or runtime error"}
+
+DEV_BAD_BLOCK, DEV_BAD_POS, DEV_TIMEOUT, DEV_BAD_CELL, DEV_BAD_SEQ = 0x1, 0x2, 0x4, 0x8, 0x10
+
+
+class KvqError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__("%s failed: %s (status %d)" % (fn, _STATUS.get(status, "?"), status))
+        self.status = status
+
+
+class _Cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
+                ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class _DecodeOpts(ctypes.Structure):
+    _fields_ = [("split_rows", ctypes.c_int32), ("route_threshold", ctypes.c_int32),
+                ("force_route", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libkvq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libkvq.so is not built (%s); run int8_kv_cache_quant_gb300.build.build()"
+                               % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        cp = ctypes.POINTER(_Cache)
+        L.kvq_version.restype = ctypes.c_int
+        L.kvq_status_string.restype = ctypes.c_char_p
+        L.kvq_status_string.argtypes = [ctypes.c_int]
+        L.kvq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
+        L.kvq_quant_write.argtypes = [cp, vp, vp, i32, vp, vp, vp, i32, i32, vp]
+        L.kvq_decode_workspace_bytes.restype = sz
+        L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
+        L.kvq_attn_decode_int8kv.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
+                                             ctypes.POINTER(_DecodeOpts), vp]
+        L.kvq_prefill_workspace_bytes.restype = sz
+        L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32]
+        L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
+        L.kvq_attn_sparse_int8kv.argtypes = [cp, vp, i32, i32, vp, vp, vp, i32, f32, vp, vp]
+        L.kvq_debug_prefill_q_codes.argtypes = [vp, i32, i32, i32, vp, vp, vp]
+        L.kvq_debug_prefill_qk_int32.argtypes = [cp, vp, i32, i32, vp, i32, i32, i32, i32, i32, vp, vp]
+        _lib = L
+    return _lib
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _check(fn, status):
+    if status != 0:
+        raise KvqError(fn, status)
+
+
+class KVCache:
+    """A paged int8 K/V cache on the GPU in the library's layout:
+    k [num_blocks][n_kv_heads][head_dim/16][16][16] int8, v [num_blocks][n_kv_heads][head_dim][16]
+    int8, k_scale / v_scale [num_blocks][n_kv_heads][16] fp32."""
+
+    def __init__(self, num_blocks, n_kv_heads, head_dim, device="cuda"):
+        self.num_blocks, self.n_kv_heads, self.head_dim = num_blocks, n_kv_heads, head_dim
+        self.k = torch.zeros((num_blocks, n_kv_heads, head_dim // 16, BLOCK_SIZE, 16),
+                             dtype=torch.int8, device=device)
+        self.v = torch.zeros((num_blocks, n_kv_heads, head_dim, BLOCK_SIZE), dtype=torch.int8,
+                             device=device)
+        self.k_scale = torch.zeros((num_blocks, n_kv_heads, BLOCK_SIZE), dtype=torch.float32,
+                                   device=device)
+        self.v_scale = torch.zeros_like(self.k_scale)
+
+    def struct(self):
+        return _Cache(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
+                      self.v_scale.data_ptr(), self.num_blocks, BLOCK_SIZE, self.n_kv_heads,
+                      self.head_dim)
+
+
+def kvq_version():
+    return lib().kvq_version()
+
+
+def kvq_device_status(stream=None):
+    flags = ctypes.c_uint32(0)
+    _check("kvq_device_status", lib().kvq_device_status(ctypes.byref(flags), _stream(stream)))
+    return flags.value
+
+
+def kvq_quant_write(cache, k_new, v_new, seq_idx, pos, block_table, stream=None):
+    """k_new, v_new: bf16 [T][Hkv][D]; seq_idx, pos: int32 [T]; block_table: int32 [S][M]."""
+    bt = block_table if block_table.dim() == 2 else block_table.view(1, -1)
+    c = cache.struct()
+    _check("kvq_quant_write", lib().kvq_quant_write(
+        ctypes.byref(c), _p(k_new), _p(v_new), int(seq_idx.numel()), _p(seq_idx), _p(pos), _p(bt),
+        int(bt.shape[0]), int(bt.shape[1]), _stream(stream)))
+
+
+def _decode_opts(split_rows, route_threshold, force_route):
+    return _DecodeOpts(int(split_rows), int(route_threshold), int(force_route))
+
+
+def kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, split_rows=0,
+                               route_threshold=0, force_route=0):
+    o = _decode_opts(split_rows, route_threshold, force_route)
+    return int(lib().kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, ctypes.byref(o)))
+
+
+def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_scale, out=None,
+                           workspace=None, split_rows=0, route_threshold=0, force_route=0,
+                           stream=None):
+    """q: bf16 [B][Hq][D]; block_table int32 [B][M]; ctx_lens int32 [B] (device);
+    max_ctx: host bound of ctx_lens.  Returns out fp32 [B][Hq][D]."""
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    o = _decode_opts(split_rows, route_threshold, force_route)
+    need = int(lib().kvq_decode_workspace_bytes(B, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    c = cache.struct()
+    _check("kvq_attn_decode_int8kv", lib().kvq_attn_decode_int8kv(
+        ctypes.byref(c), _p(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
+        _stream(stream)))
+    return out
+
+
+def kvq_prefill_workspace_bytes(n_tokens, n_q_heads, head_dim):
+    return int(lib().kvq_prefill_workspace_bytes(n_tokens, n_q_heads, head_dim))
+
+
+def kvq_attn_prefill_int8(cache, q, history_len, block_table_row, softmax_scale, out=None,
+                          workspace=None, stream=None):
+    """q: bf16 [T][Hq][D]; block_table_row int32 [n]; returns out fp32 [T][Hq][D]."""
+    T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=q.device)
+    need = kvq_prefill_workspace_bytes(T, Hq, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    c = cache.struct()
+    _check("kvq_attn_prefill_int8", lib().kvq_attn_prefill_int8(
+        ctypes.byref(c), _p(q), T, Hq, int(history_len), _p(block_table_row),
+        int(block_table_row.numel()), float(softmax_scale), _p(out), _p(workspace), wbytes,
+        _stream(stream)))
+    return out
+
+
+def kvq_attn_sparse_int8kv(cache, q, cell_offsets, cells, block_table_row, softmax_scale,
+                           out=None, stream=None):
+    """q: bf16 [N][Hq][D]; cell_offsets int32 [N+1]; cells int32; returns fp32 [N][Hq][D]."""
+    N, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((N, Hq, D), dtype=torch.float32, device=q.device)
+    c = cache.struct()
+    _check("kvq_attn_sparse_int8kv", lib().kvq_attn_sparse_int8kv(
+        ctypes.byref(c), _p(q), N, Hq, _p(cell_offsets), _p(cells), _p(block_table_row),
+        int(block_table_row.numel()), float(softmax_scale), _p(out), _stream(stream)))
+    return out
+
+
+def kvq_debug_prefill_q_codes(q, stream=None):
+    """Q quantisation step alone: returns (int8 codes [T][Hq][D], fp32 scales [T][Hq])."""
+    T, Hq, D = q.shape
+    codes = torch.empty((T, Hq, D), dtype=torch.int8, device=q.device)
+    scales = torch.empty((T, Hq), dtype=torch.float32, device=q.device)
+    _check("kvq_debug_prefill_q_codes", lib().kvq_debug_prefill_q_codes(
+        _p(q), T, Hq, D, _p(codes), _p(scales), _stream(stream)))
+    return codes, scales
+
+
+def kvq_debug_prefill_qk_int32(cache, q_codes, block_table_row, q_head, q0, k0, nk, stream=None):
+    """Tensor-core QK tile alone: int32 [128][nk] for query rows q0..q0+127, keys k0..k0+nk-1."""
+    T, Hq, D = q_codes.shape
+    s = torch.empty((128, nk), dtype=torch.int32, device=q_codes.device)
+    c = cache.struct()
+    _check("kvq_debug_prefill_qk_int32", lib().kvq_debug_prefill_qk_int32(
+        ctypes.byref(c), _p(q_codes), T, Hq, _p(block_table_row), int(block_table_row.numel()),
+        int(q_head), int(q0), int(k0), int(nk), _p(s), _stream(stream)))
+    return s

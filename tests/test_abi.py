@@ -1,0 +1,54 @@
+"""The C-ABI library loads and exports every entry point include/kvq.h declares (no GPU
+needed: only symbol lookup and the pure host helpers are exercised)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    from int8_kv_cache_quant_gb300 import build
+    path = build.build()
+    lib = ctypes.CDLL(path)
+    names = declared_symbols()
+    assert len(names) >= 10
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_helpers_without_gpu():
+    import int8_kv_cache_quant_gb300 as k
+    L = k.lib()
+    assert L.kvq_version() == 1
+    assert L.kvq_status_string(4) == b"workspace missing or too small"
+    # workspace sizes are pure host arithmetic
+    assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 64 * 24 * 256 * 4 + 64 * 24 * 16
+    assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 0  # single-CTA route
+    assert k.kvq_prefill_workspace_bytes(2048, 24, 256) == 2048 * 24 * 256 + 2048 * 24 * 4
+
+
+def test_invalid_arguments_rejected_before_launch():
+    import int8_kv_cache_quant_gb300 as k
+    L = k.lib()
+    c = k.kvq._Cache(16, 16, 16, 16, 4, 16, 4, 192)  # head_dim 192 unsupported
+    assert L.kvq_quant_write(ctypes.byref(c), 16, 16, 1, 16, 16, 16, 1, 1, None) == 2
+    c = k.kvq._Cache(16, 16, 16, 16, 4, 8, 4, 256)  # block size 8 unsupported
+    assert L.kvq_quant_write(ctypes.byref(c), 16, 16, 1, 16, 16, 16, 1, 1, None) == 2
+    c = k.kvq._Cache(17, 16, 16, 16, 4, 16, 4, 256)  # misaligned K
+    assert L.kvq_quant_write(ctypes.byref(c), 16, 16, 1, 16, 16, 16, 1, 1, None) == 3
+    c = k.kvq._Cache(16, 16, 16, 16, 4, 16, 4, 256)
+    assert L.kvq_quant_write(ctypes.byref(c), None, 16, 1, 16, 16, 16, 1, 1, None) == 1
+    # decode: Hq not a multiple of Hkv; group above 8; workspace too small
+    assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 6, 16, 4, 16, 100, 1.0, 16, None, 0,
+                                    None, None) == 1
+    assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 40, 16, 4, 16, 100, 1.0, 16, None, 0,
+                                    None, None) == 2
+    assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 8, 16, 4000, 16, 60000, 1.0, 16, None,
+                                    0, None, None) == 4

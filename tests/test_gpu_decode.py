@@ -1,0 +1,136 @@
+"""kvq_attn_decode_int8kv on the GPU against the oracle (FP64 Part A).
+
+Gates: the spec acceptance is <= 5e-3 normalised max-abs error against the FP64
+reference over the dequantised K/V (and <= 2e-3 against the int8-emulated output, which for
+decode is the same Part A: decode quantises neither Q nor P).  The design itself keeps
+~22-bit softmax weights (fp16 hi + lo) and fp32 accumulation, so errors land near 1e-6;
+DESIGN_TOL = 1e-4 catches regressions well inside the gate.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+from helpers import gpu_cache_from, host_cache_from, norm_max_err, sample_units, to_bf16_tensor, to_i32
+
+pytestmark = pytest.mark.gpu
+
+GATE = 2e-3
+DESIGN_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import int8_kv_cache_quant_gb300 as k
+    k.lib()
+    return k
+
+
+def _run(kvq, w, **opts):
+    cache, bt = gpu_cache_from(w, kvq)
+    q = to_bf16_tensor(w["q"])
+    ctx = to_i32(w["ctx_lens"])
+    out = kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], **opts)
+    return out.cpu().numpy(), cache, bt
+
+
+@pytest.mark.parametrize("route", [1, 2])
+@pytest.mark.parametrize("ctx", [1, 15, 17, 511, 513, 1000])
+def test_small_contexts_both_routes(kvq, oracle, route, ctx):
+    w = W.make("decode_32k", seed=200 + ctx, batch=2, ctx=ctx, hq=24, hkv=4, d=256)
+    got, _, _ = _run(kvq, w, force_route=route)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    err = norm_max_err(got, ref)
+    assert err <= GATE and err <= DESIGN_TOL, err
+    assert kvq.kvq_device_status() == 0
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 8, 1), (256, 16, 2), (128, 4, 4)])
+def test_head_geometries(kvq, oracle, d, hq, hkv):
+    w = W.make("decode_b64", seed=300 + hq, batch=5, ctx_range=(1, 1500), hq=hq, hkv=hkv, d=d)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    for route in (1, 2):
+        got, _, _ = _run(kvq, w, force_route=route, split_rows=128)
+        err = norm_max_err(got, ref)
+        assert err <= DESIGN_TOL, (route, err)
+
+
+@pytest.mark.parametrize("split", [16, 64, 512, 2048])
+def test_split_size_invariance(kvq, oracle, split):
+    w = W.make("decode_b64", seed=400, batch=3, ctx_range=(900, 3000), hq=24, hkv=4, d=256)
+    got, _, _ = _run(kvq, w, force_route=2, split_rows=split)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_split_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], split)
+    assert norm_max_err(got, ref) <= DESIGN_TOL
+
+
+def test_zero_context_and_mixed_lengths(kvq, oracle):
+    w = W.make("decode_b64", seed=401, batch=4, ctx_range=(100, 700), hq=8, hkv=2, d=128)
+    w["ctx_lens"] = w["ctx_lens"].copy()
+    w["ctx_lens"][1] = 0
+    got, _, _ = _run(kvq, w, force_route=2, split_rows=64)
+    assert not got[1].any()
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    assert norm_max_err(got, ref) <= DESIGN_TOL
+
+
+def test_bad_block_is_flagged_not_faulted(kvq):
+    w = W.make("decode_32k", seed=402, batch=1, ctx=64, hq=6, hkv=1, d=128)
+    cache, bt = gpu_cache_from(w, kvq)
+    kvq.kvq_device_status()
+    bad = bt.clone()
+    bad[0, 2] = 10 ** 6
+    q = to_bf16_tensor(w["q"])
+    out = kvq.kvq_attn_decode_int8kv(cache, q, bad, to_i32(w["ctx_lens"]), 64, w["softmax_scale"])
+    flags = kvq.kvq_device_status()
+    assert flags & kvq.kvq.DEV_BAD_BLOCK
+    assert np.isfinite(out.cpu().numpy()).all()
+
+
+def test_decode_1k_full(kvq, oracle):
+    """Workload decode_1k: ctx 1024, contiguous cache, single-CTA route (default)."""
+    w = W.make("decode_1k")
+    got, _, _ = _run(kvq, w)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    err = norm_max_err(got, ref)
+    print("decode_1k normalised max err", err)
+    assert err <= GATE and err <= DESIGN_TOL
+
+
+def test_decode_32k_full(kvq, oracle):
+    """Workload decode_32k at full size in the benchmark's launch configuration (split-K,
+    512-key splits, shuffled pages, K outliers): every output against FP64."""
+    w = W.make("decode_32k")
+    got, _, _ = _run(kvq, w, split_rows=w["split_rows"])
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    err = norm_max_err(got, ref)
+    print("decode_32k normalised max err", err)
+    assert err <= GATE and err <= DESIGN_TOL
+
+
+def test_decode_b64_full_sampled(kvq, oracle):
+    """Workload decode_b64 at full size (64 sequences, ctx up to 16384, head_dim 128) with the
+    step's kv_quant_write of one new token per sequence; sampled (sequence, head) outputs."""
+    import torch
+    w = W.make("decode_b64")
+    cache, bt = gpu_cache_from(w, kvq)
+    rng = np.random.default_rng(9)
+    kn = W.normal_bf16(rng, (w["batch"], w["hkv"], w["d"]))
+    vn = W.normal_bf16(rng, (w["batch"], w["hkv"], w["d"]))
+    kvq.kvq_quant_write(cache, to_bf16_tensor(kn), to_bf16_tensor(vn), to_i32(w["new_seq"]),
+                        to_i32(w["new_pos"]), bt)
+    out = kvq.kvq_attn_decode_int8kv(cache, to_bf16_tensor(w["q"]), bt, to_i32(w["ctx_lens"]),
+                                     w["max_ctx"], w["softmax_scale"]).cpu().numpy()
+    hc = host_cache_from(w, oracle)
+    oracle.kv_quant_write(hc, kn, vn, w["new_seq"], w["new_pos"], w["block_table"])
+    units = sample_units(w["batch"], w["hq"], 96, seed=10)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], units=units)
+    got = out.reshape(-1, w["d"])[units]
+    err = norm_max_err(got, ref)
+    print("decode_b64 normalised max err (sampled)", err)
+    assert err <= GATE and err <= DESIGN_TOL
+    del torch
