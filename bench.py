@@ -1,0 +1,435 @@
+"""Benchmark of the INT8-KV-cache attention hot path on GB300.
+
+A step of the headline workload (decode_32k: one sequence, ctx 32768, 24 query / 4 KV heads,
+head_dim 256, int8 K/V in 16-token pages behind a shuffled block table, K outliers) is one
+pass of the decode path: kv_quant_write of the step's new token, then split-K decode over
+the whole context (512-key splits, stage 1 + merge).  value = K/V bytes the step reads
+(2080 B per token) / device time of the step, in GB/s, with the L2 flushed (256 MB write)
+before every timed step, outside its events.
+
+Prints one JSON line.  --impl reference times the CPU oracle (the plain reference) on the
+host cores on a bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
+an independent replica (the path has no cross-GPU exchange) and value sums the ranks' bytes
+over the slowest rank's time.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode KV GB/s + µs/call at 32K ctx; prefill int8 TOPS; % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- kvq arm
+
+def bench_decode_32k(args, world, rank, local, extra_out):
+    import numpy as np
+    import torch
+
+    import int8_kv_cache_quant_gb300 as kvq
+    import workloads as W
+    from int8_kv_cache_quant_gb300 import build as kbuild
+
+    kbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = W.make("decode_32k")
+    D, Hq, Hkv = w["d"], w["hq"], w["hkv"]
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    cache = kvq.KVCache(w["num_blocks"], Hkv, D, device=dev)
+    bt = i32(w["block_table"])
+    kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]),
+                        i32(w["fill_pos"]), bt)
+    q = bf16(w["q"])
+    k_new, v_new = bf16(w["k_new"]), bf16(w["v_new"])
+    new_seq, new_pos = i32(w["new_seq"]), i32(w["new_pos"])
+    ctx = i32(w["ctx_lens"])
+    max_ctx = w["max_ctx"]
+    split = w["split_rows"]
+    ws = torch.empty(kvq.kvq_decode_workspace_bytes(1, Hq, max_ctx, D, split_rows=split),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((1, Hq, D), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+
+    def step(ev=None):
+        kvq.kvq_quant_write(cache, k_new, v_new, new_seq, new_pos, bt)
+        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, max_ctx, w["softmax_scale"], out=out,
+                                   workspace=ws, split_rows=split, stage1_events=ev)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    assert kvq.kvq_device_status() == 0
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in k0 + k1:  # create the underlying CUDA events; the library re-records them
+        e.record(s)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev0[i].record(s)
+            step((k0[i], k1[i]))
+            ev1[i].record(s)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+    ms_step = statistics.mean(step_ms)
+    ms_step_max = max_over_ranks(ms_step, world)
+    kv_bytes = max_ctx * (2 * Hkv * D + 2 * Hkv * 4)  # 2080 B per token at 4 x 256
+
+    # end to end through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, the step, D2H of the result, all inside the events
+    q_h = torch.from_numpy(np.ascontiguousarray(w["q"]).view(np.int16)).pin_memory()
+    kn_h = torch.from_numpy(np.ascontiguousarray(w["k_new"]).view(np.int16)).pin_memory()
+    vn_h = torch.from_numpy(np.ascontiguousarray(w["v_new"]).view(np.int16)).pin_memory()
+    sp_h = torch.from_numpy(np.concatenate([w["new_seq"], w["new_pos"]]).astype(np.int32)).pin_memory()
+    out_h = torch.empty((1, Hq, D), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(q_h, device=dev)
+    kn_d = torch.empty_like(kn_h, device=dev)
+    vn_d = torch.empty_like(vn_h, device=dev)
+    sp_d = torch.empty_like(sp_h, device=dev)
+    h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + sp_h.numel() * 4
+    d2h = out_h.numel() * 4
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kn_d.copy_(kn_h, non_blocking=True)
+        vn_d.copy_(vn_h, non_blocking=True)
+        sp_d.copy_(sp_h, non_blocking=True)
+        kvq.kvq_quant_write(cache, kn_d.view(torch.bfloat16), vn_d.view(torch.bfloat16), sp_d[:1],
+                            sp_d[1:], bt)
+        kvq.kvq_attn_decode_int8kv(cache, q_d.view(torch.bfloat16), bt, ctx, max_ctx,
+                                   w["softmax_scale"], out=out, workspace=ws, split_rows=split)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        flush.fill_(2)
+        e2e_step()
+    torch.cuda.synchronize()
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        e0[i].record(s)
+        e2e_step()
+        e1[i].record(s)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(e0, e1)), world)
+    got = out_h.numpy().copy()
+    assert np.isfinite(got).all()
+
+    hbm, _, peak_kind = load_peaks()
+    kern_avg = statistics.mean(kern_ms)
+    achieved = kv_bytes / (kern_avg * 1e-3) / 1e9
+    res = {
+        "metric": METRIC,
+        "value": round(world * kv_bytes / (ms_step_max * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step_max, 5),
+        "us_per_call": round(ms_step_max * 1e3, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V quantised to int8 codes + fp32 scales; K outliers x8 p=0.01)",
+        "config": {"workload": "decode_32k", "batch": 1, "ctx": max_ctx, "q_heads": Hq, "kv_heads": Hkv,
+                   "head_dim": D, "block_size": 16, "block_table": "random permutation",
+                   "split_rows": split, "kv_bytes_per_step": kv_bytes,
+                   "step": "kv_quant_write(1 token) + decode stage1 + merge",
+                   "l2": "flushed before every timed step (256 MB write outside the events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "kernel": "decode_stage1_kernel<256,4,12,split>", "peak_kind": peak_kind,
+                     "kernel_us": round(kern_avg * 1e3, 2)},
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * K,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    return res
+
+
+def bench_extra(args, local, hbm, tflops):
+    """Secondary figures on the other workloads (one JSON object, not the headline)."""
+    import numpy as np
+    import torch
+
+    import int8_kv_cache_quant_gb300 as kvq
+    import workloads as W
+    dev = torch.device("cuda", local)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            flush.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for i in range(reps):
+            flush.fill_(i & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fn()
+            b.record(s)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.median(ms)
+
+    res = {}
+    # decode_1k: single-CTA route, launch/latency bound
+    w = W.make("decode_1k")
+    cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
+    bt = i32(w["block_table"])
+    kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
+    q, ctx = bf16(w["q"]), i32(w["ctx_lens"])
+    out = torch.empty((1, w["hq"], w["d"]), dtype=torch.float32, device=dev)
+    ms = timed(lambda: kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out), 50)
+    kvb = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
+    res["decode_1k"] = {"us_per_call": round(ms * 1e3, 2), "kv_GBps": round(kvb / ms / 1e6, 1)}
+    del cache
+
+    # sparse_32k
+    w = W.make("sparse_32k")
+    cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
+    bt = i32(w["block_table"])
+    kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
+    q, off, cells, row = bf16(w["q"]), i32(w["cell_offsets"]), i32(w["cells"]), i32(w["block_table"][0])
+    out = torch.empty((w["n_queries"], w["hq"], w["d"]), dtype=torch.float32, device=dev)
+    ms = timed(lambda: kvq.kvq_attn_sparse_int8kv(cache, q, off, cells, row, w["softmax_scale"], out=out), 10)
+    pairs = int(len(w["cells"]))
+    fma = pairs * w["hq"] * w["d"] * 2
+    res["sparse_32k"] = {"ms_per_call": round(ms, 4), "GFMA_per_s": round(fma / ms / 1e6, 1),
+                         "pairs": pairs}
+    del cache
+    return res
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def bench_reference(args, world, rank):
+    """The CPU oracle (test infrastructure, the plain reference) on the host cores: each step is
+    a bounded sample of decode_32k (the new token's quantise-and-write, then FP64 decode of a
+    subset of the query heads over all 32768 keys)."""
+    import numpy as np
+
+    import oracle
+    import workloads as W
+    w = W.make("decode_32k")
+    hc = oracle.HostCache(w["num_blocks"], w["hkv"], w["d"])
+    oracle.kv_quant_write(hc, w["k_fill"], w["v_fill"], w["fill_seq"], w["fill_pos"], w["block_table"])
+    cores = os.cpu_count() or 1
+    heads = int(os.environ.get("KVQ_REF_HEADS", "24"))
+    units = np.arange(heads, dtype=np.int64)
+    kv_bytes = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
+    frac = heads / w["hq"]
+
+    def step():
+        oracle.kv_quant_write(hc, w["k_new"], w["v_new"], w["new_seq"], w["new_pos"], w["block_table"])
+        oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"],
+                          units=units, n_threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t) / args.steps
+    value = kv_bytes * frac / dt / 1e9
+    sample = "%d of %d query heads (units 0..%d) of decode_32k per step, all 32768 keys" % (
+        heads, w["hq"], heads - 1)
+    return {
+        "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "impl": "reference",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode_32k", "ctx": w["max_ctx"], "q_heads": w["hq"],
+                   "kv_heads": w["hkv"], "head_dim": w["d"], "sample_heads": heads},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_for_line(budget_s=12.0):
+    """The oracle timed on the host cores on a bounded sample of decode_32k (reported beside
+    the GPU number; not the target)."""
+    import numpy as np
+
+    import oracle
+    import workloads as W
+    w = W.make("decode_32k")
+    hc = oracle.HostCache(w["num_blocks"], w["hkv"], w["d"])
+    oracle.kv_quant_write(hc, w["k_fill"], w["v_fill"], w["fill_seq"], w["fill_pos"], w["block_table"])
+    cores = os.cpu_count() or 1
+    kv_bytes = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
+    units = np.arange(w["hq"], dtype=np.int64)
+    t = time.perf_counter()
+    n = 0
+    while True:
+        oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], units=units,
+                          n_threads=cores)
+        n += 1
+        if time.perf_counter() - t > budget_s or n >= 64:
+            break
+    dt = (time.perf_counter() - t) / n
+    return {"value": round(kv_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "%d full decode_32k calls (all 24 query heads, FP64 Part A), %.1f s" % (n, dt * n)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(bench_reference(args, world, rank)))
+        return
+    res = bench_decode_32k(args, world, rank, local, None)
+    if rank == 0:
+        hbm, tflops, _ = load_peaks()
+        if not args.no_extra:
+            res["extra"] = bench_extra(args, local, hbm, tflops)
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline_for_line()
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

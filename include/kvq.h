@@ -110,6 +110,10 @@ typedef struct kvq_decode_opts {
   int32_t split_rows;      /* keys per split in the split route; 0 -> 512; multiple of 16 */
   int32_t route_threshold; /* max_ctx <= threshold -> single-CTA route; 0 -> 2048 ([DOT4] route table) */
   int32_t force_route;     /* 0 auto, 1 single CTA per (sequence, KV head), 2 split-K */
+  /* Optional profiling hooks: two cudaEvent_t (as void*) recorded on `stream` right before
+   * and right after the stage-1 (K/V streaming) kernel launch; NULL to skip. */
+  void* stage1_event_begin;
+  void* stage1_event_end;
 } kvq_decode_opts;
 
 /* Workspace (bytes) the split route of kvq_attn_decode_int8kv needs; 0 when the call

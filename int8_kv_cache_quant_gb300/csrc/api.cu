@@ -45,11 +45,13 @@ int check_cache(const kvq_cache* c) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
 kvq_decode_opts decode_defaults(const kvq_decode_opts* o) {
-  kvq_decode_opts r = {KVQ_DEFAULT_SPLIT_ROWS, 2048, 0};
+  kvq_decode_opts r = {KVQ_DEFAULT_SPLIT_ROWS, 2048, 0, nullptr, nullptr};
   if (o) {
     if (o->split_rows > 0) r.split_rows = o->split_rows;
     if (o->route_threshold > 0) r.route_threshold = o->route_threshold;
     r.force_route = o->force_route;
+    r.stage1_event_begin = o->stage1_event_begin;
+    r.stage1_event_end = o->stage1_event_end;
   }
   return r;
 }
@@ -166,6 +168,8 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   a.out = out;
   a.split_rows = o.split_rows;
   a.status = status_ptr();
+  a.ev_begin = static_cast<cudaEvent_t>(o.stage1_event_begin);
+  a.ev_end = static_cast<cudaEvent_t>(o.stage1_event_end);
   if (split) {
     const long long n_split = (static_cast<long long>(mc) + o.split_rows - 1) / o.split_rows;
     if (n_split > kMaxSplits) return KVQ_ERR_UNSUPPORTED;

@@ -46,34 +46,63 @@ __device__ __forceinline__ int row_token(int row) {
   return base + (((r >= 4) != (hi != 0)) ? 2 : 0);
 }
 
-template <int D, int NW, int STAGES>
+template <int D, int NP, int DEPTH>
 struct DecodeSmem {
-  static constexpr int kKvBytes = D * KVQ_BLOCK_SIZE;            // one (page, head) of K or V
-  static constexpr int kStageBytes = 2 * kKvBytes + 2 * 64;      // K, V, k_scale, v_scale
-  static constexpr int kRingBytes = STAGES * kStageBytes;
-  static constexpr int kBarOffset = kRingBytes;
-  static constexpr int kFlagOffset = kBarOffset + 2 * STAGES * 8;
-  static constexpr int kTotal = kFlagOffset + STAGES * 4;
-  static constexpr int kMergeBytes = NW * 8 * (D + 4) * 4;       // per-warp O and stats
+  static constexpr int kKvBytes = D * KVQ_BLOCK_SIZE;             // one (page, head) of K or V
+  static constexpr int kStageBytes = 2 * kKvBytes + 2 * 64;       // K, V, k_scale, v_scale
+  static constexpr int kStages = NP * DEPTH;                      // DEPTH private stages per pair
+  static constexpr int kRingBytes = kStages * kStageBytes;
+  static constexpr int kQOffset = kRingBytes;                     // Q^T fragments (fp16)
+  static constexpr int kQBytes = D * 16;                          // D/16 chunks x 2 x 8 heads x 16 B
+  static constexpr int kXOffset = kQOffset + kQBytes;             // partial-S exchange
+  static constexpr int kXBytes = NP * 2 * 2 * 32 * 16;            // [pair][buffer][half][lane] float4
+  static constexpr int kBarOffset = kXOffset + kXBytes;           // full barriers [pair][DEPTH]
+  static constexpr int kFlagOffset = kBarOffset + kStages * 8;    // page-ok flags [pair][DEPTH]
+  static constexpr int kCqOffset = kFlagOffset + kStages * 4;     // score factor per group head
+  static constexpr int kTotal = kCqOffset + 8 * 4;
+  static constexpr int kMergeBytes = (NP * 8 * (D + 4) + NP * 8 * 4 + 8 * NP + 32) * 4;  // merge scratch
   static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the ring");
-  static_assert(STAGES % NW == 0, "each stage belongs to one consumer warp");
+  static_assert(NP >= 4 && NP <= 8, "8..16 warps: one warp per group head prepares Q");
 };
+
+// AND of `pred` over the 64 threads of named barrier `id` (both warps of a pair).
+__device__ __forceinline__ bool pair_sync_and(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, 64, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id)
+      : "memory");
+  return r != 0;
+}
+
+constexpr float kLazyRescale = 8.0f;  // keep a running maximum until the tile exceeds it by 2^8
 
 }  // namespace
 
-template <int D, int NW, int STAGES, bool SPLIT>
-__global__ void __launch_bounds__((NW + 1) * 32) decode_stage1_kernel(DecodeArgs a) {
-  using L = DecodeSmem<D, NW, STAGES>;
+// Stage 1.  CTA = NP warp pairs over the key range of one (split, KV head, sequence); pair p
+// takes pages p, p + NP, ... of the range and streams them into its own DEPTH-stage ring
+// (warp 0 of the pair issues the 1-D bulk copies).  The two warps of a pair split the head
+// dimension: each computes a partial S^T over its half, the halves are summed through shared
+// memory (both warps then hold the same S and run the same softmax), and each warp
+// accumulates O^T for its half of the head dimension.
+template <int D, int NP, int DEPTH, bool SPLIT>
+__global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
+  using L = DecodeSmem<D, NP, DEPTH>;
   constexpr int KB = L::kKvBytes;
-  constexpr int NCH = D / 16;  // 16-dim chunks
-  constexpr int NMT = D / 16;  // 16-dim m-tiles of O^T
+  constexpr int NCH_H = D / 32;  // 16-dim chunks per half of the head dimension
+  constexpr int NMT_H = D / 32;  // 16-dim m-tiles of O^T per half
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;
+  uint8_t* q_s = smem + L::kQOffset;
+  float4* xs = reinterpret_cast<float4*>(smem + L::kXOffset);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
-  uint64_t* empty = full + STAGES;
   int* stage_ok = reinterpret_cast<int*>(smem + L::kFlagOffset);
+  float* cq_s = reinterpret_cast<float*>(smem + L::kCqOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int p = warp >> 1, hf = warp & 1;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
 
@@ -99,267 +128,278 @@ __global__ void __launch_bounds__((NW + 1) * 32) decode_stage1_kernel(DecodeArgs
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
+    for (int s = 0; s < L::kStages; ++s) mbar_init(&full[s], 1);
     mbar_fence_init();
+  }
+  // ---- Q^T fragments: warp h prepares head h of the group (zeros past G).  The fp16 values
+  // are q * 2^e (e brings max|q| into [2^14, 2^15): exact for bf16).  Chunk j (16 dims) is
+  // two 8 x 8 b16 matrices, rows = heads, whose columns are the k-slots of the MMA: slots
+  // (2c, 2c+1) carry dims (4c, 4c+1) and slots (2c+8, 2c+9) carry dims (4c+2, 4c+3).
+  if (warp < 8) {
+    const int h = warp;
+    const bool real = h < G;
+    constexpr int PER = D / 32;  // dims per lane
+    float x[PER];
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + (static_cast<long long>(b) * Hq + kvh * G + h) * D + lane * PER;
+    if constexpr (PER == 8) {
+      const uint4 raw = real ? __ldg(reinterpret_cast<const uint4*>(qrow)) : make_uint4(0, 0, 0, 0);
+      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[2 * i] = __uint_as_float(w4[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+      }
+    } else {
+      const uint2 raw = real ? __ldg(reinterpret_cast<const uint2*>(qrow)) : make_uint2(0, 0);
+      const uint32_t w2[2] = {raw.x, raw.y};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        x[2 * i] = __uint_as_float(w2[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w2[i] & 0xFFFF0000u);
+      }
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    int e = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 : 0;
+    e = max(-100, min(e, 127));
+    const float qs = __uint_as_float(static_cast<uint32_t>(127 + 14 - e) << 23);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int d = lane * PER + i;
+      const int j = d >> 4, w = d & 15, c = w >> 2, bb = w & 3;
+      const int half = bb >> 1, el = 2 * c + (bb & 1);
+      *reinterpret_cast<__half*>(q_s + ((j * 2 + half) * 8 + h) * 16 + el * 2) = __float2half_rn(x[i] * qs);
+    }
+    if (lane == 0) cq_s[h] = a.softmax_scale * kLog2e / qs;
   }
   __syncthreads();
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer warp
-    const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
-    bool alive = true;
-    for (int j0 = 0; j0 < n_pages && alive; j0 += 32) {
-      int pg = -1;
-      if (j0 + lane < n_pages) pg = __ldg(bt + j0 + lane);
-      const int cnt = min(32, n_pages - j0);
-      for (int jj = 0; jj < cnt; ++jj) {
-        const int j = j0 + jj;
-        const int page = __shfl_sync(0xffffffffu, pg, jj);
-        const int s = j % STAGES;
-        int ok_wait = 1;
-        if (lane == 0 && j >= STAGES) ok_wait = mbar_wait(&empty[s], ((j / STAGES) - 1) & 1, a.status);
-        ok_wait = __shfl_sync(0xffffffffu, ok_wait, 0);
-        if (!ok_wait) {
-          alive = false;
-          break;
-        }
-        if (lane == 0) {
-          const bool ok = page >= 0 && page < a.num_blocks;
-          stage_ok[s] = ok ? 1 : 0;
-          if (ok) {
-            uint8_t* st = ring + s * L::kStageBytes;
-            const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
-            mbar_arrive_expect_tx(&full[s], 2 * KB + 128);
-            bulk_g2s(st, a.k + ph * KB, KB, &full[s]);
-            bulk_g2s(st + KB, a.v + ph * KB, KB, &full[s]);
-            bulk_g2s(st + 2 * KB, a.k_scale + ph * KVQ_BLOCK_SIZE, 64, &full[s]);
-            bulk_g2s(st + 2 * KB + 64, a.v_scale + ph * KVQ_BLOCK_SIZE, 64, &full[s]);
-          } else {
-            set_status(a.status, KVQ_DEV_BAD_BLOCK);
-            mbar_arrive(&full[s]);
-          }
-        }
+  const int npp = (p < n_pages) ? (n_pages - p + NP - 1) / NP : 0;  // pages of this pair
+  const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
+  uint64_t* pfull = full + p * DEPTH;
+  int* pok = stage_ok + p * DEPTH;
+  uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
+
+  // page ids of this pair, a window of 32 in warp 0's lanes (lane i <-> page k = wb + i)
+  int wb = 0, pg = -1;
+  if (hf == 0 && lane < npp) pg = __ldg(bt + p + lane * NP);
+  // warp 0 of the pair, collectively: issue the copy of pair page k into its slot
+  auto issue = [&](int k) {
+    while (k >= wb + 32) {
+      wb += 32;
+      pg = (wb + lane < npp) ? __ldg(bt + p + (wb + lane) * NP) : -1;
+    }
+    const int page = __shfl_sync(0xffffffffu, pg, k - wb);
+    if (lane == 0) {
+      const int s = k % DEPTH;
+      const bool ok = page >= 0 && page < a.num_blocks;
+      pok[s] = ok ? 1 : 0;
+      if (ok) {
+        uint8_t* st = pring + s * L::kStageBytes;
+        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&pfull[s], 2 * KB + 128);
+        bulk_g2s(st, a.k + ph * KB, KB, &pfull[s]);
+        bulk_g2s(st + KB, a.v + ph * KB, KB, &pfull[s]);
+        bulk_g2s(st + 2 * KB, a.k_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[s]);
+        bulk_g2s(st + 2 * KB + 64, a.v_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[s]);
+      } else {
+        set_status(a.status, KVQ_DEV_BAD_BLOCK);
+        mbar_arrive(&pfull[s]);
       }
     }
+  };
+  if (hf == 0) {
+    for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
   }
 
-  // ------------------------------------------------------------ consumer warps
   const int g = lane >> 2, c = lane & 3;
-  float o_acc[NMT][4];
+  float o_acc[NMT_H][4];
+#pragma unroll
+  for (int i = 0; i < NMT_H; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
   float ms[2] = {-INFINITY, -INFINITY}, mz[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
-  if (warp > 0) {
-    const int cw = warp - 1;
-#pragma unroll
-    for (int i = 0; i < NMT; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
+  const float cq0 = cq_s[2 * c], cq1 = cq_s[2 * c + 1];
 
-    // Q^T fragments: head g of the group, dims 16j + 4c .. 16j + 4c + 3 of chunk j (the
-    // chunk's k-slots (2c, 2c+1, 2c+8, 2c+9) carry dims (4c, 4c+1, 4c+2, 4c+3)).
-    uint32_t qb[NCH][2];
-    float qscale_self = 1.0f;
-    {
-      const bool real = g < G;
-      const uint16_t* qrow = static_cast<const uint16_t*>(a.q) +
-                             (static_cast<long long>(b) * Hq + kvh * G + (real ? g : 0)) * D;
-      float qv[NCH][4];
-      float amax = 0.f;
+  // per-lane ldmatrix offsets: K rows are tokens (in row_token order), Q^T rows are heads,
+  // V rows are head dimensions
+  const int mi = lane >> 3, r = lane & 7;
+  const uint32_t k_lane_off = (mi >> 1) * 256 + row_token((mi & 1) * 8 + r) * 16 + hf * (NCH_H * 256);
+  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + (hf * NCH_H * 2 + mi) * 128 + r * 16;
+  const uint32_t v_lane_off = hf * (D / 2) * 16 + lane * 16;
+  const int tk0 = row_token(g), tk1 = row_token(g + 8);
+  const uint32_t selA = (c < 2) ? kSelB01 : kSelB23;
+  const uint32_t selB = (c < 2) ? kSelB23 : kSelB01;
+
+  for (int k = 0; k < npp; ++k) {
+    const int s = k % DEPTH;
+    const bool got = mbar_wait(&pfull[s], (k / DEPTH) & 1, a.status);
+    uint8_t* st = pring + s * L::kStageBytes;
+    const uint32_t kbase = smem_u32(st);
+    const uint32_t vbase = kbase + KB;
+    const float* sks = reinterpret_cast<const float*>(st + 2 * KB);
+    const float* svs = reinterpret_cast<const float*>(st + 2 * KB + 64);
+
+    // ---- partial S^T = K * Q^T over this warp's half of the head dimension
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        const uint2 raw = real ? __ldg(reinterpret_cast<const uint2*>(qrow + 16 * j + 4 * c)) : make_uint2(0, 0);
-        qv[j][0] = __uint_as_float(raw.x << 16);
-        qv[j][1] = __uint_as_float(raw.x & 0xFFFF0000u);
-        qv[j][2] = __uint_as_float(raw.y << 16);
-        qv[j][3] = __uint_as_float(raw.y & 0xFFFF0000u);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(qv[j][i]));
-      }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      // power of two that brings max|q| into [2^14, 2^15): exact for bf16 inputs
-      int e = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 : 0;
-      e = max(-100, min(e, 127));
-      qscale_self = __uint_as_float(static_cast<uint32_t>(127 + 14 - e) << 23);
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        qb[j][0] = pack_half2(qv[j][0] * qscale_self, qv[j][1] * qscale_self);
-        qb[j][1] = pack_half2(qv[j][2] * qscale_self, qv[j][3] * qscale_self);
-      }
+    for (int jj = 0; jj < NCH_H / 2; ++jj) {
+      uint32_t r0, r1, r2, r3, a0, a1, a2, a3, q0, q1, q2, q3;
+      ldsm_x4(kbase + jj * 512 + k_lane_off, r0, r1, r2, r3);
+      ldsm_x4(q_lane_off + jj * 512, q0, q1, q2, q3);
+      i8x4_to_h2x2(r0, kSelB01, kSelB23, a0, a2);
+      i8x4_to_h2x2(r1, kSelB01, kSelB23, a1, a3);
+      mma_f16_16816(sa, a0, a1, a2, a3, q0, q1);
+      i8x4_to_h2x2(r2, kSelB01, kSelB23, a0, a2);
+      i8x4_to_h2x2(r3, kSelB01, kSelB23, a1, a3);
+      mma_f16_16816(sb, a0, a1, a2, a3, q2, q3);
     }
-    // score factor of this thread's two heads 2c, 2c+1: softmax_scale * log2(e) / qscale
-    float cq[2];
+    float4* xb = xs + ((p * 2 + (k & 1)) * 2) * 32;
+    xb[hf * 32 + lane] = make_float4(sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]);
+    if (!pair_sync_and(1 + p, got)) break;  // both warps of the pair leave together
+    const float4 x0 = xb[lane], x1 = xb[32 + lane];
+    const float S[4] = {x0.x + x1.x, x0.y + x1.y, x0.z + x1.z, x0.w + x1.w};
+    // the slot of the previous page is free in both warps: refill it
+    if (hf == 0 && k >= 1 && k - 1 + DEPTH < npp) issue(k - 1 + DEPTH);
+
+    // ---- online softmax (identical in both warps of the pair)
+    const bool page_ok = pok[s] != 0;
+    const int tpage = t_begin + (p + k * NP) * KVQ_BLOCK_SIZE;
+    const bool v0 = page_ok && (tpage + tk0 < t_end);
+    const bool v1 = page_ok && (tpage + tk1 < t_end);
+    const float sk0 = sks[tk0], sk1 = sks[tk1];
+    const float lv0 = v0 ? fast_log2(svs[tk0]) : -INFINITY;
+    const float lv1 = v1 ? fast_log2(svs[tk1]) : -INFINITY;
+    float w[2][2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const float qs = __shfl_sync(0xffffffffu, qscale_self, (2 * c + i) * 4);
-      cq[i] = a.softmax_scale * kLog2e / qs;
-    }
-
-    // per-lane ldmatrix offsets
-    const int mi = lane >> 3, r = lane & 7;
-    const uint32_t k_lane_off = (mi >> 1) * 256 + row_token((mi & 1) * 8 + r) * 16;
-    const uint32_t v_lane_off = lane * 16;
-    const int tk0 = row_token(g), tk1 = row_token(g + 8);
-    const uint32_t selA = (c < 2) ? kSelB01 : kSelB23;
-    const uint32_t selB = (c < 2) ? kSelB23 : kSelB01;
-
-    for (int j = cw; j < n_pages; j += NW) {
-      const int s = j % STAGES;
-      if (!mbar_wait(&full[s], (j / STAGES) & 1, a.status)) break;
-      uint8_t* st = ring + s * L::kStageBytes;
-      const uint32_t kbase = smem_u32(st);
-      const uint32_t vbase = kbase + KB;
-      const float* sks = reinterpret_cast<const float*>(st + 2 * KB);
-      const float* svs = reinterpret_cast<const float*>(st + 2 * KB + 64);
-      const bool page_ok = stage_ok[s] != 0;
-      const int tpage = t_begin + j * KVQ_BLOCK_SIZE;
-
-      // ---- S^T = K * Q^T over the head dimension
-      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+      const float cqi = i ? cq1 : cq0;
+      const float s0 = v0 ? S[i] * sk0 * cqi : -INFINITY;
+      const float s1 = v1 ? S[2 + i] * sk1 * cqi : -INFINITY;
+      const float z0 = s0 + lv0, z1 = s1 + lv1;
+      float tms = fmaxf(s0, s1), tmz = fmaxf(z0, z1);
 #pragma unroll
-      for (int jj = 0; jj < NCH / 2; ++jj) {
-        uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-        ldsm_x4(kbase + jj * 512 + k_lane_off, r0, r1, r2, r3);
-        i8x4_to_h2x2(r0, kSelB01, kSelB23, a0, a2);
-        i8x4_to_h2x2(r1, kSelB01, kSelB23, a1, a3);
-        mma_f16_16816(sa, a0, a1, a2, a3, qb[2 * jj][0], qb[2 * jj][1]);
-        i8x4_to_h2x2(r2, kSelB01, kSelB23, a0, a2);
-        i8x4_to_h2x2(r3, kSelB01, kSelB23, a1, a3);
-        mma_f16_16816(sb, a0, a1, a2, a3, qb[2 * jj + 1][0], qb[2 * jj + 1][1]);
+      for (int off = 4; off < 32; off <<= 1) {
+        tms = fmaxf(tms, __shfl_xor_sync(0xffffffffu, tms, off));
+        tmz = fmaxf(tmz, __shfl_xor_sync(0xffffffffu, tmz, off));
       }
-      // rows g (token tk0) and g + 8 (token tk1); columns = heads 2c, 2c + 1
-      const bool v0 = page_ok && (tpage + tk0 < t_end);
-      const bool v1 = page_ok && (tpage + tk1 < t_end);
-      const float sk0 = sks[tk0], sk1 = sks[tk1];
-      const float lv0 = v0 ? fast_log2(svs[tk0]) : -INFINITY;
-      const float lv1 = v1 ? fast_log2(svs[tk1]) : -INFINITY;
-      float s2[2][2], z[2][2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        s2[0][i] = v0 ? (sa[i] + sb[i]) * sk0 * cq[i] : -INFINITY;
-        s2[1][i] = v1 ? (sa[2 + i] + sb[2 + i]) * sk1 * cq[i] : -INFINITY;
-        z[0][i] = s2[0][i] + lv0;
-        z[1][i] = s2[1][i] + lv1;
+      // lazy references: move them only when the tile exceeds them by 2^8
+      if (tms > ms[i] + kLazyRescale) {
+        lsum[i] *= (ms[i] == -INFINITY) ? 0.f : fast_exp2(ms[i] - tms);
+        ms[i] = tms;
       }
-      float w[2][2];
+      if (tmz > mz[i] + kLazyRescale) {
+        const float az = (mz[i] == -INFINITY) ? 0.f : fast_exp2(mz[i] - tmz);
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        float tms = fmaxf(s2[0][i], s2[1][i]);
-        float tmz = fmaxf(z[0][i], z[1][i]);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          tms = fmaxf(tms, __shfl_xor_sync(0xffffffffu, tms, off));
-          tmz = fmaxf(tmz, __shfl_xor_sync(0xffffffffu, tmz, off));
-        }
-        const float ms_new = fmaxf(ms[i], tms);
-        const float mz_new = fmaxf(mz[i], tmz);
-        const float msr = (ms_new == -INFINITY) ? 0.f : ms_new;
-        const float mzr = (mz_new == -INFINITY) ? 0.f : mz_new;
-        const float as = fast_exp2(ms[i] - msr);
-        const float az = fast_exp2(mz[i] - mzr);
-        lsum[i] = lsum[i] * as + fast_exp2(s2[0][i] - msr) + fast_exp2(s2[1][i] - msr);
-        w[0][i] = fast_exp2(z[0][i] - mzr);
-        w[1][i] = fast_exp2(z[1][i] - mzr);
-        ms[i] = ms_new;
-        mz[i] = mz_new;
-#pragma unroll
-        for (int mt = 0; mt < NMT; ++mt) {
+        for (int mt = 0; mt < NMT_H; ++mt) {
           o_acc[mt][i] *= az;
           o_acc[mt][2 + i] *= az;
         }
+        mz[i] = tmz;
       }
-      // ---- W fragments: hi + lo fp16 parts, transposed to the PV B layout
-      const uint32_t h0 = pack_half2(w[0][0], w[0][1]);
-      const uint32_t h1 = pack_half2(w[1][0], w[1][1]);
-      const __half2 hh0 = *reinterpret_cast<const __half2*>(&h0);
-      const __half2 hh1 = *reinterpret_cast<const __half2*>(&h1);
-      const uint32_t l0 = pack_half2(w[0][0] - __low2float(hh0), w[0][1] - __high2float(hh0));
-      const uint32_t l1 = pack_half2(w[1][0] - __low2float(hh1), w[1][1] - __high2float(hh1));
-      const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
-      const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
-
-      // ---- O^T += V^T * W
-#pragma unroll
-      for (int gg = 0; gg < D / 32; ++gg) {
-        uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-        ldsm_x4(vbase + gg * 512 + v_lane_off, r0, r1, r2, r3);
-        i8x4_to_h2x2(r0, selA, selB, a0, a2);
-        i8x4_to_h2x2(r1, selA, selB, a1, a3);
-        mma_f16_16816(o_acc[2 * gg], a0, a1, a2, a3, bh0, bh1);
-        mma_f16_16816(o_acc[2 * gg], a0, a1, a2, a3, bl0, bl1);
-        i8x4_to_h2x2(r2, selA, selB, a0, a2);
-        i8x4_to_h2x2(r3, selA, selB, a1, a3);
-        mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bh0, bh1);
-        mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bl0, bl1);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      const float msr = (ms[i] == -INFINITY) ? 0.f : ms[i];
+      const float mzr = (mz[i] == -INFINITY) ? 0.f : mz[i];
+      lsum[i] += fast_exp2(s0 - msr) + fast_exp2(s1 - msr);
+      w[0][i] = fast_exp2(z0 - mzr);
+      w[1][i] = fast_exp2(z1 - mzr);
     }
-    // l over all tokens of the warp for heads 2c, 2c + 1
+    // ---- W fragments: hi + lo fp16 parts, transposed to the PV B layout
+    const uint32_t h0 = pack_half2(w[0][0], w[0][1]);
+    const uint32_t h1 = pack_half2(w[1][0], w[1][1]);
+    const __half2 hh0 = *reinterpret_cast<const __half2*>(&h0);
+    const __half2 hh1 = *reinterpret_cast<const __half2*>(&h1);
+    const uint32_t l0 = pack_half2(w[0][0] - __low2float(hh0), w[0][1] - __high2float(hh0));
+    const uint32_t l1 = pack_half2(w[1][0] - __low2float(hh1), w[1][1] - __high2float(hh1));
+    const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
+    const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+
+    // ---- O^T += V^T * W over this warp's half of the head dimension
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], off);
+    for (int gg = 0; gg < NMT_H / 2; ++gg) {
+      uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+      ldsm_x4(vbase + v_lane_off + gg * 512, r0, r1, r2, r3);
+      i8x4_to_h2x2(r0, selA, selB, a0, a2);
+      i8x4_to_h2x2(r1, selA, selB, a1, a3);
+      mma_f16_16816(o_acc[2 * gg], a0, a1, a2, a3, bh0, bh1);
+      mma_f16_16816(o_acc[2 * gg], a0, a1, a2, a3, bl0, bl1);
+      i8x4_to_h2x2(r2, selA, selB, a0, a2);
+      i8x4_to_h2x2(r3, selA, selB, a1, a3);
+      mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bh0, bh1);
+      mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bl0, bl1);
     }
   }
+  // l over all tokens of the pair for heads 2c, 2c + 1
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], off);
+  }
 
-  // ------------------------------------------------------------ merge the consumer warps
-  __syncthreads();  // every fill was waited for by its consumer: the ring is free
-  float* mo = reinterpret_cast<float*>(smem);                 // [NW][8][D]
-  float* mstat = mo + NW * 8 * D;                              // [NW][8][4]
-  if (warp > 0) {
-    const int cw = warp - 1;
+  // ------------------------------------------------------------ merge the pairs
+  __syncthreads();  // every issued copy was waited for by its pair: the ring is free
+  constexpr int RS = D + 4;                                     // padded row: no bank conflicts
+  float* mo = reinterpret_cast<float*>(smem);                   // [NP][8][RS]
+  float* mstat = mo + NP * 8 * RS;                              // [NP][8][4]
+  float* mw = mstat + NP * 8 * 4;                               // [8][NP] weights of the pairs' O
+  float* mfin = mw + 8 * NP;                                    // [8][4]: Ms, Mz, l, final factor
 #pragma unroll
-    for (int mt = 0; mt < NMT; ++mt) {
-      const int d0 = mt * 16 + g;
+  for (int mt = 0; mt < NMT_H; ++mt) {
+    const int d0 = hf * (D / 2) + mt * 16 + g;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        mo[(cw * 8 + 2 * c + i) * D + d0] = o_acc[mt][i];
-        mo[(cw * 8 + 2 * c + i) * D + d0 + 8] = o_acc[mt][2 + i];
-      }
+    for (int i = 0; i < 2; ++i) {
+      mo[(p * 8 + 2 * c + i) * RS + d0] = o_acc[mt][i];
+      mo[(p * 8 + 2 * c + i) * RS + d0 + 8] = o_acc[mt][2 + i];
     }
-    if (g == 0) {
+  }
+  if (hf == 0 && g == 0) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        float* st = mstat + (cw * 8 + 2 * c + i) * 4;
-        st[0] = ms[i];
-        st[1] = mz[i];
-        st[2] = lsum[i];
-      }
+    for (int i = 0; i < 2; ++i) {
+      float* stt = mstat + (p * 8 + 2 * c + i) * 4;
+      stt[0] = ms[i];
+      stt[1] = mz[i];
+      stt[2] = lsum[i];
     }
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    // per head: the pairs' maxima, the merged l and one weight per pair (exp once per pair)
+    const int hh = threadIdx.x;
+    float Ms = -INFINITY, Mz = -INFINITY;
+    for (int q2 = 0; q2 < NP; ++q2) {
+      Ms = fmaxf(Ms, mstat[(q2 * 8 + hh) * 4 + 0]);
+      Mz = fmaxf(Mz, mstat[(q2 * 8 + hh) * 4 + 1]);
+    }
+    float lsum_all = 0.f;
+    for (int q2 = 0; q2 < NP; ++q2) {
+      const float* stt = mstat + (q2 * 8 + hh) * 4;
+      if (Ms != -INFINITY && stt[0] != -INFINITY) lsum_all += stt[2] * fast_exp2(stt[0] - Ms);
+      mw[hh * NP + q2] = (Mz != -INFINITY && stt[1] != -INFINITY) ? fast_exp2(stt[1] - Mz) : 0.f;
+    }
+    mfin[hh * 4 + 0] = Ms;
+    mfin[hh * 4 + 1] = Mz;
+    mfin[hh * 4 + 2] = lsum_all;
+    mfin[hh * 4 + 3] = (lsum_all > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / lsum_all : 0.f;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int hh = idx / D, d = idx % D;
-    float Ms = -INFINITY, Mz = -INFINITY;
+    float o = 0.f;
 #pragma unroll
-    for (int w2 = 0; w2 < NW; ++w2) {
-      Ms = fmaxf(Ms, mstat[(w2 * 8 + hh) * 4 + 0]);
-      Mz = fmaxf(Mz, mstat[(w2 * 8 + hh) * 4 + 1]);
-    }
-    float lsum_all = 0.f, o = 0.f;
-    if (Ms != -INFINITY) {
-#pragma unroll
-      for (int w2 = 0; w2 < NW; ++w2) {
-        const float* st = mstat + (w2 * 8 + hh) * 4;
-        if (st[0] != -INFINITY) lsum_all += st[2] * fast_exp2(st[0] - Ms);
-        if (Mz != -INFINITY && st[1] != -INFINITY) o += mo[(w2 * 8 + hh) * D + d] * fast_exp2(st[1] - Mz);
-      }
-    }
+    for (int q2 = 0; q2 < NP; ++q2) o = fmaf(mo[(q2 * 8 + hh) * RS + d], mw[hh * NP + q2], o);
     const int h = kvh * G + hh;
     if (SPLIT) {
       const long long pu = (static_cast<long long>(b) * Hq + h) * a.n_split + blockIdx.x;
       a.part_acc[pu * D + d] = o;
       if (d == 0) {
-        a.part_stats[pu * 4 + 0] = Ms;
-        a.part_stats[pu * 4 + 1] = Mz;
-        a.part_stats[pu * 4 + 2] = lsum_all;
+        a.part_stats[pu * 4 + 0] = mfin[hh * 4 + 0];
+        a.part_stats[pu * 4 + 1] = mfin[hh * 4 + 1];
+        a.part_stats[pu * 4 + 2] = mfin[hh * 4 + 2];
         a.part_stats[pu * 4 + 3] = 0.f;
       }
     } else {
-      float res = 0.f;
-      if (lsum_all > 0.f && Mz != -INFINITY) res = o * fast_exp2(Mz - Ms) / lsum_all;
-      a.out[(static_cast<long long>(b) * Hq + h) * D + d] = res;
+      a.out[(static_cast<long long>(b) * Hq + h) * D + d] = o * mfin[hh * 4 + 3];
     }
   }
 }
@@ -436,28 +476,31 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_di
   return static_cast<size_t>(((acc + 255) / 256) * 256 + stats);
 }
 
-template <int D, int NW, int STAGES, bool SPLIT>
+template <int D, int NP, int DEPTH, bool SPLIT>
 static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
-  using L = DecodeSmem<D, NW, STAGES>;
-  auto kern = decode_stage1_kernel<D, NW, STAGES, SPLIT>;
+  using L = DecodeSmem<D, NP, DEPTH>;
+  auto kern = decode_stage1_kernel<D, NP, DEPTH, SPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
-  kern<<<grid, (NW + 1) * 32, L::kTotal, stream>>>(a);
-  return cudaGetLastError();
+  if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, stream)) != cudaSuccess) return e;
+  kern<<<grid, NP * 64, L::kTotal, stream>>>(a);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (a.ev_end && (e = cudaEventRecord(a.ev_end, stream)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream) {
   if (route == DecodeRoute::kSingle) {
     dim3 grid(1, a.n_kv_heads, a.batch);
-    if (a.head_dim == 256) return launch_stage1<256, 8, 24, false>(a, grid, stream);
-    return launch_stage1<128, 8, 32, false>(a, grid, stream);
+    if (a.head_dim == 256) return launch_stage1<256, 8, 3, false>(a, grid, stream);
+    return launch_stage1<128, 8, 4, false>(a, grid, stream);
   }
   dim3 grid(a.n_split, a.n_kv_heads, a.batch);
   cudaError_t e;
   if (a.head_dim == 256)
-    e = launch_stage1<256, 4, 12, true>(a, grid, stream);
+    e = launch_stage1<256, 4, 3, true>(a, grid, stream);
   else
-    e = launch_stage1<128, 4, 16, true>(a, grid, stream);
+    e = launch_stage1<128, 4, 4, true>(a, grid, stream);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.n_split) * sizeof(float);
   dim3 g2(a.n_q_heads, a.batch);

@@ -49,6 +49,8 @@ struct DecodeArgs {
   int split_rows;      // keys per split (split route); ignored by the single route
   int n_split;         // splits per sequence in the grid (split route)
   unsigned int* status;
+  cudaEvent_t ev_begin;  // optional events around the stage-1 launch
+  cudaEvent_t ev_end;
 };
 enum class DecodeRoute { kSingle = 1, kSplit = 2 };
 size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_dim, int split_rows);

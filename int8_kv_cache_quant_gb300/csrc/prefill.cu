@@ -1,13 +1,35 @@
-// prefill.cu — chunked causal prefill over the int8 paged K/V cache (placeholder: the Q
-// quantisation step only; the tensor-core attention kernel follows).
+// prefill.cu — chunked causal prefill over the int8 paged K/V cache on the 5th-generation
+// tensor cores.
+//
+// Method: "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §3.2 (a non-first prefill
+// chunk: INT8 Q, history and chunk K/V in one online softmax), §1.3 and the §3.3 fragment
+// code (Score = MMA_int8(Q, K^T) * sQ * sK / sqrt(d); each token's sV folded into the softmax
+// weight; the weights re-quantised per block with scale absmax / 127; Output += MMA_int8(P,
+// V) * p_scale), §2.1 (Q quantised per (token, head) by the same absmax rule).
+//
+// GB300 design.
+// * sm_103a has no tcgen05 kind::i8, so the int8 codes are widened to integer-valued fp16 in
+//   shared memory and the contractions use tcgen05.mma kind::f16 with fp32 accumulators in
+//   tensor memory.  This is exact: every QK partial sum is an integer of magnitude at most
+//   256 * 127 * 127 < 2^24, every per-tile PV sum at most 128 * 127 * 127 < 2^24.
+// * One CTA per (128 query rows, query head).  Q (128 x D), the K tile (128 keys x D), the V
+//   tile (D x 128 keys) and the P tile (128 x 128) live in shared memory in the K-major
+//   128-byte-swizzle layout; S (128 x 128) and O (128 x D) live in tensor memory.
+// * Thread r of the CTA owns query row r (tensor-memory lane r): it reads its S row, runs the
+//   online softmax and the per-tile P re-quantisation, writes its P codes, and rescales its O
+//   row when the P scale changes (O holds sum_tiles (ps_tile / ps_ref) * PV_tile).
+// * Every P-code decision is the page's fp32 sequence with a specified exp2 (exp2_det) and the
+//   running maximum after each 128-key tile, so the codes are reproducible off the GPU.
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
+#include "tcgen05.cuh"
 
 namespace kvq {
 
-// Q quantisation per (token, query head): the kvq_quant_write rule applied to Q
-// ("gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §2.1, §2.2: the query is quantised
-// once and reused).  One warp per row; IEEE fp32 divisions, round to nearest even.
+// ============================================================================ Q quantisation
+// Per (token, query head): the kvq_quant_write rule applied to Q ("gfx936 ..." §2.1, §2.2:
+// the query is quantised once and reused).  One warp per row; IEEE fp32 divisions, round to
+// nearest even.
 template <int D>
 __global__ void __launch_bounds__(256) q_quant_kernel(PrefillArgs a) {
   constexpr int kPerLane = D / 32;
@@ -60,6 +82,439 @@ __global__ void __launch_bounds__(256) q_quant_kernel(PrefillArgs a) {
   if (lane == 0 && a.q_scales) a.q_scales[row] = scale;
 }
 
+namespace {
+
+// ============================================================================ layout
+template <int D>
+struct PrefillSmem {
+  static constexpr int kQ = 128 * D * 2;   // Q tile: 128 rows x D, fp16
+  static constexpr int kK = 128 * D * 2;   // K tile: 128 keys x D
+  static constexpr int kV = D * 128 * 2;   // V tile: D rows x 128 keys
+  static constexpr int kP = 128 * 128 * 2; // P tile: 128 rows x 128 keys
+  static constexpr int offQ = 0;
+  static constexpr int offK = offQ + kQ;
+  static constexpr int offV = offK + kK;
+  static constexpr int offP = offV + kV;
+  static constexpr int offSK = offP + kP;      // float[128] key scales of the tile
+  static constexpr int offSV = offSK + 512;    // float[128] value scales
+  static constexpr int offPage = offSV + 512;  // int[8] pages of the tile (-1 = none)
+  static constexpr int offBar = offPage + 64;  // mbarriers: QK done, PV done
+  static constexpr int offTmem = offBar + 16;  // TMEM base address
+  static constexpr int kBytes = offTmem + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
+  static constexpr uint32_t kTmemCols = (D == 256) ? 512 : 256;
+  static constexpr uint32_t kOCol = (D == 256) ? 256 : 128;  // O after S (128 columns)
+};
+
+constexpr float kLog2eP = 1.44269504088896341f;
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+
+// The specified exp2 of the P-code decisions (the same function, step for step, as the CPU
+// reference): Cody-Waite reduction x = n + f with n = rint(x), 2^f by the degree-5 Taylor
+// polynomial of e^{f ln 2} (Horner, fp32 fma), times 2^n; x < -125 gives 0.
+__device__ __forceinline__ float exp2_det(float x) {
+  if (!(x >= -125.0f)) return 0.0f;
+  x = fminf(x, 125.0f);
+  const float t = __fadd_rn(x, kMagic);
+  const float n = __fsub_rn(t, kMagic);
+  const float f = __fsub_rn(x, n);
+  float p = __fmaf_rn(0.00133335581464284f, f, 0.00961812910762848f);
+  p = __fmaf_rn(p, f, 0.0555041086648216f);
+  p = __fmaf_rn(p, f, 0.240226506959101f);
+  p = __fmaf_rn(p, f, 0.693147180559945f);
+  p = __fmaf_rn(p, f, 1.0f);
+  const int ni = __float2int_rz(n);
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+// 16 int8 codes (one int4) -> two 16-byte chunks of 8 fp16 (exact integer values).
+__device__ __forceinline__ void widen16(const int4 raw, uint4& c0, uint4& c1) {
+  uint32_t lo, hi;
+  i8x4_to_h2x2(static_cast<uint32_t>(raw.x), kSelB01, kSelB23, lo, hi);
+  c0.x = lo;
+  c0.y = hi;
+  i8x4_to_h2x2(static_cast<uint32_t>(raw.y), kSelB01, kSelB23, lo, hi);
+  c0.z = lo;
+  c0.w = hi;
+  i8x4_to_h2x2(static_cast<uint32_t>(raw.z), kSelB01, kSelB23, lo, hi);
+  c1.x = lo;
+  c1.y = hi;
+  i8x4_to_h2x2(static_cast<uint32_t>(raw.w), kSelB01, kSelB23, lo, hi);
+  c1.z = lo;
+  c1.w = hi;
+}
+
+__device__ __forceinline__ void sts128(uint8_t* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// Q tile: rows q0 .. q0+127 of query head h; row r -> tile row r.  K-block stride 128 * 128 B.
+template <int D>
+__device__ void load_q_tile(uint8_t* qs, const int8_t* q_codes, int T, int Hq, int h, int q0, int tid) {
+  const int r = tid;
+  const bool ok = q0 + r < T;
+  const int8_t* src = q_codes + (static_cast<long long>(q0 + r) * Hq + h) * D;
+#pragma unroll 4
+  for (int c16 = 0; c16 < D / 16; ++c16) {
+    int4 raw = make_int4(0, 0, 0, 0);
+    if (ok) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
+    uint4 c0, c1;
+    widen16(raw, c0, c1);
+    uint8_t* blk = qs + (c16 >> 2) * (128 * 128);
+    const int cc = (c16 & 3) * 2;
+    sts128(blk + tc::sw128_off(r, cc), c0);
+    sts128(blk + tc::sw128_off(r, cc + 1), c1);
+  }
+}
+
+// K tile j (keys 128j .. 128j+127) of KV head kvh; key n -> tile row n.  Also the tile's key
+// and value scales and its 8 page numbers.  Keys at or past `n_keys` (and keys on a bad page)
+// are zero.
+template <int D>
+__device__ void load_k_tile(uint8_t* ks, float* sk_s, float* sv_s, int* page_s, const PrefillArgs& a, int kvh,
+                            int j, int n_keys, int tid) {
+  const int n = tid;
+  const int t = 128 * j + n;
+  int page = -1;
+  if (t < n_keys) {
+    const int bi = t / KVQ_BLOCK_SIZE;
+    if (bi < a.n_blocks_row) page = a.block_table_row[bi];
+    if (page < 0 || page >= a.num_blocks) {
+      if ((t & 15) == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
+      page = -1;
+    }
+  }
+  if ((n & 15) == 0) page_s[n >> 4] = page;
+  const long long ph = static_cast<long long>(page < 0 ? 0 : page) * a.n_kv_heads + kvh;
+  const int slot = t & 15;
+  sk_s[n] = page >= 0 ? a.k_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+  sv_s[n] = page >= 0 ? a.v_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+  const int8_t* src = a.k + ph * D * KVQ_BLOCK_SIZE + slot * 16;
+#pragma unroll 4
+  for (int c16 = 0; c16 < D / 16; ++c16) {
+    int4 raw = make_int4(0, 0, 0, 0);
+    if (page >= 0) raw = __ldg(reinterpret_cast<const int4*>(src + c16 * 256));
+    uint4 c0, c1;
+    widen16(raw, c0, c1);
+    uint8_t* blk = ks + (c16 >> 2) * (128 * 128);
+    const int cc = (c16 & 3) * 2;
+    sts128(blk + tc::sw128_off(n, cc), c0);
+    sts128(blk + tc::sw128_off(n, cc + 1), c1);
+  }
+}
+
+// V tile j: tile row d (head dimension) holds keys 128j .. 128j+127 along K.  Page pl of the
+// tile supplies keys 16 pl .. 16 pl + 15, i.e. 16-byte chunks 2 (pl % 4), 2 (pl % 4) + 1 of
+// K-block pl / 4.  Pages past the context are zero.
+template <int D>
+__device__ void load_v_tile(uint8_t* vs, const int* page_s, const PrefillArgs& a, int kvh, int tid) {
+#pragma unroll
+  for (int rr = 0; rr < D / 128; ++rr) {
+    const int d = tid + 128 * rr;
+#pragma unroll 2
+    for (int pl = 0; pl < 8; ++pl) {
+      const int page = page_s[pl];
+      int4 raw = make_int4(0, 0, 0, 0);
+      if (page >= 0) {
+        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        raw = __ldg(reinterpret_cast<const int4*>(a.v + (ph * D + d) * KVQ_BLOCK_SIZE));
+      }
+      uint4 c0, c1;
+      widen16(raw, c0, c1);
+      uint8_t* blk = vs + (pl >> 2) * (D * 128);
+      const int cc = (pl & 3) * 2;
+      sts128(blk + tc::sw128_off(d, cc), c0);
+      sts128(blk + tc::sw128_off(d, cc + 1), c1);
+    }
+  }
+}
+
+// S = Q K^T over the head dimension (M = 128 rows, N = 128 keys, K = D), one thread.
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t qs, uint32_t ks, uint32_t tmem_s) {
+  constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
+#pragma unroll
+  for (int k = 0; k < D / 16; ++k) {
+    const uint32_t off = (k >> 2) * (128 * 128) + (k & 3) * 32;
+    tc::mma_f16_ss(tmem_s, tc::sdesc_sw128(qs + off), tc::sdesc_sw128(ks + off), idesc, k > 0 ? 1u : 0u);
+  }
+}
+
+// O += P V (M = 128 rows, N = D, K = 128 keys), one thread.
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t ps, uint32_t vs, uint32_t tmem_o) {
+  constexpr uint32_t idesc = tc::idesc_f16_f32(128, D);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t aoff = (k >> 2) * (128 * 128) + (k & 3) * 32;
+    const uint32_t boff = (k >> 2) * (D * 128) + (k & 3) * 32;
+    tc::mma_f16_ss(tmem_o, tc::sdesc_sw128(ps + aoff), tc::sdesc_sw128(vs + boff), idesc, 1u);
+  }
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t s = smem_u32(p);
+  return p + (((s + 1023u) & ~1023u) - s);
+}
+
+}  // namespace
+
+// ============================================================================ prefill kernel
+template <int D>
+__global__ void __launch_bounds__(128, 1) prefill_kernel(PrefillArgs a) {
+  using L = PrefillSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* qs = sm + L::offQ;
+  uint8_t* ks = sm + L::offK;
+  uint8_t* vs = sm + L::offV;
+  uint8_t* ps = sm + L::offP;
+  float* sk_s = reinterpret_cast<float*>(sm + L::offSK);
+  float* sv_s = reinterpret_cast<float*>(sm + L::offSV);
+  int* page_s = reinterpret_cast<int*>(sm + L::offPage);
+  uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + L::offBar);
+  uint64_t* bar_pv = bar_qk + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offTmem);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int h = blockIdx.y;
+  const int q0 = blockIdx.x * 128;
+  const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, kvh = h / G;
+  const int T = a.n_tokens;
+  const int n_keys = a.history_len + T;  // keys in the cache for this chunk
+
+  if (warp == 0) tc::tmem_alloc(tmem_slot, L::kTmemCols);
+  if (tid == 0) {
+    mbar_init(bar_qk, 1);
+    mbar_init(bar_pv, 1);
+    mbar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tm_s = tmem + lane_base;              // this warp's lanes, S columns
+  const uint32_t tm_o = tmem + lane_base + L::kOCol;   // this warp's lanes, O columns
+
+  load_q_tile<D>(qs, a.q_codes, T, Hq, h, q0, tid);
+  {
+    uint32_t z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) tc::st_32x32b_x32(tm_o + 32 * c, z);
+    tc::wait_st();
+  }
+
+  // per-row state (thread tid = query row tid)
+  const int row = tid;
+  const bool row_real = q0 + row < T;
+  const int pos_r = a.history_len + q0 + row;  // the row's absolute position
+  const float c2 = __fmul_rn(a.softmax_scale, kLog2eP);
+  const float a_row = row_real ? __fmul_rn(a.q_scales[static_cast<long long>(q0 + row) * Hq + h], c2) : 0.0f;
+  float m = -INFINITY, l = 0.0f, ps_ref = 0.0f;
+  bool started = false;
+  bool timed_out = false;
+
+  const int last_pos = a.history_len + min(q0 + 127, T - 1);
+  const int n_tiles = last_pos / 128 + 1;
+  const uint32_t qs_a = smem_u32(qs), ks_a = smem_u32(ks), vs_a = smem_u32(vs), ps_a = smem_u32(ps);
+
+  for (int j = 0; j < n_tiles; ++j) {
+    load_k_tile<D>(ks, sk_s, sv_s, page_s, a, kvh, j, n_keys, tid);
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    // a bounded wait that ran out anywhere in the CTA ends the walk for every thread
+    if (__syncthreads_or(timed_out ? 1 : 0)) break;
+    if (tid == 0) {
+      tc::fence_after_sync();
+      issue_qk<D>(qs_a, ks_a, tmem);
+      tc::commit(bar_qk);
+    }
+    load_v_tile<D>(vs, page_s, a, kvh, tid);
+    tc::fence_proxy_async_smem();
+    if (!mbar_wait(bar_qk, j & 1, a.status)) timed_out = true;
+    tc::fence_after_sync();
+
+    // ---- S row -> online softmax -> P codes (thread = row)
+    uint32_t sraw[128];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tc::ld_32x32b_x32(tm_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sraw[32 * c]));
+    tc::wait_ld();
+    const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128);  // visible keys of this tile
+    float ymax = -INFINITY;
+#pragma unroll
+    for (int n = 0; n < 128; ++n) {
+      const float y = (n < lim) ? __fmul_rn(__uint_as_float(sraw[n]), sk_s[n]) : -INFINITY;
+      sraw[n] = __float_as_uint(y);
+      ymax = fmaxf(ymax, y);
+    }
+    const float m_new = fmaxf(m, __fmul_rn(ymax, a_row));
+    const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+    float psum = 0.0f, wmax = 0.0f;
+#pragma unroll
+    for (int n = 0; n < 128; ++n) {
+      const float p = exp2_det(__fmaf_rn(__uint_as_float(sraw[n]), a_row, -m_new));
+      psum += p;
+      const float w = __fmul_rn(p, sv_s[n]);
+      sraw[n] = __float_as_uint(w);
+      wmax = fmaxf(wmax, w);
+    }
+    l = l * alpha + psum;
+    m = m_new;
+    // reference scale of O and the factor that moves O onto this tile's P scale
+    float f = 1.0f;
+    bool codes_on = wmax > 0.0f;
+    const float ps_new = __fdiv_rn(wmax, 127.0f);
+    if (!started) {
+      // O is still zero: nothing to rescale
+      if (codes_on) {
+        started = true;
+        ps_ref = ps_new;
+      }
+    } else if (codes_on) {
+      const float fr = ps_ref * alpha / ps_new;
+      if (fr > 1.8446744e19f) {  // 2^64: the tile is negligible against what O holds; drop it
+        codes_on = false;
+        ps_ref *= alpha;
+      } else {
+        f = fr;
+        ps_ref = ps_new;
+      }
+    } else {
+      ps_ref *= alpha;
+    }
+    const float r = codes_on ? __fdiv_rn(127.0f, wmax) : 0.0f;
+#pragma unroll
+    for (int cc = 0; cc < 16; ++cc) {
+      uint32_t hv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float c0 = 0.0f, c1 = 0.0f;
+        if (codes_on) {
+          c0 = __fsub_rn(__fmaf_rn(__uint_as_float(sraw[8 * cc + 2 * e]), r, kMagic), kMagic);
+          c1 = __fsub_rn(__fmaf_rn(__uint_as_float(sraw[8 * cc + 2 * e + 1]), r, kMagic), kMagic);
+          c0 = fminf(fmaxf(c0, 0.0f), 127.0f);
+          c1 = fminf(fmaxf(c1, 0.0f), 127.0f);
+        }
+        hv[e] = pack_half2(c0, c1);
+      }
+      sts128(ps + (cc >> 3) * (128 * 128) + tc::sw128_off(row, cc & 7), make_uint4(hv[0], hv[1], hv[2], hv[3]));
+    }
+    // tcgen05.ld / st are warp-collective: the whole warp takes this branch if any row needs it
+    if (__any_sync(0xffffffffu, f != 1.0f)) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tc::ld_32x32b_x32(tm_o + 32 * c, o);
+        tc::wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+        tc::st_32x32b_x32(tm_o + 32 * c, o);
+      }
+      tc::wait_st();
+    }
+    tc::fence_proxy_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+      issue_pv<D>(ps_a, vs_a, tmem + L::kOCol);
+      tc::commit(bar_pv);
+    }
+    if (!mbar_wait(bar_pv, j & 1, a.status)) timed_out = true;
+    tc::fence_after_sync();
+  }
+
+  // ---- epilogue: out = O * ps_ref / l
+  const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t o[32];
+    tc::ld_32x32b_x32(tm_o + 32 * c, o);
+    tc::wait_ld();
+    if (row_real) {
+      float* dst = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + 32 * c;
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(dst + e) =
+            make_float4(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
+                        __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
+// ============================================================================ debug QK tile
+// The prefill kernel's QK path alone: S for query rows q0 .. q0+127 of dbg_q_head against the
+// 128 keys of tile (dbg_k0 / 128 + blockIdx.x), written as exact int32.
+template <int D>
+__global__ void __launch_bounds__(128, 1) prefill_qk_debug_kernel(PrefillArgs a) {
+  using L = PrefillSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* qs = sm + L::offQ;
+  uint8_t* ks = sm + L::offK;
+  float* sk_s = reinterpret_cast<float*>(sm + L::offSK);
+  float* sv_s = reinterpret_cast<float*>(sm + L::offSV);
+  int* page_s = reinterpret_cast<int*>(sm + L::offPage);
+  uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + L::offBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offTmem);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, h = a.dbg_q_head, kvh = h / G;
+  const int j = a.dbg_k0 / 128 + blockIdx.x;
+
+  if (warp == 0) tc::tmem_alloc(tmem_slot, 128);
+  if (tid == 0) {
+    mbar_init(bar_qk, 1);
+    mbar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  load_q_tile<D>(qs, a.q_codes, a.n_tokens, Hq, h, a.dbg_q0, tid);
+  load_k_tile<D>(ks, sk_s, sv_s, page_s, a, kvh, j, a.n_blocks_row * KVQ_BLOCK_SIZE, tid);
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    tc::fence_after_sync();
+    issue_qk<D>(smem_u32(qs), smem_u32(ks), tmem);
+    tc::commit(bar_qk);
+  }
+  const bool ok = mbar_wait(bar_qk, 0, a.status);
+  tc::fence_after_sync();
+  const bool row_real = a.dbg_q0 + tid < a.n_tokens;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t s[32];
+    tc::ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * c, s);
+    tc::wait_ld();
+    int32_t* dst = a.dbg_s_out + static_cast<long long>(tid) * a.dbg_nk + 128 * blockIdx.x + 32 * c;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      int4 v = make_int4(0, 0, 0, 0);
+      if (row_real && ok)
+        v = make_int4(__float2int_rn(__uint_as_float(s[e])), __float2int_rn(__uint_as_float(s[e + 1])),
+                      __float2int_rn(__uint_as_float(s[e + 2])), __float2int_rn(__uint_as_float(s[e + 3])));
+      *reinterpret_cast<int4*>(dst + e) = v;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 128);
+  }
+}
+
+// ============================================================================ launchers
 size_t prefill_workspace_bytes(int n_tokens, int n_q_heads, int head_dim) {
   const long long codes = static_cast<long long>(n_tokens) * n_q_heads * head_dim;
   const long long scales = static_cast<long long>(n_tokens) * n_q_heads * 4;
@@ -76,7 +531,32 @@ cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
-cudaError_t launch_prefill_qk_debug(const PrefillArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+template <int D>
+static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
+  using L = PrefillSmem<D>;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.n_tokens + 127) / 128, a.n_q_heads);
+  prefill_kernel<D><<<grid, 128, L::kAlloc, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  return a.head_dim == 256 ? launch_prefill_d<256>(a, stream) : launch_prefill_d<128>(a, stream);
+}
+
+template <int D>
+static cudaError_t launch_qk_debug_d(const PrefillArgs& a, cudaStream_t stream) {
+  using L = PrefillSmem<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_qk_debug_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  prefill_qk_debug_kernel<D><<<a.dbg_nk / 128, 128, L::kAlloc, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_qk_debug(const PrefillArgs& a, cudaStream_t stream) {
+  return a.head_dim == 256 ? launch_qk_debug_d<256>(a, stream) : launch_qk_debug_d<128>(a, stream);
+}
 
 }  // namespace kvq

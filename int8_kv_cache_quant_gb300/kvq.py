@@ -38,7 +38,8 @@ class _Cache(ctypes.Structure):
 
 class _DecodeOpts(ctypes.Structure):
     _fields_ = [("split_rows", ctypes.c_int32), ("route_threshold", ctypes.c_int32),
-                ("force_route", ctypes.c_int32)]
+                ("force_route", ctypes.c_int32), ("stage1_event_begin", ctypes.c_void_p),
+                ("stage1_event_end", ctypes.c_void_p)]
 
 
 _lib = None
@@ -127,8 +128,11 @@ def kvq_quant_write(cache, k_new, v_new, seq_idx, pos, block_table, stream=None)
         int(bt.shape[0]), int(bt.shape[1]), _stream(stream)))
 
 
-def _decode_opts(split_rows, route_threshold, force_route):
-    return _DecodeOpts(int(split_rows), int(route_threshold), int(force_route))
+def _decode_opts(split_rows, route_threshold, force_route, events=None):
+    ev0 = ev1 = None
+    if events is not None:
+        ev0, ev1 = (ctypes.c_void_p(e.cuda_event) for e in events)
+    return _DecodeOpts(int(split_rows), int(route_threshold), int(force_route), ev0, ev1)
 
 
 def kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, split_rows=0,
@@ -139,13 +143,14 @@ def kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, split_rows=0
 
 def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_scale, out=None,
                            workspace=None, split_rows=0, route_threshold=0, force_route=0,
-                           stream=None):
+                           stream=None, stage1_events=None):
     """q: bf16 [B][Hq][D]; block_table int32 [B][M]; ctx_lens int32 [B] (device);
-    max_ctx: host bound of ctx_lens.  Returns out fp32 [B][Hq][D]."""
+    max_ctx: host bound of ctx_lens.  Returns out fp32 [B][Hq][D].  stage1_events: optional
+    pair of torch.cuda.Event recorded around the stage-1 kernel (profiling)."""
     B, Hq, D = q.shape
     if out is None:
         out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
-    o = _decode_opts(split_rows, route_threshold, force_route)
+    o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
     need = int(lib().kvq_decode_workspace_bytes(B, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
