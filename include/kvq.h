@@ -147,6 +147,32 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
                            void* workspace, size_t workspace_bytes,
                            const kvq_decode_opts* opts, void* stream);
 
+/*
+ * kvq_attn_decode_int8kv_noalloc — kvq_attn_decode_int8kv for callers that cannot allocate
+ * device memory.  The source pages have no counterpart of this call; it exists for callers
+ * that may not call cudaMalloc where they run decode (a region whose memory plan is fixed in
+ * advance, a plugin host that only hands out the tensors it owns, a runtime that reserved all
+ * device memory at start-up) and so cannot provide the split route's workspace.
+ *   Same arguments and results as kvq_attn_decode_int8kv, without workspace / workspace_bytes:
+ *   the split-K partials live in a fixed scratch array of KVQ_NOALLOC_SCRATCH_BYTES bytes
+ *   inside the library, which every GPU that loads the library holds until the process exits.
+ *   The call allocates nothing.  A problem whose split route needs more than
+ *   KVQ_NOALLOC_SCRATCH_BYTES (see kvq_decode_workspace_bytes) is rejected with
+ *   KVQ_ERR_WORKSPACE before any launch.
+ *   The first call on a device looks up the scratch array's device address for that device
+ *   (a one-time host-side set-up); make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (different streams, or
+ *   different host threads on one device) race and corrupt each other's results.  The
+ *   array keeps the last call's contents; every call writes the partials it reads, so
+ *   nothing in it has to start at zero.
+ */
+#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+int kvq_attn_decode_int8kv_noalloc(const kvq_cache* cache, const void* q, int32_t batch,
+                                   int32_t n_q_heads, const int32_t* block_table,
+                                   int32_t max_blocks_per_seq, const int32_t* ctx_lens,
+                                   int32_t max_ctx, float softmax_scale, float* out,
+                                   const kvq_decode_opts* opts, void* stream);
+
 /* Workspace (bytes) of kvq_attn_prefill_int8: the int8 Q codes and their fp32 scales. */
 size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t head_dim);
 

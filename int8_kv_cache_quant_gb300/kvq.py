@@ -64,6 +64,8 @@ def lib():
         L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
         L.kvq_attn_decode_int8kv.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
                                              ctypes.POINTER(_DecodeOpts), vp]
+        L.kvq_attn_decode_int8kv_noalloc.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp,
+                                                     ctypes.POINTER(_DecodeOpts), vp]
         L.kvq_prefill_workspace_bytes.restype = sz
         L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32]
         L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
@@ -160,6 +162,23 @@ def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
         ctypes.byref(c), _p(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
         int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def kvq_attn_decode_int8kv_noalloc(cache, q, block_table, ctx_lens, max_ctx, softmax_scale, out,
+                                   split_rows=0, route_threshold=0, force_route=0, stream=None):
+    """kvq_attn_decode_int8kv without a workspace argument, for callers that cannot allocate:
+    the split-K partials live in a fixed scratch array inside the library.  `out` (fp32
+    [B][Hq][D]) must be provided by the caller; nothing is allocated here."""
+    B, Hq, D = q.shape
+    o = _decode_opts(split_rows, route_threshold, force_route)
+    c = cache.struct()
+    _check("kvq_attn_decode_int8kv_noalloc", lib().kvq_attn_decode_int8kv_noalloc(
+        ctypes.byref(c), _p(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), float(softmax_scale), _p(out), ctypes.byref(o), _stream(stream)))
     return out
 
 
