@@ -38,41 +38,62 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
+    """nvidia-smi clock / throttle sampling (every 50 ms) in a background thread; summary()
+    reports the samples taken between mark_begin() and mark_end() widened by `pad_s` on each
+    side (a timed region of a few milliseconds is shorter than one sampling interval)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, gpu_index, pad_s=0.25):
+        self.gpu, self.pad = gpu_index, pad_s
+        self.proc, self.samples, self.t0, self.t1 = None, [], None, None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            if line.strip():
+                self.samples.append((time.perf_counter(), line))
 
     def __enter__(self):
+        import threading
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._reader, daemon=True)
+            self.thread.start()
+            deadline = time.perf_counter() + 3.0
+            while not self.samples and time.perf_counter() < deadline:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
+    def mark_begin(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+        time.sleep(self.pad)
+
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             self.proc.terminate()
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        lo = (self.t0 or 0) - self.pad
+        hi = (self.t1 or time.perf_counter()) + self.pad
+        for t, l in self.samples:
+            if not (lo <= t <= hi):
+                continue
             parts = [p.strip() for p in l.split(",")]
             try:
                 sm.append(float(parts[0]))
@@ -85,7 +106,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "timed region +- %.2f s" % self.pad}
 
 
 def dist_setup():
@@ -152,7 +173,14 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                      dtype=torch.uint8, device=dev)
     out = torch.empty((1, Hq, D), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sweep = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream()
+
+    def cold_l2(i):
+        # write 256 MB (> the 129 MB L2), then read another 256 MB so that the L2 holds clean
+        # lines of an unrelated buffer: the timed step then starts cold and pays no write-back
+        flush.fill_(i & 0xFF)
+        sweep.sum()
 
     def step(ev=None):
         kvq.kvq_quant_write(cache, k_new, v_new, new_seq, new_pos, bt)
@@ -160,7 +188,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                                    workspace=ws, split_rows=split, stage1_events=ev)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        cold_l2(1)
         step()
     torch.cuda.synchronize()
     assert kvq.kvq_device_status() == 0
@@ -175,14 +203,20 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        for _ in range(3):  # keep the GPU busy while the sampler starts (untimed)
+            cold_l2(0)
+            step()
+        torch.cuda.synchronize()
+        clk.mark_begin()
         t_wall = time.perf_counter()
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            cold_l2(i)
             ev0[i].record(s)
             step((k0[i], k1[i]))
             ev1[i].record(s)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+        clk.mark_end()
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
@@ -216,13 +250,13 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
-        flush.fill_(2)
+        cold_l2(2)
         e2e_step()
     torch.cuda.synchronize()
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        cold_l2(i)
         e0[i].record(s)
         e2e_step()
         e1[i].record(s)
@@ -252,11 +286,11 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                    "head_dim": D, "block_size": 16, "block_table": "random permutation",
                    "split_rows": split, "kv_bytes_per_step": kv_bytes,
                    "step": "kv_quant_write(1 token) + decode stage1 + merge",
-                   "l2": "flushed before every timed step (256 MB write outside the events)",
+                   "l2": "cold before every timed step: 256 MB write then 256 MB read of another buffer, outside the events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": None,
-                     "kernel": "decode_stage1_kernel<256,4,12,split>", "peak_kind": peak_kind,
+                     "kernel": "decode_stage1_kernel<256,NP=4,DEPTH=3,split>", "peak_kind": peak_kind,
                      "kernel_us": round(kern_avg * 1e3, 2)},
         "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -283,16 +317,21 @@ def bench_extra(args, local, hbm, tflops):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    sweep = torch.ones(64 << 20, dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream()
+
+    def cold_l2(i):
+        flush.fill_(i & 0xFF)
+        sweep.sum()
 
     def timed(fn, reps):
         for _ in range(3):
-            flush.fill_(1)
+            cold_l2(1)
             fn()
         torch.cuda.synchronize()
         ms = []
         for i in range(reps):
-            flush.fill_(i & 0xFF)
+            cold_l2(i)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(s)
             fn()
@@ -312,6 +351,30 @@ def bench_extra(args, local, hbm, tflops):
     ms = timed(lambda: kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out), 50)
     kvb = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
     res["decode_1k"] = {"us_per_call": round(ms * 1e3, 2), "kv_GBps": round(kvb / ms / 1e6, 1)}
+    del cache
+
+    # prefill_32k: the chunk's K/V written by kv_quant_write first (timed separately)
+    w = W.make("prefill_32k")
+    cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
+    bt = i32(w["block_table"])
+    kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
+    q = bf16(w["q"])
+    T, Hq, D = w["n_tokens"], w["hq"], w["d"]
+    out = torch.empty((T, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(kvq.kvq_prefill_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
+    row = bt[0]
+    ms = timed(lambda: kvq.kvq_attn_prefill_int8(cache, q, w["history"], row, w["softmax_scale"], out=out,
+                                                  workspace=ws), 10)
+    hist = w["history"]
+    triples = Hq * sum(hist + i + 1 for i in range(T))
+    ops = 2.0 * 2 * D * triples
+    chunk_seq = torch.zeros(T, dtype=torch.int32, device=dev)
+    chunk_pos = torch.arange(hist, hist + T, dtype=torch.int32, device=dev)
+    kc, vc = bf16(w["k_fill"][hist:]), bf16(w["v_fill"][hist:])
+    ms_qw = timed(lambda: kvq.kvq_quant_write(cache, kc, vc, chunk_seq, chunk_pos, bt), 10)
+    res["prefill_32k"] = {"ms_per_call": round(ms, 4), "int8_equiv_TOPS": round(ops / ms / 1e9, 1),
+                          "frac_of_bf16_peak": round(ops / ms / 1e9 / tflops, 4), "peak_TFLOPS": tflops,
+                          "chunk_kv_quant_write_ms": round(ms_qw, 4), "ops": ops}
     del cache
 
     # sparse_32k

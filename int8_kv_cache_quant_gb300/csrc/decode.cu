@@ -106,6 +106,7 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
 
+  grid_dep_wait();  // inputs may come from the previous kernel of the stream
   int ctx = a.ctx_lens[b];
   const int cap = a.max_blocks_per_seq * KVQ_BLOCK_SIZE;
   if (ctx > cap) {
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
   }
 
   // ------------------------------------------------------------ merge the pairs
+  grid_dep_trigger();  // the stage-2 merge may start launching
   __syncthreads();  // every issued copy was waited for by its pair: the ring is free
   constexpr int RS = D + 4;                                     // padded row: no bank conflicts
   float* mo = reinterpret_cast<float*>(smem);                   // [NP][8][RS]
@@ -412,6 +414,7 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(DecodeArgs a) {
   extern __shared__ float wts[];  // [n_split] weights for acc, then [n_split] for l
   __shared__ float red[2][32];
   const int h = blockIdx.x, b = blockIdx.y, Hq = a.n_q_heads;
+  grid_dep_wait();  // the partials come from stage 1
   int ctx = a.ctx_lens[b];
   ctx = max(0, min(ctx, a.max_blocks_per_seq * KVQ_BLOCK_SIZE));
   const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
@@ -483,8 +486,7 @@ static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, stream)) != cudaSuccess) return e;
-  kern<<<grid, NP * 64, L::kTotal, stream>>>(a);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(kern, grid, dim3(NP * 64), L::kTotal, stream, a)) != cudaSuccess) return e;
   if (a.ev_end && (e = cudaEventRecord(a.ev_end, stream)) != cudaSuccess) return e;
   return cudaSuccess;
 }
@@ -510,14 +512,16 @@ cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t s
                                static_cast<int>(wbytes));
       if (e != cudaSuccess) return e;
     }
-    decode_merge_kernel<256><<<g2, 256, wbytes, stream>>>(a);
+    e = launch_pdl(decode_merge_kernel<256>, g2, dim3(256), wbytes, stream, a);
+    if (e != cudaSuccess) return e;
   } else {
     if (wbytes > 48 * 1024) {
       e = cudaFuncSetAttribute(decode_merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(wbytes));
       if (e != cudaSuccess) return e;
     }
-    decode_merge_kernel<128><<<g2, 128, wbytes, stream>>>(a);
+    e = launch_pdl(decode_merge_kernel<128>, g2, dim3(128), wbytes, stream, a);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

@@ -449,6 +449,398 @@ __global__ void __launch_bounds__(128, 1) prefill_kernel(PrefillArgs a) {
   }
 }
 
+// ============================================================================ warp-specialised prefill
+// One CTA per (128 query rows, query head), 13 warps:
+//   warps 0-7   softmax: thread (row r, half h) owns keys 64h .. 64h+63 of row r's S row and O
+//               columns 128h .. 128h+127 (head_dim 256; 64h .. for 128); the two halves of a row
+//               exchange their partial maxima through shared memory at named barrier 1.
+//   warps 8-11  transform: Q once, then per tile the K and V tiles (int8 from the cache, widened to
+//               fp16, 128-byte-swizzled K-major in shared memory) and the tile's key/value scales.
+//   warp 12     MMA issue (lane 0) and tensor-memory allocation.
+// Tensor memory: S0 | S1 (128 columns each, double-buffered) | O (head_dim columns).  P (fp16,
+// 64 columns) is written back over the first 64 columns of its S buffer and read by the PV MMA
+// as its A operand; the next QK into that buffer is issued after that PV, and one thread's
+// tcgen05.mma operations execute in issue order.
+// Per tile j (buffer b = j % 2):  MMA: QK_j (after k_full) -> commit s_full[b], k_free; then
+// PV_{j-1} (after p_full, v_full) -> commit pv_done.  Transform: K_j after k_free(j-1), scales
+// after scales_free(j-2), V_j after pv_done(j-1).  Softmax: S_j after s_full[b]; P_j and the O
+// rescale after pv_done(j-1) -> arrive p_full.
+namespace {
+
+template <int D>
+struct PrefillWsSmem {
+  static constexpr int kQ = 128 * D * 2;
+  static constexpr int kK = 128 * D * 2;
+  static constexpr int kV = D * 128 * 2;
+  static constexpr int offQ = 0;
+  static constexpr int offK = offQ + kQ;
+  static constexpr int offV = offK + kK;
+  static constexpr int offScale = offV + kV;        // [2 buffers][2: k, v][128] float
+  static constexpr int offRed = offScale + 2 * 2 * 128 * 4;  // [2 exchanges][2 halves][128] float
+  static constexpr int offPage = offRed + 2 * 2 * 128 * 4;   // [2 buffers][8] int
+  static constexpr int offBar = offPage + 2 * 8 * 4;         // 10 mbarriers
+  static constexpr int offFlag = offBar + 10 * 8;             // abort flag, TMEM base
+  static constexpr int kBytes = offFlag + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O (head_dim columns)
+  static constexpr uint32_t kOCol = 256;      // after S0 | S1
+};
+
+// kBarScalesFree0/1: per scale buffer, so that no waiter can fall two phases behind.
+enum { kBarKFull = 0, kBarVFull, kBarS0, kBarS1, kBarKFree, kBarPvDone, kBarPFull, kBarScalesFree0,
+       kBarScalesFree1 };
+
+constexpr int kSoftmaxThreads = 256;
+constexpr int kTransformThreads = 128;
+constexpr int kPrefillThreads = kSoftmaxThreads + kTransformThreads + 32;
+
+// Bounded wait that also gives up as soon as another thread of the CTA has given up.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned int* status,
+                                              volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      set_status(status, KVQ_DEV_TIMEOUT);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void named_bar(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier that also returns the OR of `pred` over its `count` threads: every thread of
+// the group takes the same decision.
+__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, %2, %3, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+}  // namespace
+
+template <int D>
+__global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillArgs a) {
+  using L = PrefillWsSmem<D>;
+  constexpr int OCOLS_H = D / 2;  // O columns per softmax thread
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  uint8_t* qs = sm + L::offQ;
+  uint8_t* ks = sm + L::offK;
+  uint8_t* vs = sm + L::offV;
+  float* scale_s = reinterpret_cast<float*>(sm + L::offScale);  // [buf][0: k, 1: v][128]
+  float* red = reinterpret_cast<float*>(sm + L::offRed);        // [exchange][half][128]
+  int* page_s = reinterpret_cast<int*>(sm + L::offPage);        // [buf][8]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::offBar);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::offFlag);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offFlag + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int h = blockIdx.y;
+  const int q0 = blockIdx.x * 128;
+  const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, kvh = h / G;
+  const int T = a.n_tokens;
+  const int n_keys = a.history_len + T;
+  const int last_pos = a.history_len + min(q0 + 127, T - 1);
+  const int n_tiles = last_pos / 128 + 1;
+
+  grid_dep_wait();  // Q codes and scales come from the quantisation kernel
+  if (warp == 12) tc::tmem_alloc(tmem_slot, L::kTmemCols);
+  if (tid == 0) {
+    mbar_init(&bars[kBarKFull], kTransformThreads);
+    mbar_init(&bars[kBarVFull], kTransformThreads);
+    mbar_init(&bars[kBarS0], 1);
+    mbar_init(&bars[kBarS1], 1);
+    mbar_init(&bars[kBarKFree], 1);
+    mbar_init(&bars[kBarPvDone], 1);
+    mbar_init(&bars[kBarPFull], kSoftmaxThreads);
+    mbar_init(&bars[kBarScalesFree0], kSoftmaxThreads);
+    mbar_init(&bars[kBarScalesFree1], kSoftmaxThreads);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 8) {
+    // ================================================================ softmax warps
+    const int row = tid & 127, half = tid >> 7;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool row_real = q0 + row < T;
+    const int pos_r = a.history_len + q0 + row;
+    const float c2 = __fmul_rn(a.softmax_scale, kLog2eP);
+    const float a_row = row_real ? __fmul_rn(a.q_scales[static_cast<long long>(q0 + row) * Hq + h], c2) : 0.0f;
+    float m = -INFINITY, l_part = 0.0f, ps_ref = 0.0f;
+    bool started = false;
+    const uint32_t tm_o = tmem + lane_base + L::kOCol + half * OCOLS_H;
+    {
+      uint32_t z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = 0u;
+#pragma unroll
+      for (int c = 0; c < OCOLS_H / 32; ++c) tc::st_32x32b_x32(tm_o + 32 * c, z);
+      tc::wait_st();
+    }
+    float* red_max = red;                  // exchange 1: [half][row]
+    float* red_wmax = red + 2 * 128;       // exchange 2
+    bool failed = false;  // a wait of this thread gave up; the group leaves together below
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j & 1;
+      failed |= !wait_or_abort(&bars[kBarS0 + b], (j >> 1) & 1, a.status, abort_flag);
+      tc::fence_after_sync();
+      const uint32_t tm_s = tmem + lane_base + b * 128 + half * 64;
+      uint32_t sv[64];
+      tc::ld_32x32b_x32(tm_s, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tc::ld_32x32b_x32(tm_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tc::wait_ld();
+      const float* sk_t = scale_s + (b * 2 + 0) * 128 + half * 64;
+      const float* sv_t = scale_s + (b * 2 + 1) * 128 + half * 64;
+      // visible keys of this row in this tile, counted from the tile start
+      const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128) - half * 64;
+      float ymax0 = -INFINITY, ymax1 = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 64; n += 2) {
+        const float y0 = (n < lim) ? __fmul_rn(__uint_as_float(sv[n]), sk_t[n]) : -INFINITY;
+        const float y1 = (n + 1 < lim) ? __fmul_rn(__uint_as_float(sv[n + 1]), sk_t[n + 1]) : -INFINITY;
+        sv[n] = __float_as_uint(y0);
+        sv[n + 1] = __float_as_uint(y1);
+        ymax0 = fmaxf(ymax0, y0);
+        ymax1 = fmaxf(ymax1, y1);
+      }
+      red_max[half * 128 + row] = fmaxf(ymax0, ymax1);
+      tc::fence_before_sync();
+      if (named_bar_or(1, kSoftmaxThreads, failed)) break;  // all softmax threads leave together
+      tc::fence_after_sync();
+      const float ymax = fmaxf(red_max[row], red_max[128 + row]);
+      const float m_new = fmaxf(m, __fmul_rn(ymax, a_row));
+      const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+      float psum0 = 0.0f, psum1 = 0.0f, wmax0 = 0.0f, wmax1 = 0.0f;
+#pragma unroll
+      for (int n = 0; n < 64; n += 2) {
+        const float p0 = exp2_det(__fmaf_rn(__uint_as_float(sv[n]), a_row, -m_new));
+        const float p1 = exp2_det(__fmaf_rn(__uint_as_float(sv[n + 1]), a_row, -m_new));
+        psum0 += p0;
+        psum1 += p1;
+        const float w0 = __fmul_rn(p0, sv_t[n]);
+        const float w1 = __fmul_rn(p1, sv_t[n + 1]);
+        sv[n] = __float_as_uint(w0);
+        sv[n + 1] = __float_as_uint(w1);
+        wmax0 = fmaxf(wmax0, w0);
+        wmax1 = fmaxf(wmax1, w1);
+      }
+      mbar_arrive(&bars[kBarScalesFree0 + b]);  // this tile's scales are no longer read
+      l_part = l_part * alpha + (psum0 + psum1);
+      m = m_new;
+      red_wmax[half * 128 + row] = fmaxf(wmax0, wmax1);
+      tc::fence_before_sync();  // both halves have read their S before either writes P over it
+      named_bar(1, kSoftmaxThreads);
+      tc::fence_after_sync();
+      const float wmax = fmaxf(red_wmax[row], red_wmax[128 + row]);
+      // reference scale of O and the factor that moves O onto this tile's P scale (the same
+      // decisions in both halves of the row)
+      float f = 1.0f;
+      bool codes_on = wmax > 0.0f;
+      const float ps_new = __fdiv_rn(wmax, 127.0f);
+      if (!started) {
+        if (codes_on) {
+          started = true;
+          ps_ref = ps_new;
+        }
+      } else if (codes_on) {
+        const float fr = ps_ref * alpha / ps_new;
+        if (fr > 1.8446744e19f) {  // 2^64: the tile is negligible against what O holds; drop it
+          codes_on = false;
+          ps_ref *= alpha;
+        } else {
+          f = fr;
+          ps_ref = ps_new;
+        }
+      } else {
+        ps_ref *= alpha;
+      }
+      const float rr = codes_on ? __fdiv_rn(127.0f, wmax) : 0.0f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        float c0 = 0.0f, c1 = 0.0f;
+        if (codes_on) {  // rint(w * r) with one rounding; w <= wmax keeps it in [0, 127]
+          c0 = __fsub_rn(__fmaf_rn(__uint_as_float(sv[2 * e]), rr, kMagic), kMagic);
+          c1 = __fsub_rn(__fmaf_rn(__uint_as_float(sv[2 * e + 1]), rr, kMagic), kMagic);
+        }
+        pk[e] = pack_half2(c0, c1);
+      }
+      // O must hold PV_{j-1} before it is rescaled (and P_{j-1} must be consumed: it is)
+      if (j > 0) {
+        failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
+        tc::fence_after_sync();
+      }
+      tc::st_32x32b_x32(tmem + lane_base + b * 128 + half * 32, pk);  // P over S's first 64 columns
+      if (__any_sync(0xffffffffu, f != 1.0f)) {
+#pragma unroll
+        for (int c = 0; c < OCOLS_H / 32; ++c) {
+          uint32_t o[32];
+          tc::ld_32x32b_x32(tm_o + 32 * c, o);
+          tc::wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+          tc::st_32x32b_x32(tm_o + 32 * c, o);
+        }
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(&bars[kBarPFull]);
+    }
+    // ---- epilogue: out = O * ps_ref / l (l summed over both halves)
+    if (!*abort_flag) {
+      wait_or_abort(&bars[kBarPvDone], (n_tiles - 1) & 1, a.status, abort_flag);
+      tc::fence_after_sync();
+    }
+    red_max[half * 128 + row] = l_part;
+    named_bar(1, kSoftmaxThreads);
+    const float l = red_max[row] + red_max[128 + row];
+    const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
+#pragma unroll
+    for (int c = 0; c < OCOLS_H / 32; ++c) {
+      uint32_t o[32];
+      tc::ld_32x32b_x32(tm_o + 32 * c, o);
+      tc::wait_ld();
+      if (row_real) {
+        float* dst = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + half * OCOLS_H + 32 * c;
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + e) =
+              make_float4(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
+                          __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
+      }
+    }
+  } else if (warp < 12) {
+    // ================================================================ transform warps
+    const int t = tid - kSoftmaxThreads;  // 0..127
+    load_q_tile<D>(qs, a.q_codes, T, Hq, h, q0, t);
+    bool failed = false;  // a wait of this thread gave up; the group leaves together below
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j & 1;
+      if (j > 0) failed |= !wait_or_abort(&bars[kBarKFree], (j - 1) & 1, a.status, abort_flag);
+      // K tile j: key n = t; its page, its 16-dim chunks, its scales
+      const int key = 128 * j + t;
+      int page = -1;
+      if (key < n_keys) {
+        const int bi = key / KVQ_BLOCK_SIZE;
+        if (bi < a.n_blocks_row) page = a.block_table_row[bi];
+        if (page < 0 || page >= a.num_blocks) {
+          if ((key & 15) == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
+          page = -1;
+        }
+      }
+      const long long ph = static_cast<long long>(page < 0 ? 0 : page) * a.n_kv_heads + kvh;
+      const int slot = key & 15;
+      const int8_t* src = a.k + ph * D * KVQ_BLOCK_SIZE + slot * 16;
+      int4 raw[D / 16];
+#pragma unroll
+      for (int c16 = 0; c16 < D / 16; ++c16)
+        raw[c16] = (page >= 0) ? __ldg(reinterpret_cast<const int4*>(src + c16 * 256)) : make_int4(0, 0, 0, 0);
+      const float skv = page >= 0 ? a.k_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+      const float svv = page >= 0 ? a.v_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+#pragma unroll
+      for (int c16 = 0; c16 < D / 16; ++c16) {
+        uint4 c0, c1;
+        widen16(raw[c16], c0, c1);
+        uint8_t* blk = ks + (c16 >> 2) * (128 * 128);
+        const int cc = (c16 & 3) * 2;
+        sts128(blk + tc::sw128_off(t, cc), c0);
+        sts128(blk + tc::sw128_off(t, cc + 1), c1);
+      }
+      if ((t & 15) == 0) page_s[b * 8 + (t >> 4)] = page;
+      if (j >= 2) failed |= !wait_or_abort(&bars[kBarScalesFree0 + b], ((j - 2) >> 1) & 1, a.status, abort_flag);
+      scale_s[(b * 2 + 0) * 128 + t] = skv;
+      scale_s[(b * 2 + 1) * 128 + t] = svv;
+      tc::fence_proxy_async_smem();
+      mbar_arrive(&bars[kBarKFull]);
+      // page_s of this tile is complete; all transform threads leave together on a failure
+      if (named_bar_or(2, kTransformThreads, failed)) break;
+      // V tile j: rows = head dims d = t, t + 128; 8 pages of 16 keys along K
+      if (j > 0) failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
+#pragma unroll
+      for (int rr = 0; rr < D / 128; ++rr) {
+        const int d = t + 128 * rr;
+        int4 vraw[8];
+#pragma unroll
+        for (int pl = 0; pl < 8; ++pl) {
+          const int pg = page_s[b * 8 + pl];
+          vraw[pl] = make_int4(0, 0, 0, 0);
+          if (pg >= 0) {
+            const long long vph = static_cast<long long>(pg) * a.n_kv_heads + kvh;
+            vraw[pl] = __ldg(reinterpret_cast<const int4*>(a.v + (vph * D + d) * KVQ_BLOCK_SIZE));
+          }
+        }
+#pragma unroll
+        for (int pl = 0; pl < 8; ++pl) {
+          uint4 c0, c1;
+          widen16(vraw[pl], c0, c1);
+          uint8_t* blk = vs + (pl >> 2) * (D * 128);
+          const int cc = (pl & 3) * 2;
+          sts128(blk + tc::sw128_off(d, cc), c0);
+          sts128(blk + tc::sw128_off(d, cc + 1), c1);
+        }
+      }
+      tc::fence_proxy_async_smem();
+      mbar_arrive(&bars[kBarVFull]);
+    }
+  } else if (lane == 0) {
+    // ================================================================ MMA issue (one thread)
+    const uint32_t qs_a = smem_u32(qs), ks_a = smem_u32(ks), vs_a = smem_u32(vs);
+    constexpr uint32_t idesc_qk = tc::idesc_f16_f32(128, 128);
+    constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, D);
+    const uint32_t tm_o = tmem + L::kOCol;
+    for (int j = 0; j <= n_tiles; ++j) {
+      if (j < n_tiles) {
+        const int b = j & 1;
+        if (!wait_or_abort(&bars[kBarKFull], j & 1, a.status, abort_flag)) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (128 * 128) + (k & 3) * 32;
+          tc::mma_f16_ss(tmem + b * 128, tc::sdesc_sw128(qs_a + off), tc::sdesc_sw128(ks_a + off), idesc_qk,
+                         k > 0 ? 1u : 0u);
+        }
+        tc::commit(&bars[kBarS0 + b]);
+        tc::commit(&bars[kBarKFree]);
+      }
+      if (j >= 1) {
+        const int jp = j - 1, bp = jp & 1;
+        if (!wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag)) break;
+        if (!wait_or_abort(&bars[kBarVFull], jp & 1, a.status, abort_flag)) break;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t boff = (k >> 2) * (D * 128) + (k & 3) * 32;
+          tc::mma_f16_ts(tm_o, tmem + bp * 128 + 8 * k, tc::sdesc_sw128(vs_a + boff), idesc_pv, 1u);
+        }
+        tc::commit(&bars[kBarPvDone]);
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 12) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, L::kTmemCols);
+  }
+}
+
 // ============================================================================ debug QK tile
 // The prefill kernel's QK path alone: S for query rows q0 .. q0+127 of dbg_q_head against the
 // 128 keys of tile (dbg_k0 / 128 + blockIdx.x), written as exact int32.
@@ -533,12 +925,12 @@ cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
 
 template <int D>
 static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
-  using L = PrefillSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  using L = PrefillWsSmem<D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(prefill_ws_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((a.n_tokens + 127) / 128, a.n_q_heads);
-  prefill_kernel<D><<<grid, 128, L::kAlloc, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(prefill_ws_kernel<D>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {

@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(256) quant_write_kernel(QuantWriteArgs a) {
   const int tok = static_cast<int>(th / H);
   const int h = static_cast<int>(th % H);
 
+  grid_dep_wait();     // the new rows may come from the previous kernel of the stream
+  grid_dep_trigger();  // the attention kernel may start launching; it waits for this grid
   const int seq = a.seq_idx[tok];
   const int pos = a.pos[tok];
   if (seq < 0 || seq >= a.num_seqs) {
@@ -118,11 +120,8 @@ cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream) {
   const int warps_per_block = 8;
   const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (a.head_dim == 256)
-    quant_write_kernel<256><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
-  else
-    quant_write_kernel<128><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  if (a.head_dim == 256) return launch_pdl(quant_write_kernel<256>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
+  return launch_pdl(quant_write_kernel<128>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
 }
 
 }  // namespace kvq
