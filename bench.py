@@ -301,7 +301,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     return res
 
 
-def bench_extra(args, local, hbm, tflops):
+def bench_extra(args, local, hbm, tflops, only=None):
     """Secondary figures on the other workloads (one JSON object, not the headline)."""
     import numpy as np
     import torch
@@ -341,19 +341,40 @@ def bench_extra(args, local, hbm, tflops):
         return statistics.median(ms)
 
     res = {}
+    reps = args.steps if only else None
+
+    def want(name):
+        return only is None or only == name
+
     # decode_1k: single-CTA route, launch/latency bound
+    if want("decode_1k"):
+        res.update(_extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps or 50))
+    if want("prefill_32k"):
+        res.update(_extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps or 10, tflops))
+    if want("sparse_32k"):
+        res.update(_extra_sparse_32k(kvq, W, bf16, i32, timed, dev, reps or 10))
+    return res
+
+
+def _extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps):
+    import torch
+    res = {}
     w = W.make("decode_1k")
     cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
     bt = i32(w["block_table"])
     kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
     q, ctx = bf16(w["q"]), i32(w["ctx_lens"])
     out = torch.empty((1, w["hq"], w["d"]), dtype=torch.float32, device=dev)
-    ms = timed(lambda: kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out), 50)
+    ms = timed(lambda: kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out), reps)
     kvb = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
     res["decode_1k"] = {"us_per_call": round(ms * 1e3, 2), "kv_GBps": round(kvb / ms / 1e6, 1)}
-    del cache
+    return res
 
-    # prefill_32k: the chunk's K/V written by kv_quant_write first (timed separately)
+
+def _extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps, tflops):
+    """prefill_32k: the chunk's K/V written by kv_quant_write first (timed separately)."""
+    import torch
+    res = {}
     w = W.make("prefill_32k")
     cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
     bt = i32(w["block_table"])
@@ -364,32 +385,34 @@ def bench_extra(args, local, hbm, tflops):
     ws = torch.empty(kvq.kvq_prefill_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
     row = bt[0]
     ms = timed(lambda: kvq.kvq_attn_prefill_int8(cache, q, w["history"], row, w["softmax_scale"], out=out,
-                                                  workspace=ws), 10)
+                                                  workspace=ws), reps)
     hist = w["history"]
     triples = Hq * sum(hist + i + 1 for i in range(T))
     ops = 2.0 * 2 * D * triples
     chunk_seq = torch.zeros(T, dtype=torch.int32, device=dev)
     chunk_pos = torch.arange(hist, hist + T, dtype=torch.int32, device=dev)
     kc, vc = bf16(w["k_fill"][hist:]), bf16(w["v_fill"][hist:])
-    ms_qw = timed(lambda: kvq.kvq_quant_write(cache, kc, vc, chunk_seq, chunk_pos, bt), 10)
+    ms_qw = timed(lambda: kvq.kvq_quant_write(cache, kc, vc, chunk_seq, chunk_pos, bt), reps)
     res["prefill_32k"] = {"ms_per_call": round(ms, 4), "int8_equiv_TOPS": round(ops / ms / 1e9, 1),
                           "frac_of_bf16_peak": round(ops / ms / 1e9 / tflops, 4), "peak_TFLOPS": tflops,
                           "chunk_kv_quant_write_ms": round(ms_qw, 4), "ops": ops}
-    del cache
+    return res
 
-    # sparse_32k
+
+def _extra_sparse_32k(kvq, W, bf16, i32, timed, dev, reps):
+    import torch
+    res = {}
     w = W.make("sparse_32k")
     cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
     bt = i32(w["block_table"])
     kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
     q, off, cells, row = bf16(w["q"]), i32(w["cell_offsets"]), i32(w["cells"]), i32(w["block_table"][0])
     out = torch.empty((w["n_queries"], w["hq"], w["d"]), dtype=torch.float32, device=dev)
-    ms = timed(lambda: kvq.kvq_attn_sparse_int8kv(cache, q, off, cells, row, w["softmax_scale"], out=out), 10)
+    ms = timed(lambda: kvq.kvq_attn_sparse_int8kv(cache, q, off, cells, row, w["softmax_scale"], out=out), reps)
     pairs = int(len(w["cells"]))
     fma = pairs * w["hq"] * w["d"] * 2
     res["sparse_32k"] = {"ms_per_call": round(ms, 4), "GFMA_per_s": round(fma / ms / 1e6, 1),
                          "pairs": pairs}
-    del cache
     return res
 
 
@@ -473,10 +496,20 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k"],
+                    help="time only this secondary workload (profiling runs); prints its figures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     world, rank, local = dist_setup()
+    if args.only:
+        import torch
+        from int8_kv_cache_quant_gb300 import build as kbuild
+        kbuild.build()
+        torch.cuda.set_device(local)
+        hbm, tflops, _ = load_peaks()
+        print(json.dumps(bench_extra(args, local, hbm, tflops, only=args.only)))
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(bench_reference(args, world, rank)))

@@ -408,11 +408,19 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
 
 // Stage 2: log-sum-exp merge of the splits of one (sequence, query head).
 //   M_s = max m_s, M_z = max m_z;  l = sum l_s 2^{m_s - M_s};  o = sum acc_s 2^{m_z - M_z};
-//   out = o 2^{M_z - M_s} / l.  The per-split weights are computed once into shared memory.
+//   out = o 2^{M_z - M_s} / l.  The per-split weights are computed once into shared memory
+// ("ROCm/RDNA4 (gfx1201) vLLM ...", "The reduce is not free": one cooperative pass, each
+// exponential once per split).  256 threads = 4 split groups x 64 threads of 4 dims (D 256;
+// 8 groups x 32 threads at D 128); each thread keeps 8 independent loads in flight.
+constexpr int kMergeThreads = 256;
+
 template <int D>
-__global__ void __launch_bounds__(D) decode_merge_kernel(DecodeArgs a) {
-  extern __shared__ float wts[];  // [n_split] weights for acc, then [n_split] for l
-  __shared__ float red[2][32];
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a) {
+  constexpr int TPG = D / 4;                    // threads per split group (4 dims each)
+  constexpr int NG = kMergeThreads / TPG;       // split groups
+  extern __shared__ float wts[];                // [n_split] weights of the partial accumulators
+  __shared__ float red[2][kMergeThreads / 32];
+  __shared__ __align__(16) float4 part[NG][TPG];
   const int h = blockIdx.x, b = blockIdx.y, Hq = a.n_q_heads;
   grid_dep_wait();  // the partials come from stage 1
   int ctx = a.ctx_lens[b];
@@ -420,8 +428,10 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(DecodeArgs a) {
   const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
   const long long pu0 = (static_cast<long long>(b) * Hq + h) * a.n_split;
   const float* stats = a.part_stats + pu0 * 4;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+
   float Ms = -INFINITY, Mz = -INFINITY;
-  for (int s = threadIdx.x; s < n; s += blockDim.x) {
+  for (int s = tid; s < n; s += kMergeThreads) {
     Ms = fmaxf(Ms, stats[s * 4 + 0]);
     Mz = fmaxf(Mz, stats[s * 4 + 1]);
   }
@@ -430,45 +440,74 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(DecodeArgs a) {
     Ms = fmaxf(Ms, __shfl_xor_sync(0xffffffffu, Ms, off));
     Mz = fmaxf(Mz, __shfl_xor_sync(0xffffffffu, Mz, off));
   }
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = Ms;
-    red[1][threadIdx.x >> 5] = Mz;
+  if (lane == 0) {
+    red[0][wid] = Ms;
+    red[1][wid] = Mz;
   }
   __syncthreads();
   Ms = -INFINITY;
   Mz = -INFINITY;
-  for (int i = 0; i < static_cast<int>(blockDim.x + 31) / 32; ++i) {
+#pragma unroll
+  for (int i = 0; i < kMergeThreads / 32; ++i) {
     Ms = fmaxf(Ms, red[0][i]);
     Mz = fmaxf(Mz, red[1][i]);
   }
   float lpart = 0.f;
-  for (int s = threadIdx.x; s < n; s += blockDim.x) {
+  for (int s = tid; s < n; s += kMergeThreads) {
     const float ms = stats[s * 4 + 0], mz = stats[s * 4 + 1], l = stats[s * 4 + 2];
     wts[s] = (Mz != -INFINITY && mz != -INFINITY) ? fast_exp2(mz - Mz) : 0.f;
     lpart += (Ms != -INFINITY && ms != -INFINITY) ? l * fast_exp2(ms - Ms) : 0.f;
   }
-  __syncthreads();  // red[] reused below
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
-  if ((threadIdx.x & 31) == 0) red[0][threadIdx.x >> 5] = lpart;
+  __syncthreads();  // red[] and wts[] reuse
+  if (lane == 0) red[0][wid] = lpart;
   __syncthreads();
   float l = 0.f;
-  for (int i = 0; i < static_cast<int>(blockDim.x + 31) / 32; ++i) l += red[0][i];
-  const int d = threadIdx.x;
-  const float* acc = a.part_acc + pu0 * D + d;
-  float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  int s = 0;
-  for (; s + 4 <= n; s += 4) {
-    o0 += acc[(s + 0) * D] * wts[s + 0];
-    o1 += acc[(s + 1) * D] * wts[s + 1];
-    o2 += acc[(s + 2) * D] * wts[s + 2];
-    o3 += acc[(s + 3) * D] * wts[s + 3];
+#pragma unroll
+  for (int i = 0; i < kMergeThreads / 32; ++i) l += red[0][i];
+
+  const int grp = tid / TPG, dq = tid % TPG;
+  const float4* acc = reinterpret_cast<const float4*>(a.part_acc + pu0 * D) + dq;
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = grp;
+  for (; s + 7 * NG < n; s += 8 * NG) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = acc[static_cast<long long>(s + u * NG) * (D / 4)];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wgt = wts[s + u * NG];
+      o.x = fmaf(v[u].x, wgt, o.x);
+      o.y = fmaf(v[u].y, wgt, o.y);
+      o.z = fmaf(v[u].z, wgt, o.z);
+      o.w = fmaf(v[u].w, wgt, o.w);
+    }
   }
-  for (; s < n; ++s) o0 += acc[s * D] * wts[s];
-  const float o = (o0 + o1) + (o2 + o3);
-  float res = 0.f;
-  if (l > 0.f && Mz != -INFINITY) res = o * fast_exp2(Mz - Ms) / l;
-  a.out[(static_cast<long long>(b) * Hq + h) * D + d] = res;
+  for (; s < n; s += NG) {
+    const float4 v = acc[static_cast<long long>(s) * (D / 4)];
+    const float wgt = wts[s];
+    o.x = fmaf(v.x, wgt, o.x);
+    o.y = fmaf(v.y, wgt, o.y);
+    o.z = fmaf(v.z, wgt, o.z);
+    o.w = fmaf(v.w, wgt, o.w);
+  }
+  part[grp][dq] = o;
+  __syncthreads();
+  if (grp == 0) {
+    float4 t = part[0][dq];
+#pragma unroll
+    for (int g2 = 1; g2 < NG; ++g2) {
+      const float4 u = part[g2][dq];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float sc = (l > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / l : 0.f;
+    reinterpret_cast<float4*>(a.out + (static_cast<long long>(b) * Hq + h) * D)[dq] =
+        make_float4(t.x * sc, t.y * sc, t.z * sc, t.w * sc);
+  }
 }
 
 size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_dim, int split_rows) {
@@ -512,17 +551,16 @@ cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t s
                                static_cast<int>(wbytes));
       if (e != cudaSuccess) return e;
     }
-    e = launch_pdl(decode_merge_kernel<256>, g2, dim3(256), wbytes, stream, a);
-    if (e != cudaSuccess) return e;
+    e = launch_pdl(decode_merge_kernel<256>, g2, dim3(kMergeThreads), wbytes, stream, a);
   } else {
     if (wbytes > 48 * 1024) {
       e = cudaFuncSetAttribute(decode_merge_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(wbytes));
       if (e != cudaSuccess) return e;
     }
-    e = launch_pdl(decode_merge_kernel<128>, g2, dim3(128), wbytes, stream, a);
-    if (e != cudaSuccess) return e;
+    e = launch_pdl(decode_merge_kernel<128>, g2, dim3(kMergeThreads), wbytes, stream, a);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

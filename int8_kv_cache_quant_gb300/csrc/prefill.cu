@@ -12,12 +12,14 @@
 //   shared memory and the contractions use tcgen05.mma kind::f16 with fp32 accumulators in
 //   tensor memory.  This is exact: every QK partial sum is an integer of magnitude at most
 //   256 * 127 * 127 < 2^24, every per-tile PV sum at most 128 * 127 * 127 < 2^24.
-// * One CTA per (128 query rows, query head).  Q (128 x D), the K tile (128 keys x D), the V
-//   tile (D x 128 keys) and the P tile (128 x 128) live in shared memory in the K-major
-//   128-byte-swizzle layout; S (128 x 128) and O (128 x D) live in tensor memory.
-// * Thread r of the CTA owns query row r (tensor-memory lane r): it reads its S row, runs the
-//   online softmax and the per-tile P re-quantisation, writes its P codes, and rescales its O
-//   row when the P scale changes (O holds sum_tiles (ps_tile / ps_ref) * PV_tile).
+// * One CTA per (128 query rows, query head).  Q (128 x D), the K tile (128 keys x D) and the
+//   V tile (D x 128 keys) live in shared memory in the K-major 128-byte-swizzle layout; S
+//   (128 x 128, two buffers), the P codes (fp16, over the first half of their S buffer) and O
+//   (128 x D) live in tensor memory.
+// * Two softmax threads share query row r (tensor-memory lane r), one per half of the key
+//   tile: they read their S halves, run the online softmax and the per-tile P re-quantisation,
+//   write their P codes, and rescale their halves of the O row when the P scale changes (O
+//   holds sum_tiles (ps_tile / ps_ref) * PV_tile).
 // * Every P-code decision is the page's fp32 sequence with a specified exp2 (exp2_det) and the
 //   running maximum after each 128-key tile, so the codes are reproducible off the GPU.
 #include "kvq_dev.cuh"
@@ -127,6 +129,67 @@ __device__ __forceinline__ float exp2_det(float x) {
   return __fmul_rn(p, __int_as_float((ni + 127) << 23));
 }
 
+// Packed fp32 pairs (add / mul / fma .rn.f32x2): each lane is rounded exactly like the scalar
+// operation, so these give the same bits as __fadd_rn / __fmul_rn / __fmaf_rn per element with
+// half the instructions.
+struct f2 {
+  unsigned long long v;
+};
+__device__ __forceinline__ f2 mk2(float x, float y) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ float lo2(f2 a) {
+  float x, y;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(a.v));
+  (void)y;
+  return x;
+}
+__device__ __forceinline__ float hi2(f2 a) {
+  float x, y;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(a.v));
+  (void)x;
+  return y;
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b) {
+  f2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+  return r;
+}
+
+// exp2_det of a pair, the same operations per element: x < -125 -> 0, x > 125 clamped;
+// n = rint(x) through the 1.5 * 2^23 magic sum t, f = x - n (exact, as one fma), the degree-5
+// Horner polynomial, and the factor 2^n built from t's bits: bits(t) = 0x4B400000 + n, so
+// bits(t) * 2^23 + (127 - 0x4B400000) * 2^23 = (n + 127) << 23 (mod 2^32), one integer multiply-add.
+__device__ __forceinline__ f2 exp2_det2(float x0, float x1) {
+  const bool v0 = x0 >= -125.0f, v1 = x1 >= -125.0f;
+  const f2 x = mk2(fminf(x0, 125.0f), fminf(x1, 125.0f));
+  const f2 t = add2(x, mk2(kMagic, kMagic));
+  const f2 n = add2(t, mk2(-kMagic, -kMagic));
+  const f2 f = fma2(n, mk2(-1.0f, -1.0f), x);
+  f2 p = fma2(mk2(0.00133335581464284f, 0.00133335581464284f), f, mk2(0.00961812910762848f, 0.00961812910762848f));
+  p = fma2(p, f, mk2(0.0555041086648216f, 0.0555041086648216f));
+  p = fma2(p, f, mk2(0.240226506959101f, 0.240226506959101f));
+  p = fma2(p, f, mk2(0.693147180559945f, 0.693147180559945f));
+  p = fma2(p, f, mk2(1.0f, 1.0f));
+  constexpr uint32_t kExpBias = (127u - 0x4B400000u) << 23;
+  const uint32_t s0 = __float_as_uint(lo2(t)) * (1u << 23) + kExpBias;
+  const uint32_t s1 = __float_as_uint(hi2(t)) * (1u << 23) + kExpBias;
+  p = mul2(p, mk2(__uint_as_float(s0), __uint_as_float(s1)));
+  return mk2(v0 ? lo2(p) : 0.0f, v1 ? hi2(p) : 0.0f);
+}
+
 // 16 int8 codes (one int4) -> two 16-byte chunks of 8 fp16 (exact integer values).
 __device__ __forceinline__ void widen16(const int4 raw, uint4& c0, uint4& c1) {
   uint32_t lo, hi;
@@ -201,32 +264,6 @@ __device__ void load_k_tile(uint8_t* ks, float* sk_s, float* sv_s, int* page_s, 
   }
 }
 
-// V tile j: tile row d (head dimension) holds keys 128j .. 128j+127 along K.  Page pl of the
-// tile supplies keys 16 pl .. 16 pl + 15, i.e. 16-byte chunks 2 (pl % 4), 2 (pl % 4) + 1 of
-// K-block pl / 4.  Pages past the context are zero.
-template <int D>
-__device__ void load_v_tile(uint8_t* vs, const int* page_s, const PrefillArgs& a, int kvh, int tid) {
-#pragma unroll
-  for (int rr = 0; rr < D / 128; ++rr) {
-    const int d = tid + 128 * rr;
-#pragma unroll 2
-    for (int pl = 0; pl < 8; ++pl) {
-      const int page = page_s[pl];
-      int4 raw = make_int4(0, 0, 0, 0);
-      if (page >= 0) {
-        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
-        raw = __ldg(reinterpret_cast<const int4*>(a.v + (ph * D + d) * KVQ_BLOCK_SIZE));
-      }
-      uint4 c0, c1;
-      widen16(raw, c0, c1);
-      uint8_t* blk = vs + (pl >> 2) * (D * 128);
-      const int cc = (pl & 3) * 2;
-      sts128(blk + tc::sw128_off(d, cc), c0);
-      sts128(blk + tc::sw128_off(d, cc + 1), c1);
-    }
-  }
-}
-
 // S = Q K^T over the head dimension (M = 128 rows, N = 128 keys, K = D), one thread.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t qs, uint32_t ks, uint32_t tmem_s) {
@@ -238,18 +275,6 @@ __device__ __forceinline__ void issue_qk(uint32_t qs, uint32_t ks, uint32_t tmem
   }
 }
 
-// O += P V (M = 128 rows, N = D, K = 128 keys), one thread.
-template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t ps, uint32_t vs, uint32_t tmem_o) {
-  constexpr uint32_t idesc = tc::idesc_f16_f32(128, D);
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const uint32_t aoff = (k >> 2) * (128 * 128) + (k & 3) * 32;
-    const uint32_t boff = (k >> 2) * (D * 128) + (k & 3) * 32;
-    tc::mma_f16_ss(tmem_o, tc::sdesc_sw128(ps + aoff), tc::sdesc_sw128(vs + boff), idesc, 1u);
-  }
-}
-
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t s = smem_u32(p);
   return p + (((s + 1023u) & ~1023u) - s);
@@ -257,206 +282,16 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 }  // namespace
 
-// ============================================================================ prefill kernel
-template <int D>
-__global__ void __launch_bounds__(128, 1) prefill_kernel(PrefillArgs a) {
-  using L = PrefillSmem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  uint8_t* qs = sm + L::offQ;
-  uint8_t* ks = sm + L::offK;
-  uint8_t* vs = sm + L::offV;
-  uint8_t* ps = sm + L::offP;
-  float* sk_s = reinterpret_cast<float*>(sm + L::offSK);
-  float* sv_s = reinterpret_cast<float*>(sm + L::offSV);
-  int* page_s = reinterpret_cast<int*>(sm + L::offPage);
-  uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + L::offBar);
-  uint64_t* bar_pv = bar_qk + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offTmem);
-
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int h = blockIdx.y;
-  const int q0 = blockIdx.x * 128;
-  const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, kvh = h / G;
-  const int T = a.n_tokens;
-  const int n_keys = a.history_len + T;  // keys in the cache for this chunk
-
-  if (warp == 0) tc::tmem_alloc(tmem_slot, L::kTmemCols);
-  if (tid == 0) {
-    mbar_init(bar_qk, 1);
-    mbar_init(bar_pv, 1);
-    mbar_fence_init();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tm_s = tmem + lane_base;              // this warp's lanes, S columns
-  const uint32_t tm_o = tmem + lane_base + L::kOCol;   // this warp's lanes, O columns
-
-  load_q_tile<D>(qs, a.q_codes, T, Hq, h, q0, tid);
-  {
-    uint32_t z[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) tc::st_32x32b_x32(tm_o + 32 * c, z);
-    tc::wait_st();
-  }
-
-  // per-row state (thread tid = query row tid)
-  const int row = tid;
-  const bool row_real = q0 + row < T;
-  const int pos_r = a.history_len + q0 + row;  // the row's absolute position
-  const float c2 = __fmul_rn(a.softmax_scale, kLog2eP);
-  const float a_row = row_real ? __fmul_rn(a.q_scales[static_cast<long long>(q0 + row) * Hq + h], c2) : 0.0f;
-  float m = -INFINITY, l = 0.0f, ps_ref = 0.0f;
-  bool started = false;
-  bool timed_out = false;
-
-  const int last_pos = a.history_len + min(q0 + 127, T - 1);
-  const int n_tiles = last_pos / 128 + 1;
-  const uint32_t qs_a = smem_u32(qs), ks_a = smem_u32(ks), vs_a = smem_u32(vs), ps_a = smem_u32(ps);
-
-  for (int j = 0; j < n_tiles; ++j) {
-    load_k_tile<D>(ks, sk_s, sv_s, page_s, a, kvh, j, n_keys, tid);
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    // a bounded wait that ran out anywhere in the CTA ends the walk for every thread
-    if (__syncthreads_or(timed_out ? 1 : 0)) break;
-    if (tid == 0) {
-      tc::fence_after_sync();
-      issue_qk<D>(qs_a, ks_a, tmem);
-      tc::commit(bar_qk);
-    }
-    load_v_tile<D>(vs, page_s, a, kvh, tid);
-    tc::fence_proxy_async_smem();
-    if (!mbar_wait(bar_qk, j & 1, a.status)) timed_out = true;
-    tc::fence_after_sync();
-
-    // ---- S row -> online softmax -> P codes (thread = row)
-    uint32_t sraw[128];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tc::ld_32x32b_x32(tm_s + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sraw[32 * c]));
-    tc::wait_ld();
-    const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128);  // visible keys of this tile
-    float ymax = -INFINITY;
-#pragma unroll
-    for (int n = 0; n < 128; ++n) {
-      const float y = (n < lim) ? __fmul_rn(__uint_as_float(sraw[n]), sk_s[n]) : -INFINITY;
-      sraw[n] = __float_as_uint(y);
-      ymax = fmaxf(ymax, y);
-    }
-    const float m_new = fmaxf(m, __fmul_rn(ymax, a_row));
-    const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
-    float psum = 0.0f, wmax = 0.0f;
-#pragma unroll
-    for (int n = 0; n < 128; ++n) {
-      const float p = exp2_det(__fmaf_rn(__uint_as_float(sraw[n]), a_row, -m_new));
-      psum += p;
-      const float w = __fmul_rn(p, sv_s[n]);
-      sraw[n] = __float_as_uint(w);
-      wmax = fmaxf(wmax, w);
-    }
-    l = l * alpha + psum;
-    m = m_new;
-    // reference scale of O and the factor that moves O onto this tile's P scale
-    float f = 1.0f;
-    bool codes_on = wmax > 0.0f;
-    const float ps_new = __fdiv_rn(wmax, 127.0f);
-    if (!started) {
-      // O is still zero: nothing to rescale
-      if (codes_on) {
-        started = true;
-        ps_ref = ps_new;
-      }
-    } else if (codes_on) {
-      const float fr = ps_ref * alpha / ps_new;
-      if (fr > 1.8446744e19f) {  // 2^64: the tile is negligible against what O holds; drop it
-        codes_on = false;
-        ps_ref *= alpha;
-      } else {
-        f = fr;
-        ps_ref = ps_new;
-      }
-    } else {
-      ps_ref *= alpha;
-    }
-    const float r = codes_on ? __fdiv_rn(127.0f, wmax) : 0.0f;
-#pragma unroll
-    for (int cc = 0; cc < 16; ++cc) {
-      uint32_t hv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float c0 = 0.0f, c1 = 0.0f;
-        if (codes_on) {
-          c0 = __fsub_rn(__fmaf_rn(__uint_as_float(sraw[8 * cc + 2 * e]), r, kMagic), kMagic);
-          c1 = __fsub_rn(__fmaf_rn(__uint_as_float(sraw[8 * cc + 2 * e + 1]), r, kMagic), kMagic);
-          c0 = fminf(fmaxf(c0, 0.0f), 127.0f);
-          c1 = fminf(fmaxf(c1, 0.0f), 127.0f);
-        }
-        hv[e] = pack_half2(c0, c1);
-      }
-      sts128(ps + (cc >> 3) * (128 * 128) + tc::sw128_off(row, cc & 7), make_uint4(hv[0], hv[1], hv[2], hv[3]));
-    }
-    // tcgen05.ld / st are warp-collective: the whole warp takes this branch if any row needs it
-    if (__any_sync(0xffffffffu, f != 1.0f)) {
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tc::ld_32x32b_x32(tm_o + 32 * c, o);
-        tc::wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-        tc::st_32x32b_x32(tm_o + 32 * c, o);
-      }
-      tc::wait_st();
-    }
-    tc::fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      tc::fence_after_sync();
-      issue_pv<D>(ps_a, vs_a, tmem + L::kOCol);
-      tc::commit(bar_pv);
-    }
-    if (!mbar_wait(bar_pv, j & 1, a.status)) timed_out = true;
-    tc::fence_after_sync();
-  }
-
-  // ---- epilogue: out = O * ps_ref / l
-  const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint32_t o[32];
-    tc::ld_32x32b_x32(tm_o + 32 * c, o);
-    tc::wait_ld();
-    if (row_real) {
-      float* dst = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + 32 * c;
-#pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(dst + e) =
-            make_float4(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
-                        __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
-    }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, L::kTmemCols);
-  }
-}
-
 // ============================================================================ warp-specialised prefill
-// One CTA per (128 query rows, query head), 13 warps:
+// One CTA per (128 query rows, query head), 17 warps:
 //   warps 0-7   softmax: thread (row r, half h) owns keys 64h .. 64h+63 of row r's S row and O
 //               columns 128h .. 128h+127 (head_dim 256; 64h .. for 128); the two halves of a row
 //               exchange their partial maxima through shared memory at named barrier 1.
-//   warps 8-11  transform: Q once, then per tile the K and V tiles (int8 from the cache, widened to
+//   warps 8-11  K transform: Q once, then per tile the K tile (int8 from the cache, widened to
 //               fp16, 128-byte-swizzled K-major in shared memory) and the tile's key/value scales.
-//   warp 12     MMA issue (lane 0) and tensor-memory allocation.
+//   warps 12-15 V transform: per tile the V tile.  Both transform groups load the next tile's
+//               codes into registers before they wait for their shared-memory buffer.
+//   warp 16     MMA issue (lane 0) and tensor-memory allocation.
 // Tensor memory: S0 | S1 (128 columns each, double-buffered) | O (head_dim columns).  P (fp16,
 // 64 columns) is written back over the first 64 columns of its S buffer and read by the PV MMA
 // as its A operand; the next QK into that buffer is issued after that PV, and one thread's
@@ -491,8 +326,9 @@ enum { kBarKFull = 0, kBarVFull, kBarS0, kBarS1, kBarKFree, kBarPvDone, kBarPFul
        kBarScalesFree1 };
 
 constexpr int kSoftmaxThreads = 256;
-constexpr int kTransformThreads = 128;
-constexpr int kPrefillThreads = kSoftmaxThreads + kTransformThreads + 32;
+constexpr int kTransformThreads = 128;  // per transform group (K group, V group)
+constexpr int kPrefillThreads = kSoftmaxThreads + 2 * kTransformThreads + 32;
+constexpr int kMmaWarp = (kSoftmaxThreads + 2 * kTransformThreads) / 32;
 
 // Bounded wait that also gives up as soon as another thread of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned int* status,
@@ -555,7 +391,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
   const int n_tiles = last_pos / 128 + 1;
 
   grid_dep_wait();  // Q codes and scales come from the quantisation kernel
-  if (warp == 12) tc::tmem_alloc(tmem_slot, L::kTmemCols);
+  if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, L::kTmemCols);
   if (tid == 0) {
     mbar_init(&bars[kBarKFull], kTransformThreads);
     mbar_init(&bars[kBarVFull], kTransformThreads);
@@ -605,19 +441,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       tc::ld_32x32b_x32(tm_s, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       tc::ld_32x32b_x32(tm_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tc::wait_ld();
-      const float* sk_t = scale_s + (b * 2 + 0) * 128 + half * 64;
-      const float* sv_t = scale_s + (b * 2 + 1) * 128 + half * 64;
-      // visible keys of this row in this tile, counted from the tile start
+      const float4* sk_t = reinterpret_cast<const float4*>(scale_s + (b * 2 + 0) * 128 + half * 64);
+      const float4* sv_t = reinterpret_cast<const float4*>(scale_s + (b * 2 + 1) * 128 + half * 64);
+      // visible keys of this row in this tile, counted from the start of this thread's half
       const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128) - half * 64;
       float ymax0 = -INFINITY, ymax1 = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < 64; n += 2) {
-        const float y0 = (n < lim) ? __fmul_rn(__uint_as_float(sv[n]), sk_t[n]) : -INFINITY;
-        const float y1 = (n + 1 < lim) ? __fmul_rn(__uint_as_float(sv[n + 1]), sk_t[n + 1]) : -INFINITY;
-        sv[n] = __float_as_uint(y0);
-        sv[n + 1] = __float_as_uint(y1);
-        ymax0 = fmaxf(ymax0, y0);
-        ymax1 = fmaxf(ymax1, y1);
+      for (int n = 0; n < 64; n += 4) {
+        const float4 k4 = sk_t[n >> 2];
+        const f2 ya = mul2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), mk2(k4.x, k4.y));
+        const f2 yb = mul2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), mk2(k4.z, k4.w));
+        float y[4] = {lo2(ya), hi2(ya), lo2(yb), hi2(yb)};
+        if (lim < 64) {  // only tiles on the diagonal or past the context carry masked keys
+#pragma unroll
+          for (int e = 0; e < 4; ++e) y[e] = (n + e < lim) ? y[e] : -INFINITY;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sv[n + e] = __float_as_uint(y[e]);
+        ymax0 = fmaxf(ymax0, fmaxf(y[0], y[1]));
+        ymax1 = fmaxf(ymax1, fmaxf(y[2], y[3]));
       }
       red_max[half * 128 + row] = fmaxf(ymax0, ymax1);
       tc::fence_before_sync();
@@ -626,22 +468,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       const float ymax = fmaxf(red_max[row], red_max[128 + row]);
       const float m_new = fmaxf(m, __fmul_rn(ymax, a_row));
       const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
-      float psum0 = 0.0f, psum1 = 0.0f, wmax0 = 0.0f, wmax1 = 0.0f;
+      f2 psum = mk2(0.0f, 0.0f);
+      float wmax0 = 0.0f, wmax1 = 0.0f;
+      const f2 a2 = mk2(a_row, a_row), nm2 = mk2(-m_new, -m_new);
 #pragma unroll
-      for (int n = 0; n < 64; n += 2) {
-        const float p0 = exp2_det(__fmaf_rn(__uint_as_float(sv[n]), a_row, -m_new));
-        const float p1 = exp2_det(__fmaf_rn(__uint_as_float(sv[n + 1]), a_row, -m_new));
-        psum0 += p0;
-        psum1 += p1;
-        const float w0 = __fmul_rn(p0, sv_t[n]);
-        const float w1 = __fmul_rn(p1, sv_t[n + 1]);
-        sv[n] = __float_as_uint(w0);
-        sv[n + 1] = __float_as_uint(w1);
-        wmax0 = fmaxf(wmax0, w0);
-        wmax1 = fmaxf(wmax1, w1);
+      for (int n = 0; n < 64; n += 4) {
+        const float4 v4 = sv_t[n >> 2];
+        const f2 xa = fma2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), a2, nm2);
+        const f2 xb = fma2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), a2, nm2);
+        const f2 pa = exp2_det2(lo2(xa), hi2(xa));
+        const f2 pb = exp2_det2(lo2(xb), hi2(xb));
+        psum = add2(psum, add2(pa, pb));
+        const f2 wa = mul2(pa, mk2(v4.x, v4.y));
+        const f2 wb = mul2(pb, mk2(v4.z, v4.w));
+        sv[n] = __float_as_uint(lo2(wa));
+        sv[n + 1] = __float_as_uint(hi2(wa));
+        sv[n + 2] = __float_as_uint(lo2(wb));
+        sv[n + 3] = __float_as_uint(hi2(wb));
+        wmax0 = fmaxf(wmax0, fmaxf(lo2(wa), hi2(wa)));
+        wmax1 = fmaxf(wmax1, fmaxf(lo2(wb), hi2(wb)));
       }
       mbar_arrive(&bars[kBarScalesFree0 + b]);  // this tile's scales are no longer read
-      l_part = l_part * alpha + (psum0 + psum1);
+      l_part = l_part * alpha + (lo2(psum) + hi2(psum));
       m = m_new;
       red_wmax[half * 128 + row] = fmaxf(wmax0, wmax1);
       tc::fence_before_sync();  // both halves have read their S before either writes P over it
@@ -672,14 +520,12 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       }
       const float rr = codes_on ? __fdiv_rn(127.0f, wmax) : 0.0f;
       uint32_t pk[32];
+      const f2 r2 = mk2(rr, rr), mg = mk2(kMagic, kMagic), nmg = mk2(-kMagic, -kMagic);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        float c0 = 0.0f, c1 = 0.0f;
-        if (codes_on) {  // rint(w * r) with one rounding; w <= wmax keeps it in [0, 127]
-          c0 = __fsub_rn(__fmaf_rn(__uint_as_float(sv[2 * e]), rr, kMagic), kMagic);
-          c1 = __fsub_rn(__fmaf_rn(__uint_as_float(sv[2 * e + 1]), rr, kMagic), kMagic);
-        }
-        pk[e] = pack_half2(c0, c1);
+        // rint(w * r) with one rounding; w <= wmax keeps it in [0, 127]
+        const f2 c = add2(fma2(mk2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), r2, mg), nmg);
+        pk[e] = codes_on ? pack_half2(lo2(c), hi2(c)) : 0u;
       }
       // O must hold PV_{j-1} before it is rescaled (and P_{j-1} must be consumed: it is)
       if (j > 0) {
@@ -726,16 +572,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       }
     }
   } else if (warp < 12) {
-    // ================================================================ transform warps
-    const int t = tid - kSoftmaxThreads;  // 0..127
+    // ================================================================ K transform warps
+    const int t = tid - kSoftmaxThreads;  // 0..127: key t of each tile
     load_q_tile<D>(qs, a.q_codes, T, Hq, h, q0, t);
     bool failed = false;  // a wait of this thread gave up; the group leaves together below
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      if (j > 0) failed |= !wait_or_abort(&bars[kBarKFree], (j - 1) & 1, a.status, abort_flag);
-      // K tile j: key n = t; its page, its 16-dim chunks, its scales
+    int4 raw[D / 16];
+    float skv = 0.0f, svv = 0.0f;
+    int page = -1;
+    // codes and scales of key t of tile j into registers
+    auto fetch = [&](int j) {
       const int key = 128 * j + t;
-      int page = -1;
+      page = -1;
       if (key < n_keys) {
         const int bi = key / KVQ_BLOCK_SIZE;
         if (bi < a.n_blocks_row) page = a.block_table_row[bi];
@@ -747,12 +594,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       const long long ph = static_cast<long long>(page < 0 ? 0 : page) * a.n_kv_heads + kvh;
       const int slot = key & 15;
       const int8_t* src = a.k + ph * D * KVQ_BLOCK_SIZE + slot * 16;
-      int4 raw[D / 16];
 #pragma unroll
       for (int c16 = 0; c16 < D / 16; ++c16)
         raw[c16] = (page >= 0) ? __ldg(reinterpret_cast<const int4*>(src + c16 * 256)) : make_int4(0, 0, 0, 0);
-      const float skv = page >= 0 ? a.k_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
-      const float svv = page >= 0 ? a.v_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+      skv = page >= 0 ? a.k_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+      svv = page >= 0 ? a.v_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
+    };
+    fetch(0);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int b = j & 1;
+      if (j > 0) failed |= !wait_or_abort(&bars[kBarKFree], (j - 1) & 1, a.status, abort_flag);
 #pragma unroll
       for (int c16 = 0; c16 < D / 16; ++c16) {
         uint4 c0, c1;
@@ -762,33 +613,47 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
         sts128(blk + tc::sw128_off(t, cc), c0);
         sts128(blk + tc::sw128_off(t, cc + 1), c1);
       }
-      if ((t & 15) == 0) page_s[b * 8 + (t >> 4)] = page;
       if (j >= 2) failed |= !wait_or_abort(&bars[kBarScalesFree0 + b], ((j - 2) >> 1) & 1, a.status, abort_flag);
       scale_s[(b * 2 + 0) * 128 + t] = skv;
       scale_s[(b * 2 + 1) * 128 + t] = svv;
       tc::fence_proxy_async_smem();
       mbar_arrive(&bars[kBarKFull]);
-      // page_s of this tile is complete; all transform threads leave together on a failure
-      if (named_bar_or(2, kTransformThreads, failed)) break;
-      // V tile j: rows = head dims d = t, t + 128; 8 pages of 16 keys along K
+      if (j + 1 < n_tiles) fetch(j + 1);  // next tile's codes are in flight while we wait
+      if (named_bar_or(2, kTransformThreads, failed)) break;  // the group leaves together
+    }
+  } else if (warp < 16) {
+    // ================================================================ V transform warps
+    const int t = tid - kSoftmaxThreads - kTransformThreads;  // head dims t, t + 128
+    bool failed = false;
+    int4 vraw[D / 128][8];
+    auto fetch = [&](int j) {
+#pragma unroll
+      for (int pl = 0; pl < 8; ++pl) {
+        const int key0 = 128 * j + 16 * pl;
+        int pg = -1;
+        if (key0 < n_keys && key0 / KVQ_BLOCK_SIZE < a.n_blocks_row) {
+          pg = a.block_table_row[key0 / KVQ_BLOCK_SIZE];
+          if (pg < 0 || pg >= a.num_blocks) pg = -1;  // flagged by the K group
+        }
+        const long long vph = static_cast<long long>(pg < 0 ? 0 : pg) * a.n_kv_heads + kvh;
+#pragma unroll
+        for (int rr = 0; rr < D / 128; ++rr) {
+          const int d = t + 128 * rr;
+          vraw[rr][pl] = (pg >= 0) ? __ldg(reinterpret_cast<const int4*>(a.v + (vph * D + d) * KVQ_BLOCK_SIZE))
+                                   : make_int4(0, 0, 0, 0);
+        }
+      }
+    };
+    fetch(0);
+    for (int j = 0; j < n_tiles; ++j) {
       if (j > 0) failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
 #pragma unroll
       for (int rr = 0; rr < D / 128; ++rr) {
         const int d = t + 128 * rr;
-        int4 vraw[8];
-#pragma unroll
-        for (int pl = 0; pl < 8; ++pl) {
-          const int pg = page_s[b * 8 + pl];
-          vraw[pl] = make_int4(0, 0, 0, 0);
-          if (pg >= 0) {
-            const long long vph = static_cast<long long>(pg) * a.n_kv_heads + kvh;
-            vraw[pl] = __ldg(reinterpret_cast<const int4*>(a.v + (vph * D + d) * KVQ_BLOCK_SIZE));
-          }
-        }
 #pragma unroll
         for (int pl = 0; pl < 8; ++pl) {
           uint4 c0, c1;
-          widen16(vraw[pl], c0, c1);
+          widen16(vraw[rr][pl], c0, c1);
           uint8_t* blk = vs + (pl >> 2) * (D * 128);
           const int cc = (pl & 3) * 2;
           sts128(blk + tc::sw128_off(d, cc), c0);
@@ -797,6 +662,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       }
       tc::fence_proxy_async_smem();
       mbar_arrive(&bars[kBarVFull]);
+      if (j + 1 < n_tiles) fetch(j + 1);
+      if (named_bar_or(3, kTransformThreads, failed)) break;
     }
   } else if (lane == 0) {
     // ================================================================ MMA issue (one thread)
@@ -835,7 +702,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
 
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 12) {
+  if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, L::kTmemCols);
   }
