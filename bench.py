@@ -382,7 +382,8 @@ def _extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps, tflops):
     q = bf16(w["q"])
     T, Hq, D = w["n_tokens"], w["hq"], w["d"]
     out = torch.empty((T, Hq, D), dtype=torch.float32, device=dev)
-    ws = torch.empty(kvq.kvq_prefill_workspace_bytes(T, Hq, D), dtype=torch.uint8, device=dev)
+    ws = torch.empty(kvq.kvq_prefill_workspace_bytes(T, Hq, w["hkv"], w["history"], D), dtype=torch.uint8,
+                     device=dev)
     row = bt[0]
     ms = timed(lambda: kvq.kvq_attn_prefill_int8(cache, q, w["history"], row, w["softmax_scale"], out=out,
                                                   workspace=ws), reps)

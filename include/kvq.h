@@ -173,8 +173,14 @@ int kvq_attn_decode_int8kv_noalloc(const kvq_cache* cache, const void* q, int32_
                                    int32_t max_ctx, float softmax_scale, float* out,
                                    const kvq_decode_opts* opts, void* stream);
 
-/* Workspace (bytes) of kvq_attn_prefill_int8: the int8 Q codes and their fp32 scales. */
-size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t head_dim);
+/* Workspace (bytes) of kvq_attn_prefill_int8 for a chunk of n_tokens queries after
+ * history_len keys: the int8 Q codes and their fp32 scales, and the K/V codes of every
+ * (KV head, 128-key tile) of the history_len + n_tokens keys widened once to fp16 in the
+ * attention kernel's shared-memory operand layout (2 * 2 * head_dim bytes per key and KV
+ * head), with the tiles' key and value scales.  0 if an argument is not positive
+ * (history_len may be 0). */
+size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads,
+                                   int32_t history_len, int32_t head_dim);
 
 /*
  * kvq_attn_prefill_int8 — a chunk of n_tokens causal queries of one sequence against
@@ -194,7 +200,9 @@ size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t 
  *   q              : device bf16 [n_tokens][n_q_heads][head_dim]
  *   block_table_row: device int32 [n_blocks_row], covering history_len + n_tokens keys
  *   out            : device fp32 [n_tokens][n_q_heads][head_dim]
- *   workspace      : device, >= kvq_prefill_workspace_bytes(...), 16-byte aligned
+ *   softmax_scale  : finite and > 0, else KVQ_ERR_INVALID_ARG
+ *   workspace      : device, >= kvq_prefill_workspace_bytes(n_tokens, n_q_heads,
+ *                    cache->n_kv_heads, history_len, cache->head_dim), 16-byte aligned
  */
 int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_tokens,
                           int32_t n_q_heads, int32_t history_len,

@@ -1,6 +1,7 @@
 // api.cu — the C ABI of libkvq (include/kvq.h): host-side validation, routing and launch.
 // Every entry point checks its arguments before launching anything, allocates nothing and
 // never synchronises (except kvq_device_status).
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -187,9 +188,10 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   return cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSingle, static_cast<cudaStream_t>(stream)));
 }
 
-size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t head_dim) {
-  if (n_tokens <= 0 || n_q_heads <= 0 || head_dim <= 0) return 0;
-  return kvq::prefill_workspace_bytes(n_tokens, n_q_heads, head_dim);
+size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads, int32_t history_len,
+                                   int32_t head_dim) {
+  if (n_tokens <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || history_len < 0 || head_dim <= 0) return 0;
+  return static_cast<size_t>(kvq::prefill_workspace(n_tokens, n_q_heads, n_kv_heads, history_len, head_dim).bytes);
 }
 
 static kvq::PrefillArgs prefill_args(const kvq_cache* cache, const void* q, int32_t n_tokens,
@@ -212,9 +214,18 @@ static kvq::PrefillArgs prefill_args(const kvq_cache* cache, const void* q, int3
   a.n_blocks_row = n_blocks_row;
   a.softmax_scale = softmax_scale;
   a.out = out;
-  const long long codes = static_cast<long long>(n_tokens) * n_q_heads * cache->head_dim;
-  a.q_codes = static_cast<int8_t*>(workspace);
-  a.q_scales = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((codes + 255) / 256) * 256);
+  if (workspace) {
+    const kvq::PrefillWorkspace w =
+        kvq::prefill_workspace(n_tokens, n_q_heads, cache->n_kv_heads, history_len, cache->head_dim);
+    char* base = static_cast<char*>(workspace);
+    a.q_codes = reinterpret_cast<int8_t*>(base);
+    a.q_scales = reinterpret_cast<float*>(base + w.off_q_scales);
+    a.n_kv_tiles = w.n_kv_tiles;
+    a.kw = reinterpret_cast<uint8_t*>(base + w.off_kw);
+    a.vw = reinterpret_cast<uint8_t*>(base + w.off_vw);
+    a.skw = reinterpret_cast<float*>(base + w.off_skw);
+    a.svw = reinterpret_cast<float*>(base + w.off_svw);
+  }
   a.status = status_ptr();
   return a;
 }
@@ -228,10 +239,12 @@ int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_token
   if (!q || !block_table_row || !out) return KVQ_ERR_INVALID_ARG;
   if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
   if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (static_cast<long long>(history_len) + n_tokens > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
     return KVQ_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(out) || !aligned4(block_table_row)) return KVQ_ERR_MISALIGNED;
-  const size_t need = kvq::prefill_workspace_bytes(n_tokens, n_q_heads, cache->head_dim);
+  const size_t need = kvq_prefill_workspace_bytes(n_tokens, n_q_heads, cache->n_kv_heads, history_len,
+                                                  cache->head_dim);
   if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
   if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
   kvq::PrefillArgs a = prefill_args(cache, q, n_tokens, n_q_heads, history_len, block_table_row,

@@ -88,12 +88,23 @@ struct PrefillArgs {
   float* out;        // fp32 [T][Hq][D]
   int8_t* q_codes;   // workspace int8 [T][Hq][D]
   float* q_scales;   // workspace fp32 [T][Hq]
+  // workspace: K/V of every (KV head, 128-key tile) widened to the attention kernel's
+  // shared-memory operand image, and the tiles' key / value scales
+  int n_kv_tiles;
+  uint8_t* kw;       // [Hkv][n_kv_tiles][D/64 pieces of 16 KB]
+  uint8_t* vw;       // [Hkv][n_kv_tiles][D/64 pieces of 16 KB]
+  float* skw;        // [Hkv][n_kv_tiles][128]
+  float* svw;        // [Hkv][n_kv_tiles][128]
   unsigned int* status;
   // debug QK tile (kvq_debug_prefill_qk_int32)
   int dbg_q_head, dbg_q0, dbg_k0, dbg_nk;
   int32_t* dbg_s_out;
 };
-size_t prefill_workspace_bytes(int n_tokens, int n_q_heads, int head_dim);
+struct PrefillWorkspace {
+  int n_kv_tiles;
+  long long off_q_scales, off_kw, off_vw, off_skw, off_svw, bytes;
+};
+PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim);
 cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_qk_debug(const PrefillArgs& a, cudaStream_t stream);

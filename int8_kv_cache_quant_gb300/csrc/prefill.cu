@@ -168,13 +168,15 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
   return r;
 }
 
-// exp2_det of a pair, the same operations per element: x < -125 -> 0, x > 125 clamped;
+// exp2_det of a pair, the same operations per element, for arguments x <= 0 up to one rounding
+// (the attention kernels pass x = fma(y, a, -m) with m >= fl(ymax * a) >= fl(y * a) and a >= 0,
+// so the specified clamp at +125 never acts and is left out): x < -125 (or NaN) -> 0;
 // n = rint(x) through the 1.5 * 2^23 magic sum t, f = x - n (exact, as one fma), the degree-5
-// Horner polynomial, and the factor 2^n built from t's bits: bits(t) = 0x4B400000 + n, so
-// bits(t) * 2^23 + (127 - 0x4B400000) * 2^23 = (n + 127) << 23 (mod 2^32), one integer multiply-add.
-__device__ __forceinline__ f2 exp2_det2(float x0, float x1) {
-  const bool v0 = x0 >= -125.0f, v1 = x1 >= -125.0f;
-  const f2 x = mk2(fminf(x0, 125.0f), fminf(x1, 125.0f));
+// Horner polynomial p = 2^f in [0.70, 1.42], and p * 2^n as an exponent-field add: the product
+// is normal for n in [-125, 0], so it equals bits(p) + n * 2^23, and n * 2^23 == bits(t) * 2^23
+// (mod 2^32) because bits(t) = 0x4B400000 + n and 0x4B400000 * 2^23 == 0 (mod 2^32).
+__device__ __forceinline__ f2 exp2_det2(f2 x) {
+  const bool v0 = lo2(x) >= -125.0f, v1 = hi2(x) >= -125.0f;
   const f2 t = add2(x, mk2(kMagic, kMagic));
   const f2 n = add2(t, mk2(-kMagic, -kMagic));
   const f2 f = fma2(n, mk2(-1.0f, -1.0f), x);
@@ -183,11 +185,9 @@ __device__ __forceinline__ f2 exp2_det2(float x0, float x1) {
   p = fma2(p, f, mk2(0.240226506959101f, 0.240226506959101f));
   p = fma2(p, f, mk2(0.693147180559945f, 0.693147180559945f));
   p = fma2(p, f, mk2(1.0f, 1.0f));
-  constexpr uint32_t kExpBias = (127u - 0x4B400000u) << 23;
-  const uint32_t s0 = __float_as_uint(lo2(t)) * (1u << 23) + kExpBias;
-  const uint32_t s1 = __float_as_uint(hi2(t)) * (1u << 23) + kExpBias;
-  p = mul2(p, mk2(__uint_as_float(s0), __uint_as_float(s1)));
-  return mk2(v0 ? lo2(p) : 0.0f, v1 ? hi2(p) : 0.0f);
+  const uint32_t r0 = __float_as_uint(lo2(p)) + (__float_as_uint(lo2(t)) << 23);
+  const uint32_t r1 = __float_as_uint(hi2(p)) + (__float_as_uint(hi2(t)) << 23);
+  return mk2(v0 ? __uint_as_float(r0) : 0.0f, v1 ? __uint_as_float(r1) : 0.0f);
 }
 
 // 16 int8 codes (one int4) -> two 16-byte chunks of 8 fp16 (exact integer values).
@@ -282,53 +282,147 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 }  // namespace
 
-// ============================================================================ warp-specialised prefill
-// One CTA per (128 query rows, query head), 17 warps:
-//   warps 0-7   softmax: thread (row r, half h) owns keys 64h .. 64h+63 of row r's S row and O
-//               columns 128h .. 128h+127 (head_dim 256; 64h .. for 128); the two halves of a row
-//               exchange their partial maxima through shared memory at named barrier 1.
-//   warps 8-11  K transform: Q once, then per tile the K tile (int8 from the cache, widened to
-//               fp16, 128-byte-swizzled K-major in shared memory) and the tile's key/value scales.
-//   warps 12-15 V transform: per tile the V tile.  Both transform groups load the next tile's
-//               codes into registers before they wait for their shared-memory buffer.
-//   warp 16     MMA issue (lane 0) and tensor-memory allocation.
-// Tensor memory: S0 | S1 (128 columns each, double-buffered) | O (head_dim columns).  P (fp16,
-// 64 columns) is written back over the first 64 columns of its S buffer and read by the PV MMA
-// as its A operand; the next QK into that buffer is issued after that PV, and one thread's
-// tcgen05.mma operations execute in issue order.
-// Per tile j (buffer b = j % 2):  MMA: QK_j (after k_full) -> commit s_full[b], k_free; then
-// PV_{j-1} (after p_full, v_full) -> commit pv_done.  Transform: K_j after k_free(j-1), scales
-// after scales_free(j-2), V_j after pv_done(j-1).  Softmax: S_j after s_full[b]; P_j and the O
-// rescale after pv_done(j-1) -> arrive p_full.
-namespace {
+// ============================================================================ K/V widening pre-pass
+// The attention kernel reads every K/V tile of its KV head once per (query tile, query head);
+// widening the int8 codes to fp16 there would repeat the same work for every query head of the
+// group and every query tile.  So one pass per prefill call widens each (KV head, 128-key tile)
+// once, into the exact byte image of the attention kernel's shared-memory operands (128-byte
+// swizzle, K-major), cut into 16 KB pieces that one bulk copy each brings in:
+//   K tile: piece a (a < D/64) = head dims 64a .. 64a+63 of the 128 keys (rows = keys);
+//   V tile: piece kh * (D/128) + dh = keys 64kh .. 64kh+63 (the K extent of the PV MMA) of head
+//           dims 128dh .. 128dh+127 (rows = dims);
+// plus the tile's key and value scales (fp32 [128] each).  Keys at or past the context, and keys
+// on pages outside the pool, get zero codes and zero scales.
+constexpr int kPieceBytes = 16384;
 
 template <int D>
-struct PrefillWsSmem {
-  static constexpr int kQ = 128 * D * 2;
-  static constexpr int kK = 128 * D * 2;
-  static constexpr int kV = D * 128 * 2;
-  static constexpr int offQ = 0;
-  static constexpr int offK = offQ + kQ;
-  static constexpr int offV = offK + kK;
-  static constexpr int offScale = offV + kV;        // [2 buffers][2: k, v][128] float
-  static constexpr int offRed = offScale + 2 * 2 * 128 * 4;  // [2 exchanges][2 halves][128] float
-  static constexpr int offPage = offRed + 2 * 2 * 128 * 4;   // [2 buffers][8] int
-  static constexpr int offBar = offPage + 2 * 8 * 4;         // 10 mbarriers
-  static constexpr int offFlag = offBar + 10 * 8;             // abort flag, TMEM base
+__global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
+  grid_dep_wait();  // the chunk's own K/V were written by the previous kernels of the stream
+  const int j = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x;
+  const int n_keys = a.history_len + a.n_tokens;
+  __shared__ int page_s[8];
+  if (tid < 8) {
+    const int key0 = 128 * j + 16 * tid;
+    int page = -1;
+    if (key0 < n_keys) {
+      const int bi = key0 / KVQ_BLOCK_SIZE;
+      if (bi < a.n_blocks_row) page = a.block_table_row[bi];
+      if (page < 0 || page >= a.num_blocks) {
+        set_status(a.status, KVQ_DEV_BAD_BLOCK);
+        page = -1;
+      }
+    }
+    page_s[tid] = page;
+  }
+  __syncthreads();
+  const long long tile = static_cast<long long>(kvh) * a.n_kv_tiles + j;
+  uint8_t* kdst = a.kw + tile * (D / 64) * kPieceBytes;
+  uint8_t* vdst = a.vw + tile * (D / 64) * kPieceBytes;
+  // K: item i = (16-dim chunk c16 = i / 128, key n = i % 128); one key's chunk is 16 bytes of
+  // the [page][head][D/16][slot][16] cache block.
+  for (int i = tid; i < 128 * (D / 16); i += 256) {
+    const int n = i & 127, c16 = i >> 7;
+    const int page = page_s[n >> 4];
+    int4 raw = make_int4(0, 0, 0, 0);
+    if (page >= 0 && 128 * j + n < n_keys)
+      raw = __ldg(reinterpret_cast<const int4*>(
+          a.k + ((static_cast<long long>(page) * a.n_kv_heads + kvh) * (D / 16) + c16) * 256 + (n & 15) * 16));
+    uint4 c0, c1;
+    widen16(raw, c0, c1);
+    uint8_t* piece = kdst + (c16 >> 2) * kPieceBytes;
+    const int cc = (c16 & 3) * 2;
+    sts128(piece + tc::sw128_off(n, cc), c0);  // global stores (same helper, generic address)
+    sts128(piece + tc::sw128_off(n, cc + 1), c1);
+  }
+  // V: item i = (page pl = i / D, dim d = i % D); the 16 keys of page pl for dim d are 16
+  // bytes of the [page][head][D][slot] cache block.  Keys past the context carry whatever the
+  // slot holds: their P codes are zero, and int8 codes are finite, so they add nothing.
+  for (int i = tid; i < 8 * D; i += 256) {
+    const int d = i % D, pl = i / D;
+    const int page = page_s[pl];
+    int4 raw = make_int4(0, 0, 0, 0);
+    if (page >= 0)
+      raw = __ldg(reinterpret_cast<const int4*>(
+          a.v + ((static_cast<long long>(page) * a.n_kv_heads + kvh) * D + d) * KVQ_BLOCK_SIZE));
+    uint4 c0, c1;
+    widen16(raw, c0, c1);
+    uint8_t* piece = vdst + ((pl >> 2) * (D / 128) + (d >> 7)) * kPieceBytes;
+    const int cc = (pl & 3) * 2;
+    sts128(piece + tc::sw128_off(d & 127, cc), c0);
+    sts128(piece + tc::sw128_off(d & 127, cc + 1), c1);
+  }
+  if (tid < 128) {
+    const int n = tid, page = page_s[n >> 4];
+    float sk = 0.0f, sv = 0.0f;
+    if (page >= 0 && 128 * j + n < n_keys) {
+      const long long idx = (static_cast<long long>(page) * a.n_kv_heads + kvh) * KVQ_BLOCK_SIZE + (n & 15);
+      sk = a.k_scale[idx];
+      sv = a.v_scale[idx];
+    }
+    a.skw[tile * 128 + n] = sk;
+    a.svw[tile * 128 + n] = sv;
+  }
+  // Only now: an attention CTA made resident early would hold most of an SM's registers while
+  // it waits for this grid.
+  grid_dep_trigger();
+}
+
+// ============================================================================ warp-specialised prefill
+// One CTA per (128 query rows, query head), 18 warps:
+//   warps 0-15  softmax: thread (row r, part p = warp / 4) owns keys 32p .. 32p+31 of row r's S
+//               row and O columns p*D/4 .. (p+1)*D/4 - 1; the four parts of a row (warps w, w+4,
+//               w+8, w+12: the same tensor-memory lanes) exchange their partial maxima through
+//               shared memory at their own named barrier.  They also widen Q at the start.
+//   warp 16     MMA issue (lane 0) and tensor-memory allocation.
+//   warp 17     bulk-copy producer (lane 0): the widened K/V pieces through a ring of 16 KB
+//               shared-memory slots in the order the MMAs consume them, and the scales.
+// Tensor memory: S0 | S1 (128 columns each, double-buffered) | O (head_dim columns).  P codes
+// (fp16, 64 columns) are written back over the first 64 columns of their S buffer and read by
+// the PV MMA as its A operand; the next QK into that buffer is issued after that PV, and one
+// thread's tcgen05.mma operations execute in issue order.
+// A P code c is stored as the fp16 bit pattern c, i.e. the subnormal c * 2^-24: its two bytes
+// come straight from the rounding sum fma(w, r, 1.5 * 2^23), whose low byte is c.  The products
+// c * v * 2^-24 and their sums are exact in fp32 (a power-of-two scaling of the integer sums), so
+// O holds 2^-24 * sum_tiles (ps_tile / ps_ref) * PV_tile, and the epilogue multiplies by 2^24.
+// Per tile j (S buffer b = j % 2): MMA: QK_j (pieces of K_j) -> commit s_full[b]; then PV_{j-1}
+// (after p_full, pieces of V_{j-1}) -> commit pv_done; every piece's slot is released by a commit
+// after its MMAs.  Softmax: S_j after s_full[b] and the scales; P_j and the O rescale after
+// pv_done(j-1) -> arrive p_full.
+namespace {
+
+constexpr int kRingSlots = 9;
+constexpr int kScaleBufs = 4;
+
+template <int D>
+struct PrefillTmaSmem {
+  static constexpr int offQ = 0;                                        // D/64 pieces
+  static constexpr int offRing = offQ + (D / 64) * kPieceBytes;         // kRingSlots pieces
+  static constexpr int offScale = offRing + kRingSlots * kPieceBytes;   // [buf][k, v][128] fp32
+  static constexpr int offRed = offScale + kScaleBufs * 2 * 128 * 4;    // [exchange][part][128]
+  static constexpr int offBar = offRed + 2 * 4 * 128 * 4;
+  static constexpr int kNumBars = 2 * kRingSlots + 2 * kScaleBufs + 6;
+  static constexpr int offFlag = offBar + kNumBars * 8;                 // abort flag, TMEM base
   static constexpr int kBytes = offFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O (head_dim columns)
-  static constexpr uint32_t kOCol = 256;      // after S0 | S1
+  static constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O
+  static constexpr uint32_t kOCol = 256;
 };
 
-// kBarScalesFree0/1: per scale buffer, so that no waiter can fall two phases behind.
-enum { kBarKFull = 0, kBarVFull, kBarS0, kBarS1, kBarKFree, kBarPvDone, kBarPFull, kBarScalesFree0,
-       kBarScalesFree1 };
+// mbarrier indices
+constexpr int kBarFull = 0;                            // [kRingSlots] piece landed (tx)
+constexpr int kBarEmpty = kBarFull + kRingSlots;       // [kRingSlots] piece consumed (commit)
+constexpr int kBarSclFull = kBarEmpty + kRingSlots;    // [kScaleBufs] scales landed (tx)
+constexpr int kBarSclFree = kBarSclFull + kScaleBufs;  // [kScaleBufs] scales read (softmax)
+constexpr int kBarS0 = kBarSclFree + kScaleBufs;       // S_j complete, buffer 0 / 1
+constexpr int kBarPvDone = kBarS0 + 2;
+constexpr int kBarPFull = kBarPvDone + 1;
+constexpr int kBarQFull = kBarPFull + 1;
+constexpr int kBarDrain = kBarQFull + 1;
 
-constexpr int kSoftmaxThreads = 256;
-constexpr int kTransformThreads = 128;  // per transform group (K group, V group)
-constexpr int kPrefillThreads = kSoftmaxThreads + 2 * kTransformThreads + 32;
-constexpr int kMmaWarp = (kSoftmaxThreads + 2 * kTransformThreads) / 32;
+constexpr int kSoftmaxThreads = 512;
+constexpr int kMmaWarp = kSoftmaxThreads / 32;
+constexpr int kProducerWarp = kMmaWarp + 1;
+constexpr int kPrefillThreads = kSoftmaxThreads + 64;
 
 // Bounded wait that also gives up as soon as another thread of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned int* status,
@@ -363,20 +457,29 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
   return r != 0;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__device__ __forceinline__ float max4_col(const float* p, int row) {
+  return fmaxf(fmaxf(p[row], p[128 + row]), fmaxf(p[256 + row], p[384 + row]));
+}
+
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillArgs a) {
-  using L = PrefillWsSmem<D>;
-  constexpr int OCOLS_H = D / 2;  // O columns per softmax thread
+__global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(PrefillArgs a) {
+  using L = PrefillTmaSmem<D>;
+  constexpr int OCOLS = D / 4;   // O columns per softmax thread
+  constexpr int NP = D / 64;     // pieces per K tile and per V tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* qs = sm + L::offQ;
-  uint8_t* ks = sm + L::offK;
-  uint8_t* vs = sm + L::offV;
+  uint8_t* ring = sm + L::offRing;
   float* scale_s = reinterpret_cast<float*>(sm + L::offScale);  // [buf][0: k, 1: v][128]
-  float* red = reinterpret_cast<float*>(sm + L::offRed);        // [exchange][half][128]
-  int* page_s = reinterpret_cast<int*>(sm + L::offPage);        // [buf][8]
+  float* red = reinterpret_cast<float*>(sm + L::offRed);        // [exchange][part][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::offBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::offFlag);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offFlag + 4);
@@ -389,19 +492,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
   const int n_keys = a.history_len + T;
   const int last_pos = a.history_len + min(q0 + 127, T - 1);
   const int n_tiles = last_pos / 128 + 1;
+  const long long tile0 = static_cast<long long>(kvh) * a.n_kv_tiles;  // first tile of this head
 
-  grid_dep_wait();  // Q codes and scales come from the quantisation kernel
+  grid_dep_wait();  // Q codes, widened K/V and scales come from the preceding kernels
   if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, L::kTmemCols);
   if (tid == 0) {
-    mbar_init(&bars[kBarKFull], kTransformThreads);
-    mbar_init(&bars[kBarVFull], kTransformThreads);
+    for (int s = 0; s < kRingSlots; ++s) {
+      mbar_init(&bars[kBarFull + s], 1);
+      mbar_init(&bars[kBarEmpty + s], 1);
+    }
+    for (int s = 0; s < kScaleBufs; ++s) {
+      mbar_init(&bars[kBarSclFull + s], 1);
+      mbar_init(&bars[kBarSclFree + s], kSoftmaxThreads);
+    }
     mbar_init(&bars[kBarS0], 1);
-    mbar_init(&bars[kBarS1], 1);
-    mbar_init(&bars[kBarKFree], 1);
+    mbar_init(&bars[kBarS0 + 1], 1);
     mbar_init(&bars[kBarPvDone], 1);
     mbar_init(&bars[kBarPFull], kSoftmaxThreads);
-    mbar_init(&bars[kBarScalesFree0], kSoftmaxThreads);
-    mbar_init(&bars[kBarScalesFree1], kSoftmaxThreads);
+    mbar_init(&bars[kBarQFull], kSoftmaxThreads);
+    mbar_init(&bars[kBarDrain], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -410,74 +519,88 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 8) {
+  if (warp < kMmaWarp) {
     // ================================================================ softmax warps
-    const int row = tid & 127, half = tid >> 7;
+    const int row = tid & 127, part = tid >> 7;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int gbar = 1 + (warp & 3);  // named barrier of the four warps on these lanes
     const bool row_real = q0 + row < T;
     const int pos_r = a.history_len + q0 + row;
+    {
+      // Q: this thread's D/64 16-code chunks of its row, widened into the swizzled Q operand
+      const int8_t* src = a.q_codes + (static_cast<long long>(q0 + row) * Hq + h) * D;
+#pragma unroll
+      for (int i = 0; i < NP; ++i) {
+        const int c16 = part * NP + i;
+        int4 raw = make_int4(0, 0, 0, 0);
+        if (row_real) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
+        uint4 c0, c1;
+        widen16(raw, c0, c1);
+        uint8_t* piece = qs + (c16 >> 2) * kPieceBytes;
+        const int cc = (c16 & 3) * 2;
+        sts128(piece + tc::sw128_off(row, cc), c0);
+        sts128(piece + tc::sw128_off(row, cc + 1), c1);
+      }
+      tc::fence_proxy_async_smem();
+      mbar_arrive(&bars[kBarQFull]);
+    }
     const float c2 = __fmul_rn(a.softmax_scale, kLog2eP);
     const float a_row = row_real ? __fmul_rn(a.q_scales[static_cast<long long>(q0 + row) * Hq + h], c2) : 0.0f;
     float m = -INFINITY, l_part = 0.0f, ps_ref = 0.0f;
     bool started = false;
-    const uint32_t tm_o = tmem + lane_base + L::kOCol + half * OCOLS_H;
+    const uint32_t tm_o = tmem + lane_base + L::kOCol + part * OCOLS;
     {
       uint32_t z[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) z[i] = 0u;
 #pragma unroll
-      for (int c = 0; c < OCOLS_H / 32; ++c) tc::st_32x32b_x32(tm_o + 32 * c, z);
+      for (int c = 0; c < OCOLS / 32; ++c) tc::st_32x32b_x32(tm_o + 32 * c, z);
       tc::wait_st();
     }
-    float* red_max = red;                  // exchange 1: [half][row]
-    float* red_wmax = red + 2 * 128;       // exchange 2
+    float* red_max = red;             // exchange 1: [part][row]
+    float* red_wmax = red + 4 * 128;  // exchange 2
     bool failed = false;  // a wait of this thread gave up; the group leaves together below
     for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
+      const int b = j & 1, sb = j & (kScaleBufs - 1);
       failed |= !wait_or_abort(&bars[kBarS0 + b], (j >> 1) & 1, a.status, abort_flag);
       tc::fence_after_sync();
-      const uint32_t tm_s = tmem + lane_base + b * 128 + half * 64;
-      uint32_t sv[64];
-      tc::ld_32x32b_x32(tm_s, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tc::ld_32x32b_x32(tm_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      uint32_t sv[32];
+      tc::ld_32x32b_x32(tmem + lane_base + b * 128 + 32 * part, sv);
+      failed |= !wait_or_abort(&bars[kBarSclFull + sb], (j / kScaleBufs) & 1, a.status, abort_flag);
       tc::wait_ld();
-      const float4* sk_t = reinterpret_cast<const float4*>(scale_s + (b * 2 + 0) * 128 + half * 64);
-      const float4* sv_t = reinterpret_cast<const float4*>(scale_s + (b * 2 + 1) * 128 + half * 64);
-      // visible keys of this row in this tile, counted from the start of this thread's half
-      const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128) - half * 64;
-      float ymax0 = -INFINITY, ymax1 = -INFINITY;
+      const float4* sk_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 0) * 128 + 32 * part);
+      const float4* sv_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 1) * 128 + 32 * part);
+      // visible keys of this row in this tile, counted from the start of this thread's part
+      const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128) - 32 * part;
+      float ymax = -INFINITY;
 #pragma unroll
-      for (int n = 0; n < 64; n += 4) {
+      for (int n = 0; n < 32; n += 4) {
         const float4 k4 = sk_t[n >> 2];
         const f2 ya = mul2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), mk2(k4.x, k4.y));
         const f2 yb = mul2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), mk2(k4.z, k4.w));
         float y[4] = {lo2(ya), hi2(ya), lo2(yb), hi2(yb)};
-        if (lim < 64) {  // only tiles on the diagonal or past the context carry masked keys
+        if (lim < 32) {  // only tiles on the diagonal or past the context carry masked keys
 #pragma unroll
           for (int e = 0; e < 4; ++e) y[e] = (n + e < lim) ? y[e] : -INFINITY;
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) sv[n + e] = __float_as_uint(y[e]);
-        ymax0 = fmaxf(ymax0, fmaxf(y[0], y[1]));
-        ymax1 = fmaxf(ymax1, fmaxf(y[2], y[3]));
+        ymax = fmax3(ymax, fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
       }
-      red_max[half * 128 + row] = fmaxf(ymax0, ymax1);
+      red_max[part * 128 + row] = ymax;
       tc::fence_before_sync();
-      if (named_bar_or(1, kSoftmaxThreads, failed)) break;  // all softmax threads leave together
+      if (named_bar_or(gbar, 128, failed)) break;  // the four parts of these rows leave together
       tc::fence_after_sync();
-      const float ymax = fmaxf(red_max[row], red_max[128 + row]);
-      const float m_new = fmaxf(m, __fmul_rn(ymax, a_row));
+      const float m_new = fmaxf(m, __fmul_rn(max4_col(red_max, row), a_row));
       const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
       f2 psum = mk2(0.0f, 0.0f);
-      float wmax0 = 0.0f, wmax1 = 0.0f;
+      float wmax = 0.0f;
       const f2 a2 = mk2(a_row, a_row), nm2 = mk2(-m_new, -m_new);
 #pragma unroll
-      for (int n = 0; n < 64; n += 4) {
+      for (int n = 0; n < 32; n += 4) {
         const float4 v4 = sv_t[n >> 2];
-        const f2 xa = fma2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), a2, nm2);
-        const f2 xb = fma2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), a2, nm2);
-        const f2 pa = exp2_det2(lo2(xa), hi2(xa));
-        const f2 pb = exp2_det2(lo2(xb), hi2(xb));
+        const f2 pa = exp2_det2(fma2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), a2, nm2));
+        const f2 pb = exp2_det2(fma2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), a2, nm2));
         psum = add2(psum, add2(pa, pb));
         const f2 wa = mul2(pa, mk2(v4.x, v4.y));
         const f2 wb = mul2(pb, mk2(v4.z, v4.w));
@@ -485,22 +608,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
         sv[n + 1] = __float_as_uint(hi2(wa));
         sv[n + 2] = __float_as_uint(lo2(wb));
         sv[n + 3] = __float_as_uint(hi2(wb));
-        wmax0 = fmaxf(wmax0, fmaxf(lo2(wa), hi2(wa)));
-        wmax1 = fmaxf(wmax1, fmaxf(lo2(wb), hi2(wb)));
+        wmax = fmax3(wmax, lo2(wa), hi2(wa));
+        wmax = fmax3(wmax, lo2(wb), hi2(wb));
       }
-      mbar_arrive(&bars[kBarScalesFree0 + b]);  // this tile's scales are no longer read
+      mbar_arrive(&bars[kBarSclFree + sb]);  // this tile's scales are no longer read
       l_part = l_part * alpha + (lo2(psum) + hi2(psum));
       m = m_new;
-      red_wmax[half * 128 + row] = fmaxf(wmax0, wmax1);
-      tc::fence_before_sync();  // both halves have read their S before either writes P over it
-      named_bar(1, kSoftmaxThreads);
+      red_wmax[part * 128 + row] = wmax;
+      tc::fence_before_sync();  // every part has read its S before any writes P over it
+      named_bar(gbar, 128);
       tc::fence_after_sync();
-      const float wmax = fmaxf(red_wmax[row], red_wmax[128 + row]);
+      const float wmax_row = max4_col(red_wmax, row);
       // reference scale of O and the factor that moves O onto this tile's P scale (the same
-      // decisions in both halves of the row)
+      // decisions in all four parts of the row)
       float f = 1.0f;
-      bool codes_on = wmax > 0.0f;
-      const float ps_new = __fdiv_rn(wmax, 127.0f);
+      bool codes_on = wmax_row > 0.0f;
+      const float ps_new = __fdiv_rn(wmax_row, 127.0f);
       if (!started) {
         if (codes_on) {
           started = true;
@@ -518,29 +641,35 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       } else {
         ps_ref *= alpha;
       }
-      const float rr = codes_on ? __fdiv_rn(127.0f, wmax) : 0.0f;
-      uint32_t pk[32];
-      const f2 r2 = mk2(rr, rr), mg = mk2(kMagic, kMagic), nmg = mk2(-kMagic, -kMagic);
+      // c = rint(w * r) with one rounding, as the low byte of fma(w, r, 1.5 * 2^23) (w <= wmax
+      // keeps c in [0, 127]; r = 0 gives c = 0); two codes per 32-bit column
+      const float rr = codes_on ? __fdiv_rn(127.0f, wmax_row) : 0.0f;
+      uint32_t pk[16];
+      const f2 r2 = mk2(rr, rr), mg = mk2(kMagic, kMagic);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        // rint(w * r) with one rounding; w <= wmax keeps it in [0, 127]
-        const f2 c = add2(fma2(mk2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), r2, mg), nmg);
-        pk[e] = codes_on ? pack_half2(lo2(c), hi2(c)) : 0u;
+      for (int e = 0; e < 16; ++e) {
+        const f2 c = fma2(mk2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), r2, mg);
+        pk[e] = __byte_perm(__float_as_uint(lo2(c)), __float_as_uint(hi2(c)), 0x5410u);
       }
       // O must hold PV_{j-1} before it is rescaled (and P_{j-1} must be consumed: it is)
       if (j > 0) {
         failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
         tc::fence_after_sync();
       }
-      tc::st_32x32b_x32(tmem + lane_base + b * 128 + half * 32, pk);  // P over S's first 64 columns
+      tc::st_32x32b_x16(tmem + lane_base + b * 128 + 16 * part, pk);  // P over S's first 64 columns
       if (__any_sync(0xffffffffu, f != 1.0f)) {
+        const f2 f2v = mk2(f, f);
 #pragma unroll
-        for (int c = 0; c < OCOLS_H / 32; ++c) {
+        for (int c = 0; c < OCOLS / 32; ++c) {
           uint32_t o[32];
           tc::ld_32x32b_x32(tm_o + 32 * c, o);
           tc::wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+          for (int e = 0; e < 32; e += 2) {
+            const f2 r = mul2(mk2(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), f2v);
+            o[e] = __float_as_uint(lo2(r));
+            o[e + 1] = __float_as_uint(hi2(r));
+          }
           tc::st_32x32b_x32(tm_o + 32 * c, o);
         }
       }
@@ -548,156 +677,137 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_ws_kernel(PrefillA
       tc::fence_before_sync();
       mbar_arrive(&bars[kBarPFull]);
     }
-    // ---- epilogue: out = O * ps_ref / l (l summed over both halves)
+    // ---- epilogue: out = O * 2^24 * ps_ref / l (l summed over the four parts)
     if (!*abort_flag) {
       wait_or_abort(&bars[kBarPvDone], (n_tiles - 1) & 1, a.status, abort_flag);
       tc::fence_after_sync();
     }
-    red_max[half * 128 + row] = l_part;
-    named_bar(1, kSoftmaxThreads);
-    const float l = red_max[row] + red_max[128 + row];
+    red_max[part * 128 + row] = l_part;
+    named_bar(gbar, 128);
+    const float l = (red_max[row] + red_max[128 + row]) + (red_max[256 + row] + red_max[384 + row]);
     const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
 #pragma unroll
-    for (int c = 0; c < OCOLS_H / 32; ++c) {
+    for (int c = 0; c < OCOLS / 32; ++c) {
       uint32_t o[32];
       tc::ld_32x32b_x32(tm_o + 32 * c, o);
       tc::wait_ld();
       if (row_real) {
-        float* dst = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + half * OCOLS_H + 32 * c;
+        float* dst = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + part * OCOLS + 32 * c;
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + e) =
-              make_float4(__uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
-                          __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
+          *reinterpret_cast<float4*>(dst + e) = make_float4(
+              __uint_as_float(o[e]) * 16777216.0f * sc, __uint_as_float(o[e + 1]) * 16777216.0f * sc,
+              __uint_as_float(o[e + 2]) * 16777216.0f * sc, __uint_as_float(o[e + 3]) * 16777216.0f * sc);
       }
     }
-  } else if (warp < 12) {
-    // ================================================================ K transform warps
-    const int t = tid - kSoftmaxThreads;  // 0..127: key t of each tile
-    load_q_tile<D>(qs, a.q_codes, T, Hq, h, q0, t);
-    bool failed = false;  // a wait of this thread gave up; the group leaves together below
-    int4 raw[D / 16];
-    float skv = 0.0f, svv = 0.0f;
-    int page = -1;
-    // codes and scales of key t of tile j into registers
-    auto fetch = [&](int j) {
-      const int key = 128 * j + t;
-      page = -1;
-      if (key < n_keys) {
-        const int bi = key / KVQ_BLOCK_SIZE;
-        if (bi < a.n_blocks_row) page = a.block_table_row[bi];
-        if (page < 0 || page >= a.num_blocks) {
-          if ((key & 15) == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
-          page = -1;
+  } else if (warp == kMmaWarp) {
+    // ================================================================ MMA issue (one thread)
+    if (lane == 0) {
+      const uint32_t qs_a = smem_u32(qs), ring_a = smem_u32(ring);
+      constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
+      const uint32_t tm_o = tmem + L::kOCol;
+      int slot = 0;
+      uint32_t ph = 0;
+      bool ok = wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag);
+      tc::fence_after_sync();
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles) {
+          const int b = j & 1;
+          for (int qa = 0; ok && qa < NP; ++qa) {
+            ok = wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const uint32_t kp = ring_a + slot * kPieceBytes, qp = qs_a + qa * kPieceBytes;
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              tc::mma_f16_ss(tmem + b * 128, tc::sdesc_sw128(qp + 32 * s), tc::sdesc_sw128(kp + 32 * s), idesc,
+                             (qa | s) ? 1u : 0u);
+            tc::commit(&bars[kBarEmpty + slot]);
+            if (++slot == kRingSlots) {
+              slot = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc::commit(&bars[kBarS0 + b]);
+        }
+        if (j >= 1) {
+          const int jp = j - 1, bp = jp & 1;
+          ok = wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag);
+          if (!ok) break;
+          tc::fence_after_sync();
+          for (int qv = 0; ok && qv < NP; ++qv) {
+            const int kh = qv / (D / 128), dh = qv % (D / 128);
+            ok = wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag);
+            if (!ok) break;
+            tc::fence_after_sync();
+            const uint32_t vp = ring_a + slot * kPieceBytes;
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              tc::mma_f16_ts(tm_o + 128 * dh, tmem + bp * 128 + 32 * kh + 8 * s, tc::sdesc_sw128(vp + 32 * s), idesc,
+                             1u);
+            tc::commit(&bars[kBarEmpty + slot]);
+            if (++slot == kRingSlots) {
+              slot = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc::commit(&bars[kBarPvDone]);
         }
       }
-      const long long ph = static_cast<long long>(page < 0 ? 0 : page) * a.n_kv_heads + kvh;
-      const int slot = key & 15;
-      const int8_t* src = a.k + ph * D * KVQ_BLOCK_SIZE + slot * 16;
-#pragma unroll
-      for (int c16 = 0; c16 < D / 16; ++c16)
-        raw[c16] = (page >= 0) ? __ldg(reinterpret_cast<const int4*>(src + c16 * 256)) : make_int4(0, 0, 0, 0);
-      skv = page >= 0 ? a.k_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
-      svv = page >= 0 ? a.v_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
-    };
-    fetch(0);
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      if (j > 0) failed |= !wait_or_abort(&bars[kBarKFree], (j - 1) & 1, a.status, abort_flag);
-#pragma unroll
-      for (int c16 = 0; c16 < D / 16; ++c16) {
-        uint4 c0, c1;
-        widen16(raw[c16], c0, c1);
-        uint8_t* blk = ks + (c16 >> 2) * (128 * 128);
-        const int cc = (c16 & 3) * 2;
-        sts128(blk + tc::sw128_off(t, cc), c0);
-        sts128(blk + tc::sw128_off(t, cc + 1), c1);
-      }
-      if (j >= 2) failed |= !wait_or_abort(&bars[kBarScalesFree0 + b], ((j - 2) >> 1) & 1, a.status, abort_flag);
-      scale_s[(b * 2 + 0) * 128 + t] = skv;
-      scale_s[(b * 2 + 1) * 128 + t] = svv;
-      tc::fence_proxy_async_smem();
-      mbar_arrive(&bars[kBarKFull]);
-      if (j + 1 < n_tiles) fetch(j + 1);  // next tile's codes are in flight while we wait
-      if (named_bar_or(2, kTransformThreads, failed)) break;  // the group leaves together
-    }
-  } else if (warp < 16) {
-    // ================================================================ V transform warps
-    const int t = tid - kSoftmaxThreads - kTransformThreads;  // head dims t, t + 128
-    bool failed = false;
-    int4 vraw[D / 128][8];
-    auto fetch = [&](int j) {
-#pragma unroll
-      for (int pl = 0; pl < 8; ++pl) {
-        const int key0 = 128 * j + 16 * pl;
-        int pg = -1;
-        if (key0 < n_keys && key0 / KVQ_BLOCK_SIZE < a.n_blocks_row) {
-          pg = a.block_table_row[key0 / KVQ_BLOCK_SIZE];
-          if (pg < 0 || pg >= a.num_blocks) pg = -1;  // flagged by the K group
-        }
-        const long long vph = static_cast<long long>(pg < 0 ? 0 : pg) * a.n_kv_heads + kvh;
-#pragma unroll
-        for (int rr = 0; rr < D / 128; ++rr) {
-          const int d = t + 128 * rr;
-          vraw[rr][pl] = (pg >= 0) ? __ldg(reinterpret_cast<const int4*>(a.v + (vph * D + d) * KVQ_BLOCK_SIZE))
-                                   : make_int4(0, 0, 0, 0);
-        }
-      }
-    };
-    fetch(0);
-    for (int j = 0; j < n_tiles; ++j) {
-      if (j > 0) failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
-#pragma unroll
-      for (int rr = 0; rr < D / 128; ++rr) {
-        const int d = t + 128 * rr;
-#pragma unroll
-        for (int pl = 0; pl < 8; ++pl) {
-          uint4 c0, c1;
-          widen16(vraw[rr][pl], c0, c1);
-          uint8_t* blk = vs + (pl >> 2) * (D * 128);
-          const int cc = (pl & 3) * 2;
-          sts128(blk + tc::sw128_off(d, cc), c0);
-          sts128(blk + tc::sw128_off(d, cc + 1), c1);
-        }
-      }
-      tc::fence_proxy_async_smem();
-      mbar_arrive(&bars[kBarVFull]);
-      if (j + 1 < n_tiles) fetch(j + 1);
-      if (named_bar_or(3, kTransformThreads, failed)) break;
+      // every MMA this thread issued has completed before the CTA releases tensor memory
+      tc::commit(&bars[kBarDrain]);
+      mbar_wait(&bars[kBarDrain], 0, a.status);
     }
   } else if (lane == 0) {
-    // ================================================================ MMA issue (one thread)
-    const uint32_t qs_a = smem_u32(qs), ks_a = smem_u32(ks), vs_a = smem_u32(vs);
-    constexpr uint32_t idesc_qk = tc::idesc_f16_f32(128, 128);
-    constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, D);
-    const uint32_t tm_o = tmem + L::kOCol;
-    for (int j = 0; j <= n_tiles; ++j) {
+    // ================================================================ bulk-copy producer (one thread)
+    int slot = 0, fills = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    auto push = [&](const uint8_t* src) {
+      if (fills >= kRingSlots && !wait_or_abort(&bars[kBarEmpty + slot], ph ^ 1u, a.status, abort_flag)) {
+        ok = false;
+        return;
+      }
+      mbar_arrive_expect_tx(&bars[kBarFull + slot], kPieceBytes);
+      bulk_g2s(ring + slot * kPieceBytes, src, kPieceBytes, &bars[kBarFull + slot]);
+      ++fills;
+      if (++slot == kRingSlots) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    };
+    int scl_loads = 0;
+    auto push_scales = [&](int j) {
+      const int sb = j & (kScaleBufs - 1);
+      if (j >= kScaleBufs &&
+          !wait_or_abort(&bars[kBarSclFree + sb], ((j - kScaleBufs) / kScaleBufs) & 1, a.status, abort_flag)) {
+        ok = false;
+        return;
+      }
+      mbar_arrive_expect_tx(&bars[kBarSclFull + sb], 1024);
+      bulk_g2s(scale_s + sb * 256, a.skw + (tile0 + j) * 128, 512, &bars[kBarSclFull + sb]);
+      bulk_g2s(scale_s + sb * 256 + 128, a.svw + (tile0 + j) * 128, 512, &bars[kBarSclFull + sb]);
+      ++scl_loads;
+    };
+    for (int j = 0; ok && j <= n_tiles; ++j) {
       if (j < n_tiles) {
-        const int b = j & 1;
-        if (!wait_or_abort(&bars[kBarKFull], j & 1, a.status, abort_flag)) break;
-        tc::fence_after_sync();
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * (128 * 128) + (k & 3) * 32;
-          tc::mma_f16_ss(tmem + b * 128, tc::sdesc_sw128(qs_a + off), tc::sdesc_sw128(ks_a + off), idesc_qk,
-                         k > 0 ? 1u : 0u);
-        }
-        tc::commit(&bars[kBarS0 + b]);
-        tc::commit(&bars[kBarKFree]);
+        const uint8_t* kt = a.kw + (tile0 + j) * NP * kPieceBytes;
+        for (int qa = 0; ok && qa < NP; ++qa) push(kt + qa * kPieceBytes);
+        if (ok) push_scales(j);
       }
       if (j >= 1) {
-        const int jp = j - 1, bp = jp & 1;
-        if (!wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag)) break;
-        if (!wait_or_abort(&bars[kBarVFull], jp & 1, a.status, abort_flag)) break;
-        tc::fence_after_sync();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t boff = (k >> 2) * (D * 128) + (k & 3) * 32;
-          tc::mma_f16_ts(tm_o, tmem + bp * 128 + 8 * k, tc::sdesc_sw128(vs_a + boff), idesc_pv, 1u);
-        }
-        tc::commit(&bars[kBarPvDone]);
+        const uint8_t* vt = a.vw + (tile0 + j - 1) * NP * kPieceBytes;
+        for (int qv = 0; ok && qv < NP; ++qv) push(vt + qv * kPieceBytes);
       }
     }
+    // Copies still in flight (only after an abort) land before the CTA exits: wait for the
+    // last fill of every slot and the last load of every scale buffer.
+    for (int i = (fills > kRingSlots ? fills - kRingSlots : 0); i < fills; ++i)
+      mbar_wait(&bars[kBarFull + i % kRingSlots], (i / kRingSlots) & 1, a.status);
+    for (int i = (scl_loads > kScaleBufs ? scl_loads - kScaleBufs : 0); i < scl_loads; ++i)
+      mbar_wait(&bars[kBarSclFull + i % kScaleBufs], (i / kScaleBufs) & 1, a.status);
   }
 
   tc::fence_before_sync();
@@ -774,10 +884,21 @@ __global__ void __launch_bounds__(128, 1) prefill_qk_debug_kernel(PrefillArgs a)
 }
 
 // ============================================================================ launchers
-size_t prefill_workspace_bytes(int n_tokens, int n_q_heads, int head_dim) {
-  const long long codes = static_cast<long long>(n_tokens) * n_q_heads * head_dim;
-  const long long scales = static_cast<long long>(n_tokens) * n_q_heads * 4;
-  return static_cast<size_t>(((codes + 255) / 256) * 256 + scales);
+// Workspace: int8 Q codes | Q scales | widened K tiles | widened V tiles | K scales | V scales
+// (each part starting on a 1024-byte boundary of the workspace).
+static long long round1k(long long x) { return (x + 1023) / 1024 * 1024; }
+
+PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim) {
+  PrefillWorkspace w{};
+  w.n_kv_tiles = static_cast<int>((static_cast<long long>(history_len) + n_tokens + 127) / 128);
+  const long long tiles = static_cast<long long>(n_kv_heads) * w.n_kv_tiles;
+  w.off_q_scales = round1k(static_cast<long long>(n_tokens) * n_q_heads * head_dim);
+  w.off_kw = w.off_q_scales + round1k(static_cast<long long>(n_tokens) * n_q_heads * 4);
+  w.off_vw = w.off_kw + tiles * 128 * head_dim * 2;
+  w.off_skw = w.off_vw + tiles * 128 * head_dim * 2;
+  w.off_svw = w.off_skw + tiles * 128 * 4;
+  w.bytes = w.off_svw + tiles * 128 * 4;
+  return w;
 }
 
 cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
@@ -792,12 +913,13 @@ cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
 
 template <int D>
 static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
-  using L = PrefillWsSmem<D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_ws_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  using L = PrefillTmaSmem<D>;
+  cudaError_t e = launch_pdl(kv_widen_kernel<D>, dim3(a.n_kv_tiles, a.n_kv_heads), dim3(256), 0, stream, a);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(prefill_tma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((a.n_tokens + 127) / 128, a.n_q_heads);
-  return launch_pdl(prefill_ws_kernel<D>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
+  return launch_pdl(prefill_tma_kernel<D>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {

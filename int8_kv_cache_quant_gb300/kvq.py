@@ -67,7 +67,7 @@ def lib():
         L.kvq_attn_decode_int8kv_noalloc.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp,
                                                      ctypes.POINTER(_DecodeOpts), vp]
         L.kvq_prefill_workspace_bytes.restype = sz
-        L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32]
+        L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
         L.kvq_attn_sparse_int8kv.argtypes = [cp, vp, i32, i32, vp, vp, vp, i32, f32, vp, vp]
         L.kvq_debug_prefill_q_codes.argtypes = [vp, i32, i32, i32, vp, vp, vp]
@@ -182,8 +182,8 @@ def kvq_attn_decode_int8kv_noalloc(cache, q, block_table, ctx_lens, max_ctx, sof
     return out
 
 
-def kvq_prefill_workspace_bytes(n_tokens, n_q_heads, head_dim):
-    return int(lib().kvq_prefill_workspace_bytes(n_tokens, n_q_heads, head_dim))
+def kvq_prefill_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, history_len, head_dim):
+    return int(lib().kvq_prefill_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, history_len, head_dim))
 
 
 def kvq_attn_prefill_int8(cache, q, history_len, block_table_row, softmax_scale, out=None,
@@ -192,7 +192,7 @@ def kvq_attn_prefill_int8(cache, q, history_len, block_table_row, softmax_scale,
     T, Hq, D = q.shape
     if out is None:
         out = torch.empty((T, Hq, D), dtype=torch.float32, device=q.device)
-    need = kvq_prefill_workspace_bytes(T, Hq, D)
+    need = kvq_prefill_workspace_bytes(T, Hq, cache.n_kv_heads, int(history_len), D)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     wbytes = workspace.numel() * workspace.element_size()

@@ -31,7 +31,12 @@ def test_host_helpers_without_gpu():
     # workspace sizes are pure host arithmetic
     assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 64 * 24 * 256 * 4 + 64 * 24 * 16
     assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 0  # single-CTA route
-    assert k.kvq_prefill_workspace_bytes(2048, 24, 256) == 2048 * 24 * 256 + 2048 * 24 * 4
+    # prefill: Q codes | Q scales | widened K and V of 256 tiles x 4 KV heads (2 bytes per code) |
+    # their key and value scales
+    tiles = 4 * ((30720 + 2048 + 127) // 128)
+    assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 30720, 256) == (
+        2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4)
+    assert k.kvq_prefill_workspace_bytes(2048, 24, 4, -1, 256) == 0
 
 
 def test_invalid_arguments_rejected_before_launch():
@@ -52,3 +57,7 @@ def test_invalid_arguments_rejected_before_launch():
                                     None, None) == 2
     assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 8, 16, 4000, 16, 60000, 1.0, 16, None,
                                     0, None, None) == 4
+    # prefill: the softmax scale must be finite and positive (the kernel's exp2 relies on it)
+    for bad in (0.0, -0.5, float("inf"), float("nan")):
+        assert L.kvq_attn_prefill_int8(ctypes.byref(c), 16, 16, 8, 0, 16, 1, bad, 16, 16, 1 << 30,
+                                       None) == 1
