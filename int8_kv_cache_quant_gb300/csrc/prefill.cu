@@ -157,6 +157,11 @@ __device__ __forceinline__ f2 add2(f2 a, f2 b) {
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
   return r;
 }
+__device__ __forceinline__ f2 sub2(f2 a, f2 b) {
+  f2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+  return r;
+}
 __device__ __forceinline__ f2 mul2(f2 a, f2 b) {
   f2 r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
@@ -177,9 +182,10 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
 // (mod 2^32) because bits(t) = 0x4B400000 + n and 0x4B400000 * 2^23 == 0 (mod 2^32).
 __device__ __forceinline__ f2 exp2_det2(f2 x) {
   const bool v0 = lo2(x) >= -125.0f, v1 = hi2(x) >= -125.0f;
-  const f2 t = add2(x, mk2(kMagic, kMagic));
-  const f2 n = add2(t, mk2(-kMagic, -kMagic));
-  const f2 f = fma2(n, mk2(-1.0f, -1.0f), x);
+  const f2 magic = mk2(kMagic, kMagic);
+  const f2 t = add2(x, magic);
+  const f2 n = sub2(t, magic);
+  const f2 f = sub2(x, n);
   f2 p = fma2(mk2(0.00133335581464284f, 0.00133335581464284f), f, mk2(0.00961812910762848f, 0.00961812910762848f));
   p = fma2(p, f, mk2(0.0555041086648216f, 0.0555041086648216f));
   p = fma2(p, f, mk2(0.240226506959101f, 0.240226506959101f));
@@ -373,7 +379,10 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
 //               row and O columns p*D/4 .. (p+1)*D/4 - 1; the four parts of a row (warps w, w+4,
 //               w+8, w+12: the same tensor-memory lanes) exchange their partial maxima through
 //               shared memory at their own named barrier.  They also widen Q at the start.
-//   warp 16     MMA issue (lane 0) and tensor-memory allocation.
+//   warp 16     MMA issue and tensor-memory allocation: the whole warp runs the loop and one
+//               elected lane issues, so the descriptors stay on the uniform datapath (the MMA
+//               warp shares its SM sub-partition with four busy softmax warps; fewer instructions
+//               per MMA keep the tensor pipe fed).  PV uses N = head_dim, one MMA per k-step.
 //   warp 17     bulk-copy producer (lane 0): the widened K/V pieces through a ring of 16 KB
 //               shared-memory slots in the order the MMAs consume them, and the scales.
 // Tensor memory: S0 | S1 (128 columns each, double-buffered) | O (head_dim columns).  P codes
@@ -390,7 +399,7 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
 // pv_done(j-1) -> arrive p_full.
 namespace {
 
-constexpr int kRingSlots = 9;
+constexpr int kRingSlots = 8;  // one K tile and one V tile: keeps each V piece pair in adjacent slots
 constexpr int kScaleBufs = 4;
 
 template <int D>
@@ -438,6 +447,14 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
     }
   }
   return true;
+}
+
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r));
+  return r != 0;
 }
 
 __device__ __forceinline__ void named_bar(int id, int count) {
@@ -572,20 +589,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       const float4* sv_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 1) * 128 + 32 * part);
       // visible keys of this row in this tile, counted from the start of this thread's part
       const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128) - 32 * part;
-      float ymax = -INFINITY;
+      float ym0 = -INFINITY, ym1 = -INFINITY;
 #pragma unroll
       for (int n = 0; n < 32; n += 4) {
         const float4 k4 = sk_t[n >> 2];
         const f2 ya = mul2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), mk2(k4.x, k4.y));
         const f2 yb = mul2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), mk2(k4.z, k4.w));
-        float y[4] = {lo2(ya), hi2(ya), lo2(yb), hi2(yb)};
-        if (lim < 32) {  // only tiles on the diagonal or past the context carry masked keys
+        sv[n] = __float_as_uint(lo2(ya));
+        sv[n + 1] = __float_as_uint(hi2(ya));
+        sv[n + 2] = __float_as_uint(lo2(yb));
+        sv[n + 3] = __float_as_uint(hi2(yb));
+        ym0 = fmax3(ym0, lo2(ya), hi2(ya));
+        ym1 = fmax3(ym1, lo2(yb), hi2(yb));
+      }
+      float ymax = fmaxf(ym0, ym1);
+      if (lim < 32) {  // only tiles on the diagonal or past the context carry masked keys
+        ymax = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) y[e] = (n + e < lim) ? y[e] : -INFINITY;
+        for (int n = 0; n < 32; ++n) {
+          const float y = (n < lim) ? __uint_as_float(sv[n]) : -INFINITY;
+          sv[n] = __float_as_uint(y);
+          ymax = fmaxf(ymax, y);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sv[n + e] = __float_as_uint(y[e]);
-        ymax = fmax3(ymax, fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
       }
       red_max[part * 128 + row] = ymax;
       tc::fence_before_sync();
@@ -594,7 +619,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       const float m_new = fmaxf(m, __fmul_rn(max4_col(red_max, row), a_row));
       const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
       f2 psum = mk2(0.0f, 0.0f);
-      float wmax = 0.0f;
+      float wm0 = 0.0f, wm1 = 0.0f;
       const f2 a2 = mk2(a_row, a_row), nm2 = mk2(-m_new, -m_new);
 #pragma unroll
       for (int n = 0; n < 32; n += 4) {
@@ -608,9 +633,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
         sv[n + 1] = __float_as_uint(hi2(wa));
         sv[n + 2] = __float_as_uint(lo2(wb));
         sv[n + 3] = __float_as_uint(hi2(wb));
-        wmax = fmax3(wmax, lo2(wa), hi2(wa));
-        wmax = fmax3(wmax, lo2(wb), hi2(wb));
+        wm0 = fmax3(wm0, lo2(wa), hi2(wa));
+        wm1 = fmax3(wm1, lo2(wb), hi2(wb));
       }
+      const float wmax = fmaxf(wm0, wm1);
       mbar_arrive(&bars[kBarSclFree + sb]);  // this tile's scales are no longer read
       l_part = l_part * alpha + (lo2(psum) + hi2(psum));
       m = m_new;
@@ -701,65 +727,74 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       }
     }
   } else if (warp == kMmaWarp) {
-    // ================================================================ MMA issue (one thread)
-    if (lane == 0) {
-      const uint32_t qs_a = smem_u32(qs), ring_a = smem_u32(ring);
-      constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
-      const uint32_t tm_o = tmem + L::kOCol;
-      int slot = 0;
-      uint32_t ph = 0;
-      bool ok = wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag);
-      tc::fence_after_sync();
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int b = j & 1;
-          for (int qa = 0; ok && qa < NP; ++qa) {
-            ok = wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag);
-            if (!ok) break;
+    // ================================================================ MMA issue (the whole warp
+    // runs the loop, one elected lane issues): descriptors stay on the uniform datapath and a
+    // piece's k-steps differ only in the start-address field (+32 bytes = +2 per step).
+    const uint64_t qd0 = tc::sdesc_sw128(smem_u32(qs)), rd0 = tc::sdesc_sw128(smem_u32(ring));
+    constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
+    const uint32_t tm_o = tmem + L::kOCol;
+    int slot = 0;
+    uint32_t ph = 0;
+    bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag));
+    for (int j = 0; ok && j <= n_tiles; ++j) {
+      if (j < n_tiles) {
+        const int b = j & 1;
+        for (int qa = 0; ok && qa < NP; ++qa) {
+          ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag));
+          if (!ok) break;
+          if (elect_one()) {
             tc::fence_after_sync();
-            const uint32_t kp = ring_a + slot * kPieceBytes, qp = qs_a + qa * kPieceBytes;
+            const uint64_t kd = rd0 + static_cast<uint64_t>((slot * kPieceBytes) >> 4);
+            const uint64_t qd = qd0 + static_cast<uint64_t>((qa * kPieceBytes) >> 4);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-              tc::mma_f16_ss(tmem + b * 128, tc::sdesc_sw128(qp + 32 * s), tc::sdesc_sw128(kp + 32 * s), idesc,
-                             (qa | s) ? 1u : 0u);
+              tc::mma_f16_ss(tmem + b * 128, qd + 2 * s, kd + 2 * s, idesc, (qa | s) ? 1u : 0u);
             tc::commit(&bars[kBarEmpty + slot]);
-            if (++slot == kRingSlots) {
-              slot = 0;
-              ph ^= 1u;
-            }
+            if (qa == NP - 1) tc::commit(&bars[kBarS0 + b]);
           }
-          if (!ok) break;
-          tc::commit(&bars[kBarS0 + b]);
-        }
-        if (j >= 1) {
-          const int jp = j - 1, bp = jp & 1;
-          ok = wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          for (int qv = 0; ok && qv < NP; ++qv) {
-            const int kh = qv / (D / 128), dh = qv % (D / 128);
-            ok = wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag);
-            if (!ok) break;
-            tc::fence_after_sync();
-            const uint32_t vp = ring_a + slot * kPieceBytes;
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-              tc::mma_f16_ts(tm_o + 128 * dh, tmem + bp * 128 + 32 * kh + 8 * s, tc::sdesc_sw128(vp + 32 * s), idesc,
-                             1u);
-            tc::commit(&bars[kBarEmpty + slot]);
-            if (++slot == kRingSlots) {
-              slot = 0;
-              ph ^= 1u;
-            }
+          __syncwarp();
+          if (++slot == kRingSlots) {
+            slot = 0;
+            ph ^= 1u;
           }
-          if (!ok) break;
-          tc::commit(&bars[kBarPvDone]);
         }
       }
-      // every MMA this thread issued has completed before the CTA releases tensor memory
+      if (ok && j >= 1) {
+        // PV_{j-1}: for each 64-key half kh, the D/128 pieces of V rows (head dims) sit in adjacent
+        // slots, so one N = D MMA per k-step covers all of O.
+        const int jp = j - 1, bp = jp & 1;
+        constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, D);
+        ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag));
+        for (int kh = 0; ok && kh < 2; ++kh) {
+          const int s0 = slot;
+          for (int dh = 0; ok && dh < D / 128; ++dh) {
+            ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag));
+            if (++slot == kRingSlots) {
+              slot = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (elect_one()) {
+            tc::fence_after_sync();
+            const uint64_t vd = rd0 + static_cast<uint64_t>((s0 * kPieceBytes) >> 4);
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              tc::mma_f16_ts(tm_o, tmem + bp * 128 + 32 * kh + 8 * s, vd + 2 * s, idesc_pv, 1u);
+#pragma unroll
+            for (int dh = 0; dh < D / 128; ++dh) tc::commit(&bars[kBarEmpty + s0 + dh]);
+            if (kh == 1) tc::commit(&bars[kBarPvDone]);
+          }
+          __syncwarp();
+        }
+      }
+    }
+    // every MMA this warp issued has completed before the CTA releases tensor memory
+    if (elect_one()) {
       tc::commit(&bars[kBarDrain]);
       mbar_wait(&bars[kBarDrain], 0, a.status);
     }
+    __syncwarp();
   } else if (lane == 0) {
     // ================================================================ bulk-copy producer (one thread)
     int slot = 0, fills = 0;
