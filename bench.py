@@ -28,6 +28,24 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
 
+# DRAM bytes (read + written) of one decode_32k stage-1 launch, from an ncu capture of this
+# kernel (dram__bytes_read.sum + dram__bytes_write.sum), and the SHA-256 prefix of the kernel's
+# sources at that capture.  Once the sources differ, the figure no longer describes the kernel
+# and the line reports null.
+STAGE1_TRAFFIC_BYTES = 68209408 + 203520
+STAGE1_TRAFFIC_SOURCES = ("int8_kv_cache_quant_gb300/csrc/decode.cu", "int8_kv_cache_quant_gb300/csrc/kvq_dev.cuh")
+STAGE1_TRAFFIC_SHA = "dd2eda9e584b1777"
+
+
+def stage1_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    for f in STAGE1_TRAFFIC_SOURCES:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), f), "rb") as fh:
+            h.update(fh.read())
+    return STAGE1_TRAFFIC_BYTES if h.hexdigest()[:16] == STAGE1_TRAFFIC_SHA else None
+
+
 def load_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -289,7 +307,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                    "l2": "cold before every timed step: 256 MB write then 256 MB read of another buffer, outside the events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(achieved / hbm, 4), "traffic": None,
+                     "frac": round(achieved / hbm, 4), "traffic": stage1_traffic(),
                      "kernel": "decode_stage1_kernel<256,NP=4,DEPTH=3,split>", "peak_kind": peak_kind,
                      "kernel_us": round(kern_avg * 1e3, 2)},
         "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
