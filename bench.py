@@ -3,7 +3,7 @@
 A step of the headline workload (decode_32k: one sequence, ctx 32768, 24 query / 4 KV heads,
 head_dim 256, int8 K/V in 16-token pages behind a shuffled block table, K outliers) is one
 pass of the decode path: kv_quant_write of the step's new token, then split-K decode over
-the whole context (512-key splits, stage 1 + merge).  value = K/V bytes the step reads
+the whole context (split-K with the library's split size for this GPU, stage 1 + merge).  value = K/V bytes the step reads
 (2080 B per token) / device time of the step, in GB/s, with the L2 flushed (256 MB write)
 before every timed step, outside its events.
 
@@ -186,8 +186,9 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     new_seq, new_pos = i32(w["new_seq"]), i32(w["new_pos"])
     ctx = i32(w["ctx_lens"])
     max_ctx = w["max_ctx"]
-    split = w["split_rows"]
-    ws = torch.empty(kvq.kvq_decode_workspace_bytes(1, Hq, max_ctx, D, split_rows=split),
+    # the library's default split (split_rows 0): sized so that stage 1 fills the GPU in one wave
+    split = kvq.kvq_decode_auto_split_rows(1, Hkv, max_ctx, torch.cuda.get_device_properties(local).multi_processor_count)
+    ws = torch.empty(kvq.kvq_decode_workspace_bytes(1, Hq, max_ctx, D),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((1, Hq, D), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -203,7 +204,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     def step(ev=None):
         kvq.kvq_quant_write(cache, k_new, v_new, new_seq, new_pos, bt)
         kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, max_ctx, w["softmax_scale"], out=out,
-                                   workspace=ws, split_rows=split, stage1_events=ev)
+                                   workspace=ws, stage1_events=ev)
 
     for _ in range(args.warmup):
         cold_l2(1)
@@ -264,7 +265,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         kvq.kvq_quant_write(cache, kn_d.view(torch.bfloat16), vn_d.view(torch.bfloat16), sp_d[:1],
                             sp_d[1:], bt)
         kvq.kvq_attn_decode_int8kv(cache, q_d.view(torch.bfloat16), bt, ctx, max_ctx,
-                                   w["softmax_scale"], out=out, workspace=ws, split_rows=split)
+                                   w["softmax_scale"], out=out, workspace=ws)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -367,6 +368,8 @@ def bench_extra(args, local, hbm, tflops, only=None):
     # decode_1k: single-CTA route, launch/latency bound
     if want("decode_1k"):
         res.update(_extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps or 50))
+    if want("decode_b64"):
+        res.update(_extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps or 20, hbm))
     if want("prefill_32k"):
         res.update(_extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps or 10, tflops))
     if want("sparse_32k"):
@@ -386,6 +389,33 @@ def _extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps):
     ms = timed(lambda: kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out), reps)
     kvb = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
     res["decode_1k"] = {"us_per_call": round(ms * 1e3, 2), "kv_GBps": round(kvb / ms / 1e6, 1)}
+    return res
+
+
+def _extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps, hbm):
+    """decode_b64: one batched step (kv_quant_write of one new token per sequence, then decode)
+    over 64 sequences of ctx 512..16384, 32 query / 8 KV heads, head_dim 128."""
+    import numpy as np
+    import torch
+    res = {}
+    w = W.make("decode_b64")
+    cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
+    bt = i32(w["block_table"])
+    kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
+    q, ctx = bf16(w["q"]), i32(w["ctx_lens"])
+    kn, vn, ns, npos = bf16(w["k_new"]), bf16(w["v_new"]), i32(w["new_seq"]), i32(w["new_pos"])
+    B, Hq, D = w["batch"], w["hq"], w["d"]
+    out = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, kvq.kvq_decode_workspace_bytes(B, Hq, w["max_ctx"], D)), dtype=torch.uint8, device=dev)
+
+    def step():
+        kvq.kvq_quant_write(cache, kn, vn, ns, npos, bt)
+        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out, workspace=ws)
+    ms = timed(step, reps)
+    kvb = int(w["ctx_lens"].astype(np.int64).sum()) * w["hkv"] * (2 * D + 8)
+    res["decode_b64"] = {"us_per_step": round(ms * 1e3, 2), "kv_bytes": kvb, "kv_GBps": round(kvb / ms / 1e6, 1),
+                         "frac_of_hbm_peak": round(kvb / ms / 1e6 / hbm, 4),
+                         "step": "kv_quant_write(64 tokens) + decode (split route)"}
     return res
 
 
@@ -515,7 +545,7 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k"],
+    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k", "decode_b64"],
                     help="time only this secondary workload (profiling runs); prints its figures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -55,7 +55,6 @@ extern "C" {
 #define KVQ_ABI_VERSION 1
 #define KVQ_BLOCK_SIZE 16          /* tokens per cache page */
 #define KVQ_PV_TILE 128            /* keys per P re-quantisation tile in prefill */
-#define KVQ_DEFAULT_SPLIT_ROWS 512 /* keys per split in the split-K decode route */
 
 typedef enum kvq_status {
   KVQ_OK = 0,
@@ -107,7 +106,8 @@ int kvq_quant_write(const kvq_cache* cache, const void* k_new, const void* v_new
 
 /* Options of kvq_attn_decode_int8kv (pass NULL for the defaults). */
 typedef struct kvq_decode_opts {
-  int32_t split_rows;      /* keys per split in the split route; 0 -> 512; multiple of 16 */
+  int32_t split_rows;      /* keys per split in the split route, a multiple of 16; 0 -> sized to
+                            * the GPU by kvq_decode_auto_split_rows */
   int32_t route_threshold; /* max_ctx <= threshold -> single-CTA route; 0 -> 2048 ([DOT4] route table) */
   int32_t force_route;     /* 0 auto, 1 single CTA per (sequence, KV head), 2 split-K */
   /* Optional profiling hooks: two cudaEvent_t (as void*) recorded on `stream` right before
@@ -117,7 +117,8 @@ typedef struct kvq_decode_opts {
 } kvq_decode_opts;
 
 /* Workspace (bytes) the split route of kvq_attn_decode_int8kv needs; 0 when the call
- * will take the single-CTA route. */
+ * will take the single-CTA route.  With opts->split_rows == 0 it is the bound for the
+ * smallest split the automatic rule can choose (256 keys), so it does not depend on the GPU. */
 size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_ctx,
                                   int32_t head_dim, const kvq_decode_opts* opts);
 
@@ -140,6 +141,21 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
  *   workspace  : device, >= kvq_decode_workspace_bytes(...), 16-byte aligned; its
  *                contents on entry do not matter
  */
+/*
+ * kvq_decode_auto_split_rows — the split size the split route uses when opts->split_rows is
+ * 0, for a GPU with n_sms SMs (pure host arithmetic).  Stage 1 holds two CTAs per SM.
+ *   units = batch * n_kv_heads, pages = ceil(max_ctx / 16).
+ *   If units * ceil(pages / 32) > 4 * n_sms (at 512-key splits the grid is over two waves),
+ *   the split takes clamp(units * pages / (8 * n_sms), 32, 128) pages: longer splits
+ *   amortise each CTA's start-up over more pages.
+ *   Otherwise the split takes max(16, ceil(pages / floor(2 * n_sms / units))) pages: the
+ *   grid fills every SM in one wave.
+ * Returns keys (pages * 16); 0 if an argument is not positive.  The source pages use a
+ * fixed 512 ([DOT4] route table); any split size gives the same result up to fp32
+ * rounding.
+ */
+int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t max_ctx, int32_t n_sms);
+
 int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
                            int32_t n_q_heads, const int32_t* block_table,
                            int32_t max_blocks_per_seq, const int32_t* ctx_lens,

@@ -1,6 +1,7 @@
 // api.cu — the C ABI of libkvq (include/kvq.h): host-side validation, routing and launch.
 // Every entry point checks its arguments before launching anything, allocates nothing and
 // never synchronises (except kvq_device_status).
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -46,7 +47,7 @@ int check_cache(const kvq_cache* c) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
 kvq_decode_opts decode_defaults(const kvq_decode_opts* o) {
-  kvq_decode_opts r = {KVQ_DEFAULT_SPLIT_ROWS, 2048, 0, nullptr, nullptr};
+  kvq_decode_opts r = {0, 2048, 0, nullptr, nullptr};  // split_rows 0: sized to the GPU
   if (o) {
     if (o->split_rows > 0) r.split_rows = o->split_rows;
     if (o->route_threshold > 0) r.route_threshold = o->route_threshold;
@@ -124,12 +125,44 @@ static bool decode_split_route(const kvq_decode_opts& o, int32_t max_ctx) {
   return max_ctx > o.route_threshold;
 }
 
+int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t max_ctx, int32_t n_sms) {
+  if (batch <= 0 || n_kv_heads <= 0 || max_ctx <= 0 || n_sms <= 0) return 0;
+  const long long units = static_cast<long long>(batch) * n_kv_heads;
+  const long long pages = (static_cast<long long>(max_ctx) + KVQ_BLOCK_SIZE - 1) / KVQ_BLOCK_SIZE;
+  long long split_pages;
+  if (units * ((pages + 31) / 32) > 4LL * n_sms) {
+    split_pages = std::min(128LL, std::max(32LL, units * pages / (8LL * n_sms)));
+  } else {
+    const long long per_unit = std::max(1LL, (2LL * n_sms) / units);
+    split_pages = std::max(16LL, (pages + per_unit - 1) / per_unit);
+  }
+  return static_cast<int32_t>(split_pages * KVQ_BLOCK_SIZE);
+}
+
+// Smallest split the automatic rule chooses: the workspace bound when split_rows is 0.
+constexpr int kAutoSplitMinRows = 16 * KVQ_BLOCK_SIZE;
+
+static int device_sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_ctx,
                                   int32_t head_dim, const kvq_decode_opts* opts) {
   const kvq_decode_opts o = decode_defaults(opts);
-  if (batch <= 0 || n_q_heads <= 0 || max_ctx <= 0 || head_dim <= 0 || o.split_rows <= 0) return 0;
+  if (batch <= 0 || n_q_heads <= 0 || max_ctx <= 0 || head_dim <= 0 || o.split_rows < 0) return 0;
   if (!decode_split_route(o, max_ctx)) return 0;
-  return kvq::decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, o.split_rows);
+  const int rows = o.split_rows > 0 ? o.split_rows : kAutoSplitMinRows;
+  return kvq::decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, rows);
 }
 
 int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_q_heads,
@@ -146,10 +179,16 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   if (G > 8) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
   if (!aligned4(block_table) || !aligned4(ctx_lens)) return KVQ_ERR_MISALIGNED;
-  const kvq_decode_opts o = decode_defaults(opts);
+  kvq_decode_opts o = decode_defaults(opts);
   if (o.split_rows % KVQ_BLOCK_SIZE != 0 || o.force_route < 0 || o.force_route > 2) return KVQ_ERR_INVALID_ARG;
   const int mc = max_ctx > 0 ? max_ctx : 1;
   const bool split = decode_split_route(o, mc);
+  if (split && !workspace) return KVQ_ERR_WORKSPACE;
+  if (split && o.split_rows == 0) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return KVQ_ERR_CUDA;
+    o.split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, mc, sms);
+  }
   kvq::DecodeArgs a{};
   a.k = cache->k;
   a.v = cache->v;

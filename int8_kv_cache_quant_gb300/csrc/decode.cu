@@ -132,6 +132,48 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
     for (int s = 0; s < L::kStages; ++s) mbar_init(&full[s], 1);
     mbar_fence_init();
   }
+  __syncthreads();  // the barriers are initialised before any copy completes on them
+
+  const int npp = (p < n_pages) ? (n_pages - p + NP - 1) / NP : 0;  // pages of this pair
+  const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
+  uint64_t* pfull = full + p * DEPTH;
+  int* pok = stage_ok + p * DEPTH;
+  uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
+
+  // page ids of this pair, a window of 32 in warp 0's lanes (lane i <-> page k = wb + i)
+  int wb = 0, pg = -1;
+  if (hf == 0 && lane < npp) pg = __ldg(bt + p + lane * NP);
+  // warp 0 of the pair, collectively: issue the copy of pair page k into its slot
+  auto issue = [&](int k) {
+    while (k >= wb + 32) {
+      wb += 32;
+      pg = (wb + lane < npp) ? __ldg(bt + p + (wb + lane) * NP) : -1;
+    }
+    const int page = __shfl_sync(0xffffffffu, pg, k - wb);
+    if (lane == 0) {
+      const int s = k % DEPTH;
+      const bool ok = page >= 0 && page < a.num_blocks;
+      pok[s] = ok ? 1 : 0;
+      if (ok) {
+        uint8_t* st = pring + s * L::kStageBytes;
+        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive_expect_tx(&pfull[s], 2 * KB + 128);
+        bulk_g2s(st, a.k + ph * KB, KB, &pfull[s]);
+        bulk_g2s(st + KB, a.v + ph * KB, KB, &pfull[s]);
+        bulk_g2s(st + 2 * KB, a.k_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[s]);
+        bulk_g2s(st + 2 * KB + 64, a.v_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[s]);
+      } else {
+        set_status(a.status, KVQ_DEV_BAD_BLOCK);
+        mbar_arrive(&pfull[s]);
+      }
+    }
+  };
+  // The first copies go out before Q is prepared, so their HBM latency overlaps it.
+  if (hf == 0) {
+    for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
+  }
+
   // ---- Q^T fragments: warp h prepares head h of the group (zeros past G).  The fp16 values
   // are q * 2^e (e brings max|q| into [2^14, 2^15): exact for bf16).  Chunk j (16 dims) is
   // two 8 x 8 b16 matrices, rows = heads, whose columns are the k-slots of the MMA: slots
@@ -178,44 +220,6 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
   }
   __syncthreads();
 
-  const int npp = (p < n_pages) ? (n_pages - p + NP - 1) / NP : 0;  // pages of this pair
-  const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
-  uint64_t* pfull = full + p * DEPTH;
-  int* pok = stage_ok + p * DEPTH;
-  uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
-
-  // page ids of this pair, a window of 32 in warp 0's lanes (lane i <-> page k = wb + i)
-  int wb = 0, pg = -1;
-  if (hf == 0 && lane < npp) pg = __ldg(bt + p + lane * NP);
-  // warp 0 of the pair, collectively: issue the copy of pair page k into its slot
-  auto issue = [&](int k) {
-    while (k >= wb + 32) {
-      wb += 32;
-      pg = (wb + lane < npp) ? __ldg(bt + p + (wb + lane) * NP) : -1;
-    }
-    const int page = __shfl_sync(0xffffffffu, pg, k - wb);
-    if (lane == 0) {
-      const int s = k % DEPTH;
-      const bool ok = page >= 0 && page < a.num_blocks;
-      pok[s] = ok ? 1 : 0;
-      if (ok) {
-        uint8_t* st = pring + s * L::kStageBytes;
-        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        mbar_arrive_expect_tx(&pfull[s], 2 * KB + 128);
-        bulk_g2s(st, a.k + ph * KB, KB, &pfull[s]);
-        bulk_g2s(st + KB, a.v + ph * KB, KB, &pfull[s]);
-        bulk_g2s(st + 2 * KB, a.k_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[s]);
-        bulk_g2s(st + 2 * KB + 64, a.v_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[s]);
-      } else {
-        set_status(a.status, KVQ_DEV_BAD_BLOCK);
-        mbar_arrive(&pfull[s]);
-      }
-    }
-  };
-  if (hf == 0) {
-    for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
-  }
 
   const int g = lane >> 2, c = lane & 3;
   float o_acc[NMT_H][4];
@@ -410,18 +414,20 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
 //   M_s = max m_s, M_z = max m_z;  l = sum l_s 2^{m_s - M_s};  o = sum acc_s 2^{m_z - M_z};
 //   out = o 2^{M_z - M_s} / l.  The per-split weights are computed once into shared memory
 // ("ROCm/RDNA4 (gfx1201) vLLM ...", "The reduce is not free": one cooperative pass, each
-// exponential once per split).  256 threads = 4 split groups x 64 threads of 4 dims (D 256;
-// 8 groups x 32 threads at D 128); each thread keeps 8 independent loads in flight.
+// exponential once per split).  One CTA per (query head, sequence, 64-dim column block), so that
+// a small batch still spreads over many SMs; 256 threads = 16 split groups x 16 threads of 4
+// dims; each thread keeps 8 independent loads in flight.
 constexpr int kMergeThreads = 256;
+constexpr int kMergeCols = 64;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a) {
-  constexpr int TPG = D / 4;                    // threads per split group (4 dims each)
+  constexpr int TPG = kMergeCols / 4;           // threads per split group (4 dims each)
   constexpr int NG = kMergeThreads / TPG;       // split groups
   extern __shared__ float wts[];                // [n_split] weights of the partial accumulators
   __shared__ float red[2][kMergeThreads / 32];
   __shared__ __align__(16) float4 part[NG][TPG];
-  const int h = blockIdx.x, b = blockIdx.y, Hq = a.n_q_heads;
+  const int h = blockIdx.x, b = blockIdx.y, Hq = a.n_q_heads, col0 = blockIdx.z * kMergeCols;
   grid_dep_wait();  // the partials come from stage 1
   int ctx = a.ctx_lens[b];
   ctx = max(0, min(ctx, a.max_blocks_per_seq * KVQ_BLOCK_SIZE));
@@ -468,7 +474,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
   for (int i = 0; i < kMergeThreads / 32; ++i) l += red[0][i];
 
   const int grp = tid / TPG, dq = tid % TPG;
-  const float4* acc = reinterpret_cast<const float4*>(a.part_acc + pu0 * D) + dq;
+  const float4* acc = reinterpret_cast<const float4*>(a.part_acc + pu0 * D + col0) + dq;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   int s = grp;
   for (; s + 7 * NG < n; s += 8 * NG) {
@@ -505,7 +511,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
       t.w += u.w;
     }
     const float sc = (l > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / l : 0.f;
-    reinterpret_cast<float4*>(a.out + (static_cast<long long>(b) * Hq + h) * D)[dq] =
+    reinterpret_cast<float4*>(a.out + (static_cast<long long>(b) * Hq + h) * D + col0)[dq] =
         make_float4(t.x * sc, t.y * sc, t.z * sc, t.w * sc);
   }
 }
@@ -544,7 +550,7 @@ cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t s
     e = launch_stage1<128, 4, 4, true>(a, grid, stream);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.n_split) * sizeof(float);
-  dim3 g2(a.n_q_heads, a.batch);
+  dim3 g2(a.n_q_heads, a.batch, a.head_dim / kMergeCols);
   if (a.head_dim == 256) {
     if (wbytes > 48 * 1024) {
       e = cudaFuncSetAttribute(decode_merge_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -14,7 +14,6 @@ LIB_PATH = os.path.join(_HERE, "libkvq.so")
 
 BLOCK_SIZE = 16
 PV_TILE = 128
-DEFAULT_SPLIT_ROWS = 512
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape or option",
            3: "device pointer not 16-byte aligned", 4: "workspace missing or too small",
@@ -61,6 +60,8 @@ def lib():
         L.kvq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.kvq_quant_write.argtypes = [cp, vp, vp, i32, vp, vp, vp, i32, i32, vp]
         L.kvq_decode_workspace_bytes.restype = sz
+        L.kvq_decode_auto_split_rows.restype = i32
+        L.kvq_decode_auto_split_rows.argtypes = [i32, i32, i32, i32]
         L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
         L.kvq_attn_decode_int8kv.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
                                              ctypes.POINTER(_DecodeOpts), vp]
@@ -135,6 +136,10 @@ def _decode_opts(split_rows, route_threshold, force_route, events=None):
     if events is not None:
         ev0, ev1 = (ctypes.c_void_p(e.cuda_event) for e in events)
     return _DecodeOpts(int(split_rows), int(route_threshold), int(force_route), ev0, ev1)
+
+
+def kvq_decode_auto_split_rows(batch, n_kv_heads, max_ctx, n_sms):
+    return int(lib().kvq_decode_auto_split_rows(batch, n_kv_heads, max_ctx, n_sms))
 
 
 def kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, split_rows=0,

@@ -29,7 +29,16 @@ def test_host_helpers_without_gpu():
     assert L.kvq_version() == 1
     assert L.kvq_status_string(4) == b"workspace missing or too small"
     # workspace sizes are pure host arithmetic
-    assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 64 * 24 * 256 * 4 + 64 * 24 * 16
+    # automatic split size: the workspace is the bound for its smallest split (256 keys)
+    assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 128 * 24 * 256 * 4 + 128 * 24 * 16
+    assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256, split_rows=512) == 64 * 24 * 256 * 4 + 64 * 24 * 16
+    # the automatic rule: one wave of two CTAs per SM for few (sequence, KV head) units,
+    # 2048-key splits for a large batch; never below 256 keys
+    assert k.kvq_decode_auto_split_rows(1, 4, 32768, 152) == 432      # 76 splits x 4 = 304 CTAs
+    assert k.kvq_decode_auto_split_rows(64, 8, 16384, 152) == 2048
+    assert k.kvq_decode_auto_split_rows(1, 4, 4096, 152) == 256
+    assert k.kvq_decode_auto_split_rows(1, 1, 1 << 20, 152) == 848
+    assert k.kvq_decode_auto_split_rows(0, 4, 4096, 152) == 0
     assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 0  # single-CTA route
     # prefill: Q codes | Q scales | widened K and V of 256 tiles x 4 KV heads (2 bytes per code) |
     # their key and value scales
