@@ -32,9 +32,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel (dram__bytes_read.sum + dram__bytes_write.sum), and the SHA-256 prefix of the kernel's
 # sources at that capture.  Once the sources differ, the figure no longer describes the kernel
 # and the line reports null.
-STAGE1_TRAFFIC_BYTES = 68209408 + 203520
+STAGE1_TRAFFIC_BYTES = 68208896 + 151808
 STAGE1_TRAFFIC_SOURCES = ("int8_kv_cache_quant_gb300/csrc/decode.cu", "int8_kv_cache_quant_gb300/csrc/kvq_dev.cuh")
-STAGE1_TRAFFIC_SHA = "dd2eda9e584b1777"
+STAGE1_TRAFFIC_SHA = "c6cdcdcd36996b26"
 
 
 def stage1_traffic():
@@ -231,14 +231,27 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         for i in range(K):
             cold_l2(i)
             ev0[i].record(s)
-            step((k0[i], k1[i]))
+            step()
             ev1[i].record(s)
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
         clk.mark_end()
     barrier(world)
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    # Stage-1 duration for the roofline: a second pass of K steps with events recorded on the
+    # library's stream right around the stage-1 launch.  They are kept out of the headline
+    # pass because an event between two launches ends the programmatic-dependent-launch
+    # overlap of quant_write -> stage 1 -> merge (measured: about 8 us per step).
+    ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev3 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        cold_l2(i)
+        ev2[i].record(s)
+        step((k0[i], k1[i]))
+        ev3[i].record(s)
+    torch.cuda.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+    step_ms_events = statistics.mean(a.elapsed_time(b) for a, b in zip(ev2, ev3))
     ms_step = statistics.mean(step_ms)
     ms_step_max = max_over_ranks(ms_step, world)
     kv_bytes = max_ctx * (2 * Hkv * D + 2 * Hkv * 4)  # 2080 B per token at 4 x 256
@@ -295,6 +308,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         "steps": K,
         "warmup": args.warmup,
         "ms_per_step": round(ms_step_max, 5),
+        "ms_per_step_with_stage1_events": round(step_ms_events, 5),
         "us_per_call": round(ms_step_max * 1e3, 2),
         "higher_is_better": True,
         "scaling": "weak",
