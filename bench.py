@@ -32,9 +32,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel (dram__bytes_read.sum + dram__bytes_write.sum), and the SHA-256 prefix of the kernel's
 # sources at that capture.  Once the sources differ, the figure no longer describes the kernel
 # and the line reports null.
-STAGE1_TRAFFIC_BYTES = 68208896 + 151808
+STAGE1_TRAFFIC_BYTES = 68210944 + 150272
 STAGE1_TRAFFIC_SOURCES = ("int8_kv_cache_quant_gb300/csrc/decode.cu", "int8_kv_cache_quant_gb300/csrc/kvq_dev.cuh")
-STAGE1_TRAFFIC_SHA = "c6cdcdcd36996b26"
+STAGE1_TRAFFIC_SHA = "7a97b3fdb6e979b4"
 
 
 def stage1_traffic():
@@ -187,7 +187,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     ctx = i32(w["ctx_lens"])
     max_ctx = w["max_ctx"]
     # the library's default split (split_rows 0): sized so that stage 1 fills the GPU in one wave
-    split = kvq.kvq_decode_auto_split_rows(1, Hkv, max_ctx, torch.cuda.get_device_properties(local).multi_processor_count)
+    split = kvq.kvq_decode_auto_split_rows(1, Hkv, D, max_ctx, torch.cuda.get_device_properties(local).multi_processor_count)
     ws = torch.empty(kvq.kvq_decode_workspace_bytes(1, Hq, max_ctx, D),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((1, Hq, D), dtype=torch.float32, device=dev)
@@ -323,7 +323,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": stage1_traffic(),
-                     "kernel": "decode_stage1_kernel<256,NP=4,DEPTH=3,split>", "peak_kind": peak_kind,
+                     "kernel": "decode_stage1_kernel<256,warps=8,DEPTH=3,split>", "peak_kind": peak_kind,
                      "kernel_us": round(kern_avg * 1e3, 2)},
         "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

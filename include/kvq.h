@@ -143,18 +143,20 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
  */
 /*
  * kvq_decode_auto_split_rows — the split size the split route uses when opts->split_rows is
- * 0, for a GPU with n_sms SMs (pure host arithmetic).  Stage 1 holds two CTAs per SM.
+ * 0, for a GPU with n_sms SMs (pure host arithmetic).  Stage 1 holds one CTA per SM at head_dim
+ * 256 and two at head_dim 128: slots = n_sms * (1 or 2).
  *   units = batch * n_kv_heads, pages = ceil(max_ctx / 16).
- *   If units * ceil(pages / 32) > 4 * n_sms (at 512-key splits the grid is over two waves),
- *   the split takes clamp(units * pages / (8 * n_sms), 32, 128) pages: longer splits
- *   amortise each CTA's start-up over more pages.
- *   Otherwise the split takes max(16, ceil(pages / floor(2 * n_sms / units))) pages: the
- *   grid fills every SM in one wave.
- * Returns keys (pages * 16); 0 if an argument is not positive.  The source pages use a
- * fixed 512 ([DOT4] route table); any split size gives the same result up to fp32
- * rounding.
+ *   If units * ceil(pages / 32) > 2 * slots (at 512-key splits the grid is over two waves),
+ *   the split takes clamp(units * pages / (4 * slots), 32, 128) pages: longer splits amortise
+ *   each CTA's start-up over more pages.
+ *   Otherwise the split takes max(16, ceil(pages / floor(slots / units))) pages: the grid fills
+ *   every SM in one wave.
+ * Returns keys (pages * 16); 0 if an argument is not positive or head_dim is not 128 / 256.
+ * The source pages use a fixed 512 ([DOT4] route table); any split size gives the same result
+ * up to fp32 rounding.
  */
-int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t max_ctx, int32_t n_sms);
+int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                                   int32_t n_sms);
 
 int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
                            int32_t n_q_heads, const int32_t* block_table,

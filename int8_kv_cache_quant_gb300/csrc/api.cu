@@ -125,15 +125,18 @@ static bool decode_split_route(const kvq_decode_opts& o, int32_t max_ctx) {
   return max_ctx > o.route_threshold;
 }
 
-int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t max_ctx, int32_t n_sms) {
+int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
+                                   int32_t n_sms) {
   if (batch <= 0 || n_kv_heads <= 0 || max_ctx <= 0 || n_sms <= 0) return 0;
+  if (head_dim != 128 && head_dim != 256) return 0;
+  const long long slots = static_cast<long long>(n_sms) * (head_dim == 256 ? 1 : 2);  // resident stage-1 CTAs
   const long long units = static_cast<long long>(batch) * n_kv_heads;
   const long long pages = (static_cast<long long>(max_ctx) + KVQ_BLOCK_SIZE - 1) / KVQ_BLOCK_SIZE;
   long long split_pages;
-  if (units * ((pages + 31) / 32) > 4LL * n_sms) {
-    split_pages = std::min(128LL, std::max(32LL, units * pages / (8LL * n_sms)));
+  if (units * ((pages + 31) / 32) > 2 * slots) {
+    split_pages = std::min(128LL, std::max(32LL, units * pages / (4 * slots)));
   } else {
-    const long long per_unit = std::max(1LL, (2LL * n_sms) / units);
+    const long long per_unit = std::max(1LL, slots / units);
     split_pages = std::max(16LL, (pages + per_unit - 1) / per_unit);
   }
   return static_cast<int32_t>(split_pages * KVQ_BLOCK_SIZE);
@@ -187,7 +190,7 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   if (split && o.split_rows == 0) {
     const int sms = device_sm_count();
     if (sms <= 0) return KVQ_ERR_CUDA;
-    o.split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, mc, sms);
+    o.split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, cache->head_dim, mc, sms);
   }
   kvq::DecodeArgs a{};
   a.k = cache->k;

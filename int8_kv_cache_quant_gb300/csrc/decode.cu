@@ -9,10 +9,14 @@
 // group is folded into the matrix dimension so each K/V page is read once per KV head).
 //
 // GB300 design.
-// * Grid over (split, KV head, sequence); one producer warp streams whole (page, head)
-//   blocks of K and V (4 KB each at head_dim 256, contiguous in the cache layout) and
-//   their 64-byte scale runs into a shared-memory ring with 1-D bulk copies (TMA) behind
-//   full/empty mbarriers.  Consumer warps each own whole pages of the ring.
+// * Grid over (split, KV head, sequence).  Each of the CTA's eight warps takes whole pages
+//   (warp w: pages w, w + 8, ...) and streams each (page, head) block of K and V (4 KB each
+//   at head_dim 256, contiguous in the cache layout) and its two 64-byte scale runs into its
+//   own DEPTH-stage shared-memory ring with 1-D bulk copies (TMA) completing on mbarriers;
+//   it refills a slot as soon as it has read the page in it.  A warp does QK, the online
+//   softmax and PV of a page over the whole head dimension: no exchange with another warp
+//   and no softmax computed twice.  The warps' partial results are merged at the end of the
+//   CTA.
 // * QK and PV of a 16-token page run on the tensor cores (mma.sync m16n8k16, fp32
 //   accumulate) with the int8 codes widened to integer-valued fp16 in registers (exact:
 //   |code| <= 127).  S^T = K * Q^T puts the 16 tokens on M and the GQA group (<= 8 heads)
@@ -46,63 +50,45 @@ __device__ __forceinline__ int row_token(int row) {
   return base + (((r >= 4) != (hi != 0)) ? 2 : 0);
 }
 
-template <int D, int NP, int DEPTH>
+template <int D, int NP, int DEPTH>  // NP consumer warps, DEPTH stages each
 struct DecodeSmem {
   static constexpr int kKvBytes = D * KVQ_BLOCK_SIZE;             // one (page, head) of K or V
   static constexpr int kStageBytes = 2 * kKvBytes + 2 * 64;       // K, V, k_scale, v_scale
-  static constexpr int kStages = NP * DEPTH;                      // DEPTH private stages per pair
+  static constexpr int kStages = NP * DEPTH;                      // DEPTH private stages per warp
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kQOffset = kRingBytes;                     // Q^T fragments (fp16)
   static constexpr int kQBytes = D * 16;                          // D/16 chunks x 2 x 8 heads x 16 B
-  static constexpr int kXOffset = kQOffset + kQBytes;             // partial-S exchange
-  static constexpr int kXBytes = NP * 2 * 2 * 32 * 16;            // [pair][buffer][half][lane] float4
-  static constexpr int kBarOffset = kXOffset + kXBytes;           // full barriers [pair][DEPTH]
-  static constexpr int kFlagOffset = kBarOffset + kStages * 8;    // page-ok flags [pair][DEPTH]
+  static constexpr int kBarOffset = kQOffset + kQBytes;           // full barriers [warp][DEPTH]
+  static constexpr int kFlagOffset = kBarOffset + kStages * 8;    // page-ok flags [warp][DEPTH]
   static constexpr int kCqOffset = kFlagOffset + kStages * 4;     // score factor per group head
   static constexpr int kTotal = kCqOffset + 8 * 4;
   static constexpr int kMergeBytes = (NP * 8 * (D + 4) + NP * 8 * 4 + 8 * NP + 32) * 4;  // merge scratch
   static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the ring");
-  static_assert(NP >= 4 && NP <= 8, "8..16 warps: one warp per group head prepares Q");
+  static_assert(NP >= 8 && NP <= 16, "8..16 warps: one warp per group head prepares Q");
 };
-
-// AND of `pred` over the 64 threads of named barrier `id` (both warps of a pair).
-__device__ __forceinline__ bool pair_sync_and(int id, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, 64, q;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u), "r"(id)
-      : "memory");
-  return r != 0;
-}
 
 constexpr float kLazyRescale = 8.0f;  // keep a running maximum until the tile exceeds it by 2^8
 
 }  // namespace
 
-// Stage 1.  CTA = NP warp pairs over the key range of one (split, KV head, sequence); pair p
-// takes pages p, p + NP, ... of the range and streams them into its own DEPTH-stage ring
-// (warp 0 of the pair issues the 1-D bulk copies).  The two warps of a pair split the head
-// dimension: each computes a partial S^T over its half, the halves are summed through shared
-// memory (both warps then hold the same S and run the same softmax), and each warp
-// accumulates O^T for its half of the head dimension.
+// Stage 1.  CTA = NP warps over the key range of one (split, KV head, sequence); warp p takes
+// pages p, p + NP, ... of the range through its own DEPTH-stage ring and accumulates S^T, the
+// softmax statistics and O^T over the whole head dimension.
 template <int D, int NP, int DEPTH, bool SPLIT>
-__global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
   using L = DecodeSmem<D, NP, DEPTH>;
   constexpr int KB = L::kKvBytes;
-  constexpr int NCH_H = D / 32;  // 16-dim chunks per half of the head dimension
-  constexpr int NMT_H = D / 32;  // 16-dim m-tiles of O^T per half
+  constexpr int NCH_H = D / 16;  // 16-dim chunks of the head dimension (whole, one warp)
+  constexpr int NMT_H = D / 16;  // 16-dim m-tiles of O^T
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;
   uint8_t* q_s = smem + L::kQOffset;
-  float4* xs = reinterpret_cast<float4*>(smem + L::kXOffset);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
   int* stage_ok = reinterpret_cast<int*>(smem + L::kFlagOffset);
   float* cq_s = reinterpret_cast<float*>(smem + L::kCqOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = warp >> 1, hf = warp & 1;
+  const int p = warp;  // each warp takes whole pages
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
 
@@ -134,16 +120,16 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
   }
   __syncthreads();  // the barriers are initialised before any copy completes on them
 
-  const int npp = (p < n_pages) ? (n_pages - p + NP - 1) / NP : 0;  // pages of this pair
+  const int npp = (p < n_pages) ? (n_pages - p + NP - 1) / NP : 0;  // pages of this warp
   const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
   uint64_t* pfull = full + p * DEPTH;
   int* pok = stage_ok + p * DEPTH;
   uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
 
-  // page ids of this pair, a window of 32 in warp 0's lanes (lane i <-> page k = wb + i)
+  // page ids of this warp, a window of 32 in its lanes (lane i <-> page k = wb + i)
   int wb = 0, pg = -1;
-  if (hf == 0 && lane < npp) pg = __ldg(bt + p + lane * NP);
-  // warp 0 of the pair, collectively: issue the copy of pair page k into its slot
+  if (lane < npp) pg = __ldg(bt + p + lane * NP);
+  // the warp, collectively: issue the copy of its page k into its slot
   auto issue = [&](int k) {
     while (k >= wb + 32) {
       wb += 32;
@@ -170,9 +156,7 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
     }
   };
   // The first copies go out before Q is prepared, so their HBM latency overlaps it.
-  if (hf == 0) {
-    for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
-  }
+  for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
 
   // ---- Q^T fragments: warp h prepares head h of the group (zeros past G).  The fp16 values
   // are q * 2^e (e brings max|q| into [2^14, 2^15): exact for bf16).  Chunk j (16 dims) is
@@ -231,9 +215,9 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
   // per-lane ldmatrix offsets: K rows are tokens (in row_token order), Q^T rows are heads,
   // V rows are head dimensions
   const int mi = lane >> 3, r = lane & 7;
-  const uint32_t k_lane_off = (mi >> 1) * 256 + row_token((mi & 1) * 8 + r) * 16 + hf * (NCH_H * 256);
-  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + (hf * NCH_H * 2 + mi) * 128 + r * 16;
-  const uint32_t v_lane_off = hf * (D / 2) * 16 + lane * 16;
+  const uint32_t k_lane_off = (mi >> 1) * 256 + row_token((mi & 1) * 8 + r) * 16;
+  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + mi * 128 + r * 16;
+  const uint32_t v_lane_off = lane * 16;
   const int tk0 = row_token(g), tk1 = row_token(g + 8);
   const uint32_t selA = (c < 2) ? kSelB01 : kSelB23;
   const uint32_t selB = (c < 2) ? kSelB23 : kSelB01;
@@ -247,7 +231,7 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
     const float* sks = reinterpret_cast<const float*>(st + 2 * KB);
     const float* svs = reinterpret_cast<const float*>(st + 2 * KB + 64);
 
-    // ---- partial S^T = K * Q^T over this warp's half of the head dimension
+    // ---- S^T = K * Q^T over the head dimension
     float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int jj = 0; jj < NCH_H / 2; ++jj) {
@@ -261,15 +245,10 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
       i8x4_to_h2x2(r3, kSelB01, kSelB23, a1, a3);
       mma_f16_16816(sb, a0, a1, a2, a3, q2, q3);
     }
-    float4* xb = xs + ((p * 2 + (k & 1)) * 2) * 32;
-    xb[hf * 32 + lane] = make_float4(sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]);
-    if (!pair_sync_and(1 + p, got)) break;  // both warps of the pair leave together
-    const float4 x0 = xb[lane], x1 = xb[32 + lane];
-    const float S[4] = {x0.x + x1.x, x0.y + x1.y, x0.z + x1.z, x0.w + x1.w};
-    // the slot of the previous page is free in both warps: refill it
-    if (hf == 0 && k >= 1 && k - 1 + DEPTH < npp) issue(k - 1 + DEPTH);
+    if (!__all_sync(0xffffffffu, got)) break;  // the warp leaves together
+    const float S[4] = {sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]};
 
-    // ---- online softmax (identical in both warps of the pair)
+    // ---- online softmax
     const bool page_ok = pok[s] != 0;
     const int tpage = t_begin + (p + k * NP) * KVQ_BLOCK_SIZE;
     const bool v0 = page_ok && (tpage + tk0 < t_end);
@@ -320,7 +299,7 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
     const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
     const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
 
-    // ---- O^T += V^T * W over this warp's half of the head dimension
+    // ---- O^T += V^T * W over the head dimension
 #pragma unroll
     for (int gg = 0; gg < NMT_H / 2; ++gg) {
       uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
@@ -334,32 +313,35 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
       mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bh0, bh1);
       mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bl0, bl1);
     }
+    // this page's slot is read: refill it with the warp's page k + DEPTH
+    __syncwarp();
+    if (k + DEPTH < npp) issue(k + DEPTH);
   }
-  // l over all tokens of the pair for heads 2c, 2c + 1
+  // l over all tokens of the warp for heads 2c, 2c + 1
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) lsum[i] += __shfl_xor_sync(0xffffffffu, lsum[i], off);
   }
 
-  // ------------------------------------------------------------ merge the pairs
+  // ------------------------------------------------------------ merge the warps
   grid_dep_trigger();  // the stage-2 merge may start launching
-  __syncthreads();  // every issued copy was waited for by its pair: the ring is free
+  __syncthreads();  // every issued copy was waited for by its warp: the ring is free
   constexpr int RS = D + 4;                                     // padded row: no bank conflicts
   float* mo = reinterpret_cast<float*>(smem);                   // [NP][8][RS]
   float* mstat = mo + NP * 8 * RS;                              // [NP][8][4]
-  float* mw = mstat + NP * 8 * 4;                               // [8][NP] weights of the pairs' O
+  float* mw = mstat + NP * 8 * 4;                               // [8][NP] weights of the warps' O
   float* mfin = mw + 8 * NP;                                    // [8][4]: Ms, Mz, l, final factor
 #pragma unroll
   for (int mt = 0; mt < NMT_H; ++mt) {
-    const int d0 = hf * (D / 2) + mt * 16 + g;
+    const int d0 = mt * 16 + g;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       mo[(p * 8 + 2 * c + i) * RS + d0] = o_acc[mt][i];
       mo[(p * 8 + 2 * c + i) * RS + d0 + 8] = o_acc[mt][2 + i];
     }
   }
-  if (hf == 0 && g == 0) {
+  if (g == 0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       float* stt = mstat + (p * 8 + 2 * c + i) * 4;
@@ -370,7 +352,7 @@ __global__ void __launch_bounds__(NP * 64) decode_stage1_kernel(DecodeArgs a) {
   }
   __syncthreads();
   if (threadIdx.x < G) {
-    // per head: the pairs' maxima, the merged l and one weight per pair (exp once per pair)
+    // per head: the warps' maxima, the merged l and one weight per warp (exp once per warp)
     const int hh = threadIdx.x;
     float Ms = -INFINITY, Mz = -INFINITY;
     for (int q2 = 0; q2 < NP; ++q2) {
@@ -531,7 +513,7 @@ static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t st
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, stream)) != cudaSuccess) return e;
-  if ((e = launch_pdl(kern, grid, dim3(NP * 64), L::kTotal, stream, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(kern, grid, dim3(NP * 32), L::kTotal, stream, a)) != cudaSuccess) return e;
   if (a.ev_end && (e = cudaEventRecord(a.ev_end, stream)) != cudaSuccess) return e;
   return cudaSuccess;
 }
@@ -540,14 +522,14 @@ cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t s
   if (route == DecodeRoute::kSingle) {
     dim3 grid(1, a.n_kv_heads, a.batch);
     if (a.head_dim == 256) return launch_stage1<256, 8, 3, false>(a, grid, stream);
-    return launch_stage1<128, 8, 4, false>(a, grid, stream);
+    return launch_stage1<128, 8, 3, false>(a, grid, stream);
   }
   dim3 grid(a.n_split, a.n_kv_heads, a.batch);
   cudaError_t e;
   if (a.head_dim == 256)
-    e = launch_stage1<256, 4, 3, true>(a, grid, stream);
+    e = launch_stage1<256, 8, 3, true>(a, grid, stream);
   else
-    e = launch_stage1<128, 4, 4, true>(a, grid, stream);
+    e = launch_stage1<128, 8, 3, true>(a, grid, stream);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.n_split) * sizeof(float);
   dim3 g2(a.n_q_heads, a.batch, a.head_dim / kMergeCols);

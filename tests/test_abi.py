@@ -32,13 +32,15 @@ def test_host_helpers_without_gpu():
     # automatic split size: the workspace is the bound for its smallest split (256 keys)
     assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 128 * 24 * 256 * 4 + 128 * 24 * 16
     assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256, split_rows=512) == 64 * 24 * 256 * 4 + 64 * 24 * 16
-    # the automatic rule: one wave of two CTAs per SM for few (sequence, KV head) units,
-    # 2048-key splits for a large batch; never below 256 keys
-    assert k.kvq_decode_auto_split_rows(1, 4, 32768, 152) == 432      # 76 splits x 4 = 304 CTAs
-    assert k.kvq_decode_auto_split_rows(64, 8, 16384, 152) == 2048
-    assert k.kvq_decode_auto_split_rows(1, 4, 4096, 152) == 256
-    assert k.kvq_decode_auto_split_rows(1, 1, 1 << 20, 152) == 848
-    assert k.kvq_decode_auto_split_rows(0, 4, 4096, 152) == 0
+    # the automatic rule: one wave of resident CTAs (one per SM at head_dim 256, two at 128) for
+    # few (sequence, KV head) units, 2048-key splits for a large batch; never below 256 keys
+    assert k.kvq_decode_auto_split_rows(1, 4, 256, 32768, 152) == 864   # 38 splits x 4 = 152 CTAs
+    assert k.kvq_decode_auto_split_rows(1, 4, 128, 32768, 152) == 432   # 76 x 4 = 304 (two per SM)
+    assert k.kvq_decode_auto_split_rows(64, 8, 128, 16384, 152) == 2048
+    assert k.kvq_decode_auto_split_rows(1, 4, 256, 4096, 152) == 256
+    assert k.kvq_decode_auto_split_rows(1, 1, 256, 1 << 20, 152) == 1712
+    assert k.kvq_decode_auto_split_rows(0, 4, 256, 4096, 152) == 0
+    assert k.kvq_decode_auto_split_rows(1, 4, 192, 4096, 152) == 0
     assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 0  # single-CTA route
     # prefill: Q codes | Q scales | widened K and V of 256 tiles x 4 KV heads (2 bytes per code) |
     # their key and value scales
