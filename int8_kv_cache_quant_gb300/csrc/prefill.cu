@@ -111,24 +111,6 @@ struct PrefillSmem {
 constexpr float kLog2eP = 1.44269504088896341f;
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
-// The specified exp2 of the P-code decisions (the same function, step for step, as the CPU
-// reference): Cody-Waite reduction x = n + f with n = rint(x), 2^f by the degree-5 Taylor
-// polynomial of e^{f ln 2} (Horner, fp32 fma), times 2^n; x < -125 gives 0.
-__device__ __forceinline__ float exp2_det(float x) {
-  if (!(x >= -125.0f)) return 0.0f;
-  x = fminf(x, 125.0f);
-  const float t = __fadd_rn(x, kMagic);
-  const float n = __fsub_rn(t, kMagic);
-  const float f = __fsub_rn(x, n);
-  float p = __fmaf_rn(0.00133335581464284f, f, 0.00961812910762848f);
-  p = __fmaf_rn(p, f, 0.0555041086648216f);
-  p = __fmaf_rn(p, f, 0.240226506959101f);
-  p = __fmaf_rn(p, f, 0.693147180559945f);
-  p = __fmaf_rn(p, f, 1.0f);
-  const int ni = __float2int_rz(n);
-  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
-}
-
 // Packed fp32 pairs (add / mul / fma .rn.f32x2): each lane is rounded exactly like the scalar
 // operation, so these give the same bits as __fadd_rn / __fmul_rn / __fmaf_rn per element with
 // half the instructions.
@@ -173,23 +155,25 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
   return r;
 }
 
-// exp2_det of a pair, the same operations per element, for arguments x <= 0 up to one rounding
-// (the attention kernels pass x = fma(y, a, -m) with m >= fl(ymax * a) >= fl(y * a) and a >= 0,
-// so the specified clamp at +125 never acts and is left out): x < -125 (or NaN) -> 0;
-// n = rint(x) through the 1.5 * 2^23 magic sum t, f = x - n (exact, as one fma), the degree-5
-// Horner polynomial p = 2^f in [0.70, 1.42], and p * 2^n as an exponent-field add: the product
-// is normal for n in [-125, 0], so it equals bits(p) + n * 2^23, and n * 2^23 == bits(t) * 2^23
-// (mod 2^32) because bits(t) = 0x4B400000 + n and 0x4B400000 * 2^23 == 0 (mod 2^32).
+// The specified exp2 of the P-code decisions (the same function, step for step, as the CPU
+// reference): Cody-Waite reduction x = n + f with n = rint(x), 2^f by the degree-4 polynomial
+// with constant term 1 fitted to the minimax relative error of 2^f on [-1/2, 1/2] (Horner,
+// fp32 fma), times 2^n; x < -125 gives 0.  Here on a pair, the same operations per element,
+// for arguments x <= 0 up to one rounding (the attention kernels pass x = fma(y, a, -m) with
+// m >= fl(ymax * a) >= fl(y * a) and a >= 0, so the specified clamp at +125 never acts and is
+// left out): n = rint(x) through the 1.5 * 2^23 magic sum t, f = x - n (exact), the
+// polynomial p in [0.70, 1.42], and p * 2^n as an exponent-field add: the product is normal for
+// n in [-125, 0], so it equals bits(p) + n * 2^23, and n * 2^23 == bits(t) * 2^23 (mod 2^32)
+// because bits(t) = 0x4B400000 + n and 0x4B400000 * 2^23 == 0 (mod 2^32).
 __device__ __forceinline__ f2 exp2_det2(f2 x) {
   const bool v0 = lo2(x) >= -125.0f, v1 = hi2(x) >= -125.0f;
   const f2 magic = mk2(kMagic, kMagic);
   const f2 t = add2(x, magic);
   const f2 n = sub2(t, magic);
   const f2 f = sub2(x, n);
-  f2 p = fma2(mk2(0.00133335581464284f, 0.00133335581464284f), f, mk2(0.00961812910762848f, 0.00961812910762848f));
-  p = fma2(p, f, mk2(0.0555041086648216f, 0.0555041086648216f));
-  p = fma2(p, f, mk2(0.240226506959101f, 0.240226506959101f));
-  p = fma2(p, f, mk2(0.693147180559945f, 0.693147180559945f));
+  f2 p = fma2(mk2(0.00966636837f, 0.00966636837f), f, mk2(0.0559219755f, 0.0559219755f));
+  p = fma2(p, f, mk2(0.240223497f, 0.240223497f));
+  p = fma2(p, f, mk2(0.693121016f, 0.693121016f));
   p = fma2(p, f, mk2(1.0f, 1.0f));
   const uint32_t r0 = __float_as_uint(lo2(p)) + (__float_as_uint(lo2(t)) << 23);
   const uint32_t r1 = __float_as_uint(hi2(p)) + (__float_as_uint(hi2(t)) << 23);
