@@ -369,18 +369,20 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
 //               per MMA keep the tensor pipe fed).  PV uses N = head_dim, one MMA per k-step.
 //   warp 17     bulk-copy producer (lane 0): the widened K/V pieces through a ring of 16 KB
 //               shared-memory slots in the order the MMAs consume them, and the scales.
-// Tensor memory: S0 | S1 (128 columns each, double-buffered) | O (head_dim columns).  P codes
-// (fp16, 64 columns) are written back over the first 64 columns of their S buffer and read by
-// the PV MMA as its A operand; the next QK into that buffer is issued after that PV, and one
-// thread's tcgen05.mma operations execute in issue order.
+// Tensor memory: S (128 columns) | Q (head_dim / 2 columns of fp16 pairs, the A operand of QK) |
+// O (head_dim columns).  Q in tensor memory leaves QK reading only K from shared memory: with A
+// and B both there a 128 x 128 x 16 MMA needs the whole shared-memory bandwidth, which the
+// ring's bulk copies also use.  S is single-buffered: each softmax thread loads its S_j into
+// registers and releases the buffer at once, so QK_{j+1} overlaps the rest of the tile's softmax.
+// The P codes go to one of two shared-memory tiles (the A operand of PV).
 // A P code c is stored as the fp16 bit pattern c, i.e. the subnormal c * 2^-24: its two bytes
 // come straight from the rounding sum fma(w, r, 1.5 * 2^23), whose low byte is c.  The products
 // c * v * 2^-24 and their sums are exact in fp32 (a power-of-two scaling of the integer sums), so
 // O holds 2^-24 * sum_tiles (ps_tile / ps_ref) * PV_tile, and the epilogue multiplies by 2^24.
-// Per tile j (S buffer b = j % 2): MMA: QK_j (pieces of K_j) -> commit s_full[b]; then PV_{j-1}
-// (after p_full, pieces of V_{j-1}) -> commit pv_done; every piece's slot is released by a commit
-// after its MMAs.  Softmax: S_j after s_full[b] and the scales; P_j and the O rescale after
-// pv_done(j-1) -> arrive p_full.
+// Per tile j: MMA: QK_j (after s_free(j-1), pieces of K_j) -> commit s_full; then PV_{j-1} (after
+// p_full, pieces of V_{j-1}, P tile (j-1) % 2) -> commit pv_done; every piece's slot is released
+// by a commit after its MMAs.  Softmax: S_j after s_full and the scales -> arrive s_free; P_j
+// (into P tile j % 2, last read by PV_{j-2}) and the O rescale after pv_done(j-1) -> arrive p_full.
 namespace {
 
 constexpr int kRingSlots = 8;  // one K tile and one V tile: keeps each V piece pair in adjacent slots
@@ -388,8 +390,9 @@ constexpr int kScaleBufs = 4;
 
 template <int D>
 struct PrefillTmaSmem {
-  static constexpr int offQ = 0;                                        // D/64 pieces
-  static constexpr int offRing = offQ + (D / 64) * kPieceBytes;         // kRingSlots pieces
+  static constexpr int offP = 0;                                        // 2 P tiles [128 x 128] fp16
+  static constexpr int kPBytes = 2 * kPieceBytes;                        // two 64-key atom columns
+  static constexpr int offRing = offP + 2 * kPBytes;                    // kRingSlots pieces
   static constexpr int offScale = offRing + kRingSlots * kPieceBytes;   // [buf][k, v][128] fp32
   static constexpr int offRed = offScale + kScaleBufs * 2 * 128 * 4;    // [exchange][part][128]
   static constexpr int offBar = offRed + 2 * 4 * 128 * 4;
@@ -397,7 +400,8 @@ struct PrefillTmaSmem {
   static constexpr int offFlag = offBar + kNumBars * 8;                 // abort flag, TMEM base
   static constexpr int kBytes = offFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;
-  static constexpr uint32_t kTmemCols = 512;  // S0 | S1 | O
+  static constexpr uint32_t kTmemCols = 512;  // S | Q | O
+  static constexpr uint32_t kQCol = 128;      // Q codes as fp16 pairs: D/2 columns
   static constexpr uint32_t kOCol = 256;
 };
 
@@ -406,7 +410,7 @@ constexpr int kBarFull = 0;                            // [kRingSlots] piece lan
 constexpr int kBarEmpty = kBarFull + kRingSlots;       // [kRingSlots] piece consumed (commit)
 constexpr int kBarSclFull = kBarEmpty + kRingSlots;    // [kScaleBufs] scales landed (tx)
 constexpr int kBarSclFree = kBarSclFull + kScaleBufs;  // [kScaleBufs] scales read (softmax)
-constexpr int kBarS0 = kBarSclFree + kScaleBufs;       // S_j complete, buffer 0 / 1
+constexpr int kBarS0 = kBarSclFree + kScaleBufs;       // S_j complete (+0), S_j loaded by the softmax (+1)
 constexpr int kBarPvDone = kBarS0 + 2;
 constexpr int kBarPFull = kBarPvDone + 1;
 constexpr int kBarQFull = kBarPFull + 1;
@@ -477,7 +481,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
   constexpr int NP = D / 64;     // pieces per K tile and per V tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* qs = sm + L::offQ;
+  uint8_t* ps_smem = sm + L::offP;
   uint8_t* ring = sm + L::offRing;
   float* scale_s = reinterpret_cast<float*>(sm + L::offScale);  // [buf][0: k, 1: v][128]
   float* red = reinterpret_cast<float*>(sm + L::offRed);        // [exchange][part][128]
@@ -507,7 +511,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       mbar_init(&bars[kBarSclFree + s], kSoftmaxThreads);
     }
     mbar_init(&bars[kBarS0], 1);
-    mbar_init(&bars[kBarS0 + 1], 1);
+    mbar_init(&bars[kBarS0 + 1], kSoftmaxThreads);
     mbar_init(&bars[kBarPvDone], 1);
     mbar_init(&bars[kBarPFull], kSoftmaxThreads);
     mbar_init(&bars[kBarQFull], kSoftmaxThreads);
@@ -528,8 +532,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     const bool row_real = q0 + row < T;
     const int pos_r = a.history_len + q0 + row;
     {
-      // Q: this thread's D/64 16-code chunks of its row, widened into the swizzled Q operand
+      // Q: this thread's D/4 codes of its row, widened to fp16 pairs into tensor memory, the A
+      // operand of QK (lane = row, dim d in column kQCol + d / 2, even dims in the low half)
       const int8_t* src = a.q_codes + (static_cast<long long>(q0 + row) * Hq + h) * D;
+      uint32_t qw[D / 8];
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
         const int c16 = part * NP + i;
@@ -537,12 +543,22 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
         if (row_real) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
         uint4 c0, c1;
         widen16(raw, c0, c1);
-        uint8_t* piece = qs + (c16 >> 2) * kPieceBytes;
-        const int cc = (c16 & 3) * 2;
-        sts128(piece + tc::sw128_off(row, cc), c0);
-        sts128(piece + tc::sw128_off(row, cc + 1), c1);
+        qw[8 * i + 0] = c0.x;
+        qw[8 * i + 1] = c0.y;
+        qw[8 * i + 2] = c0.z;
+        qw[8 * i + 3] = c0.w;
+        qw[8 * i + 4] = c1.x;
+        qw[8 * i + 5] = c1.y;
+        qw[8 * i + 6] = c1.z;
+        qw[8 * i + 7] = c1.w;
       }
-      tc::fence_proxy_async_smem();
+      if constexpr (D == 256) {
+        tc::st_32x32b_x32(tmem + lane_base + L::kQCol + 32 * part, qw);
+      } else {
+        tc::st_32x32b_x16(tmem + lane_base + L::kQCol + 16 * part, qw);
+      }
+      tc::wait_st();
+      tc::fence_before_sync();
       mbar_arrive(&bars[kBarQFull]);
     }
     const float c2 = __fmul_rn(a.softmax_scale, kLog2eP);
@@ -563,12 +579,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     bool failed = false;  // a wait of this thread gave up; the group leaves together below
     for (int j = 0; j < n_tiles; ++j) {
       const int b = j & 1, sb = j & (kScaleBufs - 1);
-      failed |= !wait_or_abort(&bars[kBarS0 + b], (j >> 1) & 1, a.status, abort_flag);
+      failed |= !wait_or_abort(&bars[kBarS0], j & 1, a.status, abort_flag);
       tc::fence_after_sync();
       uint32_t sv[32];
-      tc::ld_32x32b_x32(tmem + lane_base + b * 128 + 32 * part, sv);
+      tc::ld_32x32b_x32(tmem + lane_base + 32 * part, sv);
       failed |= !wait_or_abort(&bars[kBarSclFull + sb], (j / kScaleBufs) & 1, a.status, abort_flag);
       tc::wait_ld();
+      tc::fence_before_sync();
+      mbar_arrive(&bars[kBarS0 + 1]);  // S_j is in registers: the next QK may overwrite it
       const float4* sk_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 0) * 128 + 32 * part);
       const float4* sv_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 1) * 128 + 32 * part);
       // visible keys of this row in this tile, counted from the start of this thread's part
@@ -625,7 +643,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       l_part = l_part * alpha + (lo2(psum) + hi2(psum));
       m = m_new;
       red_wmax[part * 128 + row] = wmax;
-      tc::fence_before_sync();  // every part has read its S before any writes P over it
+      tc::fence_before_sync();
       named_bar(gbar, 128);
       tc::fence_after_sync();
       const float wmax_row = max4_col(red_wmax, row);
@@ -666,7 +684,15 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
         failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
         tc::fence_after_sync();
       }
-      tc::st_32x32b_x16(tmem + lane_base + b * 128 + 16 * part, pk);  // P over S's first 64 columns
+      {
+        // P codes of keys 32 part .. 32 part + 31: four 16-byte chunks of row `row` in atom column
+        // part / 2 of P buffer b (buffer b was last read by PV_{j-2}, complete by pv_done(j-1))
+        uint8_t* pa = ps_smem + b * L::kPBytes + (part >> 1) * kPieceBytes;
+        const int cb = (part & 1) * 4;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          sts128(pa + tc::sw128_off(row, cb + q4), make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]));
+      }
       if (__any_sync(0xffffffffu, f != 1.0f)) {
         const f2 f2v = mk2(f, f);
 #pragma unroll
@@ -684,6 +710,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
         }
       }
       tc::wait_st();
+      tc::fence_proxy_async_smem();  // the P codes are read by the tensor core
       tc::fence_before_sync();
       mbar_arrive(&bars[kBarPFull]);
     }
@@ -714,7 +741,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     // ================================================================ MMA issue (the whole warp
     // runs the loop, one elected lane issues): descriptors stay on the uniform datapath and a
     // piece's k-steps differ only in the start-address field (+32 bytes = +2 per step).
-    const uint64_t qd0 = tc::sdesc_sw128(smem_u32(qs)), rd0 = tc::sdesc_sw128(smem_u32(ring));
+    const uint64_t pd0 = tc::sdesc_sw128(smem_u32(ps_smem)), rd0 = tc::sdesc_sw128(smem_u32(ring));
     constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
     const uint32_t tm_o = tmem + L::kOCol;
     int slot = 0;
@@ -722,19 +749,19 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag));
     for (int j = 0; ok && j <= n_tiles; ++j) {
       if (j < n_tiles) {
-        const int b = j & 1;
+        // S is single-buffered: QK_j overwrites it once every softmax thread has loaded S_{j-1}
+        if (j >= 1) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarS0 + 1], (j - 1) & 1, a.status, abort_flag));
         for (int qa = 0; ok && qa < NP; ++qa) {
           ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag));
           if (!ok) break;
           if (elect_one()) {
             tc::fence_after_sync();
             const uint64_t kd = rd0 + static_cast<uint64_t>((slot * kPieceBytes) >> 4);
-            const uint64_t qd = qd0 + static_cast<uint64_t>((qa * kPieceBytes) >> 4);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-              tc::mma_f16_ss(tmem + b * 128, qd + 2 * s, kd + 2 * s, idesc, (qa | s) ? 1u : 0u);
+              tc::mma_f16_ts(tmem, tmem + L::kQCol + 32 * qa + 8 * s, kd + 2 * s, idesc, (qa | s) ? 1u : 0u);
             tc::commit(&bars[kBarEmpty + slot]);
-            if (qa == NP - 1) tc::commit(&bars[kBarS0 + b]);
+            if (qa == NP - 1) tc::commit(&bars[kBarS0]);
           }
           __syncwarp();
           if (++slot == kRingSlots) {
@@ -762,9 +789,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
           if (elect_one()) {
             tc::fence_after_sync();
             const uint64_t vd = rd0 + static_cast<uint64_t>((s0 * kPieceBytes) >> 4);
+            const uint64_t pd = pd0 + static_cast<uint64_t>((bp * L::kPBytes + kh * kPieceBytes) >> 4);
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-              tc::mma_f16_ts(tm_o, tmem + bp * 128 + 32 * kh + 8 * s, vd + 2 * s, idesc_pv, 1u);
+              tc::mma_f16_ss(tm_o, pd + 2 * s, vd + 2 * s, idesc_pv, 1u);
 #pragma unroll
             for (int dh = 0; dh < D / 128; ++dh) tc::commit(&bars[kBarEmpty + s0 + dh]);
             if (kh == 1) tc::commit(&bars[kBarPvDone]);
