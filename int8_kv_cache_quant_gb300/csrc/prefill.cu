@@ -156,17 +156,17 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
 }
 
 // The specified exp2 of the P-code decisions (the same function, step for step, as the CPU
-// reference): Cody-Waite reduction x = n + f with n = rint(x), 2^f by the degree-4 polynomial
-// with constant term 1 fitted to the minimax relative error of 2^f on [-1/2, 1/2] (Horner,
-// fp32 fma), times 2^n; x < -125 gives 0.  Here on a pair, the same operations per element,
-// for arguments x <= 0 up to one rounding (the attention kernels pass x = fma(y, a, -m) with
-// m >= fl(ymax * a) >= fl(y * a) and a >= 0, so the specified clamp at +125 never acts and is
-// left out): n = rint(x) through the 1.5 * 2^23 magic sum t, f = x - n (exact), the
-// polynomial p in [0.70, 1.42], and p * 2^n as an exponent-field add: the product is normal for
-// n in [-125, 0], so it equals bits(p) + n * 2^23, and n * 2^23 == bits(t) * 2^23 (mod 2^32)
-// because bits(t) = 0x4B400000 + n and 0x4B400000 * 2^23 == 0 (mod 2^32).
-__device__ __forceinline__ f2 exp2_det2(f2 x) {
-  const bool v0 = lo2(x) >= -125.0f, v1 = hi2(x) >= -125.0f;
+// reference): the argument clamped to [-125, 125] (fmaxf / fminf: NaN becomes -125), Cody-Waite
+// reduction x = n + f with n = rint(x), 2^f by the degree-4 polynomial with constant term 1
+// fitted to the minimax relative error of 2^f on [-1/2, 1/2] (Horner, fp32 fma), times 2^n.
+// Here on a pair, the same operations per element, for arguments x <= 0 up to one rounding (the
+// attention kernels pass x = fma(y, a, -m) with m >= fl(ymax * a) >= fl(y * a) and a >= 0, so
+// the clamp at +125 never acts and is left out): n = rint(x) through the 1.5 * 2^23 magic sum t,
+// f = x - n (exact), the polynomial p in [0.70, 1.42], and p * 2^n as an exponent-field add: the
+// product is normal for n in [-125, 0], so it equals bits(p) + n * 2^23, and n * 2^23 ==
+// bits(t) * 2^23 (mod 2^32) because bits(t) = 0x4B400000 + n and 0x4B400000 * 2^23 == 0 (mod 2^32).
+__device__ __forceinline__ f2 exp2_det2(f2 xin) {
+  const f2 x = mk2(fmaxf(lo2(xin), -125.0f), fmaxf(hi2(xin), -125.0f));
   const f2 magic = mk2(kMagic, kMagic);
   const f2 t = add2(x, magic);
   const f2 n = sub2(t, magic);
@@ -177,7 +177,7 @@ __device__ __forceinline__ f2 exp2_det2(f2 x) {
   p = fma2(p, f, mk2(1.0f, 1.0f));
   const uint32_t r0 = __float_as_uint(lo2(p)) + (__float_as_uint(lo2(t)) << 23);
   const uint32_t r1 = __float_as_uint(hi2(p)) + (__float_as_uint(hi2(t)) << 23);
-  return mk2(v0 ? __uint_as_float(r0) : 0.0f, v1 ? __uint_as_float(r1) : 0.0f);
+  return mk2(__uint_as_float(r0), __uint_as_float(r1));
 }
 
 // 16 int8 codes (one int4) -> two 16-byte chunks of 8 fp16 (exact integer values).
@@ -623,11 +623,16 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       f2 psum = mk2(0.0f, 0.0f);
       float wm0 = 0.0f, wm1 = 0.0f;
       const f2 a2 = mk2(a_row, a_row), nm2 = mk2(-m_new, -m_new);
-#pragma unroll
-      for (int n = 0; n < 32; n += 4) {
+      // p of the four keys n .. n+3, w = p * sV back into sv, and the running sums; masked keys
+      // (only on tiles that carry them: the diagonal and past the context) get p = 0
+      auto pass2_step = [&](int n, bool masked) {
         const float4 v4 = sv_t[n >> 2];
-        const f2 pa = exp2_det2(fma2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), a2, nm2));
-        const f2 pb = exp2_det2(fma2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), a2, nm2));
+        f2 pa = exp2_det2(fma2(mk2(__uint_as_float(sv[n]), __uint_as_float(sv[n + 1])), a2, nm2));
+        f2 pb = exp2_det2(fma2(mk2(__uint_as_float(sv[n + 2]), __uint_as_float(sv[n + 3])), a2, nm2));
+        if (masked) {
+          pa = mk2(n < lim ? lo2(pa) : 0.0f, n + 1 < lim ? hi2(pa) : 0.0f);
+          pb = mk2(n + 2 < lim ? lo2(pb) : 0.0f, n + 3 < lim ? hi2(pb) : 0.0f);
+        }
         psum = add2(psum, add2(pa, pb));
         const f2 wa = mul2(pa, mk2(v4.x, v4.y));
         const f2 wb = mul2(pb, mk2(v4.z, v4.w));
@@ -637,6 +642,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
         sv[n + 3] = __float_as_uint(hi2(wb));
         wm0 = fmax3(wm0, lo2(wa), hi2(wa));
         wm1 = fmax3(wm1, lo2(wb), hi2(wb));
+      };
+      if (lim < 32) {
+#pragma unroll
+        for (int n = 0; n < 32; n += 4) pass2_step(n, true);
+      } else {
+#pragma unroll
+        for (int n = 0; n < 32; n += 4) pass2_step(n, false);
       }
       const float wmax = fmaxf(wm0, wm1);
       mbar_arrive(&bars[kBarSclFree + sb]);  // this tile's scales are no longer read

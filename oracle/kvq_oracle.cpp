@@ -132,15 +132,15 @@ void quant_row(const uint16_t* x, int n, int8_t* codes, float* scale_out) {
 }
 
 // Deterministic base-2 exponential shared, as a specification, by the oracle and the
-// CUDA prefill kernel (each has its own code): Cody-Waite range reduction x = n + f with
-// n = rint(x), f in [-1/2, 1/2], then 2^f by a degree-4 polynomial with constant term 1,
-// fitted to the minimax relative error of 2^f on [-1/2, 1/2], in Horner form with fp32 fma,
-// then scaling by 2^n.  Relative error against 2^x is below 3.6e-6 (fit error plus fp32
-// rounding); integers are exact (f = 0 gives p = 1).  x < -125 (and -inf) gives 0.  It exists
-// so that the P-code decisions below are the same fp32 decisions on both sides.
+// CUDA prefill kernel (each has its own code): the argument is clamped to [-125, 125] (with the
+// fmax / fmin rule, so NaN becomes -125), then Cody-Waite range reduction x = n + f with
+// n = rint(x), f in [-1/2, 1/2], 2^f by a degree-4 polynomial with constant term 1, fitted to
+// the minimax relative error of 2^f on [-1/2, 1/2], in Horner form with fp32 fma, and scaling
+// by 2^n.  Relative error against 2^x is below 3.6e-6 on [-125, 125] (fit error plus fp32
+// rounding); integers are exact (f = 0 gives p = 1); below -125 the result is 2^-125.  It
+// exists so that the P-code decisions below are the same fp32 decisions on both sides.
 float exp2_det(float x) {
-  if (!(x >= -125.0f)) return 0.0f;
-  if (x > 125.0f) x = 125.0f;
+  x = std::fmin(std::fmax(x, -125.0f), 125.0f);
   const float magic = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
   float t = x + magic;
   float n = t - magic;
