@@ -39,6 +39,9 @@ def _load():
         lib.oracle_quant_rows.argtypes = [vp, i64, i32, vp, vp]
         lib.oracle_kv_quant_write.restype = i32
         lib.oracle_kv_quant_write.argtypes = [vp, vp, vp, i32, vp, vp, vp, i32, i32]
+        lib.oracle_rope_quant_write.restype = i32
+        lib.oracle_rope_quant_write.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32,
+                                                vp, vp, vp]
         lib.oracle_decode_f64.argtypes = [vp, vp, i32, i32, vp, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_decode_split_f64.argtypes = [vp, vp, i32, i32, vp, i32, vp, f64, i32, vp, i32]
         lib.oracle_prefill_ref_f64.argtypes = [vp, vp, i32, i32, i32, vp, f64, vp, i32, vp, i32]
@@ -114,6 +117,34 @@ def kv_quant_write(cache, k_new, v_new, seq_idx, pos, block_table):
     return int(_load().oracle_kv_quant_write(ctypes.byref(s), _ptr(k_new), _ptr(v_new),
                                              len(seq_idx), _ptr(seq_idx), _ptr(pos), _ptr(bt),
                                              bt.shape[0], bt.shape[1]))
+
+
+def rope_quant_write(cache, q, k_new, v_new, seq_idx, pos, block_table, cos_sin, rotary_dim):
+    """Fused producer: RoPE on Q and K (table cos_sin [max_pos][rotary_dim] fp32), then the
+    quantisation rule; K/V into `cache`.  q: bf16 bits [T][Hq][D] or None.  Returns
+    (skipped, q_codes int8 [T][Hq][D], q_scales fp32 [T][Hq], q_rot bf16 bits [T][Hq][D])."""
+    k_new, v_new = _c(k_new, np.uint16), _c(v_new, np.uint16)
+    seq_idx, pos = _c(seq_idx, np.int32), _c(pos, np.int32)
+    cs = _c(cos_sin, np.float32)
+    bt = _c(block_table, np.int32)
+    if bt.ndim == 1:
+        bt = bt[None, :]
+    T = len(seq_idx)
+    D = cache.head_dim
+    if q is not None:
+        q = _c(q, np.uint16)
+        Hq = q.shape[1]
+    else:
+        Hq = 0
+    qc = np.zeros((T, Hq, D), np.int8)
+    qs = np.zeros((T, Hq), np.float32)
+    qr = np.zeros((T, Hq, D), np.uint16)
+    s = cache.struct()
+    skipped = int(_load().oracle_rope_quant_write(
+        ctypes.byref(s), _ptr(q) if q is not None else None, Hq, _ptr(k_new), _ptr(v_new), T,
+        _ptr(seq_idx), _ptr(pos), _ptr(bt), bt.shape[0], bt.shape[1], _ptr(cs), cs.shape[0],
+        int(rotary_dim), _ptr(qc), _ptr(qs), _ptr(qr)))
+    return skipped, qc, qs, qr
 
 
 def _units_arg(units):

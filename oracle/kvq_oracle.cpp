@@ -22,6 +22,9 @@
 // Parity status per function (what pins it is in tests/test_oracle_pins.py):
 //   oracle_quant_rows          pinned (hand-worked golden rows, closed-form properties)
 //   oracle_kv_quant_write      pinned (layout round trip, byte counts of [DCU] §1.1)
+//   oracle_rope_quant_write    pinned (identity table = plain producer; quarter and half turns
+//                              exact; norm of each rotated pair; relative-position property;
+//                              dims past rotary_dim untouched)
 //   oracle_decode_f64          pinned (closed forms: equal scores, ctx 1, two keys)
 //   oracle_decode_split_f64    pinned (equals the unsplit result for every split size)
 //   oracle_prefill_ref_f64     pinned (last row equals decode; closed forms)
@@ -114,9 +117,9 @@ void load_kv(const oracle_cache& c, const int32_t* bt_row, int pos, int head,
 // Reading: "round" is round-to-nearest-even (the IEEE default); both divisions are IEEE
 // fp32 as in the page's fragment code (§3.3 uses 127.0f); amax == 0 gives scale 0 and
 // zero codes (the page asks for a safe scale or an all-zero output).
-void quant_row(const uint16_t* x, int n, int8_t* codes, float* scale_out) {
+void quant_row_f32(const float* x, int n, int8_t* codes, float* scale_out) {
   float amax = 0.0f;
-  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(bf16_to_float(x[i])));
+  for (int i = 0; i < n; ++i) amax = std::max(amax, std::fabs(x[i]));
   float scale = amax / 127.0f;
   *scale_out = scale;
   for (int i = 0; i < n; ++i) {
@@ -124,10 +127,42 @@ void quant_row(const uint16_t* x, int n, int8_t* codes, float* scale_out) {
       codes[i] = 0;
       continue;
     }
-    float r = bf16_to_float(x[i]) / scale;
+    float r = x[i] / scale;
     float q = std::nearbyint(r);
     q = std::fmin(std::fmax(q, -127.0f), 127.0f);
     codes[i] = static_cast<int8_t>(q);
+  }
+}
+
+// B1 on a bf16 row (the values are exact in fp32).
+void quant_row(const uint16_t* x, int n, int8_t* codes, float* scale_out) {
+  std::vector<float> xf(n);
+  for (int i = 0; i < n; ++i) xf[i] = bf16_to_float(x[i]);
+  quant_row_f32(xf.data(), n, codes, scale_out);
+}
+
+// fp32 -> bf16 bits, round to nearest even (NaN stays a quiet NaN).
+uint16_t float_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return static_cast<uint16_t>((u >> 16) | 0x40u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Rotary position embedding of one row in place (fp32), the reading of [DCU] §2.2's
+// "apply_rope(q, position)": the rotate-half form over the first r = rotary_dim dims, with
+// cs = the table row of the position, cos of the r/2 frequencies then their sin:
+//   x1 = x[i], x2 = x[i + r/2] (i < r/2):  x[i] = fma(x1, c, -(x2 * s)),
+//                                          x[i + r/2] = fma(x2, c, x1 * s).
+// Dims at or past r are unchanged.  This operation order is the specification.
+void rope_row(float* x, const float* cs, int r) {
+  const int h = r / 2;
+  for (int i = 0; i < h; ++i) {
+    const float c = cs[i], sn = cs[h + i];
+    const float x1 = x[i], x2 = x[i + h];
+    x[i] = std::fma(x1, c, -(x2 * sn));
+    x[i + h] = std::fma(x2, c, x1 * sn);
   }
 }
 
@@ -263,6 +298,74 @@ int32_t oracle_kv_quant_write(oracle_cache* cache, const uint16_t* k_new,
       float sc;
       const uint16_t* krow = k_new + (static_cast<int64_t>(i) * H + h) * D;
       quant_row(krow, D, codes.data(), &sc);
+      for (int d = 0; d < D; ++d) c.k[k_offset(c, page, h, d, slot)] = codes[d];
+      c.k_scale[scale_offset(c, page, h, slot)] = sc;
+      const uint16_t* vrow = v_new + (static_cast<int64_t>(i) * H + h) * D;
+      quant_row(vrow, D, codes.data(), &sc);
+      for (int d = 0; d < D; ++d) c.v[v_offset(c, page, h, d, slot)] = codes[d];
+      c.v_scale[scale_offset(c, page, h, slot)] = sc;
+    }
+  }
+  return skipped;
+}
+
+// The fused producer ([DCU] §2.2: read Q/K/V, apply RoPE to Q and K, reduce absmax, quantise,
+// write the paged int8 K/V and their scales, quantise Q once): for token i at position pos[i],
+// the rows of K and Q are rotated by rope_row with table row cos_sin[pos[i]], then every row
+// (Q, rotated K, V) is quantised by B1 (quant_row_f32).  K/V go to the token's slot as in
+// oracle_kv_quant_write; Q gives q_codes [T][Hq][D], q_scales [T][Hq] and the rotated row
+// rounded to bf16 q_rot [T][Hq][D] (each output may be NULL; q may be NULL).  A token whose
+// position is outside [0, max_pos) writes no K/V and zero Q outputs; an invalid sequence or
+// page skips only the K/V write.  Returns the number of tokens whose K/V were not written.
+int32_t oracle_rope_quant_write(oracle_cache* cache, const uint16_t* q, int32_t n_q_heads,
+                                const uint16_t* k_new, const uint16_t* v_new, int32_t n_tokens,
+                                const int32_t* seq_idx, const int32_t* pos, const int32_t* block_table,
+                                int32_t num_seqs, int32_t max_blocks_per_seq, const float* cos_sin,
+                                int32_t max_pos, int32_t rotary_dim, int8_t* q_codes, float* q_scales,
+                                uint16_t* q_rot) {
+  const oracle_cache& c = *cache;
+  const int H = c.n_kv_heads, D = c.head_dim;
+  std::vector<int8_t> codes(D);
+  std::vector<float> row(D);
+  int32_t skipped = 0;
+  for (int i = 0; i < n_tokens; ++i) {
+    const int p = pos[i];
+    const bool pos_ok = p >= 0 && p < max_pos;
+    const float* cs = pos_ok ? cos_sin + static_cast<int64_t>(p) * rotary_dim : nullptr;
+    // Q: rotate, quantise, round the rotated row to bf16
+    for (int h = 0; q && h < n_q_heads; ++h) {
+      const int64_t u = static_cast<int64_t>(i) * n_q_heads + h;
+      float sc = 0.0f;
+      if (pos_ok) {
+        for (int d = 0; d < D; ++d) row[d] = bf16_to_float(q[u * D + d]);
+        rope_row(row.data(), cs, rotary_dim);
+        quant_row_f32(row.data(), D, codes.data(), &sc);
+      } else {
+        std::fill(row.begin(), row.end(), 0.0f);
+        std::fill(codes.begin(), codes.end(), 0);
+      }
+      if (q_codes) std::memcpy(q_codes + u * D, codes.data(), D);
+      if (q_scales) q_scales[u] = sc;
+      if (q_rot)
+        for (int d = 0; d < D; ++d) q_rot[u * D + d] = float_to_bf16(row[d]);
+    }
+    const int s = seq_idx[i];
+    if (!pos_ok || s < 0 || s >= num_seqs || p / c.block_size >= max_blocks_per_seq) {
+      ++skipped;
+      continue;
+    }
+    const int page = block_table[static_cast<int64_t>(s) * max_blocks_per_seq + p / c.block_size];
+    if (page < 0 || page >= c.num_blocks) {
+      ++skipped;
+      continue;
+    }
+    const int slot = p % c.block_size;
+    for (int h = 0; h < H; ++h) {
+      float sc;
+      const uint16_t* krow = k_new + (static_cast<int64_t>(i) * H + h) * D;
+      for (int d = 0; d < D; ++d) row[d] = bf16_to_float(krow[d]);
+      rope_row(row.data(), cs, rotary_dim);
+      quant_row_f32(row.data(), D, codes.data(), &sc);
       for (int d = 0; d < D; ++d) c.k[k_offset(c, page, h, d, slot)] = codes[d];
       c.k_scale[scale_offset(c, page, h, slot)] = sc;
       const uint16_t* vrow = v_new + (static_cast<int64_t>(i) * H + h) * D;

@@ -454,3 +454,99 @@ def test_sparse_workload_matches_page_shape():
     for i, p in enumerate(w["positions"]):
         cl = cells[off[i]:off[i + 1]]
         assert np.all(np.diff(cl) > 0) and cl[-1] == p and cl[-3] == p - 2 and cl[0] >= 0
+
+
+# --------------------------------------------------------------------------- fused producer (RoPE)
+
+def _rope_table(max_pos, r, base=10000.0):
+    inv = base ** (-np.arange(0, r, 2, dtype=np.float64) / r)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def _identity_table(max_pos, r):
+    return np.concatenate([np.ones((max_pos, r // 2)), np.zeros((max_pos, r // 2))], axis=1).astype(np.float32)
+
+
+def test_rope_identity_table_is_the_plain_producer(oracle):
+    rng = np.random.default_rng(21)
+    T, H, Hq, D = 37, 2, 6, 128
+    k = W.normal_bf16(rng, (T, H, D), outlier_p=0.02)
+    v = W.normal_bf16(rng, (T, H, D))
+    q = W.normal_bf16(rng, (T, Hq, D))
+    table = np.arange(3, dtype=np.int32)
+    c1, _ = make_cache(oracle, k, v, table=table, num_blocks=3)
+    c2 = oracle.HostCache(3, H, D)
+    skipped, qc, qs, qr = oracle.rope_quant_write(c2, q, k, v, np.zeros(T, np.int32), np.arange(T, dtype=np.int32),
+                                                  table[None, :], _identity_table(64, D), D)
+    assert skipped == 0
+    for a, b in ((c1.k, c2.k), (c1.v, c2.v), (c1.k_scale, c2.k_scale), (c1.v_scale, c2.v_scale)):
+        assert np.array_equal(a, b)
+    rc, rs = oracle.quant_rows(q)
+    assert np.array_equal(qc, rc) and np.array_equal(qs.view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(qr, q)
+
+
+def test_rope_quarter_and_half_turns_are_exact(oracle):
+    # head_dim 16, rotary_dim 8: pairs (i, i + 4) turned by 0, 90, 180, 270 degrees; the turned
+    # values are sign changes and swaps of bf16 values, so the expected row is exact:
+    # (x1, x2) -> (x1 cos - x2 sin, x2 cos + x1 sin)
+    D, r = 16, 8
+    x = np.array([1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 16], np.float32) * 0.25
+    cs = np.array([[1, 0, -1, 0, 0, 1, 0, -1]], np.float32)  # cos for the 4 pairs, then sin
+    expect = x.copy()
+    expect[0], expect[4] = x[0], x[4]        # 0 degrees
+    expect[1], expect[5] = -x[5], x[1]       # 90
+    expect[2], expect[6] = -x[2], -x[6]      # 180
+    expect[3], expect[7] = x[7], -x[3]       # 270
+    c = oracle.HostCache(1, 1, D)
+    kb = bf16(x)[None, None, :]
+    skipped, qc, qs, qr = oracle.rope_quant_write(c, kb, kb, kb, np.zeros(1, np.int32), np.zeros(1, np.int32),
+                                                  np.zeros((1, 1), np.int32), cs, r)
+    assert skipped == 0
+    assert np.array_equal(qr[0, 0], bf16(expect))
+    ec, es = oracle.quant_rows(bf16(expect)[None, :])
+    assert np.array_equal(qc[0, 0], ec[0]) and qs[0, 0] == es[0]
+    assert np.array_equal(c.k[0, 0, :, 0, :].reshape(D), ec[0]) and c.k_scale[0, 0, 0] == es[0]
+    # V is not rotated
+    vc, vs = oracle.quant_rows(kb[0])
+    assert np.array_equal(c.v[0, 0, :, 0], vc[0]) and c.v_scale[0, 0, 0] == vs[0]
+
+
+def test_rope_keeps_pair_norms_and_depends_on_relative_position(oracle):
+    rng = np.random.default_rng(22)
+    D, Hq, T = 128, 1, 12
+    base = W.normal_bf16(rng, (1, Hq, D))
+    q = np.repeat(base, T, axis=0)  # the same vector at positions 0, 7, 14, ...
+    pos = (np.arange(T) * 7).astype(np.int32)
+    cs = _rope_table(128, D)
+    c = oracle.HostCache(8, 1, D)
+    _, _, _, qr = oracle.rope_quant_write(c, q, q[:, :1], q[:, :1], np.zeros(T, np.int32), pos,
+                                          np.arange(8, dtype=np.int32)[None, :], cs, D)
+    x = W.bf16_bits_to_f32(base[0, 0]).astype(np.float64)
+    rot = W.bf16_bits_to_f32(qr[:, 0]).astype(np.float64)
+    h = D // 2
+    # each pair keeps its length (bf16 rounding of the output: 2^-8 relative)
+    n0 = x[:h] ** 2 + x[h:] ** 2
+    for t in range(T):
+        n1 = rot[t, :h] ** 2 + rot[t, h:] ** 2
+        assert np.all(np.abs(n1 - n0) <= 2 ** -7 * n0 + 1e-6)
+    # <R_m x, R_n x> depends on m - n only: positions (0, 7) vs (35, 42), (14, 28) vs (49, 63)
+    scale = float(x @ x)
+    for (a, b), (cc, dd) in (((0, 1), (5, 6)), ((2, 4), (7, 9)), ((1, 3), (8, 10))):
+        assert abs(rot[a] @ rot[b] - rot[cc] @ rot[dd]) <= 2e-2 * scale
+
+
+def test_rope_partial_rotary_and_bad_positions(oracle):
+    rng = np.random.default_rng(23)
+    D, Hq, T = 256, 3, 5
+    q = W.normal_bf16(rng, (T, Hq, D))
+    k = W.normal_bf16(rng, (T, 1, D))
+    c = oracle.HostCache(1, 1, D)
+    pos = np.array([0, 3, 9, 10, -1], np.int32)  # max_pos 10: the last two are out of range
+    skipped, qc, qs, qr = oracle.rope_quant_write(c, q, k, k, np.zeros(T, np.int32), pos,
+                                                  np.zeros((1, 1), np.int32), _rope_table(10, D // 2), D // 2)
+    assert skipped == 2
+    assert np.array_equal(qr[:3, :, D // 2:], q[:3, :, D // 2:])   # dims past rotary_dim untouched
+    assert not qr[3:].any() and not qc[3:].any() and not qs[3:].any()
+    assert np.array_equal(qr[0], q[0])                               # position 0 is the identity
