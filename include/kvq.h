@@ -104,6 +104,35 @@ int kvq_quant_write(const kvq_cache* cache, const void* k_new, const void* v_new
                     const int32_t* block_table, int32_t num_seqs,
                     int32_t max_blocks_per_seq, void* stream);
 
+/*
+ * kvq_rope_quant_write — the fused producer ([DCU] §2.2: one kernel reads Q/K/V, applies
+ * RoPE to Q and K, reduces absmax, quantises, writes the paged int8 K/V and their scales,
+ * and quantises Q once for the attention that follows).  For token i at position pos[i]:
+ *   RoPE (the pages name apply_rope(q, position); the reading is the rotate-half form over
+ *   the first r = rotary_dim dims with the caller's table row cs = cos_sin[pos[i]], the cos
+ *   of the r/2 frequencies then their sin), in fp32 with exactly these roundings:
+ *     dim j < r/2:       out = fma(x_j, cs[j], -(x_{j+r/2} * cs[r/2 + j]))
+ *     dim j + r/2:       out = fma(x_{j+r/2}, cs[j], x_j * cs[r/2 + j])
+ *     dims >= r unchanged;
+ *   then each K row (rotated), V row (not rotated) and Q row (rotated) is quantised by the
+ *   kvq_quant_write rule.  K/V codes and scales go to the token's slot as in
+ *   kvq_quant_write; Q gives q_codes, q_scales and the rotated row rounded to bf16 (q_rot).
+ *   q        : device bf16 [n_tokens][n_q_heads][head_dim], or NULL (no Q outputs)
+ *   cos_sin  : device fp32 [max_pos][rotary_dim], 16-byte aligned
+ *   rotary_dim: even, <= head_dim, (rotary_dim / 2) a multiple of head_dim / 32
+ *   q_codes  : device int8 [n_tokens][n_q_heads][head_dim] or NULL (8-byte aligned)
+ *   q_scales : device fp32 [n_tokens][n_q_heads] or NULL
+ *   q_rot    : device bf16 [n_tokens][n_q_heads][head_dim] or NULL (16-byte aligned)
+ * A token whose position is outside [0, max_pos) writes no K/V (KVQ_DEV_BAD_POS) and zero
+ * Q outputs; an invalid sequence or page skips the K/V write as in kvq_quant_write.
+ */
+int kvq_rope_quant_write(const kvq_cache* cache, const void* q, int32_t n_q_heads,
+                         const void* k_new, const void* v_new, int32_t n_tokens,
+                         const int32_t* seq_idx, const int32_t* pos, const int32_t* block_table,
+                         int32_t num_seqs, int32_t max_blocks_per_seq, const float* cos_sin,
+                         int32_t max_pos, int32_t rotary_dim, int8_t* q_codes, float* q_scales,
+                         void* q_rot, void* stream);
+
 /* Options of kvq_attn_decode_int8kv (pass NULL for the defaults). */
 typedef struct kvq_decode_opts {
   int32_t split_rows;      /* keys per split in the split route, a multiple of 16; 0 -> sized to
@@ -227,6 +256,19 @@ int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_token
                           const int32_t* block_table_row, int32_t n_blocks_row,
                           float softmax_scale, float* out, void* workspace,
                           size_t workspace_bytes, void* stream);
+
+/*
+ * kvq_attn_prefill_int8_qcodes — kvq_attn_prefill_int8 with Q already quantised (by
+ * kvq_rope_quant_write, [DCU] §2.2 "Query quantised once, reused"): the same attention, with
+ *   q_codes : device int8 [n_tokens][n_q_heads][head_dim] (16-byte aligned)
+ *   q_scales: device fp32 [n_tokens][n_q_heads]
+ * in place of bf16 q.  Same workspace.
+ */
+int kvq_attn_prefill_int8_qcodes(const kvq_cache* cache, const int8_t* q_codes, const float* q_scales,
+                                 int32_t n_tokens, int32_t n_q_heads, int32_t history_len,
+                                 const int32_t* block_table_row, int32_t n_blocks_row,
+                                 float softmax_scale, float* out, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /*
  * kvq_attn_sparse_int8kv — sparse prompt attention ([QSA] "Problem and result",

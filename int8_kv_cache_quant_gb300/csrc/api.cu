@@ -119,6 +119,53 @@ int kvq_quant_write(const kvq_cache* cache, const void* k_new, const void* v_new
   return cuda_status(kvq::launch_quant_write(a, static_cast<cudaStream_t>(stream)));
 }
 
+int kvq_rope_quant_write(const kvq_cache* cache, const void* q, int32_t n_q_heads, const void* k_new,
+                         const void* v_new, int32_t n_tokens, const int32_t* seq_idx, const int32_t* pos,
+                         const int32_t* block_table, int32_t num_seqs, int32_t max_blocks_per_seq,
+                         const float* cos_sin, int32_t max_pos, int32_t rotary_dim, int8_t* q_codes,
+                         float* q_scales, void* q_rot, void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (n_tokens < 0 || num_seqs <= 0 || max_blocks_per_seq <= 0 || max_pos <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens == 0) return KVQ_OK;
+  if (!k_new || !v_new || !seq_idx || !pos || !block_table || !cos_sin) return KVQ_ERR_INVALID_ARG;
+  if (q && n_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  const int D = cache->head_dim;
+  if (rotary_dim <= 0 || rotary_dim > D || rotary_dim % 2 != 0 || (rotary_dim / 2) % (D / 32) != 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(cos_sin)) return KVQ_ERR_MISALIGNED;
+  if ((q && !aligned16(q)) || (q_rot && !aligned16(q_rot))) return KVQ_ERR_MISALIGNED;
+  if (q_codes && reinterpret_cast<uintptr_t>(q_codes) % 8 != 0) return KVQ_ERR_MISALIGNED;
+  if ((q_scales && !aligned4(q_scales)) || !aligned4(seq_idx) || !aligned4(pos) || !aligned4(block_table))
+    return KVQ_ERR_MISALIGNED;
+  kvq::RopeQuantArgs r{};
+  r.kv.k = cache->k;
+  r.kv.v = cache->v;
+  r.kv.k_scale = cache->k_scale;
+  r.kv.v_scale = cache->v_scale;
+  r.kv.num_blocks = cache->num_blocks;
+  r.kv.n_kv_heads = cache->n_kv_heads;
+  r.kv.head_dim = D;
+  r.kv.k_new = k_new;
+  r.kv.v_new = v_new;
+  r.kv.n_tokens = n_tokens;
+  r.kv.seq_idx = seq_idx;
+  r.kv.pos = pos;
+  r.kv.block_table = block_table;
+  r.kv.num_seqs = num_seqs;
+  r.kv.max_blocks_per_seq = max_blocks_per_seq;
+  r.kv.status = status_ptr();
+  r.q = q;
+  r.n_q_heads = q ? n_q_heads : 0;
+  r.cos_sin = cos_sin;
+  r.max_pos = max_pos;
+  r.rotary_dim = rotary_dim;
+  r.q_codes = q_codes;
+  r.q_scales = q_scales;
+  r.q_rot = static_cast<uint16_t*>(q_rot);
+  return cuda_status(kvq::launch_rope_quant_write(r, static_cast<cudaStream_t>(stream)));
+}
+
 static bool decode_split_route(const kvq_decode_opts& o, int32_t max_ctx) {
   if (o.force_route == 1) return false;
   if (o.force_route == 2) return true;
@@ -297,6 +344,31 @@ int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_token
   e = kvq::launch_prefill(a, s);
   if (e != cudaSuccess) return e == cudaErrorNotSupported ? KVQ_ERR_UNSUPPORTED : KVQ_ERR_CUDA;
   return KVQ_OK;
+}
+
+int kvq_attn_prefill_int8_qcodes(const kvq_cache* cache, const int8_t* q_codes, const float* q_scales,
+                                 int32_t n_tokens, int32_t n_q_heads, int32_t history_len,
+                                 const int32_t* block_table_row, int32_t n_blocks_row, float softmax_scale,
+                                 float* out, void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q_codes || !q_scales || !block_table_row || !out) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(history_len) + n_tokens > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned4(q_scales) || !aligned16(out) || !aligned4(block_table_row))
+    return KVQ_ERR_MISALIGNED;
+  const size_t need = kvq_prefill_workspace_bytes(n_tokens, n_q_heads, cache->n_kv_heads, history_len,
+                                                  cache->head_dim);
+  if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
+  kvq::PrefillArgs a = prefill_args(cache, nullptr, n_tokens, n_q_heads, history_len, block_table_row,
+                                    n_blocks_row, softmax_scale, out, workspace);
+  a.q_codes = const_cast<int8_t*>(q_codes);
+  a.q_scales = const_cast<float*>(q_scales);
+  return cuda_status(kvq::launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
 int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_queries, int32_t n_q_heads,

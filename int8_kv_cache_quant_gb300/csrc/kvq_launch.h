@@ -27,6 +27,19 @@ struct QuantWriteArgs {
 };
 cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream);
 
+// Fused producer: RoPE on Q and K, the quantisation rule on Q, K and V; K/V into the cache.
+struct RopeQuantArgs {
+  QuantWriteArgs kv;      // the cache, k_new / v_new, tokens, slots
+  const void* q;          // bf16 [T][Hq][D] or nullptr
+  int n_q_heads;
+  const float* cos_sin;   // fp32 [max_pos][rotary_dim]: cos of rotary_dim / 2 frequencies, then sin
+  int max_pos, rotary_dim;
+  int8_t* q_codes;        // [T][Hq][D] or nullptr
+  float* q_scales;        // [T][Hq] or nullptr
+  uint16_t* q_rot;        // bf16 [T][Hq][D] or nullptr
+};
+cudaError_t launch_rope_quant_write(const RopeQuantArgs& a, cudaStream_t stream);
+
 // Decode: one query per sequence.  Stage 1 (both routes) walks a key range of one
 // (sequence, KV head); the single-CTA route writes `out` directly, the split route writes
 // partials that stage 2 merges.

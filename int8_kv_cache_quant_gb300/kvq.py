@@ -59,6 +59,9 @@ def lib():
         L.kvq_status_string.argtypes = [ctypes.c_int]
         L.kvq_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), vp]
         L.kvq_quant_write.argtypes = [cp, vp, vp, i32, vp, vp, vp, i32, i32, vp]
+        L.kvq_rope_quant_write.argtypes = [cp, vp, i32, vp, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32,
+                                           vp, vp, vp, vp]
+        L.kvq_attn_prefill_int8_qcodes.argtypes = [cp, vp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
         L.kvq_decode_workspace_bytes.restype = sz
         L.kvq_decode_auto_split_rows.restype = i32
         L.kvq_decode_auto_split_rows.argtypes = [i32, i32, i32, i32, i32]
@@ -129,6 +132,33 @@ def kvq_quant_write(cache, k_new, v_new, seq_idx, pos, block_table, stream=None)
     _check("kvq_quant_write", lib().kvq_quant_write(
         ctypes.byref(c), _p(k_new), _p(v_new), int(seq_idx.numel()), _p(seq_idx), _p(pos), _p(bt),
         int(bt.shape[0]), int(bt.shape[1]), _stream(stream)))
+
+
+def kvq_rope_quant_write(cache, q, k_new, v_new, seq_idx, pos, block_table, cos_sin, rotary_dim,
+                         q_codes=None, q_scales=None, q_rot=None, stream=None):
+    """Fused producer: RoPE on Q and K (cos_sin fp32 [max_pos][rotary_dim]), the quantisation
+    rule on Q, K and V; K/V into the cache.  q: bf16 [T][Hq][D] or None.  Returns
+    (q_codes int8 [T][Hq][D], q_scales fp32 [T][Hq], q_rot bf16 [T][Hq][D]), allocated when not
+    given (None when q is None)."""
+    bt = block_table if block_table.dim() == 2 else block_table.view(1, -1)
+    T = int(seq_idx.numel())
+    Hq = int(q.shape[1]) if q is not None else 0
+    D = cache.head_dim
+    if q is not None:
+        dev = q.device
+        if q_codes is None:
+            q_codes = torch.empty((T, Hq, D), dtype=torch.int8, device=dev)
+        if q_scales is None:
+            q_scales = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+        if q_rot is None:
+            q_rot = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    c = cache.struct()
+    _check("kvq_rope_quant_write", lib().kvq_rope_quant_write(
+        ctypes.byref(c), _p(q) if q is not None else None, Hq, _p(k_new), _p(v_new), T, _p(seq_idx), _p(pos),
+        _p(bt), int(bt.shape[0]), int(bt.shape[1]), _p(cos_sin), int(cos_sin.shape[0]), int(rotary_dim),
+        _p(q_codes) if q_codes is not None else None, _p(q_scales) if q_scales is not None else None,
+        _p(q_rot) if q_rot is not None else None, _stream(stream)))
+    return q_codes, q_scales, q_rot
 
 
 def _decode_opts(split_rows, route_threshold, force_route, events=None):
@@ -206,6 +236,23 @@ def kvq_attn_prefill_int8(cache, q, history_len, block_table_row, softmax_scale,
         ctypes.byref(c), _p(q), T, Hq, int(history_len), _p(block_table_row),
         int(block_table_row.numel()), float(softmax_scale), _p(out), _p(workspace), wbytes,
         _stream(stream)))
+    return out
+
+
+def kvq_attn_prefill_int8_qcodes(cache, q_codes, q_scales, history_len, block_table_row, softmax_scale,
+                                 out=None, workspace=None, stream=None):
+    """q_codes int8 [T][Hq][D], q_scales fp32 [T][Hq] (from kvq_rope_quant_write); returns fp32 [T][Hq][D]."""
+    T, Hq, D = q_codes.shape
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=q_codes.device)
+    need = kvq_prefill_workspace_bytes(T, Hq, cache.n_kv_heads, int(history_len), D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_codes.device)
+    wbytes = workspace.numel() * workspace.element_size()
+    c = cache.struct()
+    _check("kvq_attn_prefill_int8_qcodes", lib().kvq_attn_prefill_int8_qcodes(
+        ctypes.byref(c), _p(q_codes), _p(q_scales), T, Hq, int(history_len), _p(block_table_row),
+        int(block_table_row.numel()), float(softmax_scale), _p(out), _p(workspace), wbytes, _stream(stream)))
     return out
 
 
