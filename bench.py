@@ -384,6 +384,8 @@ def bench_extra(args, local, hbm, tflops, only=None):
         res.update(_extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps or 50))
     if want("decode_b64"):
         res.update(_extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps or 20, hbm))
+    if want("rope_quant_write"):
+        res.update(_extra_rope_quant_write(kvq, W, bf16, i32, timed, dev, reps or 20, hbm))
     if want("prefill_32k"):
         res.update(_extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps or 10, tflops))
     if want("sparse_32k"):
@@ -431,6 +433,44 @@ def _extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps, hbm):
                          "frac_of_hbm_peak": round(kvb / ms / 1e6 / hbm, 4),
                          "step": "kv_quant_write(64 tokens) + decode (split route)"}
     return res
+
+
+def _extra_rope_quant_write(kvq, W, bf16, i32, timed, dev, reps, hbm):
+    """The fused producer (RoPE on Q and K, quantisation of Q, K and V, paged K/V write) at two
+    shapes: the prefill_32k chunk (2048 tokens at positions 30720..32767, 24/4 heads, head_dim
+    256) and one decode_b64 step (64 tokens, 32/8 heads, head_dim 128).  Bytes: bf16 Q/K/V and
+    the table rows read; K/V codes and scales, Q codes, Q scales and bf16 rotated Q written."""
+    import numpy as np
+    import torch
+    res = {}
+    rng = np.random.default_rng(77)
+    for name, T, hq, hkv, d, max_pos, first in (("prefill_chunk", 2048, 24, 4, 256, 32768, 30720),
+                                                ("decode_b64_step", 64, 32, 8, 128, 16384, None)):
+        n_blocks = max_pos // 16
+        cache = kvq.KVCache(n_blocks * (1 if first is not None else 1), hkv, d, device=dev)
+        if first is not None:
+            pos = np.arange(first, first + T, dtype=np.int32)
+            seq = np.zeros(T, np.int32)
+            table = rng.permutation(n_blocks).astype(np.int32)[None, :]
+        else:  # one sequence per token, each with its own slice of pages
+            per = n_blocks // T
+            pos = rng.integers(0, per * 16, size=T).astype(np.int32)
+            seq = np.arange(T, dtype=np.int32)
+            table = rng.permutation(n_blocks)[: per * T].astype(np.int32).reshape(T, per)
+        inv = 1.0e6 ** (-np.arange(0, d, 2, dtype=np.float64) / d)
+        ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+        cs = torch.from_numpy(np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)).to(dev)
+        q, k, v = (bf16(W.normal_bf16(rng, (T, h, d))) for h in (hq, hkv, hkv))
+        qc = torch.empty((T, hq, d), dtype=torch.int8, device=dev)
+        qs = torch.empty((T, hq), dtype=torch.float32, device=dev)
+        qr = torch.empty((T, hq, d), dtype=torch.bfloat16, device=dev)
+        pos_d, seq_d, tab_d = i32(pos), i32(seq), i32(table)
+        ms = timed(lambda: kvq.kvq_rope_quant_write(cache, q, k, v, seq_d, pos_d, tab_d, cs, d, q_codes=qc,
+                                                    q_scales=qs, q_rot=qr), reps)
+        nbytes = T * ((hq + 2 * hkv) * d * 2 + d * 4 + 8 + 2 * hkv * (d + 4) + hq * (d + 4 + 2 * d))
+        res[name] = {"us_per_call": round(ms * 1e3, 2), "bytes": nbytes, "GBps": round(nbytes / ms / 1e6, 1),
+                     "frac_of_hbm_peak": round(nbytes / ms / 1e6 / hbm, 4)}
+    return {"rope_quant_write": res}
 
 
 def _extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps, tflops):
@@ -559,7 +599,7 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k", "decode_b64"],
+    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k", "decode_b64", "rope_quant_write"],
                     help="time only this secondary workload (profiling runs); prints its figures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
