@@ -146,13 +146,22 @@ def barrier(world):
 
 
 def max_over_ranks(x, world):
+    """Largest x over all ranks (the slowest replica's time).  The reduction tensor lives where
+    the process group's backend can reach it: device memory for NCCL, host memory for gloo."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_gbs(bytes_per_rank, ms_max, world):
+    """Whole-job throughput of N independent replicas: every rank moves bytes_per_rank per step,
+    and the job's step time is the slowest rank's."""
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------------------------- kvq arm
@@ -302,7 +311,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     achieved = kv_bytes / (kern_avg * 1e-3) / 1e9
     res = {
         "metric": METRIC,
-        "value": round(world * kv_bytes / (ms_step_max * 1e-3) / 1e9, 2),
+        "value": round(aggregate_gbs(kv_bytes, ms_step_max, world), 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
@@ -325,7 +334,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                      "frac": round(achieved / hbm, 4), "traffic": stage1_traffic(),
                      "kernel": "decode_stage1_kernel<256,warps=8,DEPTH=3,split>", "peak_kind": peak_kind,
                      "kernel_us": round(kern_avg * 1e3, 2)},
-        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(aggregate_gbs(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * K,
         "clocks": clk.summary(),
