@@ -43,6 +43,7 @@ def _load():
         lib.oracle_rope_quant_write.argtypes = [vp, vp, i32, vp, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32,
                                                 vp, vp, vp]
         lib.oracle_decode_f64.argtypes = [vp, vp, i32, i32, vp, i32, vp, f64, vp, i32, vp, i32]
+        lib.oracle_verify_f64.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_decode_split_f64.argtypes = [vp, vp, i32, i32, vp, i32, vp, f64, i32, vp, i32]
         lib.oracle_prefill_ref_f64.argtypes = [vp, vp, i32, i32, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_prefill_qk_int32.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp]
@@ -163,6 +164,20 @@ def decode_f64(cache, q, block_table, ctx_lens, scale, units=None, n_threads=0):
     out = np.zeros((B, Hq, D) if u is None else (nu, D), np.float64)
     s = cache.struct()
     _load().oracle_decode_f64(ctypes.byref(s), _ptr(q), B, Hq, _ptr(bt), bt.shape[1], _ptr(ctx),
+                              float(scale), _ptr(u), nu, _ptr(out), n_threads)
+    return out
+
+
+def verify_f64(cache, q, block_table, ctx_lens, scale, units=None, n_threads=0):
+    """Part A verify decode: q bf16 bits [B][nq][Hq][D] -> float64 [B][nq][Hq][D] (or
+    [n_units][D]).  Row i of sequence b sees keys t < ctx_lens[b] - nq + 1 + i."""
+    q = _c(q, np.uint16)
+    bt, ctx = _c(block_table, np.int32), _c(ctx_lens, np.int32)
+    B, nq, Hq, D = q.shape
+    u, nu = _units_arg(units)
+    out = np.zeros((B, nq, Hq, D) if u is None else (nu, D), np.float64)
+    s = cache.struct()
+    _load().oracle_verify_f64(ctypes.byref(s), _ptr(q), B, nq, Hq, _ptr(bt), bt.shape[1], _ptr(ctx),
                               float(scale), _ptr(u), nu, _ptr(out), n_threads)
     return out
 

@@ -407,6 +407,36 @@ void oracle_decode_f64(const oracle_cache* cache, const uint16_t* q, int32_t bat
   });
 }
 
+// Part A, verify decode (the multi-row decode of [DOT4] "Future Work", MTP verify with nq
+// query rows per sequence; "ROCm/RDNA4 (gfx1201) vLLM ..." row-shape routing, spec-verify
+// with 2-6 rows): sequence b holds ctx_lens[b] keys, the last nq of them the tokens being
+// verified; query row i of b sits at position ctx - nq + i and sees keys
+// t < ctx - nq + 1 + i (causal among the nq tokens; none when that bound is <= 0).
+// q and out are [batch][nq][n_q_heads][D]; unit u = (b * nq + i) * n_q_heads + h.
+void oracle_verify_f64(const oracle_cache* cache, const uint16_t* q, int32_t batch,
+                       int32_t nq, int32_t n_q_heads, const int32_t* block_table,
+                       int32_t max_blocks_per_seq, const int32_t* ctx_lens, double scale,
+                       const int64_t* units, int32_t n_units, double* out,
+                       int32_t n_threads) {
+  const oracle_cache& c = *cache;
+  const int D = c.head_dim, G = n_q_heads / c.n_kv_heads;
+  int64_t n = units ? n_units : static_cast<int64_t>(batch) * nq * n_q_heads;
+  parallel_for(n, n_threads, [&](int64_t j) {
+    int64_t u = unit_at(units, j);
+    int h = static_cast<int>(u % n_q_heads);
+    int64_t row = u / n_q_heads;
+    int i = static_cast<int>(row % nq), b = static_cast<int>(row / nq);
+    std::vector<double> qd(D);
+    bf16_row_to_double(q + u * D, D, qd.data());
+    int nk = std::min(ctx_lens[b], ctx_lens[b] - nq + 1 + i);
+    if (nk < 0) nk = 0;
+    std::vector<int32_t> keys(nk);
+    for (int t = 0; t < nk; ++t) keys[t] = t;
+    attend_f64(c, block_table + static_cast<int64_t>(b) * max_blocks_per_seq, qd.data(),
+               h / G, keys.data(), nk, scale, out + j * D);
+  });
+}
+
 // B5, decode through split-K ([DOT4] stage 1 + stage 2): each split of `split_rows` keys
 // yields (m_s, l_s, acc_s) with acc_s = sum_t e^{s_t - m_s} v^_t; the merge takes
 // M = max m_s, l = sum l_s e^{m_s - M}, o = sum acc_s e^{m_s - M} / l.

@@ -259,6 +259,71 @@ def test_units_sampling_matches_full(oracle):
     assert np.array_equal(part, full.reshape(-1, 128)[units])
 
 
+# --------------------------------------------------------------------------- verify decode
+
+def _verify_case(oracle, seed, ctx, nq, hq, hkv, d):
+    """Sequences b = 0.. with ctx[b] tokens in shuffled pages of one cache; returns the cache,
+    the block table, the logical K/V (bf16 bits [b][t][Hkv][D]) and q [B][nq][Hq][D]."""
+    rng = np.random.default_rng(seed)
+    B = len(ctx)
+    mb = max((c + 15) // 16 for c in ctx)
+    pages = rng.permutation(B * mb).astype(np.int32)
+    table = pages.reshape(B, mb)
+    cache = oracle.HostCache(B * mb, hkv, d)
+    ks, vs = [], []
+    for b, n in enumerate(ctx):
+        k = W.normal_bf16(rng, (n, hkv, d), outlier_p=0.02)
+        v = W.normal_bf16(rng, (n, hkv, d))
+        assert oracle.kv_quant_write(cache, k, v, np.full(n, b, np.int32), np.arange(n, dtype=np.int32),
+                                     table) == 0
+        ks.append(k)
+        vs.append(v)
+    q = W.normal_bf16(rng, (B, nq, hq, d))
+    return cache, table, ks, vs, q
+
+
+def test_verify_brute_force_causal_rows(oracle):
+    # numpy from the quantisation rule alone: row i of sequence b sees keys t <= ctx - nq + i;
+    # the second sequence is shorter than nq (its first row sees no key: zeros)
+    ctx, nq, hq, hkv, d, scale = [37, 2, 16], 3, 6, 2, 128, 0.09
+    cache, table, ks, vs, q = _verify_case(oracle, 31, ctx, nq, hq, hkv, d)
+    out = oracle.verify_f64(cache, q, table, np.array(ctx, np.int32), scale)
+    G = hq // hkv
+    qf = W.bf16_bits_to_f32(q).astype(np.float64)
+    for b, n in enumerate(ctx):
+        kc, ksc = oracle.quant_rows(ks[b])
+        vc, vsc = oracle.quant_rows(vs[b])
+        kh = kc.astype(np.float64) * ksc[..., None].astype(np.float64)   # [n][Hkv][D]
+        vh = vc.astype(np.float64) * vsc[..., None].astype(np.float64)
+        for i in range(nq):
+            nk = max(0, min(n, n - nq + 1 + i))
+            for h in range(hq):
+                if nk == 0:
+                    assert not out[b, i, h].any()
+                    continue
+                s = scale * (kh[:nk, h // G] @ qf[b, i, h])
+                p = np.exp(s - s.max())
+                ref = (p / p.sum()) @ vh[:nk, h // G]
+                assert np.allclose(out[b, i, h], ref, rtol=1e-11, atol=1e-13), (b, i, h)
+
+
+def test_verify_rows_equal_prefill_chunk_and_decode(oracle):
+    # the nq verify rows of a sequence are the causal chunk of nq queries after ctx - nq
+    # history keys; with nq = 1 verify is plain decode
+    ctx, nq, hq, hkv, d, scale = [70, 41], 4, 8, 2, 256, 0.0625
+    cache, table, _, _, q = _verify_case(oracle, 32, ctx, nq, hq, hkv, d)
+    out = oracle.verify_f64(cache, q, table, np.array(ctx, np.int32), scale)
+    for b, n in enumerate(ctx):
+        ref = oracle.prefill_ref_f64(cache, q[b], n - nq, table[b], scale)
+        assert np.array_equal(out[b], ref)
+    one = oracle.verify_f64(cache, q[:, :1], table, np.array(ctx, np.int32), scale)
+    dec = oracle.decode_f64(cache, q[:, 0], table, np.array(ctx, np.int32), scale)
+    assert np.array_equal(one[:, 0], dec)
+    units = np.array([0, 9, 31, 40, 63], np.int64)
+    part = oracle.verify_f64(cache, q, table, np.array(ctx, np.int32), scale, units=units)
+    assert np.array_equal(part, out.reshape(-1, d)[units])
+
+
 # --------------------------------------------------------------------------- prefill
 
 def _prefill_case(oracle, seed, history, T, hq=4, hkv=2, d=128, **kw):

@@ -17,6 +17,9 @@ involved, every input is synthetic):
   decode_b64     64 sequences, ctx uniform in [512, 16384], 32 query / 8 KV heads,
                  head_dim 128, one pool of pages shuffled and dealt to the sequences; each
                  step also writes one new token per sequence.
+  verify_32k     decode_32k's cache with 4 query rows per sequence (speculative / MTP verify):
+                 the last 4 tokens of the sequence are the ones being verified, row i at
+                 position ctx - 4 + i; each step rewrites those 4 tokens' K/V.
   sparse_32k     ctx 32768, 2048 queries at positions 30720..32767, 12 query heads on 1
                  KV head, head_dim 256, contiguous pages; query at position p attends to
                  sorted(2048 distinct positions uniform in [0, p-3] plus p-2, p-1, p).
@@ -35,6 +38,8 @@ CONFIGS = {
                         d=256, paged="shuffled", k_outlier_p=0.0),
     "decode_b64": dict(kind="decode", index=3, batch=64, ctx_range=(512, 16384), hq=32, hkv=8,
                        d=128, paged="shuffled", k_outlier_p=0.0),
+    "verify_32k": dict(kind="decode", index=5, batch=1, ctx=32768, hq=24, hkv=4, d=256, nq=4,
+                       paged="shuffled", k_outlier_p=0.01),
     "sparse_32k": dict(kind="sparse", index=4, ctx=32768, n_queries=2048, hq=12, hkv=1, d=256,
                        n_sample=2048, n_tail=3, paged="identity", k_outlier_p=0.0),
 }
@@ -126,13 +131,17 @@ def make(name, seed=None, **override):
                  split_rows=cfg.get("split_rows", 512))
         w["k_fill"] = normal_bf16(rng, (len(pos), hkv, d), cfg["k_outlier_p"])
         w["v_fill"] = normal_bf16(rng, (len(pos), hkv, d))
-        w["q"] = normal_bf16(rng, (B, hq, d))
-        # The step's new token of each sequence is its last position; its K/V rows are
-        # the ones already drawn for that position, so writing it again leaves the cache
-        # as generated and every step sees the same inputs.
-        last = np.cumsum(ctx) - 1
-        w.update(new_seq=np.arange(B, dtype=np.int32), new_pos=(ctx - 1).astype(np.int32),
-                 k_new=w["k_fill"][last], v_new=w["v_fill"][last])
+        nq = cfg.get("nq", 1)
+        w["nq"] = nq
+        w["q"] = normal_bf16(rng, (B, hq, d) if nq == 1 else (B, nq, hq, d))
+        # The step's new tokens of each sequence are its last nq positions; their K/V rows
+        # are the ones already drawn for those positions, so writing them again leaves the
+        # cache as generated and every step sees the same inputs.
+        end = np.cumsum(ctx)
+        rows = np.concatenate([np.arange(e - min(nq, c), e) for e, c in zip(end, ctx)]).astype(np.int64)
+        w.update(new_seq=np.repeat(np.arange(B, dtype=np.int32), np.minimum(nq, ctx)),
+                 new_pos=np.concatenate([np.arange(c - min(nq, c), c) for c in ctx]).astype(np.int32),
+                 k_new=w["k_fill"][rows], v_new=w["v_fill"][rows])
     elif kind == "prefill":
         hist, T = cfg["history"], cfg["chunk"]
         ctx = hist + T
