@@ -393,6 +393,8 @@ def bench_extra(args, local, hbm, tflops, only=None):
         res.update(_extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps or 50))
     if want("decode_b64"):
         res.update(_extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps or 20, hbm))
+    if want("verify_32k"):
+        res.update(_extra_verify_32k(kvq, W, bf16, i32, timed, dev, reps or 30, hbm))
     if want("rope_quant_write"):
         res.update(_extra_rope_quant_write(kvq, W, bf16, i32, timed, dev, reps or 20, hbm))
     if want("prefill_32k"):
@@ -442,6 +444,38 @@ def _extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps, hbm):
                          "frac_of_hbm_peak": round(kvb / ms / 1e6 / hbm, 4),
                          "step": "kv_quant_write(64 tokens) + decode (split route)"}
     return res
+
+
+def _extra_verify_32k(kvq, W, bf16, i32, timed, dev, reps, hbm):
+    """verify_32k: one speculative-verify step on decode_32k's cache shape (ctx 32768, 24/4,
+    head_dim 256): kv_quant_write of the 4 drafted tokens, then the 4-row verify decode
+    (automatic split).  Bytes: the K/V codes and scales of all 32768 keys, read once for
+    the 4 rows."""
+    import torch
+    w = W.make("verify_32k")
+    cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
+    bt = i32(w["block_table"])
+    kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
+    q, ctx = bf16(w["q"]), i32(w["ctx_lens"])
+    kn, vn, ns, npos = bf16(w["k_new"]), bf16(w["v_new"]), i32(w["new_seq"]), i32(w["new_pos"])
+    B, nq, Hq, D = w["batch"], w["nq"], w["hq"], w["d"]
+    out = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, kvq.kvq_verify_workspace_bytes(B, nq, Hq, w["max_ctx"], D)), dtype=torch.uint8,
+                     device=dev)
+
+    def verify():
+        kvq.kvq_attn_verify_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out, workspace=ws)
+
+    def step():
+        kvq.kvq_quant_write(cache, kn, vn, ns, npos, bt)
+        verify()
+    ms = timed(step, reps)
+    ms_verify = timed(verify, reps)
+    kvb = w["max_ctx"] * (2 * w["hkv"] * D + 8 * w["hkv"])
+    return {"verify_32k": {"us_per_step": round(ms * 1e3, 2), "us_verify": round(ms_verify * 1e3, 2),
+                           "rows": nq, "kv_bytes": kvb, "kv_GBps": round(kvb / ms / 1e6, 1),
+                           "verify_frac_of_hbm_peak": round(kvb / ms_verify / 1e6 / hbm, 4),
+                           "step": "kv_quant_write(4 tokens) + verify decode (4 rows, split route)"}}
 
 
 def _extra_rope_quant_write(kvq, W, bf16, i32, timed, dev, reps, hbm):
@@ -608,7 +642,8 @@ def main():
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k", "decode_b64", "rope_quant_write"],
+    ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k", "decode_b64", "verify_32k",
+                             "rope_quant_write"],
                     help="time only this secondary workload (profiling runs); prints its figures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -220,6 +220,41 @@ int kvq_attn_decode_int8kv_noalloc(const kvq_cache* cache, const void* q, int32_
                                    int32_t max_ctx, float softmax_scale, float* out,
                                    const kvq_decode_opts* opts, void* stream);
 
+/* Most query rows one (sequence, KV head) of kvq_attn_verify_int8kv can hold:
+ * (n_q_heads / n_kv_heads) * n_rows <= KVQ_VERIFY_MAX_ROWS. */
+#define KVQ_VERIFY_MAX_ROWS 48
+
+/* Workspace (bytes) the split route of kvq_attn_verify_int8kv needs: the decode workspace of
+ * batch * n_rows query rows; 0 when the call takes the single-CTA route or an argument is
+ * not positive. */
+size_t kvq_verify_workspace_bytes(int32_t batch, int32_t n_rows, int32_t n_q_heads, int32_t max_ctx,
+                                  int32_t head_dim, const kvq_decode_opts* opts);
+
+/*
+ * kvq_attn_verify_int8kv — decode with n_rows query rows per sequence: the verify step of
+ * speculative / multi-token-prediction decoding ([DOT4] "Future Work": MTP verify runs
+ * nq = 2-4 query rows per sequence; "ROCm/RDNA4 (gfx1201) vLLM ..." row-shape routing:
+ * spec-verify decode with 2-6 rows goes to a multi-row kernel).  The last n_rows tokens of
+ * each sequence are the drafted tokens being verified; their K/V must already be in the
+ * cache (kvq_quant_write or kvq_rope_quant_write).  With c = ctx_lens[b], row i sits at
+ * position c - n_rows + i and attends causally:
+ *   out[b][i][h][:] = sum_t softmax_t(s) * v^[t],  s[t] = softmax_scale * q[b][i][h] . k^[t],
+ *   over keys t < min(c, c - n_rows + 1 + i); a row with no key gives zeros.
+ * n_rows = 1 is kvq_attn_decode_int8kv.  Same routes, options, K/V traffic and precision as
+ * kvq_attn_decode_int8kv: every K/V page is read once for all n_rows rows of its sequence.
+ *   q          : device bf16 [batch][n_rows][n_q_heads][head_dim]
+ *   out        : device fp32 [batch][n_rows][n_q_heads][head_dim]
+ *   workspace  : >= kvq_verify_workspace_bytes(...), 16-byte aligned
+ *   other arguments as kvq_attn_decode_int8kv.
+ * KVQ_ERR_UNSUPPORTED when (n_q_heads / n_kv_heads) * n_rows > KVQ_VERIFY_MAX_ROWS, the GQA
+ * group exceeds 8, or batch * n_rows > 65535.
+ */
+int kvq_attn_verify_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_rows,
+                           int32_t n_q_heads, const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
+                           void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
+                           void* stream);
+
 /* Workspace (bytes) of kvq_attn_prefill_int8 for a chunk of n_tokens queries after
  * history_len keys: the int8 Q codes and their fp32 scales, and the K/V codes of every
  * (KV head, 128-key tile) of the history_len + n_tokens keys widened once to fp16 in the

@@ -215,18 +215,26 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
   return kvq::decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, rows);
 }
 
-int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_q_heads,
-                           const int32_t* block_table, int32_t max_blocks_per_seq,
-                           const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
-                           void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
-                           void* stream) {
+size_t kvq_verify_workspace_bytes(int32_t batch, int32_t n_rows, int32_t n_q_heads, int32_t max_ctx,
+                                  int32_t head_dim, const kvq_decode_opts* opts) {
+  if (batch <= 0 || n_rows <= 0 || static_cast<long long>(batch) * n_rows > INT32_MAX) return 0;
+  return kvq_decode_workspace_bytes(batch * n_rows, n_q_heads, max_ctx, head_dim, opts);
+}
+
+// Decode with nq query rows per sequence (nq = 1: plain decode).
+static int decode_rows(const kvq_cache* cache, const void* q, int32_t batch, int32_t nq, int32_t n_q_heads,
+                       const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* ctx_lens,
+                       int32_t max_ctx, float softmax_scale, float* out, void* workspace,
+                       size_t workspace_bytes, const kvq_decode_opts* opts, void* stream) {
   int st = check_cache(cache);
   if (st != KVQ_OK) return st;
   if (!q || !block_table || !ctx_lens || !out) return KVQ_ERR_INVALID_ARG;
-  if (batch <= 0 || n_q_heads <= 0 || max_blocks_per_seq <= 0 || max_ctx < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch <= 0 || nq <= 0 || n_q_heads <= 0 || max_blocks_per_seq <= 0 || max_ctx < 0) return KVQ_ERR_INVALID_ARG;
+  // stage 1 puts the sequences on grid z, the merge puts (sequence, row) on grid y
+  if (static_cast<long long>(batch) * nq > 65535) return KVQ_ERR_UNSUPPORTED;
   if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   const int G = n_q_heads / cache->n_kv_heads;
-  if (G > 8) return KVQ_ERR_UNSUPPORTED;
+  if (G > 8 || static_cast<long long>(G) * nq > KVQ_VERIFY_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
   if (!aligned4(block_table) || !aligned4(ctx_lens)) return KVQ_ERR_MISALIGNED;
   kvq_decode_opts o = decode_defaults(opts);
@@ -249,6 +257,7 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   a.head_dim = cache->head_dim;
   a.q = q;
   a.batch = batch;
+  a.nq = nq;
   a.n_q_heads = n_q_heads;
   a.block_table = block_table;
   a.max_blocks_per_seq = max_blocks_per_seq;
@@ -263,11 +272,11 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   if (split) {
     const long long n_split = (static_cast<long long>(mc) + o.split_rows - 1) / o.split_rows;
     if (n_split > kMaxSplits) return KVQ_ERR_UNSUPPORTED;
-    const size_t need = kvq::decode_workspace_bytes(batch, n_q_heads, mc, cache->head_dim, o.split_rows);
+    const size_t need = kvq::decode_workspace_bytes(batch * nq, n_q_heads, mc, cache->head_dim, o.split_rows);
     if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
     a.n_split = static_cast<int>(n_split);
-    const long long units = static_cast<long long>(batch) * n_q_heads * n_split;
+    const long long units = static_cast<long long>(batch) * nq * n_q_heads * n_split;
     const long long acc_bytes = ((units * cache->head_dim * 4 + 255) / 256) * 256;
     a.part_acc = static_cast<float*>(workspace);
     a.part_stats = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
@@ -275,6 +284,24 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
   }
   a.n_split = 1;
   return cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSingle, static_cast<cudaStream_t>(stream)));
+}
+
+int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_q_heads,
+                           const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
+                           void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
+                           void* stream) {
+  return decode_rows(cache, q, batch, 1, n_q_heads, block_table, max_blocks_per_seq, ctx_lens, max_ctx,
+                     softmax_scale, out, workspace, workspace_bytes, opts, stream);
+}
+
+int kvq_attn_verify_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_rows,
+                           int32_t n_q_heads, const int32_t* block_table, int32_t max_blocks_per_seq,
+                           const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
+                           void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
+                           void* stream) {
+  return decode_rows(cache, q, batch, n_rows, n_q_heads, block_table, max_blocks_per_seq, ctx_lens, max_ctx,
+                     softmax_scale, out, workspace, workspace_bytes, opts, stream);
 }
 
 size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads, int32_t history_len,

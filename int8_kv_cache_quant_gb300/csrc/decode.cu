@@ -1,4 +1,5 @@
-// decode.cu — decode attention over the int8 paged K/V cache, one query per sequence.
+// decode.cu — decode attention over the int8 paged K/V cache: one query per sequence, or nq
+// query rows per sequence (speculative / MTP verify, causal among the nq newest tokens).
 //
 // Method: "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §3.3 (locate the paged
 // int8 K/V, QK on the int8 codes, scale restore and online softmax, PV, partition merge;
@@ -28,6 +29,13 @@
 //   so PV keeps ~22 bits.  log2(sV) is folded into a second running maximum so that W
 //   stays in [0, 1] whatever the V scales are.
 // * Split route: each CTA writes (m_s, m_z, l, acc[D]) per query head; stage 2 merges.
+// * Verify rows ([DOT4] "Future Work": MTP verify at nq = 2-4; "ROCm/RDNA4 (gfx1201) vLLM
+//   ..." row-shape routing: spec-verify with 2-6 rows): the nq query rows of a sequence
+//   join the GQA group on the N side, rows = G * nq (row r = query i * G + head).  A warp
+//   holds one 8-row n-tile of S^T and O^T; NT = ceil(rows / 8) warps form a team that shares
+//   one page ring, so each K/V page is still read from HBM once for all nq rows ("Redundancy
+//   is a currency": the byte-bound decode does not re-stream K per row tile).  A slot is
+//   refilled once every warp of its team has arrived on the slot's empty barrier.
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
 
@@ -50,33 +58,41 @@ __device__ __forceinline__ int row_token(int row) {
   return base + (((r >= 4) != (hi != 0)) ? 2 : 0);
 }
 
-template <int D, int NP, int DEPTH>  // NP consumer warps, DEPTH stages each
+// NTEAM teams of NT warps; each team streams its pages through DEPTH private stages.
+template <int D, int NT, int NTEAM, int DEPTH>
 struct DecodeSmem {
+  static constexpr int kWarps = NT * NTEAM;
+  static constexpr int kRows = NT * 8;                            // query rows of the CTA (padded)
   static constexpr int kKvBytes = D * KVQ_BLOCK_SIZE;             // one (page, head) of K or V
   static constexpr int kStageBytes = 2 * kKvBytes + 2 * 64;       // K, V, k_scale, v_scale
-  static constexpr int kStages = NP * DEPTH;                      // DEPTH private stages per warp
+  static constexpr int kStages = NTEAM * DEPTH;                   // DEPTH private stages per team
   static constexpr int kRingBytes = kStages * kStageBytes;
   static constexpr int kQOffset = kRingBytes;                     // Q^T fragments (fp16)
-  static constexpr int kQBytes = D * 16;                          // D/16 chunks x 2 x 8 heads x 16 B
-  static constexpr int kBarOffset = kQOffset + kQBytes;           // full barriers [warp][DEPTH]
-  static constexpr int kFlagOffset = kBarOffset + kStages * 8;    // page-ok flags [warp][DEPTH]
-  static constexpr int kCqOffset = kFlagOffset + kStages * 4;     // score factor per group head
-  static constexpr int kTotal = kCqOffset + 8 * 4;
-  static constexpr int kMergeBytes = (NP * 8 * (D + 4) + NP * 8 * 4 + 8 * NP + 32) * 4;  // merge scratch
+  static constexpr int kQBytes = NT * D * 16;                     // per n-tile: D/16 chunks x 2 x 8 rows x 16 B
+  static constexpr int kBarOffset = kQOffset + kQBytes;           // full [team][DEPTH], then empty [team][DEPTH]
+  static constexpr int kFlagOffset = kBarOffset + (NT > 1 ? 2 : 1) * kStages * 8;  // page-ok flags [team][DEPTH]
+  static constexpr int kCqOffset = kFlagOffset + kStages * 4;     // score factor per row
+  static constexpr int kTotal = kCqOffset + kRows * 4;
+  static constexpr int kMergeBytes = (kWarps * 8 * (D + 4) + kWarps * 8 * 4 + kWarps * 8 + kRows * 4) * 4;
   static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the ring");
-  static_assert(NP >= 8 && NP <= 16, "8..16 warps: one warp per group head prepares Q");
+  static_assert(kWarps >= 8 && kWarps <= 16, "8..16 warps");
+  static_assert(kTotal <= 227 * 1024, "shared memory of one CTA");
+  static_assert(kQOffset % 16 == 0 && kBarOffset % 8 == 0, "ldmatrix / mbarrier alignment");
 };
 
 constexpr float kLazyRescale = 8.0f;  // keep a running maximum until the tile exceeds it by 2^8
 
 }  // namespace
 
-// Stage 1.  CTA = NP warps over the key range of one (split, KV head, sequence); warp p takes
-// pages p, p + NP, ... of the range through its own DEPTH-stage ring and accumulates S^T, the
-// softmax statistics and O^T over the whole head dimension.
-template <int D, int NP, int DEPTH, bool SPLIT>
-__global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
-  using L = DecodeSmem<D, NP, DEPTH>;
+// Stage 1.  CTA = NTEAM teams of NT warps over the key range of one (split, KV head,
+// sequence); team p takes pages p, p + NTEAM, ... of the range through its own DEPTH-stage
+// ring, and warp nt of the team accumulates S^T, the softmax statistics and O^T of query rows
+// 8 nt .. 8 nt + 7 over the whole head dimension.  MROW: more than one query row per sequence
+// (the causal bound among the rows applies); without it nq is 1 at compile time.
+template <int D, int NT, int NTEAM, int DEPTH, bool SPLIT, bool MROW>
+__global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeArgs a) {
+  using L = DecodeSmem<D, NT, NTEAM, DEPTH>;
+  constexpr int NW = L::kWarps;
   constexpr int KB = L::kKvBytes;
   constexpr int NCH_H = D / 16;  // 16-dim chunks of the head dimension (whole, one warp)
   constexpr int NMT_H = D / 16;  // 16-dim m-tiles of O^T
@@ -84,13 +100,16 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
   uint8_t* ring = smem;
   uint8_t* q_s = smem + L::kQOffset;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  uint64_t* empty = full + L::kStages;
   int* stage_ok = reinterpret_cast<int*>(smem + L::kFlagOffset);
   float* cq_s = reinterpret_cast<float*>(smem + L::kCqOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = warp;  // each warp takes whole pages
+  const int p = warp / NT;   // team: takes whole pages
+  const int nt = warp % NT;  // n-tile of query rows of this warp
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
+  const int nq = MROW ? a.nq : 1, R = G * nq;  // query rows of this (sequence, KV head)
 
   grid_dep_wait();  // inputs may come from the previous kernel of the stream
   int ctx = a.ctx_lens[b];
@@ -108,32 +127,39 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
     // No keys in this range: the single route writes zeros; an empty split writes nothing
     // (stage 2 only reads splits that start below ctx).
     if (!SPLIT) {
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        a.out[(static_cast<long long>(b) * Hq + kvh * G + i / D) * D + i % D] = 0.0f;
+      for (int i = threadIdx.x; i < R * D; i += blockDim.x) {
+        const int r = i / D;
+        a.out[((static_cast<long long>(b) * nq + r / G) * Hq + kvh * G + r % G) * D + i % D] = 0.0f;
+      }
     }
     return;
   }
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      if (NT > 1) mbar_init(&empty[s], NT);
+    }
     mbar_fence_init();
   }
   __syncthreads();  // the barriers are initialised before any copy completes on them
 
-  const int npp = (p < n_pages) ? (n_pages - p + NP - 1) / NP : 0;  // pages of this warp
+  const int npp = (p < n_pages) ? (n_pages - p + NTEAM - 1) / NTEAM : 0;  // pages of this team
   const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
   uint64_t* pfull = full + p * DEPTH;
+  uint64_t* pempty = empty + p * DEPTH;
   int* pok = stage_ok + p * DEPTH;
   uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
 
-  // page ids of this warp, a window of 32 in its lanes (lane i <-> page k = wb + i)
+  // page ids of this team (read by its issuing warp, nt = 0), a window of 32 in its lanes
+  // (lane i <-> page k = wb + i)
   int wb = 0, pg = -1;
-  if (lane < npp) pg = __ldg(bt + p + lane * NP);
-  // the warp, collectively: issue the copy of its page k into its slot
+  if (nt == 0 && lane < npp) pg = __ldg(bt + p + lane * NTEAM);
+  // the issuing warp, collectively: issue the copy of the team's page k into its slot
   auto issue = [&](int k) {
     while (k >= wb + 32) {
       wb += 32;
-      pg = (wb + lane < npp) ? __ldg(bt + p + (wb + lane) * NP) : -1;
+      pg = (wb + lane < npp) ? __ldg(bt + p + (wb + lane) * NTEAM) : -1;
     }
     const int page = __shfl_sync(0xffffffffu, pg, k - wb);
     if (lane == 0) {
@@ -156,18 +182,24 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
     }
   };
   // The first copies go out before Q is prepared, so their HBM latency overlaps it.
-  for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
+  if (nt == 0)
+    for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
 
-  // ---- Q^T fragments: warp h prepares head h of the group (zeros past G).  The fp16 values
-  // are q * 2^e (e brings max|q| into [2^14, 2^15): exact for bf16).  Chunk j (16 dims) is
-  // two 8 x 8 b16 matrices, rows = heads, whose columns are the k-slots of the MMA: slots
-  // (2c, 2c+1) carry dims (4c, 4c+1) and slots (2c+8, 2c+9) carry dims (4c+2, 4c+3).
-  if (warp < 8) {
-    const int h = warp;
-    const bool real = h < G;
+  // ---- Q^T fragments: row r = i * G + hh (query row i of the sequence, head hh of the
+  // group) is prepared by warp r mod NW; rows past G * nq are zeros.  The fp16 values are
+  // q * 2^e (e brings max|q| into [2^14, 2^15): exact for bf16).  Per n-tile of 8 rows,
+  // chunk j (16 dims) is two 8 x 8 b16 matrices, rows = query rows, whose columns are the
+  // k-slots of the MMA: slots (2c, 2c+1) carry dims (4c, 4c+1) and slots (2c+8, 2c+9) carry
+  // dims (4c+2, 4c+3).
+  for (int h = warp; h < L::kRows; h += NW) {
+    const bool real = h < R;
+    const int qi = (MROW && real) ? h / G : 0, hh = !MROW ? h : real ? h % G : 0;
+    uint8_t* q_tile = q_s + (h >> 3) * (D * 16);
+    const int hr = h & 7;
     constexpr int PER = D / 32;  // dims per lane
     float x[PER];
-    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + (static_cast<long long>(b) * Hq + kvh * G + h) * D + lane * PER;
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) +
+                           ((static_cast<long long>(b) * nq + qi) * Hq + kvh * G + hh) * D + lane * PER;
     if constexpr (PER == 8) {
       const uint4 raw = real ? __ldg(reinterpret_cast<const uint4*>(qrow)) : make_uint4(0, 0, 0, 0);
       const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -198,7 +230,7 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
       const int d = lane * PER + i;
       const int j = d >> 4, w = d & 15, c = w >> 2, bb = w & 3;
       const int half = bb >> 1, el = 2 * c + (bb & 1);
-      *reinterpret_cast<__half*>(q_s + ((j * 2 + half) * 8 + h) * 16 + el * 2) = __float2half_rn(x[i] * qs);
+      *reinterpret_cast<__half*>(q_tile + ((j * 2 + half) * 8 + hr) * 16 + el * 2) = __float2half_rn(x[i] * qs);
     }
     if (lane == 0) cq_s[h] = a.softmax_scale * kLog2e / qs;
   }
@@ -210,13 +242,22 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
 #pragma unroll
   for (int i = 0; i < NMT_H; ++i) o_acc[i][0] = o_acc[i][1] = o_acc[i][2] = o_acc[i][3] = 0.f;
   float ms[2] = {-INFINITY, -INFINITY}, mz[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
-  const float cq0 = cq_s[2 * c], cq1 = cq_s[2 * c + 1];
+  const float cq0 = cq_s[nt * 8 + 2 * c], cq1 = cq_s[nt * 8 + 2 * c + 1];
+  // key bound of this thread's two rows: row i of the sequence sees keys t < ctx - nq + 1 + i
+  int lim[2] = {t_end, t_end};
+  if constexpr (MROW) {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = nt * 8 + 2 * c + i;
+      if (r < R) lim[i] = min(t_end, ctx - nq + 1 + r / G);
+    }
+  }
 
   // per-lane ldmatrix offsets: K rows are tokens (in row_token order), Q^T rows are heads,
   // V rows are head dimensions
   const int mi = lane >> 3, r = lane & 7;
   const uint32_t k_lane_off = (mi >> 1) * 256 + row_token((mi & 1) * 8 + r) * 16;
-  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + mi * 128 + r * 16;
+  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + nt * (D * 16) + mi * 128 + r * 16;
   const uint32_t v_lane_off = lane * 16;
   const int tk0 = row_token(g), tk1 = row_token(g + 8);
   const uint32_t selA = (c < 2) ? kSelB01 : kSelB23;
@@ -250,9 +291,10 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
 
     // ---- online softmax
     const bool page_ok = pok[s] != 0;
-    const int tpage = t_begin + (p + k * NP) * KVQ_BLOCK_SIZE;
-    const bool v0 = page_ok && (tpage + tk0 < t_end);
-    const bool v1 = page_ok && (tpage + tk1 < t_end);
+    const int tpage = t_begin + (p + k * NTEAM) * KVQ_BLOCK_SIZE;
+    const int t0 = tpage + tk0, t1 = tpage + tk1;
+    const bool v0 = page_ok && (t0 < t_end);
+    const bool v1 = page_ok && (t1 < t_end);
     const float sk0 = sks[tk0], sk1 = sks[tk1];
     const float lv0 = v0 ? fast_log2(svs[tk0]) : -INFINITY;
     const float lv1 = v1 ? fast_log2(svs[tk1]) : -INFINITY;
@@ -260,8 +302,8 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const float cqi = i ? cq1 : cq0;
-      const float s0 = v0 ? S[i] * sk0 * cqi : -INFINITY;
-      const float s1 = v1 ? S[2 + i] * sk1 * cqi : -INFINITY;
+      const float s0 = (v0 && (!MROW || t0 < lim[i])) ? S[i] * sk0 * cqi : -INFINITY;
+      const float s1 = (v1 && (!MROW || t1 < lim[i])) ? S[2 + i] * sk1 * cqi : -INFINITY;
       const float z0 = s0 + lv0, z1 = s1 + lv1;
       float tms = fmaxf(s0, s1), tmz = fmaxf(z0, z1);
 #pragma unroll
@@ -313,9 +355,19 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
       mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bh0, bh1);
       mma_f16_16816(o_acc[2 * gg + 1], a0, a1, a2, a3, bl0, bl1);
     }
-    // this page's slot is read: refill it with the warp's page k + DEPTH
+    // this page's slot is read: refill it with the team's page k + DEPTH
     __syncwarp();
-    if (k + DEPTH < npp) issue(k + DEPTH);
+    if constexpr (NT == 1) {
+      if (k + DEPTH < npp) issue(k + DEPTH);
+    } else {
+      if (lane == 0) mbar_arrive(&pempty[s]);
+      if (nt == 0 && k + DEPTH < npp) {
+        // every warp of the team has read the slot (the (k / DEPTH)-th phase of its empty barrier)
+        bool freed = true;
+        if (lane == 0) freed = mbar_wait(&pempty[s], (k / DEPTH) & 1, a.status);
+        if (__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) issue(k + DEPTH);
+      }
+    }
   }
   // l over all tokens of the warp for heads 2c, 2c + 1
 #pragma unroll
@@ -328,42 +380,43 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
   grid_dep_trigger();  // the stage-2 merge may start launching
   __syncthreads();  // every issued copy was waited for by its warp: the ring is free
   constexpr int RS = D + 4;                                     // padded row: no bank conflicts
-  float* mo = reinterpret_cast<float*>(smem);                   // [NP][8][RS]
-  float* mstat = mo + NP * 8 * RS;                              // [NP][8][4]
-  float* mw = mstat + NP * 8 * 4;                               // [8][NP] weights of the warps' O
-  float* mfin = mw + 8 * NP;                                    // [8][4]: Ms, Mz, l, final factor
+  // slot of (team, row r) = team * 8 NT + r = warp * 8 + (r mod 8) for the warp holding r
+  float* mo = reinterpret_cast<float*>(smem);                   // [NW][8][RS]
+  float* mstat = mo + NW * 8 * RS;                              // [NW][8][4]
+  float* mw = mstat + NW * 8 * 4;                               // [rows][NTEAM] weights of the teams' O
+  float* mfin = mw + NW * 8;                                    // [rows][4]: Ms, Mz, l, final factor
 #pragma unroll
   for (int mt = 0; mt < NMT_H; ++mt) {
     const int d0 = mt * 16 + g;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      mo[(p * 8 + 2 * c + i) * RS + d0] = o_acc[mt][i];
-      mo[(p * 8 + 2 * c + i) * RS + d0 + 8] = o_acc[mt][2 + i];
+      mo[(warp * 8 + 2 * c + i) * RS + d0] = o_acc[mt][i];
+      mo[(warp * 8 + 2 * c + i) * RS + d0 + 8] = o_acc[mt][2 + i];
     }
   }
   if (g == 0) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      float* stt = mstat + (p * 8 + 2 * c + i) * 4;
+      float* stt = mstat + (warp * 8 + 2 * c + i) * 4;
       stt[0] = ms[i];
       stt[1] = mz[i];
       stt[2] = lsum[i];
     }
   }
   __syncthreads();
-  if (threadIdx.x < G) {
-    // per head: the warps' maxima, the merged l and one weight per warp (exp once per warp)
+  if (threadIdx.x < R) {
+    // per row: the teams' maxima, the merged l and one weight per team (exp once per team)
     const int hh = threadIdx.x;
     float Ms = -INFINITY, Mz = -INFINITY;
-    for (int q2 = 0; q2 < NP; ++q2) {
-      Ms = fmaxf(Ms, mstat[(q2 * 8 + hh) * 4 + 0]);
-      Mz = fmaxf(Mz, mstat[(q2 * 8 + hh) * 4 + 1]);
+    for (int q2 = 0; q2 < NTEAM; ++q2) {
+      Ms = fmaxf(Ms, mstat[(q2 * L::kRows + hh) * 4 + 0]);
+      Mz = fmaxf(Mz, mstat[(q2 * L::kRows + hh) * 4 + 1]);
     }
     float lsum_all = 0.f;
-    for (int q2 = 0; q2 < NP; ++q2) {
-      const float* stt = mstat + (q2 * 8 + hh) * 4;
+    for (int q2 = 0; q2 < NTEAM; ++q2) {
+      const float* stt = mstat + (q2 * L::kRows + hh) * 4;
       if (Ms != -INFINITY && stt[0] != -INFINITY) lsum_all += stt[2] * fast_exp2(stt[0] - Ms);
-      mw[hh * NP + q2] = (Mz != -INFINITY && stt[1] != -INFINITY) ? fast_exp2(stt[1] - Mz) : 0.f;
+      mw[hh * NTEAM + q2] = (Mz != -INFINITY && stt[1] != -INFINITY) ? fast_exp2(stt[1] - Mz) : 0.f;
     }
     mfin[hh * 4 + 0] = Ms;
     mfin[hh * 4 + 1] = Mz;
@@ -371,14 +424,16 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
     mfin[hh * 4 + 3] = (lsum_all > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / lsum_all : 0.f;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
     const int hh = idx / D, d = idx % D;
     float o = 0.f;
 #pragma unroll
-    for (int q2 = 0; q2 < NP; ++q2) o = fmaf(mo[(q2 * 8 + hh) * RS + d], mw[hh * NP + q2], o);
-    const int h = kvh * G + hh;
+    for (int q2 = 0; q2 < NTEAM; ++q2) o = fmaf(mo[(q2 * L::kRows + hh) * RS + d], mw[hh * NTEAM + q2], o);
+    // output row: query row hh / G of the sequence, query head kvh * G + hh % G
+    const long long orow = MROW ? (static_cast<long long>(b) * nq + hh / G) * Hq + kvh * G + hh % G
+                                : static_cast<long long>(b) * Hq + kvh * G + hh;
     if (SPLIT) {
-      const long long pu = (static_cast<long long>(b) * Hq + h) * a.n_split + blockIdx.x;
+      const long long pu = orow * a.n_split + blockIdx.x;
       a.part_acc[pu * D + d] = o;
       if (d == 0) {
         a.part_stats[pu * 4 + 0] = mfin[hh * 4 + 0];
@@ -387,12 +442,12 @@ __global__ void __launch_bounds__(NP * 32) decode_stage1_kernel(DecodeArgs a) {
         a.part_stats[pu * 4 + 3] = 0.f;
       }
     } else {
-      a.out[(static_cast<long long>(b) * Hq + h) * D + d] = o * mfin[hh * 4 + 3];
+      a.out[orow * D + d] = o * mfin[hh * 4 + 3];
     }
   }
 }
 
-// Stage 2: log-sum-exp merge of the splits of one (sequence, query head).
+// Stage 2: log-sum-exp merge of the splits of one (sequence, query row, query head).
 //   M_s = max m_s, M_z = max m_z;  l = sum l_s 2^{m_s - M_s};  o = sum acc_s 2^{m_z - M_z};
 //   out = o 2^{M_z - M_s} / l.  The per-split weights are computed once into shared memory
 // ("ROCm/RDNA4 (gfx1201) vLLM ...", "The reduce is not free": one cooperative pass, each
@@ -409,12 +464,13 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
   extern __shared__ float wts[];                // [n_split] weights of the partial accumulators
   __shared__ float red[2][kMergeThreads / 32];
   __shared__ __align__(16) float4 part[NG][TPG];
-  const int h = blockIdx.x, b = blockIdx.y, Hq = a.n_q_heads, col0 = blockIdx.z * kMergeCols;
+  // blockIdx.y = b * nq + i: query row i of sequence b
+  const int h = blockIdx.x, row = blockIdx.y, b = row / a.nq, Hq = a.n_q_heads, col0 = blockIdx.z * kMergeCols;
   grid_dep_wait();  // the partials come from stage 1
   int ctx = a.ctx_lens[b];
   ctx = max(0, min(ctx, a.max_blocks_per_seq * KVQ_BLOCK_SIZE));
   const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
-  const long long pu0 = (static_cast<long long>(b) * Hq + h) * a.n_split;
+  const long long pu0 = (static_cast<long long>(row) * Hq + h) * a.n_split;
   const float* stats = a.part_stats + pu0 * 4;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
@@ -493,7 +549,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
       t.w += u.w;
     }
     const float sc = (l > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / l : 0.f;
-    reinterpret_cast<float4*>(a.out + (static_cast<long long>(b) * Hq + h) * D + col0)[dq] =
+    reinterpret_cast<float4*>(a.out + (static_cast<long long>(row) * Hq + h) * D + col0)[dq] =
         make_float4(t.x * sc, t.y * sc, t.z * sc, t.w * sc);
   }
 }
@@ -506,33 +562,52 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_di
   return static_cast<size_t>(((acc + 255) / 256) * 256 + stats);
 }
 
-template <int D, int NP, int DEPTH, bool SPLIT>
+template <int D, int NT, bool SPLIT, bool MROW = true>
 static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
-  using L = DecodeSmem<D, NP, DEPTH>;
-  auto kern = decode_stage1_kernel<D, NP, DEPTH, SPLIT>;
+  // One n-tile: 8 single-warp teams x 3 stages.  More rows: up to 16 warps in as many teams
+  // as fit (pages in flight per SM), each ring 24 / NTEAM deep.
+  constexpr int NTEAM = NT == 1 ? 8 : 16 / NT;
+  constexpr int DEPTH = 24 / NTEAM;
+  using L = DecodeSmem<D, NT, NTEAM, DEPTH>;
+  auto kern = decode_stage1_kernel<D, NT, NTEAM, DEPTH, SPLIT, MROW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, stream)) != cudaSuccess) return e;
-  if ((e = launch_pdl(kern, grid, dim3(NP * 32), L::kTotal, stream, a)) != cudaSuccess) return e;
+  if ((e = launch_pdl(kern, grid, dim3(L::kWarps * 32), L::kTotal, stream, a)) != cudaSuccess) return e;
   if (a.ev_end && (e = cudaEventRecord(a.ev_end, stream)) != cudaSuccess) return e;
   return cudaSuccess;
+}
+
+template <int D, bool SPLIT>
+static cudaError_t launch_stage1_rows(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
+  if (a.nq == 1) return launch_stage1<D, 1, SPLIT, false>(a, grid, stream);  // plain decode
+  const int rows = (a.n_q_heads / a.n_kv_heads) * a.nq;
+  switch ((rows + 7) / 8) {
+    case 1: return launch_stage1<D, 1, SPLIT>(a, grid, stream);
+    case 2: return launch_stage1<D, 2, SPLIT>(a, grid, stream);
+    case 3: return launch_stage1<D, 3, SPLIT>(a, grid, stream);
+    case 4: return launch_stage1<D, 4, SPLIT>(a, grid, stream);
+    case 5: return launch_stage1<D, 5, SPLIT>(a, grid, stream);
+    case 6: return launch_stage1<D, 6, SPLIT>(a, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream) {
   if (route == DecodeRoute::kSingle) {
     dim3 grid(1, a.n_kv_heads, a.batch);
-    if (a.head_dim == 256) return launch_stage1<256, 8, 3, false>(a, grid, stream);
-    return launch_stage1<128, 8, 3, false>(a, grid, stream);
+    if (a.head_dim == 256) return launch_stage1_rows<256, false>(a, grid, stream);
+    return launch_stage1_rows<128, false>(a, grid, stream);
   }
   dim3 grid(a.n_split, a.n_kv_heads, a.batch);
   cudaError_t e;
   if (a.head_dim == 256)
-    e = launch_stage1<256, 8, 3, true>(a, grid, stream);
+    e = launch_stage1_rows<256, true>(a, grid, stream);
   else
-    e = launch_stage1<128, 8, 3, true>(a, grid, stream);
+    e = launch_stage1_rows<128, true>(a, grid, stream);
   if (e != cudaSuccess) return e;
   const size_t wbytes = static_cast<size_t>(a.n_split) * sizeof(float);
-  dim3 g2(a.n_q_heads, a.batch, a.head_dim / kMergeCols);
+  dim3 g2(a.n_q_heads, a.batch * a.nq, a.head_dim / kMergeCols);
   if (a.head_dim == 256) {
     if (wbytes > 48 * 1024) {
       e = cudaFuncSetAttribute(decode_merge_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,

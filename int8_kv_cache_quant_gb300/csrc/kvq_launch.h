@@ -40,8 +40,9 @@ struct RopeQuantArgs {
 };
 cudaError_t launch_rope_quant_write(const RopeQuantArgs& a, cudaStream_t stream);
 
-// Decode: one query per sequence.  Stage 1 (both routes) walks a key range of one
-// (sequence, KV head); the single-CTA route writes `out` directly, the split route writes
+// Decode: nq query rows per sequence (1 for plain decode; row i sees keys
+// t < ctx - nq + 1 + i).  Stage 1 (both routes) walks a key range of one (sequence, KV head)
+// for all G * nq rows; the single-CTA route writes `out` directly, the split route writes
 // partials that stage 2 merges.
 struct DecodeArgs {
   const int8_t* k;
@@ -49,16 +50,16 @@ struct DecodeArgs {
   const float* k_scale;
   const float* v_scale;
   int num_blocks, n_kv_heads, head_dim;
-  const void* q;  // bf16 [B][Hq][D]
-  int batch, n_q_heads;
+  const void* q;  // bf16 [B][nq][Hq][D]
+  int batch, nq, n_q_heads;
   const int32_t* block_table;
   int max_blocks_per_seq;
   const int32_t* ctx_lens;
   int max_ctx;
   float softmax_scale;
-  float* out;          // fp32 [B][Hq][D]
-  float* part_acc;     // fp32 [B][Hq][n_split][D]      (split route)
-  float* part_stats;   // fp32 [B][Hq][n_split][4]       (split route: m_s, m_z, l, unused)
+  float* out;          // fp32 [B][nq][Hq][D]
+  float* part_acc;     // fp32 [B][nq][Hq][n_split][D]  (split route)
+  float* part_stats;   // fp32 [B][nq][Hq][n_split][4]  (split route: m_s, m_z, l, unused)
   int split_rows;      // keys per split (split route); ignored by the single route
   int n_split;         // splits per sequence in the grid (split route)
   unsigned int* status;

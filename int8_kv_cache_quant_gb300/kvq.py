@@ -70,6 +70,10 @@ def lib():
                                              ctypes.POINTER(_DecodeOpts), vp]
         L.kvq_attn_decode_int8kv_noalloc.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp,
                                                      ctypes.POINTER(_DecodeOpts), vp]
+        L.kvq_verify_workspace_bytes.restype = sz
+        L.kvq_verify_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
+        L.kvq_attn_verify_int8kv.argtypes = [cp, vp, i32, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
+                                             ctypes.POINTER(_DecodeOpts), vp]
         L.kvq_prefill_workspace_bytes.restype = sz
         L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
@@ -178,6 +182,12 @@ def kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, split_rows=0
     return int(lib().kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, ctypes.byref(o)))
 
 
+def kvq_verify_workspace_bytes(batch, n_rows, n_q_heads, max_ctx, head_dim, split_rows=0,
+                               route_threshold=0, force_route=0):
+    o = _decode_opts(split_rows, route_threshold, force_route)
+    return int(lib().kvq_verify_workspace_bytes(batch, n_rows, n_q_heads, max_ctx, head_dim, ctypes.byref(o)))
+
+
 def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_scale, out=None,
                            workspace=None, split_rows=0, route_threshold=0, force_route=0,
                            stream=None, stage1_events=None):
@@ -195,6 +205,27 @@ def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
     c = cache.struct()
     _check("kvq_attn_decode_int8kv", lib().kvq_attn_decode_int8kv(
         ctypes.byref(c), _p(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
+        _stream(stream)))
+    return out
+
+
+def kvq_attn_verify_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_scale, out=None,
+                           workspace=None, split_rows=0, route_threshold=0, force_route=0,
+                           stream=None, stage1_events=None):
+    """q: bf16 [B][nq][Hq][D], the nq newest tokens of each sequence; row i of sequence b sees
+    keys t < ctx_lens[b] - nq + 1 + i.  Returns out fp32 [B][nq][Hq][D]."""
+    B, nq, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=q.device)
+    o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
+    need = int(lib().kvq_verify_workspace_bytes(B, nq, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    c = cache.struct()
+    _check("kvq_attn_verify_int8kv", lib().kvq_attn_verify_int8kv(
+        ctypes.byref(c), _p(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
         int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
     return out

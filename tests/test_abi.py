@@ -42,6 +42,10 @@ def test_host_helpers_without_gpu():
     assert k.kvq_decode_auto_split_rows(0, 4, 256, 4096, 152) == 0
     assert k.kvq_decode_auto_split_rows(1, 4, 192, 4096, 152) == 0
     assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 0  # single-CTA route
+    # verify: the decode workspace of batch * n_rows query rows
+    assert k.kvq_verify_workspace_bytes(2, 4, 24, 32768, 256, split_rows=512) == \
+        k.kvq_decode_workspace_bytes(8, 24, 32768, 256, split_rows=512)
+    assert k.kvq_verify_workspace_bytes(2, 0, 24, 32768, 256) == 0
     # prefill: Q codes | Q scales | widened K and V of 256 tiles x 4 KV heads (2 bytes per code) |
     # their key and value scales
     tiles = 4 * ((30720 + 2048 + 127) // 128)
@@ -68,6 +72,14 @@ def test_invalid_arguments_rejected_before_launch():
                                     None, None) == 2
     assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 8, 16, 4000, 16, 60000, 1.0, 16, None,
                                     0, None, None) == 4
+    # verify: more than 48 rows per (sequence, KV head); more than 65535 (sequence, row) pairs;
+    # no rows
+    assert L.kvq_attn_verify_int8kv(ctypes.byref(c), 16, 1, 7, 32, 16, 4, 16, 100, 1.0, 16, None, 0,
+                                    None, None) == 2    # group 8 x 7 rows = 56
+    assert L.kvq_attn_verify_int8kv(ctypes.byref(c), 16, 20000, 4, 8, 16, 4, 16, 100, 1.0, 16, None, 0,
+                                    None, None) == 2
+    assert L.kvq_attn_verify_int8kv(ctypes.byref(c), 16, 1, 0, 8, 16, 4, 16, 100, 1.0, 16, None, 0,
+                                    None, None) == 1
     # prefill: the softmax scale must be finite and positive (the kernel's exp2 relies on it)
     for bad in (0.0, -0.5, float("inf"), float("nan")):
         assert L.kvq_attn_prefill_int8(ctypes.byref(c), 16, 16, 8, 0, 16, 1, bad, 16, 16, 1 << 30,
