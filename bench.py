@@ -211,9 +211,13 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         sweep.sum()
 
     def step(ev=None):
-        kvq.kvq_quant_write(cache, k_new, v_new, new_seq, new_pos, bt)
-        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, max_ctx, w["softmax_scale"], out=out,
+        # the fused step: stage 1 writes the new token into its page, then attends
+        kvq.kvq_decode_step_int8kv(cache, k_new, v_new, q, bt, ctx, max_ctx, w["softmax_scale"], out=out,
                                    workspace=ws, stage1_events=ev)
+
+    def step_unfused():
+        kvq.kvq_quant_write(cache, k_new, v_new, new_seq, new_pos, bt)
+        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, max_ctx, w["softmax_scale"], out=out, workspace=ws)
 
     for _ in range(args.warmup):
         cold_l2(1)
@@ -250,7 +254,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     # Stage-1 duration for the roofline: a second pass of K steps with events recorded on the
     # library's stream right around the stage-1 launch.  They are kept out of the headline
     # pass because an event between two launches ends the programmatic-dependent-launch
-    # overlap of quant_write -> stage 1 -> merge (measured: about 8 us per step).
+    # overlap of stage 1 -> merge.
     ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev3 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     for i in range(K):
@@ -261,6 +265,14 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     torch.cuda.synchronize()
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
     step_ms_events = statistics.mean(a.elapsed_time(b) for a, b in zip(ev2, ev3))
+    # the same step as two calls (kvq_quant_write, then kvq_attn_decode_int8kv), for reference
+    for i in range(K):
+        cold_l2(i)
+        ev2[i].record(s)
+        step_unfused()
+        ev3[i].record(s)
+    torch.cuda.synchronize()
+    step_ms_unfused = statistics.mean(a.elapsed_time(b) for a, b in zip(ev2, ev3))
     ms_step = statistics.mean(step_ms)
     ms_step_max = max_over_ranks(ms_step, world)
     kv_bytes = max_ctx * (2 * Hkv * D + 2 * Hkv * 4)  # 2080 B per token at 4 x 256
@@ -270,24 +282,20 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     q_h = torch.from_numpy(np.ascontiguousarray(w["q"]).view(np.int16)).pin_memory()
     kn_h = torch.from_numpy(np.ascontiguousarray(w["k_new"]).view(np.int16)).pin_memory()
     vn_h = torch.from_numpy(np.ascontiguousarray(w["v_new"]).view(np.int16)).pin_memory()
-    sp_h = torch.from_numpy(np.concatenate([w["new_seq"], w["new_pos"]]).astype(np.int32)).pin_memory()
     out_h = torch.empty((1, Hq, D), dtype=torch.float32).pin_memory()
     q_d = torch.empty_like(q_h, device=dev)
     kn_d = torch.empty_like(kn_h, device=dev)
     vn_d = torch.empty_like(vn_h, device=dev)
-    sp_d = torch.empty_like(sp_h, device=dev)
-    h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2 + sp_h.numel() * 4
+    h2d = q_h.numel() * 2 + kn_h.numel() * 2 + vn_h.numel() * 2
     d2h = out_h.numel() * 4
 
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
         kn_d.copy_(kn_h, non_blocking=True)
         vn_d.copy_(vn_h, non_blocking=True)
-        sp_d.copy_(sp_h, non_blocking=True)
-        kvq.kvq_quant_write(cache, kn_d.view(torch.bfloat16), vn_d.view(torch.bfloat16), sp_d[:1],
-                            sp_d[1:], bt)
-        kvq.kvq_attn_decode_int8kv(cache, q_d.view(torch.bfloat16), bt, ctx, max_ctx,
-                                   w["softmax_scale"], out=out, workspace=ws)
+        kvq.kvq_decode_step_int8kv(cache, kn_d.view(torch.bfloat16), vn_d.view(torch.bfloat16),
+                                   q_d.view(torch.bfloat16), bt, ctx, max_ctx, w["softmax_scale"], out=out,
+                                   workspace=ws)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -318,6 +326,7 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         "warmup": args.warmup,
         "ms_per_step": round(ms_step_max, 5),
         "ms_per_step_with_stage1_events": round(step_ms_events, 5),
+        "ms_per_step_unfused": round(step_ms_unfused, 5),
         "us_per_call": round(ms_step_max * 1e3, 2),
         "higher_is_better": True,
         "scaling": "weak",
@@ -327,16 +336,16 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         "config": {"workload": "decode_32k", "batch": 1, "ctx": max_ctx, "q_heads": Hq, "kv_heads": Hkv,
                    "head_dim": D, "block_size": 16, "block_table": "random permutation",
                    "split_rows": split, "kv_bytes_per_step": kv_bytes,
-                   "step": "kv_quant_write(1 token) + decode stage1 + merge",
+                   "step": "kvq_decode_step_int8kv: the new token's quantise-and-write inside decode stage 1, then the merge",
                    "l2": "cold before every timed step: 256 MB write then 256 MB read of another buffer, outside the events",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "traffic": stage1_traffic(),
-                     "kernel": "decode_stage1_kernel<256,warps=8,DEPTH=3,split>", "peak_kind": peak_kind,
+                     "kernel": "decode_stage1_kernel<256,warps=8,DEPTH=3,split,fused write>", "peak_kind": peak_kind,
                      "kernel_us": round(kern_avg * 1e3, 2)},
         "e2e": {"value": round(aggregate_gbs(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 2 * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 4),
     }
@@ -436,28 +445,34 @@ def _extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps, hbm):
     ws = torch.empty(max(1, kvq.kvq_decode_workspace_bytes(B, Hq, w["max_ctx"], D)), dtype=torch.uint8, device=dev)
 
     def step():
+        kvq.kvq_decode_step_int8kv(cache, kn, vn, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out,
+                                   workspace=ws)
+
+    def step_unfused():
         kvq.kvq_quant_write(cache, kn, vn, ns, npos, bt)
         kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out, workspace=ws)
     ms = timed(step, reps)
+    ms_unfused = timed(step_unfused, reps)
     kvb = int(w["ctx_lens"].astype(np.int64).sum()) * w["hkv"] * (2 * D + 8)
     res["decode_b64"] = {"us_per_step": round(ms * 1e3, 2), "kv_bytes": kvb, "kv_GBps": round(kvb / ms / 1e6, 1),
                          "frac_of_hbm_peak": round(kvb / ms / 1e6 / hbm, 4),
-                         "step": "kv_quant_write(64 tokens) + decode (split route)"}
+                         "us_per_step_unfused": round(ms_unfused * 1e3, 2),
+                         "step": "kvq_decode_step_int8kv: 64 new tokens written inside decode stage 1 (split route)"}
     return res
 
 
 def _extra_verify_32k(kvq, W, bf16, i32, timed, dev, reps, hbm):
     """verify_32k: one speculative-verify step on decode_32k's cache shape (ctx 32768, 24/4,
-    head_dim 256): kv_quant_write of the 4 drafted tokens, then the 4-row verify decode
-    (automatic split).  Bytes: the K/V codes and scales of all 32768 keys, read once for
-    the 4 rows."""
+    head_dim 256): the 4 drafted tokens written into the cache inside the 4-row verify decode
+    (kvq_decode_step_int8kv, automatic split); the verify decode alone is timed too.  Bytes:
+    the K/V codes and scales of all 32768 keys, read once for the 4 rows."""
     import torch
     w = W.make("verify_32k")
     cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"], device=dev)
     bt = i32(w["block_table"])
     kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
     q, ctx = bf16(w["q"]), i32(w["ctx_lens"])
-    kn, vn, ns, npos = bf16(w["k_new"]), bf16(w["v_new"]), i32(w["new_seq"]), i32(w["new_pos"])
+    kn, vn = bf16(w["k_new"]), bf16(w["v_new"])
     B, nq, Hq, D = w["batch"], w["nq"], w["hq"], w["d"]
     out = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=dev)
     ws = torch.empty(max(1, kvq.kvq_verify_workspace_bytes(B, nq, Hq, w["max_ctx"], D)), dtype=torch.uint8,
@@ -466,16 +481,19 @@ def _extra_verify_32k(kvq, W, bf16, i32, timed, dev, reps, hbm):
     def verify():
         kvq.kvq_attn_verify_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out, workspace=ws)
 
+    kn4 = kn.view(B, nq, w["hkv"], D)
+    vn4 = vn.view(B, nq, w["hkv"], D)
+
     def step():
-        kvq.kvq_quant_write(cache, kn, vn, ns, npos, bt)
-        verify()
+        kvq.kvq_decode_step_int8kv(cache, kn4, vn4, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out,
+                                   workspace=ws)
     ms = timed(step, reps)
     ms_verify = timed(verify, reps)
     kvb = w["max_ctx"] * (2 * w["hkv"] * D + 8 * w["hkv"])
     return {"verify_32k": {"us_per_step": round(ms * 1e3, 2), "us_verify": round(ms_verify * 1e3, 2),
                            "rows": nq, "kv_bytes": kvb, "kv_GBps": round(kvb / ms / 1e6, 1),
                            "verify_frac_of_hbm_peak": round(kvb / ms_verify / 1e6 / hbm, 4),
-                           "step": "kv_quant_write(4 tokens) + verify decode (4 rows, split route)"}}
+                           "step": "kvq_decode_step_int8kv: 4 drafted tokens written inside the 4-row verify decode"}}
 
 
 def _extra_rope_quant_write(kvq, W, bf16, i32, timed, dev, reps, hbm):

@@ -255,6 +255,32 @@ int kvq_attn_verify_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
                            void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
                            void* stream);
 
+/*
+ * kvq_decode_step_int8kv — one decode step in one call: write each sequence's n_new newest
+ * tokens into the cache, then attend with their n_new query rows ([DCU] §4.2 times decode
+ * together with the producer that writes the new token; §2.2 the producer's quantise-and-
+ * write).  With c = ctx_lens[b] (the length including the new tokens), token j of sequence b
+ * sits at position c - n_new + j; the call has exactly the effect of
+ *   kvq_quant_write(k_new, v_new, seq_idx = b, pos = c - n_new + j)   (the same codes and
+ *   scales, bit for bit), then
+ *   kvq_attn_verify_int8kv(q, ...)  (kvq_attn_decode_int8kv when n_new = 1),
+ * but the write runs inside the attention kernel: the warp that is about to copy a page holding
+ * new tokens quantises and stores them first, so the step launches no separate write kernel.
+ *   k_new, v_new : device bf16 [batch][n_new][n_kv_heads][head_dim], 16-byte aligned
+ *   q            : device bf16 [batch][n_new][n_q_heads][head_dim]
+ *   out          : device fp32 [batch][n_new][n_q_heads][head_dim]
+ *   workspace    : >= kvq_verify_workspace_bytes(batch, n_new, ...)
+ *   other arguments as kvq_attn_verify_int8kv.
+ * A sequence with c < n_new or c past what its block-table row maps writes nothing
+ * (KVQ_DEV_BAD_POS); a page id outside [0, num_blocks) is skipped (KVQ_DEV_BAD_BLOCK).  The
+ * new tokens of different sequences must map to distinct slots.
+ */
+int kvq_decode_step_int8kv(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
+                           int32_t batch, int32_t n_new, int32_t n_q_heads, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t max_ctx,
+                           float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                           const kvq_decode_opts* opts, void* stream);
+
 /* Workspace (bytes) of kvq_attn_prefill_int8 for a chunk of n_tokens queries after
  * history_len keys: the int8 Q codes and their fp32 scales, and the K/V codes of every
  * (KV head, 128-key tile) of the history_len + n_tokens keys widened once to fp16 in the

@@ -221,14 +221,17 @@ size_t kvq_verify_workspace_bytes(int32_t batch, int32_t n_rows, int32_t n_q_hea
   return kvq_decode_workspace_bytes(batch * n_rows, n_q_heads, max_ctx, head_dim, opts);
 }
 
-// Decode with nq query rows per sequence (nq = 1: plain decode).
-static int decode_rows(const kvq_cache* cache, const void* q, int32_t batch, int32_t nq, int32_t n_q_heads,
-                       const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* ctx_lens,
-                       int32_t max_ctx, float softmax_scale, float* out, void* workspace,
+// Decode with nq query rows per sequence (nq = 1: plain decode); with k_new / v_new, the fused
+// step that first writes each sequence's nq newest tokens into the cache.
+static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q, int32_t batch,
+                       int32_t nq, int32_t n_q_heads, const int32_t* block_table, int32_t max_blocks_per_seq,
+                       const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out, void* workspace,
                        size_t workspace_bytes, const kvq_decode_opts* opts, void* stream) {
   int st = check_cache(cache);
   if (st != KVQ_OK) return st;
   if (!q || !block_table || !ctx_lens || !out) return KVQ_ERR_INVALID_ARG;
+  if ((k_new == nullptr) != (v_new == nullptr)) return KVQ_ERR_INVALID_ARG;
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return KVQ_ERR_MISALIGNED;
   if (batch <= 0 || nq <= 0 || n_q_heads <= 0 || max_blocks_per_seq <= 0 || max_ctx < 0) return KVQ_ERR_INVALID_ARG;
   // stage 1 puts the sequences on grid z, the merge puts (sequence, row) on grid y
   if (static_cast<long long>(batch) * nq > 65535) return KVQ_ERR_UNSUPPORTED;
@@ -264,6 +267,8 @@ static int decode_rows(const kvq_cache* cache, const void* q, int32_t batch, int
   a.ctx_lens = ctx_lens;
   a.max_ctx = mc;
   a.softmax_scale = softmax_scale;
+  a.k_new = k_new;
+  a.v_new = v_new;
   a.out = out;
   a.split_rows = o.split_rows;
   a.status = status_ptr();
@@ -291,8 +296,8 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
                            const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
                            void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
                            void* stream) {
-  return decode_rows(cache, q, batch, 1, n_q_heads, block_table, max_blocks_per_seq, ctx_lens, max_ctx,
-                     softmax_scale, out, workspace, workspace_bytes, opts, stream);
+  return decode_rows(cache, nullptr, nullptr, q, batch, 1, n_q_heads, block_table, max_blocks_per_seq, ctx_lens,
+                     max_ctx, softmax_scale, out, workspace, workspace_bytes, opts, stream);
 }
 
 int kvq_attn_verify_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_rows,
@@ -300,8 +305,18 @@ int kvq_attn_verify_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
                            const int32_t* ctx_lens, int32_t max_ctx, float softmax_scale, float* out,
                            void* workspace, size_t workspace_bytes, const kvq_decode_opts* opts,
                            void* stream) {
-  return decode_rows(cache, q, batch, n_rows, n_q_heads, block_table, max_blocks_per_seq, ctx_lens, max_ctx,
-                     softmax_scale, out, workspace, workspace_bytes, opts, stream);
+  return decode_rows(cache, nullptr, nullptr, q, batch, n_rows, n_q_heads, block_table, max_blocks_per_seq,
+                     ctx_lens, max_ctx, softmax_scale, out, workspace, workspace_bytes, opts, stream);
+}
+
+int kvq_decode_step_int8kv(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q,
+                           int32_t batch, int32_t n_new, int32_t n_q_heads, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t max_ctx,
+                           float softmax_scale, float* out, void* workspace, size_t workspace_bytes,
+                           const kvq_decode_opts* opts, void* stream) {
+  if (!k_new || !v_new) return KVQ_ERR_INVALID_ARG;
+  return decode_rows(cache, k_new, v_new, q, batch, n_new, n_q_heads, block_table, max_blocks_per_seq, ctx_lens,
+                     max_ctx, softmax_scale, out, workspace, workspace_bytes, opts, stream);
 }
 
 size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads, int32_t history_len,

@@ -36,8 +36,16 @@
 //   one page ring, so each K/V page is still read from HBM once for all nq rows ("Redundancy
 //   is a currency": the byte-bound decode does not re-stream K per row tile).  A slot is
 //   refilled once every warp of its team has arrived on the slot's empty barrier.
+// * Fused decode step ("gfx936 ..." §4.2 measures decode together with the producer; §2.2
+//   writes the new token's K/V in the producer): with k_new / v_new given, the nq newest
+//   tokens of each sequence are quantised (quant_rule.cuh, the kvq_quant_write rule) and
+//   written into their page, before its bulk copy, by the warp that will issue that copy (a
+//   proxy fence orders the generic stores before the copy's reads).  Only that warp's team
+//   reads the page, so no other CTA or launch has to wait for the write; the write sits in the
+//   CTA's prologue, off the page loop.
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
+#include "quant_rule.cuh"
 
 namespace kvq {
 
@@ -84,12 +92,44 @@ constexpr float kLazyRescale = 8.0f;  // keep a running maximum until the tile e
 
 }  // namespace
 
+// Fused step, warp-collective: quantise the new tokens at positions lo, lo + step, ... < hi
+// (token j of sequence b at position first_new + j) and store them into `page`, then order
+// those stores before the async-proxy bulk copy of the page that is issued later.
+template <int D>
+__device__ __forceinline__ void write_new_tokens(const DecodeArgs& a, int b, int kvh, int nq, int page, int lo,
+                                                 int hi, int step, int first_new, int lane) {
+  constexpr int P = D / 32;
+  const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+  for (int t = lo; t < hi; t += step) {
+    const long long row = ((static_cast<long long>(b) * nq + (t - first_new)) * a.n_kv_heads + kvh) * D + lane * P;
+    const int slot = t % KVQ_BLOCK_SIZE;
+    float x[P];
+    int8_t qc[P];
+    uint32_t packed[P / 4];
+    load_bf16_lane(static_cast<const uint16_t*>(a.k_new) + row, x);
+    const float sk = quant_rule_warp(x, qc);
+    pack_codes(qc, packed);
+    store_k_codes<D>(a.k, ph, slot, lane, packed);
+    load_bf16_lane(static_cast<const uint16_t*>(a.v_new) + row, x);
+    const float sv = quant_rule_warp(x, qc);
+    store_v_codes<D>(a.v, ph, slot, lane, qc);
+    if (lane == 0) {
+      a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = sk;
+      a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = sv;
+    }
+  }
+  // the stores above, then the bulk copy that reads them (async proxy)
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
 // Stage 1.  CTA = NTEAM teams of NT warps over the key range of one (split, KV head,
 // sequence); team p takes pages p, p + NTEAM, ... of the range through its own DEPTH-stage
 // ring, and warp nt of the team accumulates S^T, the softmax statistics and O^T of query rows
 // 8 nt .. 8 nt + 7 over the whole head dimension.  MROW: more than one query row per sequence
-// (the causal bound among the rows applies); without it nq is 1 at compile time.
-template <int D, int NT, int NTEAM, int DEPTH, bool SPLIT, bool MROW>
+// (the causal bound among the rows applies); without it nq is 1 at compile time.  WRITE: the
+// fused step's write of the new tokens is compiled in (and runs when a.k_new is set).
+template <int D, int NT, int NTEAM, int DEPTH, bool SPLIT, bool MROW, bool WRITE>
 __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeArgs a) {
   using L = DecodeSmem<D, NT, NTEAM, DEPTH>;
   constexpr int NW = L::kWarps;
@@ -114,9 +154,11 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
   grid_dep_wait();  // inputs may come from the previous kernel of the stream
   int ctx = a.ctx_lens[b];
   const int cap = a.max_blocks_per_seq * KVQ_BLOCK_SIZE;
-  if (ctx > cap) {
+  // fused step: the new tokens are written only when their positions are all mapped
+  const bool write_new = WRITE && a.k_new != nullptr && ctx >= nq && ctx <= cap;
+  if (ctx > cap || (WRITE && a.k_new != nullptr && ctx < nq)) {
     if (threadIdx.x == 0 && blockIdx.x == 0) set_status(a.status, KVQ_DEV_BAD_POS);
-    ctx = cap;
+    ctx = min(ctx, cap);
   }
   if (ctx < 0) ctx = 0;
   const int t_begin = SPLIT ? static_cast<int>(blockIdx.x) * a.split_rows : 0;
@@ -181,9 +223,35 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
       }
     }
   };
+  // Fused step: the team that owns a page holding new tokens (positions ctx - nq .. ctx - 1)
+  // writes them before that page's copy is issued.  A page among the team's first copies is
+  // written by the issuing warp before it issues them.  A later page (k >= DEPTH) is written
+  // after the CTA's Q set-up, just before the page loop, by all NT warps of the team (warp nt
+  // takes tokens nt, nt + NT, ...): each warp's stores and proxy fence precede its arrivals on
+  // the empty barriers, and the issuing warp copies page k only after acquiring one of them.
+  // The page loop has no write in it.
+  auto write_team_pages = [&](bool first_batch) {
+    if constexpr (WRITE) {
+      if (!write_new) return;
+      const int first_new = ctx - nq;
+      const int lo_all = max(first_new, t_begin);
+      if (lo_all >= t_end) return;
+      for (int pr = (lo_all - t_begin) / KVQ_BLOCK_SIZE; pr < n_pages; ++pr) {
+        if (pr % NTEAM != p || ((pr / NTEAM) < DEPTH) != first_batch) continue;
+        const int tp = t_begin + pr * KVQ_BLOCK_SIZE;
+        const int page = __ldg(bt + pr);
+        const int lo = max(tp, first_new), hi = min(tp + KVQ_BLOCK_SIZE, t_end);
+        const int w0 = first_batch ? 0 : nt, step = first_batch ? 1 : NT;
+        if (page >= 0 && page < a.num_blocks && lo + w0 < hi)
+          write_new_tokens<D>(a, b, kvh, nq, page, lo + w0, hi, step, first_new, lane);
+      }
+    }
+  };
   // The first copies go out before Q is prepared, so their HBM latency overlaps it.
-  if (nt == 0)
+  if (nt == 0) {
+    write_team_pages(true);
     for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
+  }
 
   // ---- Q^T fragments: row r = i * G + hh (query row i of the sequence, head hh of the
   // group) is prepared by warp r mod NW; rows past G * nq are zeros.  The fp16 values are
@@ -235,6 +303,7 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
     if (lane == 0) cq_s[h] = a.softmax_scale * kLog2e / qs;
   }
   __syncthreads();
+  write_team_pages(false);
 
 
   const int g = lane >> 2, c = lane & 3;
@@ -562,14 +631,14 @@ size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_di
   return static_cast<size_t>(((acc + 255) / 256) * 256 + stats);
 }
 
-template <int D, int NT, bool SPLIT, bool MROW = true>
+template <int D, int NT, bool SPLIT, bool MROW = true, bool WRITE = true>
 static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
   // One n-tile: 8 single-warp teams x 3 stages.  More rows: up to 16 warps in as many teams
   // as fit (pages in flight per SM), each ring 24 / NTEAM deep.
   constexpr int NTEAM = NT == 1 ? 8 : 16 / NT;
   constexpr int DEPTH = 24 / NTEAM;
   using L = DecodeSmem<D, NT, NTEAM, DEPTH>;
-  auto kern = decode_stage1_kernel<D, NT, NTEAM, DEPTH, SPLIT, MROW>;
+  auto kern = decode_stage1_kernel<D, NT, NTEAM, DEPTH, SPLIT, MROW, WRITE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   if (a.ev_begin && (e = cudaEventRecord(a.ev_begin, stream)) != cudaSuccess) return e;
@@ -580,7 +649,10 @@ static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t st
 
 template <int D, bool SPLIT>
 static cudaError_t launch_stage1_rows(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
-  if (a.nq == 1) return launch_stage1<D, 1, SPLIT, false>(a, grid, stream);  // plain decode
+  if (a.nq == 1) {  // plain decode, or the fused one-token step
+    if (a.k_new) return launch_stage1<D, 1, SPLIT, false, true>(a, grid, stream);
+    return launch_stage1<D, 1, SPLIT, false, false>(a, grid, stream);
+  }
   const int rows = (a.n_q_heads / a.n_kv_heads) * a.nq;
   switch ((rows + 7) / 8) {
     case 1: return launch_stage1<D, 1, SPLIT>(a, grid, stream);

@@ -45,10 +45,10 @@ cudaError_t launch_rope_quant_write(const RopeQuantArgs& a, cudaStream_t stream)
 // for all G * nq rows; the single-CTA route writes `out` directly, the split route writes
 // partials that stage 2 merges.
 struct DecodeArgs {
-  const int8_t* k;
-  const int8_t* v;
-  const float* k_scale;
-  const float* v_scale;
+  int8_t* k;          // the cache (written only by the fused step)
+  int8_t* v;
+  float* k_scale;
+  float* v_scale;
   int num_blocks, n_kv_heads, head_dim;
   const void* q;  // bf16 [B][nq][Hq][D]
   int batch, nq, n_q_heads;
@@ -57,6 +57,10 @@ struct DecodeArgs {
   const int32_t* ctx_lens;
   int max_ctx;
   float softmax_scale;
+  // fused step: bf16 [B][nq][Hkv][D] K / V of each sequence's nq newest tokens, quantised
+  // into the cache by stage 1 before it reads their page; nullptr for attention only
+  const void* k_new;
+  const void* v_new;
   float* out;          // fp32 [B][nq][Hq][D]
   float* part_acc;     // fp32 [B][nq][Hq][n_split][D]  (split route)
   float* part_stats;   // fp32 [B][nq][Hq][n_split][4]  (split route: m_s, m_z, l, unused)

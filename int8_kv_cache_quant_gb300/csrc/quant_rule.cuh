@@ -1,0 +1,94 @@
+// quant_rule.cuh — the per-(token, head) absmax int8 rule on one row held by a warp, and the
+// stores of a row's codes into the paged cache layout.  Shared by every kernel that writes
+// the cache (kvq_quant_write, the fused RoPE producer, the fused decode step), so the codes
+// and scales are the same bits whichever kernel writes them.
+//
+// Method: "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §2.1 (amax = max|x|,
+// scale = amax / 127, q = clamp(round(x / scale), -127, 127)) and §2.3 (K in 16-element
+// head-dimension chunks with the tokens of a chunk adjacent, V token-contiguous per dimension).
+// Every division is IEEE fp32 (__fdiv_rn) and rounding is to nearest even.
+#pragma once
+
+#include <cstdint>
+
+#include "kvq_dev.cuh"
+
+namespace kvq {
+
+// P consecutive bf16 values of a row (this lane's elements) to fp32.  src 4 * P-byte aligned.
+template <int P>
+__device__ __forceinline__ void load_bf16_lane(const uint16_t* src, float (&x)[P]) {
+  static_assert(P == 8 || P == 4, "head_dim 256 or 128 over 32 lanes");
+  if constexpr (P == 8) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  } else {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(src));
+    const uint32_t w[2] = {raw.x, raw.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+}
+
+// The quantisation rule over the warp's row (32 lanes x P values): returns the row's scale and
+// this lane's codes.  An all-zero row gives scale 0 and codes 0.
+template <int P>
+__device__ __forceinline__ float quant_rule_warp(const float (&x)[P], int8_t (&q)[P]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < P; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = __fdiv_rn(amax, 127.0f);
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    float c = 0.0f;
+    if (amax != 0.0f) {
+      c = rintf(__fdiv_rn(x[i], scale));
+      c = fminf(fmaxf(c, -127.0f), 127.0f);
+    }
+    q[i] = static_cast<int8_t>(static_cast<int>(c));
+  }
+  return scale;
+}
+
+// Four codes per word, element 4w in the low byte.
+template <int P>
+__device__ __forceinline__ void pack_codes(const int8_t (&q)[P], uint32_t (&packed)[P / 4]) {
+#pragma unroll
+  for (int w = 0; w < P / 4; ++w)
+    packed[w] = (uint32_t)(uint8_t)q[4 * w] | ((uint32_t)(uint8_t)q[4 * w + 1] << 8) |
+                ((uint32_t)(uint8_t)q[4 * w + 2] << 16) | ((uint32_t)(uint8_t)q[4 * w + 3] << 24);
+}
+
+// K codes of one token into its slot: [page][head][d/16][slot][16].  Lane l's dims l*P .. l*P+P-1
+// lie in chunk (l*P)/16 at byte (l*P)%16 of the 16-byte row.  ph = page * n_kv_heads + head.
+template <int D>
+__device__ __forceinline__ void store_k_codes(int8_t* k, long long ph, int slot, int lane,
+                                              const uint32_t (&packed)[D / 128]) {
+  constexpr int P = D / 32;
+  const int d0 = lane * P;
+  int8_t* dst = k + ((ph * (D / 16) + d0 / 16) * KVQ_BLOCK_SIZE + slot) * 16 + (d0 % 16);
+  if constexpr (P == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  else *reinterpret_cast<uint32_t*>(dst) = packed[0];
+}
+
+// V codes of one token into its slot: [page][head][d][slot], one byte per dimension.
+template <int D>
+__device__ __forceinline__ void store_v_codes(int8_t* v, long long ph, int slot, int lane,
+                                              const int8_t (&q)[D / 32]) {
+  constexpr int P = D / 32;
+  int8_t* dst = v + (ph * D + lane * P) * KVQ_BLOCK_SIZE + slot;
+#pragma unroll
+  for (int i = 0; i < P; ++i) dst[i * KVQ_BLOCK_SIZE] = q[i];
+}
+
+}  // namespace kvq

@@ -8,14 +8,15 @@
 // token-contiguous per dimension).
 //
 // Mapping: one warp per (token, KV head, K|V) row.  The row (head_dim bf16 values) is read
-// with one vector load per lane, amax is a warp-shuffle max, every division is IEEE fp32
-// (__fdiv_rn) and rounding is to nearest even, so the codes and scales are bit-identical
-// to the reference rule.  K codes go out as 8- or 4-byte stores into the [chunk][slot][16]
-// rows; V codes are one byte per dimension into [dim][slot].
+// with one vector load per lane and quantised by the warp (quant_rule.cuh: warp-shuffle amax,
+// IEEE fp32 divisions, round to nearest even), so the codes and scales are bit-identical to
+// the reference rule.  K codes go out as 8- or 4-byte stores into the [chunk][slot][16] rows;
+// V codes are one byte per dimension into [dim][slot].
 #include <cuda_bf16.h>
 
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
+#include "quant_rule.cuh"
 
 namespace kvq {
 
@@ -54,65 +55,18 @@ __global__ void __launch_bounds__(256) quant_write_kernel(QuantWriteArgs a) {
   const uint16_t* src = static_cast<const uint16_t*>(is_v ? a.v_new : a.k_new) +
                         (static_cast<long long>(tok) * H + h) * D + lane * kPerLane;
   float x[kPerLane];
-  if constexpr (kPerLane == 8) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  } else {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(src));
-    const uint32_t w[2] = {raw.x, raw.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float scale = __fdiv_rn(amax, 127.0f);
-
+  load_bf16_lane(src, x);
   int8_t q[kPerLane];
-#pragma unroll
-  for (int i = 0; i < kPerLane; ++i) {
-    float c = 0.0f;
-    if (amax != 0.0f) {
-      c = rintf(__fdiv_rn(x[i], scale));
-      c = fminf(fmaxf(c, -127.0f), 127.0f);
-    }
-    q[i] = static_cast<int8_t>(static_cast<int>(c));
-  }
+  const float scale = quant_rule_warp(x, q);
 
   const long long ph = static_cast<long long>(page) * H + h;
   if (!is_v) {
-    // K: [page][head][d/16][slot][16]; this lane's dims lane*kPerLane .. +kPerLane-1 lie in
-    // chunk (lane*kPerLane)/16 at byte offset (lane*kPerLane)%16 of the 16-byte row.
-    const int d0 = lane * kPerLane;
-    int8_t* dst = a.k + ((ph * (D / 16) + d0 / 16) * KVQ_BLOCK_SIZE + slot) * 16 + (d0 % 16);
-    if constexpr (kPerLane == 8) {
-      uint2 v;
-      v.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) | ((uint32_t)(uint8_t)q[2] << 16) |
-            ((uint32_t)(uint8_t)q[3] << 24);
-      v.y = (uint32_t)(uint8_t)q[4] | ((uint32_t)(uint8_t)q[5] << 8) | ((uint32_t)(uint8_t)q[6] << 16) |
-            ((uint32_t)(uint8_t)q[7] << 24);
-      *reinterpret_cast<uint2*>(dst) = v;
-    } else {
-      uint32_t v = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
-                   ((uint32_t)(uint8_t)q[2] << 16) | ((uint32_t)(uint8_t)q[3] << 24);
-      *reinterpret_cast<uint32_t*>(dst) = v;
-    }
+    uint32_t packed[kPerLane / 4];
+    pack_codes(q, packed);
+    store_k_codes<D>(a.k, ph, slot, lane, packed);
     if (lane == 0) a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
   } else {
-    // V: [page][head][d][slot]
-    int8_t* dst = a.v + (ph * D + lane * kPerLane) * KVQ_BLOCK_SIZE + slot;
-#pragma unroll
-    for (int i = 0; i < kPerLane; ++i) dst[i * KVQ_BLOCK_SIZE] = q[i];
+    store_v_codes<D>(a.v, ph, slot, lane, q);
     if (lane == 0) a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
   }
 }
@@ -160,23 +114,7 @@ __global__ void __launch_bounds__(256) rope_quant_write_kernel(RopeQuantArgs a) 
                               (static_cast<long long>(tok) * H + h) * D;
   src += lane * P;
   float x[P];
-  if constexpr (P == 8) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  } else {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(src));
-    const uint32_t w[2] = {raw.x, raw.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-  }
+  load_bf16_lane(src, x);
   // ---- RoPE (Q and K; the warp takes the branch together: kind is uniform)
   if (kind != 2 && pos_ok) {
     const int half = a.rotary_dim / 2, shift = half / P;
@@ -199,27 +137,10 @@ __global__ void __launch_bounds__(256) rope_quant_write_kernel(RopeQuantArgs a) 
     for (int e = 0; e < P; ++e) x[e] = 0.0f;
   }
   // ---- the quantisation rule (as quant_write_kernel)
-  float amax = 0.0f;
-#pragma unroll
-  for (int i = 0; i < P; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  const float scale = __fdiv_rn(amax, 127.0f);
   int8_t qc[P];
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    float c = 0.0f;
-    if (amax != 0.0f) {
-      c = rintf(__fdiv_rn(x[i], scale));
-      c = fminf(fmaxf(c, -127.0f), 127.0f);
-    }
-    qc[i] = static_cast<int8_t>(static_cast<int>(c));
-  }
+  const float scale = quant_rule_warp(x, qc);
   uint32_t packed[P / 4];
-#pragma unroll
-  for (int w = 0; w < P / 4; ++w)
-    packed[w] = (uint32_t)(uint8_t)qc[4 * w] | ((uint32_t)(uint8_t)qc[4 * w + 1] << 8) |
-                ((uint32_t)(uint8_t)qc[4 * w + 2] << 16) | ((uint32_t)(uint8_t)qc[4 * w + 3] << 24);
+  pack_codes(qc, packed);
 
   if (kind == 0) {
     const long long u = static_cast<long long>(tok) * Hq + h;
@@ -260,15 +181,10 @@ __global__ void __launch_bounds__(256) rope_quant_write_kernel(RopeQuantArgs a) 
   const int slot = p % KVQ_BLOCK_SIZE;
   const long long ph = static_cast<long long>(page) * H + h;
   if (kind == 1) {
-    const int d0 = lane * P;
-    int8_t* dst = a.kv.k + ((ph * (D / 16) + d0 / 16) * KVQ_BLOCK_SIZE + slot) * 16 + (d0 % 16);
-    if constexpr (P == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-    else *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    store_k_codes<D>(a.kv.k, ph, slot, lane, packed);
     if (lane == 0) a.kv.k_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
   } else {
-    int8_t* dst = a.kv.v + (ph * D + lane * P) * KVQ_BLOCK_SIZE + slot;
-#pragma unroll
-    for (int i = 0; i < P; ++i) dst[i * KVQ_BLOCK_SIZE] = qc[i];
+    store_v_codes<D>(a.kv.v, ph, slot, lane, qc);
     if (lane == 0) a.kv.v_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
   }
 }

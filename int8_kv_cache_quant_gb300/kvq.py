@@ -74,6 +74,8 @@ def lib():
         L.kvq_verify_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
         L.kvq_attn_verify_int8kv.argtypes = [cp, vp, i32, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
                                              ctypes.POINTER(_DecodeOpts), vp]
+        L.kvq_decode_step_int8kv.argtypes = [cp, vp, vp, vp, i32, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
+                                             ctypes.POINTER(_DecodeOpts), vp]
         L.kvq_prefill_workspace_bytes.restype = sz
         L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
@@ -229,6 +231,32 @@ def kvq_attn_verify_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
         int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
     return out
+
+
+def kvq_decode_step_int8kv(cache, k_new, v_new, q, block_table, ctx_lens, max_ctx, softmax_scale, out=None,
+                           workspace=None, split_rows=0, route_threshold=0, force_route=0,
+                           stream=None, stage1_events=None):
+    """One decode step: write each sequence's nq newest tokens (k_new / v_new bf16
+    [B][nq][Hkv][D], positions ctx_lens[b] - nq + j) into the cache, then attend with their
+    query rows q bf16 [B][nq][Hq][D].  A 3-D q ([B][Hq][D]) with 3-D k_new / v_new
+    ([B][Hkv][D]) is the one-token step.  Returns out fp32 shaped like q."""
+    squeeze = q.dim() == 3
+    if squeeze:
+        q, k_new, v_new = q[:, None], k_new[:, None], v_new[:, None]
+    B, nq, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=q.device)
+    o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
+    need = int(lib().kvq_verify_workspace_bytes(B, nq, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    c = cache.struct()
+    _check("kvq_decode_step_int8kv", lib().kvq_decode_step_int8kv(
+        ctypes.byref(c), _p(k_new), _p(v_new), _p(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]),
+        _p(ctx_lens), int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
+        _stream(stream)))
+    return out[:, 0] if squeeze else out
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

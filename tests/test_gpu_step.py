@@ -1,0 +1,111 @@
+"""kvq_decode_step_int8kv (the fused step: write each sequence's newest tokens, then attend)
+on the GPU.
+
+The cache starts with every token except the step's new ones; after the call it must equal,
+bit for bit, the oracle's cache with all tokens written by the oracle's quantiser, and the
+output must match the oracle's FP64 decode / verify (design tolerance 1e-4, acceptance
+2e-3) and the unfused kvq_quant_write + attention path on the same cache."""
+import numpy as np
+import pytest
+
+import workloads as W
+from helpers import host_cache_from, norm_max_err, to_bf16_tensor, to_i32
+
+pytestmark = pytest.mark.gpu
+
+DESIGN_TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    import int8_kv_cache_quant_gb300 as k
+    k.lib()
+    return k
+
+
+def _cache_without_new(kvq, w):
+    """Device cache holding every token of the workload but each sequence's newest nq."""
+    nq = w["nq"]
+    last = w["ctx_lens"][w["fill_seq"]] - nq
+    keep = w["fill_pos"] < last
+    cache = kvq.KVCache(w["num_blocks"], w["hkv"], w["d"])
+    bt = to_i32(w["block_table"])
+    kvq.kvq_quant_write(cache, to_bf16_tensor(w["k_fill"][keep]), to_bf16_tensor(w["v_fill"][keep]),
+                        to_i32(w["fill_seq"][keep]), to_i32(w["fill_pos"][keep]), bt)
+    return cache, bt
+
+
+def _new_rows(w):
+    B, nq = w["batch"], w["nq"]
+    shape = (B, nq, w["hkv"], w["d"])
+    return w["k_new"].reshape(shape), w["v_new"].reshape(shape)
+
+
+def _check_cache(cache, hc):
+    assert np.array_equal(cache.k.cpu().numpy(), hc.k)
+    assert np.array_equal(cache.v.cpu().numpy(), hc.v)
+    assert np.array_equal(cache.k_scale.cpu().numpy().view(np.uint32), hc.k_scale.view(np.uint32))
+    assert np.array_equal(cache.v_scale.cpu().numpy().view(np.uint32), hc.v_scale.view(np.uint32))
+
+
+@pytest.mark.parametrize("nq,d,hq,hkv,route", [(1, 128, 32, 8, 2), (1, 256, 24, 4, 1), (1, 256, 24, 4, 2),
+                                               (4, 256, 24, 4, 2), (3, 128, 8, 2, 1), (6, 128, 16, 2, 2)])
+def test_step_writes_and_attends(kvq, oracle, nq, d, hq, hkv, route):
+    w = W.make("decode_b64", seed=700 + nq + d + route, batch=5, ctx_range=(nq, 1500), hq=hq, hkv=hkv, d=d, nq=nq)
+    cache, bt = _cache_without_new(kvq, w)
+    kn, vn = _new_rows(w)
+    q = w["q"] if nq > 1 else w["q"][:, None]
+    out = kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(kn), to_bf16_tensor(vn), to_bf16_tensor(q), bt,
+                                     to_i32(w["ctx_lens"]), w["max_ctx"], w["softmax_scale"], force_route=route,
+                                     split_rows=128).cpu().numpy()
+    assert kvq.kvq_device_status() == 0
+    hc = host_cache_from(w, oracle)
+    _check_cache(cache, hc)
+    ref = oracle.verify_f64(hc, q, w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    assert norm_max_err(out, ref) <= DESIGN_TOL
+    # the unfused path on the now complete cache gives the same bits
+    sep = kvq.kvq_attn_verify_int8kv(cache, to_bf16_tensor(q), bt, to_i32(w["ctx_lens"]), w["max_ctx"],
+                                     w["softmax_scale"], force_route=route, split_rows=128).cpu().numpy()
+    assert np.array_equal(out, sep)
+
+
+def test_one_token_step_3d_and_decode_32k_shape(kvq, oracle):
+    """The headline step's shape (ctx 32768, 24/4, head_dim 256, automatic split): the new token
+    is the last of the last split."""
+    w = W.make("decode_32k")
+    cache, bt = _cache_without_new(kvq, w)
+    kn, vn = _new_rows(w)
+    out = kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(kn[:, 0]), to_bf16_tensor(vn[:, 0]),
+                                     to_bf16_tensor(w["q"]), bt, to_i32(w["ctx_lens"]), w["max_ctx"],
+                                     w["softmax_scale"]).cpu().numpy()
+    assert out.shape == (1, w["hq"], w["d"])
+    assert kvq.kvq_device_status() == 0
+    hc = host_cache_from(w, oracle)
+    _check_cache(cache, hc)
+    dec = kvq.kvq_attn_decode_int8kv(cache, to_bf16_tensor(w["q"]), bt, to_i32(w["ctx_lens"]), w["max_ctx"],
+                                     w["softmax_scale"]).cpu().numpy()
+    assert np.array_equal(out, dec)
+    units = np.array([0, 5, 11, 17, 23], np.int64)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], units=units)
+    assert norm_max_err(out.reshape(-1, w["d"])[units], ref) <= DESIGN_TOL
+
+
+def test_step_with_short_context_writes_nothing_and_flags(kvq):
+    # a sequence shorter than its new-token count has no valid positions for them
+    w = W.make("decode_b64", seed=720, batch=2, ctx_range=(40, 40), hq=8, hkv=2, d=128, nq=3)
+    cache, bt = _cache_without_new(kvq, w)
+    before_k, before_v = cache.k.cpu().numpy(), cache.v.cpu().numpy()
+    kn, vn = _new_rows(w)
+    ctx = w["ctx_lens"].copy()
+    ctx[1] = 2
+    kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(kn), to_bf16_tensor(vn), to_bf16_tensor(w["q"]), bt,
+                               to_i32(ctx), 40, w["softmax_scale"], force_route=1)
+    st = kvq.kvq_device_status()
+    assert st & 0x2  # KVQ_DEV_BAD_POS
+    # sequence 1 wrote nothing; sequence 0 wrote its 3 tokens (positions 37..39)
+    after_k, after_v = cache.k.cpu().numpy(), cache.v.cpu().numpy()
+    pages1 = w["block_table"][1][w["block_table"][1] >= 0]
+    assert np.array_equal(after_k[pages1], before_k[pages1])
+    assert np.array_equal(after_v[pages1], before_v[pages1])
+    p0 = w["block_table"][0][39 // 16]
+    assert not np.array_equal(after_k[p0], before_k[p0])
