@@ -103,15 +103,16 @@ __device__ __forceinline__ void write_new_tokens(const DecodeArgs& a, int b, int
   for (int t = lo; t < hi; t += step) {
     const long long row = ((static_cast<long long>(b) * nq + (t - first_new)) * a.n_kv_heads + kvh) * D + lane * P;
     const int slot = t % KVQ_BLOCK_SIZE;
-    float x[P];
+    float xk[P], xv[P];
     int8_t qc[P];
     uint32_t packed[P / 4];
-    load_bf16_lane(static_cast<const uint16_t*>(a.k_new) + row, x);
-    const float sk = quant_rule_warp(x, qc);
+    // both rows before any store (the stores could alias the inputs as far as the compiler knows)
+    load_bf16_lane(static_cast<const uint16_t*>(a.k_new) + row, xk);
+    load_bf16_lane(static_cast<const uint16_t*>(a.v_new) + row, xv);
+    const float sk = quant_rule_warp(xk, qc);
     pack_codes(qc, packed);
     store_k_codes<D>(a.k, ph, slot, lane, packed);
-    load_bf16_lane(static_cast<const uint16_t*>(a.v_new) + row, x);
-    const float sv = quant_rule_warp(x, qc);
+    const float sv = quant_rule_warp(xv, qc);
     store_v_codes<D>(a.v, ph, slot, lane, qc);
     if (lane == 0) {
       a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = sk;
@@ -130,7 +131,8 @@ __device__ __forceinline__ void write_new_tokens(const DecodeArgs& a, int b, int
 // (the causal bound among the rows applies); without it nq is 1 at compile time.  WRITE: the
 // fused step's write of the new tokens is compiled in (and runs when a.k_new is set).
 template <int D, int NT, int NTEAM, int DEPTH, bool SPLIT, bool MROW, bool WRITE>
-__global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeArgs a) {
+__global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8) ? 2 : 1)
+    decode_stage1_kernel(DecodeArgs a) {
   using L = DecodeSmem<D, NT, NTEAM, DEPTH>;
   constexpr int NW = L::kWarps;
   constexpr int KB = L::kKvBytes;
@@ -152,6 +154,15 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
   const int nq = MROW ? a.nq : 1, R = G * nq;  // query rows of this (sequence, KV head)
 
   grid_dep_wait();  // inputs may come from the previous kernel of the stream
+  const int t_begin = SPLIT ? static_cast<int>(blockIdx.x) * a.split_rows : 0;
+  const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
+  // The team's first 32 page ids are read together with ctx (not after it): entries past the
+  // sequence's pages are read but not used; the row bound keeps every read inside the table.
+  int pg = -1;
+  {
+    const int first = t_begin / KVQ_BLOCK_SIZE + p + lane * NTEAM;
+    if (nt == 0 && first < a.max_blocks_per_seq) pg = __ldg(bt + p + lane * NTEAM);
+  }
   int ctx = a.ctx_lens[b];
   const int cap = a.max_blocks_per_seq * KVQ_BLOCK_SIZE;
   // fused step: the new tokens are written only when their positions are all mapped
@@ -161,9 +172,20 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
     ctx = min(ctx, cap);
   }
   if (ctx < 0) ctx = 0;
-  const int t_begin = SPLIT ? static_cast<int>(blockIdx.x) * a.split_rows : 0;
   const int t_end = SPLIT ? min(ctx, t_begin + a.split_rows) : ctx;
   const int n_pages = (t_end > t_begin) ? (t_end - t_begin + KVQ_BLOCK_SIZE - 1) / KVQ_BLOCK_SIZE : 0;
+  if constexpr (WRITE) {
+    // fused step: warp 0 of a CTA whose range holds new tokens pulls their bf16 K/V rows into L2
+    // now, so the write in the prologue below finds them there
+    if (write_new && warp == 0) {
+      const int lo = max(ctx - nq, t_begin);
+      for (int t = lo + (lane >> 4); t < t_end; t += 2) {
+        const long long row = ((static_cast<long long>(b) * nq + (t - (ctx - nq))) * a.n_kv_heads + kvh) * D;
+        const char* src = static_cast<const char*>((lane & 8) ? a.v_new : a.k_new) + row * 2 + (lane & 7) * (D / 4);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+      }
+    }
+  }
 
   if (n_pages == 0) {
     // No keys in this range: the single route writes zeros; an empty split writes nothing
@@ -187,7 +209,6 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
   __syncthreads();  // the barriers are initialised before any copy completes on them
 
   const int npp = (p < n_pages) ? (n_pages - p + NTEAM - 1) / NTEAM : 0;  // pages of this team
-  const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
   uint64_t* pfull = full + p * DEPTH;
   uint64_t* pempty = empty + p * DEPTH;
   int* pok = stage_ok + p * DEPTH;
@@ -195,8 +216,8 @@ __global__ void __launch_bounds__(NT * NTEAM * 32) decode_stage1_kernel(DecodeAr
 
   // page ids of this team (read by its issuing warp, nt = 0), a window of 32 in its lanes
   // (lane i <-> page k = wb + i)
-  int wb = 0, pg = -1;
-  if (nt == 0 && lane < npp) pg = __ldg(bt + p + lane * NTEAM);
+  int wb = 0;
+  if (lane >= npp) pg = -1;
   // the issuing warp, collectively: issue the copy of the team's page k into its slot
   auto issue = [&](int k) {
     while (k >= wb + 32) {
@@ -530,21 +551,33 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs a) {
   constexpr int TPG = kMergeCols / 4;           // threads per split group (4 dims each)
   constexpr int NG = kMergeThreads / TPG;       // split groups
+  constexpr int PRE = 8;                        // partials per thread loaded before the weights
   extern __shared__ float wts[];                // [n_split] weights of the partial accumulators
   __shared__ float red[2][kMergeThreads / 32];
   __shared__ __align__(16) float4 part[NG][TPG];
   // blockIdx.y = b * nq + i: query row i of sequence b
   const int h = blockIdx.x, row = blockIdx.y, b = row / a.nq, Hq = a.n_q_heads, col0 = blockIdx.z * kMergeCols;
-  grid_dep_wait();  // the partials come from stage 1
-  int ctx = a.ctx_lens[b];
-  ctx = max(0, min(ctx, a.max_blocks_per_seq * KVQ_BLOCK_SIZE));
-  const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
   const long long pu0 = (static_cast<long long>(row) * Hq + h) * a.n_split;
   const float* stats = a.part_stats + pu0 * 4;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int grp = tid / TPG, dq = tid % TPG;
+  const float4* acc = reinterpret_cast<const float4*>(a.part_acc + pu0 * D + col0) + dq;
+  grid_dep_wait();  // the partials come from stage 1
+  // The first PRE partials of this thread and its split's statistics are loaded together with
+  // ctx, before the number of live splits is known: the reads stay inside the grid's n_split
+  // slots, and slots past the live ones are never used.
+  float4 v[PRE];
+#pragma unroll
+  for (int u = 0; u < PRE; ++u)
+    if (grp + u * NG < a.n_split) v[u] = acc[static_cast<long long>(grp + u * NG) * (D / 4)];
+  float4 st0 = make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+  if (tid < a.n_split) st0 = reinterpret_cast<const float4*>(stats)[tid];
+  int ctx = a.ctx_lens[b];
+  ctx = max(0, min(ctx, a.max_blocks_per_seq * KVQ_BLOCK_SIZE));
+  const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
 
-  float Ms = -INFINITY, Mz = -INFINITY;
-  for (int s = tid; s < n; s += kMergeThreads) {
+  float Ms = tid < n ? st0.x : -INFINITY, Mz = tid < n ? st0.y : -INFINITY;
+  for (int s = tid + kMergeThreads; s < n; s += kMergeThreads) {
     Ms = fmaxf(Ms, stats[s * 4 + 0]);
     Mz = fmaxf(Mz, stats[s * 4 + 1]);
   }
@@ -567,9 +600,9 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
   }
   float lpart = 0.f;
   for (int s = tid; s < n; s += kMergeThreads) {
-    const float ms = stats[s * 4 + 0], mz = stats[s * 4 + 1], l = stats[s * 4 + 2];
-    wts[s] = (Mz != -INFINITY && mz != -INFINITY) ? fast_exp2(mz - Mz) : 0.f;
-    lpart += (Ms != -INFINITY && ms != -INFINITY) ? l * fast_exp2(ms - Ms) : 0.f;
+    const float4 st = s == tid ? st0 : reinterpret_cast<const float4*>(stats)[s];
+    wts[s] = (Mz != -INFINITY && st.y != -INFINITY) ? fast_exp2(st.y - Mz) : 0.f;
+    lpart += (Ms != -INFINITY && st.x != -INFINITY) ? st.z * fast_exp2(st.x - Ms) : 0.f;
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) lpart += __shfl_xor_sync(0xffffffffu, lpart, off);
@@ -580,30 +613,39 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
 #pragma unroll
   for (int i = 0; i < kMergeThreads / 32; ++i) l += red[0][i];
 
-  const int grp = tid / TPG, dq = tid % TPG;
-  const float4* acc = reinterpret_cast<const float4*>(a.part_acc + pu0 * D + col0) + dq;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-  int s = grp;
-  for (; s + 7 * NG < n; s += 8 * NG) {
-    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) v[u] = acc[static_cast<long long>(s + u * NG) * (D / 4)];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float wgt = wts[s + u * NG];
+  for (int u = 0; u < PRE; ++u) {
+    const int s = grp + u * NG;
+    if (s < n) {
+      const float wgt = wts[s];
       o.x = fmaf(v[u].x, wgt, o.x);
       o.y = fmaf(v[u].y, wgt, o.y);
       o.z = fmaf(v[u].z, wgt, o.z);
       o.w = fmaf(v[u].w, wgt, o.w);
     }
   }
+  int s = grp + PRE * NG;
+  for (; s + 7 * NG < n; s += 8 * NG) {
+    float4 w8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) w8[u] = acc[static_cast<long long>(s + u * NG) * (D / 4)];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float wgt = wts[s + u * NG];
+      o.x = fmaf(w8[u].x, wgt, o.x);
+      o.y = fmaf(w8[u].y, wgt, o.y);
+      o.z = fmaf(w8[u].z, wgt, o.z);
+      o.w = fmaf(w8[u].w, wgt, o.w);
+    }
+  }
   for (; s < n; s += NG) {
-    const float4 v = acc[static_cast<long long>(s) * (D / 4)];
+    const float4 w1 = acc[static_cast<long long>(s) * (D / 4)];
     const float wgt = wts[s];
-    o.x = fmaf(v.x, wgt, o.x);
-    o.y = fmaf(v.y, wgt, o.y);
-    o.z = fmaf(v.z, wgt, o.z);
-    o.w = fmaf(v.w, wgt, o.w);
+    o.x = fmaf(w1.x, wgt, o.x);
+    o.y = fmaf(w1.y, wgt, o.y);
+    o.z = fmaf(w1.z, wgt, o.z);
+    o.w = fmaf(w1.w, wgt, o.w);
   }
   part[grp][dq] = o;
   __syncthreads();
