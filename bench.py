@@ -573,11 +573,14 @@ def _extra_sparse_32k(kvq, W, bf16, i32, timed, dev, reps):
     kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
     q, off, cells, row = bf16(w["q"]), i32(w["cell_offsets"]), i32(w["cells"]), i32(w["block_table"][0])
     out = torch.empty((w["n_queries"], w["hq"], w["d"]), dtype=torch.float32, device=dev)
-    ms = timed(lambda: kvq.kvq_attn_sparse_int8kv(cache, q, off, cells, row, w["softmax_scale"], out=out), reps)
+    ws = torch.empty(kvq.kvq_sparse_workspace_bytes(int(row.numel()), w["hkv"], w["d"]), dtype=torch.uint8,
+                     device=dev)
+    ms = timed(lambda: kvq.kvq_attn_sparse_int8kv(cache, q, off, cells, row, w["softmax_scale"], out=out,
+                                                  workspace=ws), reps)
     pairs = int(len(w["cells"]))
     fma = pairs * w["hq"] * w["d"] * 2
     res["sparse_32k"] = {"ms_per_call": round(ms, 4), "GFMA_per_s": round(fma / ms / 1e6, 1),
-                         "pairs": pairs}
+                         "pairs": pairs, "workspace_bytes": int(ws.numel())}
     return res
 
 

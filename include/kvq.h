@@ -331,11 +331,17 @@ int kvq_attn_prefill_int8_qcodes(const kvq_cache* cache, const int8_t* q_codes, 
                                  float softmax_scale, float* out, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
+/* Workspace (bytes) of kvq_attn_sparse_int8kv: one gather record per (logical page, KV head,
+ * slot) of the sequence, 2 * head_dim + 16 bytes each (the token's K codes, V codes, both
+ * scales and a page-valid word).  0 if an argument is not positive or head_dim is not 128 / 256. */
+size_t kvq_sparse_workspace_bytes(int32_t n_blocks_row, int32_t n_kv_heads, int32_t head_dim);
+
 /*
  * kvq_attn_sparse_int8kv — sparse prompt attention ([QSA] "Problem and result",
- * "Approach"): one CTA per (query, KV head) walks the query's list of selected cells
- * in 64-cell chunks with an online softmax; each chunk's sums start from zero and are
- * folded into the running sums with one fma, so no scratch and no merge pass.
+ * "Approach"): one CTA per (query, KV head) walks the query's list of selected cells with
+ * an online softmax, no scratch in HBM and no merge pass; the GQA group shares each gathered
+ * K/V row.  A pre-pass first rewrites the sequence's pages into token-major gather records
+ * in the workspace, so that each selected cell is one contiguous copy.
  *   out[i][h] = sum_{t in cells(i)} softmax_t(s) * v^[t], s as in decode.
  *   q           : device bf16 [n_queries][n_q_heads][head_dim]
  *   cell_offsets: device int32 [n_queries + 1]; cells of query i are
@@ -343,12 +349,17 @@ int kvq_attn_prefill_int8_qcodes(const kvq_cache* cache, const int8_t* q_codes, 
  *                 ascending (the order only changes fp32 rounding); an empty list gives zeros
  *   block_table_row: device int32 [n_blocks_row] mapping logical positions to pages
  *   out         : device fp32 [n_queries][n_q_heads][head_dim]
+ *   workspace   : device, >= kvq_sparse_workspace_bytes(n_blocks_row, n_kv_heads, head_dim),
+ *                 16-byte aligned; its contents on entry do not matter
+ * The GQA group (n_q_heads / n_kv_heads) may be 1..16.  A cell outside [0, 16 n_blocks_row)
+ * is skipped (KVQ_DEV_BAD_CELL); a cell on a page whose block-table entry is outside
+ * [0, num_blocks) is skipped (KVQ_DEV_BAD_BLOCK).
  */
 int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_queries,
                            int32_t n_q_heads, const int32_t* cell_offsets,
                            const int32_t* cells, const int32_t* block_table_row,
                            int32_t n_blocks_row, float softmax_scale, float* out,
-                           void* stream);
+                           void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Test entry points of the prefill path (same device code as kvq_attn_prefill_int8).

@@ -413,17 +413,26 @@ int kvq_attn_prefill_int8_qcodes(const kvq_cache* cache, const int8_t* q_codes, 
   return cuda_status(kvq::launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
+size_t kvq_sparse_workspace_bytes(int32_t n_blocks_row, int32_t n_kv_heads, int32_t head_dim) {
+  if (n_blocks_row <= 0 || n_kv_heads <= 0 || (head_dim != 128 && head_dim != 256)) return 0;
+  return kvq::sparse_workspace_bytes(n_blocks_row, n_kv_heads, head_dim);
+}
+
 int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_queries, int32_t n_q_heads,
                            const int32_t* cell_offsets, const int32_t* cells,
                            const int32_t* block_table_row, int32_t n_blocks_row, float softmax_scale,
-                           float* out, void* stream) {
+                           float* out, void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_cache(cache);
   if (st != KVQ_OK) return st;
   if (!q || !cell_offsets || !cells || !block_table_row || !out) return KVQ_ERR_INVALID_ARG;
   if (n_queries <= 0 || n_q_heads <= 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (cache->n_kv_heads > 65535) return KVQ_ERR_UNSUPPORTED;  // grid y of both kernels
   if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   const int G = n_q_heads / cache->n_kv_heads;
-  if (G != 1 && G != 2 && G != 4 && G != 6 && G != 8 && G != 12) return KVQ_ERR_UNSUPPORTED;
+  if (G > 16) return KVQ_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < kvq::sparse_workspace_bytes(n_blocks_row, cache->n_kv_heads, cache->head_dim))
+    return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
   if (!aligned4(cell_offsets) || !aligned4(cells) || !aligned4(block_table_row)) return KVQ_ERR_MISALIGNED;
   kvq::SparseArgs a{};
@@ -443,6 +452,7 @@ int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_quer
   a.n_blocks_row = n_blocks_row;
   a.softmax_scale = softmax_scale;
   a.out = out;
+  a.records = static_cast<uint8_t*>(workspace);
   a.status = status_ptr();
   return cuda_status(kvq::launch_sparse(a, static_cast<cudaStream_t>(stream)));
 }

@@ -88,8 +88,10 @@ struct SparseArgs {
   int n_blocks_row;
   float softmax_scale;
   float* out;
+  uint8_t* records;  // workspace: gather records [n_blocks_row][Hkv][16][2D + 16]
   unsigned int* status;
 };
+size_t sparse_workspace_bytes(int n_blocks_row, int n_kv_heads, int head_dim);
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
 
 struct PrefillArgs {

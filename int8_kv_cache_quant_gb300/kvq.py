@@ -79,7 +79,9 @@ def lib():
         L.kvq_prefill_workspace_bytes.restype = sz
         L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
-        L.kvq_attn_sparse_int8kv.argtypes = [cp, vp, i32, i32, vp, vp, vp, i32, f32, vp, vp]
+        L.kvq_attn_sparse_int8kv.argtypes = [cp, vp, i32, i32, vp, vp, vp, i32, f32, vp, vp, sz, vp]
+        L.kvq_sparse_workspace_bytes.restype = sz
+        L.kvq_sparse_workspace_bytes.argtypes = [i32, i32, i32]
         L.kvq_debug_prefill_q_codes.argtypes = [vp, i32, i32, i32, vp, vp, vp]
         L.kvq_debug_prefill_qk_int32.argtypes = [cp, vp, i32, i32, vp, i32, i32, i32, i32, i32, vp, vp]
         _lib = L
@@ -315,16 +317,24 @@ def kvq_attn_prefill_int8_qcodes(cache, q_codes, q_scales, history_len, block_ta
     return out
 
 
+def kvq_sparse_workspace_bytes(n_blocks_row, n_kv_heads, head_dim):
+    return int(lib().kvq_sparse_workspace_bytes(n_blocks_row, n_kv_heads, head_dim))
+
+
 def kvq_attn_sparse_int8kv(cache, q, cell_offsets, cells, block_table_row, softmax_scale,
-                           out=None, stream=None):
+                           out=None, workspace=None, stream=None):
     """q: bf16 [N][Hq][D]; cell_offsets int32 [N+1]; cells int32; returns fp32 [N][Hq][D]."""
     N, Hq, D = q.shape
     if out is None:
         out = torch.empty((N, Hq, D), dtype=torch.float32, device=q.device)
+    nb = int(block_table_row.numel())
+    if workspace is None:
+        workspace = torch.empty(kvq_sparse_workspace_bytes(nb, cache.n_kv_heads, D), dtype=torch.uint8,
+                                device=q.device)
     c = cache.struct()
     _check("kvq_attn_sparse_int8kv", lib().kvq_attn_sparse_int8kv(
         ctypes.byref(c), _p(q), N, Hq, _p(cell_offsets), _p(cells), _p(block_table_row),
-        int(block_table_row.numel()), float(softmax_scale), _p(out), _stream(stream)))
+        nb, float(softmax_scale), _p(out), _p(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

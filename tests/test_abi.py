@@ -52,6 +52,10 @@ def test_host_helpers_without_gpu():
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 30720, 256) == (
         2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4)
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, -1, 256) == 0
+    # sparse: one gather record (K row | V row | 2 scales | valid | pad) per page, KV head and slot
+    assert k.kvq_sparse_workspace_bytes(2048, 1, 256) == 2048 * 16 * (2 * 256 + 16)
+    assert k.kvq_sparse_workspace_bytes(100, 2, 128) == 100 * 2 * 16 * (2 * 128 + 16)
+    assert k.kvq_sparse_workspace_bytes(0, 1, 256) == 0 and k.kvq_sparse_workspace_bytes(8, 1, 192) == 0
 
 
 def test_invalid_arguments_rejected_before_launch():
@@ -80,6 +84,10 @@ def test_invalid_arguments_rejected_before_launch():
                                     None, None) == 2
     assert L.kvq_attn_verify_int8kv(ctypes.byref(c), 16, 1, 0, 8, 16, 4, 16, 100, 1.0, 16, None, 0,
                                     None, None) == 1
+    # sparse: group above 16; workspace missing or too small
+    assert L.kvq_attn_sparse_int8kv(ctypes.byref(c), 16, 4, 68, 16, 16, 16, 8, 1.0, 16, 16, 1 << 20, None) == 2
+    assert L.kvq_attn_sparse_int8kv(ctypes.byref(c), 16, 4, 48, 16, 16, 16, 8, 1.0, 16, None, 0, None) == 4
+    assert L.kvq_attn_sparse_int8kv(ctypes.byref(c), 16, 4, 48, 16, 16, 16, 8, 1.0, 16, 16, 100, None) == 4
     # prefill: the softmax scale must be finite and positive (the kernel's exp2 relies on it)
     for bad in (0.0, -0.5, float("inf"), float("nan")):
         assert L.kvq_attn_prefill_int8(ctypes.byref(c), 16, 16, 8, 0, 16, 1, bad, 16, 16, 1 << 30,

@@ -54,6 +54,47 @@ def test_every_cell_equals_causal_and_edge_lists(kvq, oracle):
     assert norm_max_err(got, ref) <= DESIGN_TOL
 
 
+@pytest.mark.parametrize("d,hq,hkv", [(256, 16, 1), (128, 12, 1), (128, 3, 1)])
+def test_group_sizes_and_tile_tails(kvq, oracle, d, hq, hkv):
+    # groups of 16 (two full 8-head tiles), 12 and 3; cell counts that leave ragged tiles
+    w = W.make("sparse_32k", seed=520 + hq, ctx=500, n_queries=23, n_sample=37, n_tail=2, hq=hq, hkv=hkv, d=d)
+    cache, _ = gpu_cache_from(w, kvq)
+    got = _sparse(kvq, w, cache, w["cell_offsets"], w["cells"])
+    hc = host_cache_from(w, oracle)
+    ref = oracle.sparse_f64(hc, w["q"], w["cell_offsets"], w["cells"], w["block_table"][0], w["softmax_scale"])
+    assert norm_max_err(got, ref) <= DESIGN_TOL
+    assert kvq.kvq_device_status() == 0
+
+
+def test_bad_cells_and_pages_are_skipped_and_flagged(kvq, oracle):
+    # cells past the mapped range or negative are skipped (BAD_CELL); cells on a page whose
+    # block-table entry is out of range are skipped (BAD_BLOCK); the rest is exact
+    w = W.make("sparse_32k", seed=530, ctx=320, n_queries=6, n_sample=40, hq=12, hkv=1, d=256)
+    cache, _ = gpu_cache_from(w, kvq)
+    lists = [np.sort(np.random.default_rng(531 + j).choice(300, 50, replace=False)).astype(np.int32)
+             for j in range(6)]
+    good = [x.copy() for x in lists]
+    lists[1] = np.concatenate([lists[1], [320 + 5, -3]]).astype(np.int32)
+    offsets = np.concatenate([[0], np.cumsum([len(x) for x in lists])]).astype(np.int32)
+    cells = np.concatenate(lists).astype(np.int32)
+    got = _sparse(kvq, w, cache, offsets, cells)
+    assert kvq.kvq_device_status() & 0x8  # KVQ_DEV_BAD_CELL
+    goff = np.concatenate([[0], np.cumsum([len(x) for x in good])]).astype(np.int32)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.sparse_f64(hc, w["q"], goff, np.concatenate(good), w["block_table"][0], w["softmax_scale"])
+    assert norm_max_err(got, ref) <= DESIGN_TOL
+    # a bad page: block-table entry 3 points past the cache; cells on page 3 drop out
+    row = w["block_table"][0].copy()
+    row[3] = w["num_blocks"] + 7
+    out = kvq.kvq_attn_sparse_int8kv(cache, to_bf16_tensor(w["q"]), to_i32(goff), to_i32(np.concatenate(good)),
+                                     to_i32(row), w["softmax_scale"]).cpu().numpy()
+    assert kvq.kvq_device_status() & 0x1  # KVQ_DEV_BAD_BLOCK
+    kept = [x[(x // 16) != 3] for x in good]
+    koff = np.concatenate([[0], np.cumsum([len(x) for x in kept])]).astype(np.int32)
+    ref2 = oracle.sparse_f64(hc, w["q"], koff, np.concatenate(kept), w["block_table"][0], w["softmax_scale"])
+    assert norm_max_err(out, ref2) <= DESIGN_TOL
+
+
 def test_sparse_32k_full_sampled(kvq, oracle):
     """Workload sparse_32k at full size (ctx 32768, 2048 queries x 2051 cells, 12 q heads per
     KV head, head_dim 256): sampled (query, head) outputs against FP64."""
