@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(256) sparse_prep_kernel(SparseArgs a) {
 // One CTA per (query, KV head): NTEAM teams of NT warps; team p takes tiles p, p + NTEAM, ... of
 // the query's cell list; warp nt of a team holds query heads 8 nt .. 8 nt + 7 of the group.
 template <int D, int NT, int NTEAM, int DEPTH>
-__global__ void __launch_bounds__(NT * NTEAM * 32, 1) sparse_kernel(SparseArgs a) {
+__global__ void __launch_bounds__(NT * NTEAM * 32, 2) sparse_kernel(SparseArgs a) {
   using L = SparseSmem<D, NT, NTEAM, DEPTH>;
   using R = SparseRec<D>;
   constexpr int NW = L::kWarps;
@@ -417,8 +417,11 @@ size_t sparse_workspace_bytes(int n_blocks_row, int n_kv_heads, int head_dim) {
 
 template <int D, int NT>
 static cudaError_t launch_sparse_attn(const SparseArgs& a, cudaStream_t stream) {
-  constexpr int NTEAM = NT == 1 ? 8 : 16 / NT;
-  constexpr int DEPTH = 24 / NTEAM;
+  // four teams, three stages each: two CTAs per SM, so one CTA's start-up and merge overlap
+  // the other's streaming (measured at sparse_32k: 0.668 ms, against 0.742 ms for one CTA of
+  // eight teams per SM and 0.77-1.07 ms for the other shapes tried)
+  constexpr int NTEAM = 4;
+  constexpr int DEPTH = 3;
   using L = SparseSmem<D, NT, NTEAM, DEPTH>;
   auto kern = sparse_kernel<D, NT, NTEAM, DEPTH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
