@@ -45,6 +45,7 @@ def _load():
         lib.oracle_decode_f64.argtypes = [vp, vp, i32, i32, vp, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_verify_f64.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_decode_split_f64.argtypes = [vp, vp, i32, i32, vp, i32, vp, f64, i32, vp, i32]
+        lib.oracle_prefill_first_f64.argtypes = [vp, vp, vp, i32, i32, i32, i32, f64, vp, i32, vp, i32]
         lib.oracle_prefill_ref_f64.argtypes = [vp, vp, i32, i32, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_prefill_qk_int32.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp]
         lib.oracle_prefill_int8_emul.argtypes = [vp, vp, i32, i32, i32, vp, ctypes.c_float, i32,
@@ -205,6 +206,18 @@ def prefill_ref_f64(cache, q, history, bt_row, scale, units=None, n_threads=0):
     s = cache.struct()
     _load().oracle_prefill_ref_f64(ctypes.byref(s), _ptr(q), T, Hq, int(history), _ptr(bt),
                                    float(scale), _ptr(u), nu, _ptr(out), n_threads)
+    return out
+
+
+def prefill_first_f64(q, k, v, scale, units=None, n_threads=0):
+    """The first prefill chunk in high precision: causal attention of q bf16 bits [T][Hq][D] over
+    the chunk's own bf16 k, v [T][Hkv][D] (no quantisation) -> float64 [T][Hq][D] (or [n_units][D])."""
+    q, k, v = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
+    T, Hq, D = q.shape
+    u, nu = _units_arg(units)
+    out = np.zeros((T, Hq, D) if u is None else (nu, D), np.float64)
+    _load().oracle_prefill_first_f64(_ptr(q), _ptr(k), _ptr(v), T, Hq, k.shape[1], D, float(scale), _ptr(u), nu,
+                                     _ptr(out), n_threads)
     return out
 
 

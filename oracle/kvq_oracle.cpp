@@ -492,6 +492,41 @@ void oracle_decode_split_f64(const oracle_cache* cache, const uint16_t* q, int32
   });
 }
 
+// The first prefill chunk ([DCU] §3.1: no history to read; the chunk runs the high-precision
+// attention while the producer writes its K/V as int8): causal attention of the chunk over its
+// own bf16 K/V, before any quantisation.  Query i sees keys t <= i.  q [T][Hq][D], k and v
+// [T][Hkv][D] (bf16 bits); unit u = i * Hq + h.
+void oracle_prefill_first_f64(const uint16_t* q, const uint16_t* k, const uint16_t* v, int32_t n_tokens,
+                              int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, double scale,
+                              const int64_t* units, int32_t n_units, double* out, int32_t n_threads) {
+  const int D = head_dim, Hq = n_q_heads, Hkv = n_kv_heads, G = Hq / Hkv;
+  int64_t n = units ? n_units : static_cast<int64_t>(n_tokens) * Hq;
+  parallel_for(n, n_threads, [&](int64_t j) {
+    int64_t u = unit_at(units, j);
+    const int i = static_cast<int>(u / Hq), h = static_cast<int>(u % Hq), kvh = h / G;
+    std::vector<double> qd(D), s(i + 1);
+    bf16_row_to_double(q + u * D, D, qd.data());
+    double m = -INFINITY;
+    for (int t = 0; t <= i; ++t) {
+      const uint16_t* kr = k + (static_cast<int64_t>(t) * Hkv + kvh) * D;
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qd[d] * bf16_to_float(kr[d]);
+      s[t] = scale * dot;
+      m = std::max(m, s[t]);
+    }
+    double l = 0.0;
+    double* o = out + j * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int t = 0; t <= i; ++t) {
+      const double p = std::exp(s[t] - m);
+      l += p;
+      const uint16_t* vr = v + (static_cast<int64_t>(t) * Hkv + kvh) * D;
+      for (int d = 0; d < D; ++d) o[d] += p * bf16_to_float(vr[d]);
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+  });
+}
+
 // Part A, prefill chunk ([DCU] §3.2): query i at position history + i sees keys
 // t <= history + i, history and chunk alike.
 void oracle_prefill_ref_f64(const oracle_cache* cache, const uint16_t* q, int32_t n_tokens,

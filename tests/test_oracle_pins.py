@@ -324,6 +324,40 @@ def test_verify_rows_equal_prefill_chunk_and_decode(oracle):
     assert np.array_equal(part, out.reshape(-1, d)[units])
 
 
+# --------------------------------------------------------------------------- first prefill chunk
+
+def test_prefill_first_brute_force(oracle):
+    # numpy over the bf16 values: row i is softmax over keys 0..i (causal), GQA 3
+    rng = np.random.default_rng(41)
+    T, Hq, Hkv, D, scale = 19, 6, 2, 128, 0.07
+    q, k, v = (W.normal_bf16(rng, (T, h, D)) for h in (Hq, Hkv, Hkv))
+    out = oracle.prefill_first_f64(q, k, v, scale)
+    qf, kf, vf = (W.bf16_bits_to_f32(x).astype(np.float64) for x in (q, k, v))
+    for i in range(T):
+        for h in range(Hq):
+            s = scale * (kf[:i + 1, h // 3] @ qf[i, h])
+            p = np.exp(s - s.max())
+            assert np.allclose(out[i, h], (p / p.sum()) @ vf[:i + 1, h // 3], rtol=1e-12, atol=1e-14)
+
+
+def test_prefill_first_closed_forms(oracle):
+    # row 0 sees only key 0: output is v_0 exactly; with every K row equal the weights are
+    # uniform, so row i is the mean of v_0..v_i
+    rng = np.random.default_rng(42)
+    T, Hq, D = 9, 4, 256
+    k = np.tile(W.normal_bf16(rng, (1, 1, D)), (T, 1, 1))
+    v = W.normal_bf16(rng, (T, 1, D))
+    q = W.normal_bf16(rng, (T, Hq, D))
+    out = oracle.prefill_first_f64(q, k, v, 1 / 16)
+    vf = W.bf16_bits_to_f32(v).astype(np.float64)[:, 0]
+    for h in range(Hq):
+        assert np.array_equal(out[0, h], vf[0])
+    for i in range(T):
+        assert np.allclose(out[i, 2], vf[:i + 1].mean(axis=0), rtol=1e-13, atol=1e-15)
+    units = np.array([0, 7, 35], np.int64)
+    assert np.array_equal(oracle.prefill_first_f64(q, k, v, 1 / 16, units=units), out.reshape(-1, D)[units])
+
+
 # --------------------------------------------------------------------------- prefill
 
 def _prefill_case(oracle, seed, history, T, hq=4, hkv=2, d=128, **kw):
