@@ -409,6 +409,8 @@ def bench_extra(args, local, hbm, tflops, only=None):
         res.update(_extra_rope_quant_write(kvq, W, bf16, i32, timed, dev, reps or 20, hbm))
     if want("prefill_32k"):
         res.update(_extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps or 10, tflops))
+    if want("prefill_first_4k"):
+        res.update(_extra_prefill_first_4k(kvq, W, bf16, i32, timed, dev, reps or 10, tflops))
     if want("sparse_32k"):
         res.update(_extra_sparse_32k(kvq, W, bf16, i32, timed, dev, reps or 10))
     return res
@@ -564,6 +566,28 @@ def _extra_prefill_32k(kvq, W, bf16, i32, timed, dev, reps, tflops):
     return res
 
 
+def _extra_prefill_first_4k(kvq, W, bf16, i32, timed, dev, reps, tflops):
+    """The first prefill chunk of a sequence, 4096 tokens at 24 query / 4 KV heads, head_dim 256
+    (the page's 0 + 4K chunk): the chunk's K/V written into the int8 cache and the high-precision
+    causal attention over its bf16 Q/K/V, one call.  Ops: 2 (QK, PV) x 2 x head_dim per visible
+    (query head, query, key) triple."""
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(99)
+    T, hq, hkv, d = 4096, 24, 4, 256
+    nb = T // 16
+    table = i32(rng.permutation(nb).astype(np.int32))
+    q, k, v = (bf16(W.normal_bf16(rng, (T, h, d))) for h in (hq, hkv, hkv))
+    cache = kvq.KVCache(nb, hkv, d, device=dev)
+    out = torch.empty((T, hq, d), dtype=torch.float32, device=dev)
+    ws = torch.empty(kvq.kvq_prefill_first_workspace_bytes(T, hq, hkv, d), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: kvq.kvq_attn_prefill_first_bf16(cache, q, k, v, table, 1.0 / 16, out=out, workspace=ws), reps)
+    ops = 2.0 * 2 * d * hq * (T * (T + 1) / 2)
+    return {"prefill_first_4k": {"ms_per_call": round(ms, 4), "TFLOPS": round(ops / ms / 1e9, 1),
+                                 "frac_of_bf16_peak": round(ops / ms / 1e9 / tflops, 4), "ops": ops,
+                                 "step": "kvq_attn_prefill_first_bf16: int8 K/V write + fp16-operand attention"}}
+
+
 def _extra_sparse_32k(kvq, W, bf16, i32, timed, dev, reps):
     import torch
     res = {}
@@ -665,7 +689,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default=None, choices=["prefill_32k", "sparse_32k", "decode_1k", "decode_b64", "verify_32k",
-                             "rope_quant_write"],
+                             "rope_quant_write", "prefill_first_4k"],
                     help="time only this secondary workload (profiling runs); prints its figures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

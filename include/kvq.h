@@ -361,6 +361,38 @@ int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_quer
                            int32_t n_blocks_row, float softmax_scale, float* out,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* Workspace (bytes) of kvq_attn_prefill_first_bf16: the fp16 Q rows and their scales, and the
+ * chunk's K/V as fp16 operand pieces with their scales (2 * 2 * head_dim bytes per key and KV
+ * head).  0 if an argument is not positive or head_dim is not 128 / 256. */
+size_t kvq_prefill_first_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads,
+                                         int32_t head_dim);
+
+/*
+ * kvq_attn_prefill_first_bf16 — the first prefill chunk of a sequence ([DCU] §3.1: there is no
+ * history to read, so the chunk runs a high-precision attention over its own bf16 Q/K/V while the
+ * producer writes its K/V as int8 for the chunks and decode steps that follow; §4.2 measures the
+ * int8 path as slower than bf16 for the 0 + 4K chunk).  For tokens t = 0 .. n_tokens - 1:
+ *   (1) k_new[t], v_new[t] are quantised by the kvq_quant_write rule into position t of the
+ *       sequence (the same codes and scales, bit for bit);
+ *   (2) out[t][h] = sum_{s <= t} softmax_s(softmax_scale * q[t][h] . k[s]) * v[s] over the bf16
+ *       values themselves (causal, GQA).  The tensor cores see fp16: each row of Q, K and V is
+ *       scaled by a power of two into fp16 range (exact for every value within 2^29 of the row's
+ *       largest), and the softmax weights of each 128-key tile go in as fp16 w / max w.
+ * Later chunks of the sequence use kvq_attn_prefill_int8 (history_len > 0).
+ *   q           : device bf16 [n_tokens][n_q_heads][head_dim]
+ *   k_new, v_new: device bf16 [n_tokens][n_kv_heads][head_dim]
+ *   block_table_row: device int32 [n_blocks_row] of the sequence; n_tokens <= 16 * n_blocks_row
+ *   out         : device fp32 [n_tokens][n_q_heads][head_dim]
+ *   workspace   : >= kvq_prefill_first_workspace_bytes(...), 16-byte aligned
+ *   softmax_scale: finite and > 0
+ * A page id outside [0, num_blocks) skips that page's K/V write (KVQ_DEV_BAD_BLOCK); the
+ * attention does not read the cache.
+ */
+int kvq_attn_prefill_first_bf16(const kvq_cache* cache, const void* q, const void* k_new, const void* v_new,
+                                int32_t n_tokens, int32_t n_q_heads, const int32_t* block_table_row,
+                                int32_t n_blocks_row, float softmax_scale, float* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
 /*
  * Test entry points of the prefill path (same device code as kvq_attn_prefill_int8).
  * kvq_debug_prefill_q_codes: the per-(token, query head) Q quantisation step alone.

@@ -388,6 +388,44 @@ int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_token
   return KVQ_OK;
 }
 
+size_t kvq_prefill_first_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads,
+                                         int32_t head_dim) {
+  if (n_tokens <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || (head_dim != 128 && head_dim != 256)) return 0;
+  return static_cast<size_t>(kvq::prefill_workspace(n_tokens, n_q_heads, n_kv_heads, 0, head_dim, 2).bytes);
+}
+
+int kvq_attn_prefill_first_bf16(const kvq_cache* cache, const void* q, const void* k_new, const void* v_new,
+                                int32_t n_tokens, int32_t n_q_heads, const int32_t* block_table_row,
+                                int32_t n_blocks_row, float softmax_scale, float* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!q || !k_new || !v_new || !block_table_row || !out) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens <= 0 || n_q_heads <= 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_tokens) > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out) || !aligned4(block_table_row))
+    return KVQ_ERR_MISALIGNED;
+  const kvq::PrefillWorkspace w = kvq::prefill_workspace(n_tokens, n_q_heads, cache->n_kv_heads, 0, cache->head_dim, 2);
+  if (!workspace || workspace_bytes < static_cast<size_t>(w.bytes)) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
+  kvq::PrefillArgs a = prefill_args(cache, q, n_tokens, n_q_heads, 0, block_table_row, n_blocks_row,
+                                    softmax_scale, out, nullptr);
+  char* base = static_cast<char*>(workspace);
+  a.q_f16 = reinterpret_cast<uint16_t*>(base);
+  a.q_scales = reinterpret_cast<float*>(base + w.off_q_scales);
+  a.n_kv_tiles = w.n_kv_tiles;
+  a.kw = reinterpret_cast<uint8_t*>(base + w.off_kw);
+  a.vw = reinterpret_cast<uint8_t*>(base + w.off_vw);
+  a.skw = reinterpret_cast<float*>(base + w.off_skw);
+  a.svw = reinterpret_cast<float*>(base + w.off_svw);
+  a.k_src = k_new;
+  a.v_src = v_new;
+  return cuda_status(kvq::launch_prefill_first(a, static_cast<cudaStream_t>(stream)));
+}
+
 int kvq_attn_prefill_int8_qcodes(const kvq_cache* cache, const int8_t* q_codes, const float* q_scales,
                                  int32_t n_tokens, int32_t n_q_heads, int32_t history_len,
                                  const int32_t* block_table_row, int32_t n_blocks_row, float softmax_scale,

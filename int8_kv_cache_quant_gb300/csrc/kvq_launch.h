@@ -95,10 +95,10 @@ size_t sparse_workspace_bytes(int n_blocks_row, int n_kv_heads, int head_dim);
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);
 
 struct PrefillArgs {
-  const int8_t* k;
-  const int8_t* v;
-  const float* k_scale;
-  const float* v_scale;
+  int8_t* k;          // the cache (written only by the first-chunk pass)
+  int8_t* v;
+  float* k_scale;
+  float* v_scale;
   int num_blocks, n_kv_heads, head_dim;
   const void* q;  // bf16 [T][Hq][D]
   int n_tokens, n_q_heads, history_len;
@@ -108,6 +108,11 @@ struct PrefillArgs {
   float* out;        // fp32 [T][Hq][D]
   int8_t* q_codes;   // workspace int8 [T][Hq][D]
   float* q_scales;   // workspace fp32 [T][Hq]
+  // first chunk in high precision: fp16 Q (q * 2^e per row) in place of the codes, and the
+  // chunk's own bf16 K/V [T][Hkv][D] (also written into the int8 cache by the pre-pass)
+  uint16_t* q_f16;   // workspace fp16 [T][Hq][D]
+  const void* k_src;
+  const void* v_src;
   // workspace: K/V of every (KV head, 128-key tile) widened to the attention kernel's
   // shared-memory operand image, and the tiles' key / value scales
   int n_kv_tiles;
@@ -124,9 +129,13 @@ struct PrefillWorkspace {
   int n_kv_tiles;
   long long off_q_scales, off_kw, off_vw, off_skw, off_svw, bytes;
 };
-PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim);
+PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim,
+                                   int q_elem_bytes = 1);
 cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+// first chunk: Q to fp16, the chunk's K/V into the cache and into fp16 operand pieces, then the
+// attention in high precision (fp16 P)
+cudaError_t launch_prefill_first(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_qk_debug(const PrefillArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

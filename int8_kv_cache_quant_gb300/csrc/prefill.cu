@@ -24,6 +24,7 @@
 //   running maximum after each 128-key tile, so the codes are reproducible off the GPU.
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
+#include "quant_rule.cuh"
 #include "tcgen05.cuh"
 
 namespace kvq {
@@ -357,6 +358,153 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
   grid_dep_trigger();
 }
 
+// ============================================================================ first chunk (high precision)
+// "gfx936 ..." §3.1: the first prefill chunk has no history to read; it runs the high-precision
+// attention over its own bf16 Q/K/V while the producer writes its K/V as int8 for the chunks
+// and decode steps that follow.  Here the same attention kernel runs on fp16 operands: a row x
+// of Q, K or V becomes x * 2^(14 - e) with e the exponent of max |x| (so max |x| * 2^(14 - e) lies
+// in [2^14, 2^15)), exact for every bf16 value within 2^29 of the row's maximum, and its scale
+// is 2^(e - 14).  The int8 codes and the fp16 operands are made by one pass over the chunk.
+
+// 2^(e - 14) and its inverse for a row maximum amax (1 for amax = 0), exponents clamped.
+__device__ __forceinline__ void pow2_scales(float amax, float& to_f16, float& back) {
+  int e = amax > 0.f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127 : 14;
+  e = max(-100, min(e, 100));
+  to_f16 = __uint_as_float(static_cast<uint32_t>(127 + 14 - e) << 23);
+  back = __uint_as_float(static_cast<uint32_t>(127 + e - 14) << 23);
+}
+
+// P fp32 values (this lane's elements of a row) to fp16 after scaling, packed in pairs.
+template <int P>
+__device__ __forceinline__ void to_f16_pairs(const float (&x)[P], float s, uint32_t (&h)[P / 2]) {
+#pragma unroll
+  for (int e = 0; e < P / 2; ++e) h[e] = pack_half2(x[2 * e] * s, x[2 * e + 1] * s);
+}
+
+// Q rows to fp16 (one warp per (token, query head) row).
+template <int D>
+__global__ void __launch_bounds__(256) q_pack_f16_kernel(PrefillArgs a) {
+  constexpr int P = D / 32;
+  const int lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= static_cast<long long>(a.n_tokens) * a.n_q_heads) return;
+  grid_dep_wait();
+  float x[P];
+  load_bf16_lane(static_cast<const uint16_t*>(a.q) + row * D + lane * P, x);
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < P; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  float to_f16, back;
+  pow2_scales(amax, to_f16, back);
+  uint32_t hq[P / 2];
+  to_f16_pairs(x, to_f16, hq);
+  uint16_t* dst = a.q_f16 + row * D + lane * P;
+  if constexpr (P == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(hq[0], hq[1], hq[2], hq[3]);
+  else *reinterpret_cast<uint2*>(dst) = make_uint2(hq[0], hq[1]);
+  if (lane == 0) a.q_scales[row] = back;
+}
+
+// One CTA per (128-key tile j, KV head): one warp per token row of the chunk.  Each K and V row is
+// (1) quantised by the kvq_quant_write rule into its cache slot (position t = 128 j + n of the
+// sequence whose block-table row is given), and (2) turned into fp16 with its power-of-two scale,
+// K straight into the tile's operand pieces (row = key), V through shared memory, whose
+// transpose (rows = dims) then goes out in 16-byte chunks: the layout kv_widen_kernel writes.
+template <int D>
+__global__ void __launch_bounds__(256) first_pack_kernel(PrefillArgs a) {
+  constexpr int P = D / 32;
+  extern __shared__ __align__(16) uint16_t vs[];  // [128 keys][D] fp16
+  const int j = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = a.n_tokens;
+  const long long tile = static_cast<long long>(kvh) * a.n_kv_tiles + j;
+  uint8_t* kdst = a.kw + tile * (D / 64) * kPieceBytes;
+  uint8_t* vdst = a.vw + tile * (D / 64) * kPieceBytes;
+  grid_dep_wait();  // Q packing and the chunk's rows come from the preceding kernels
+  for (int n = warp; n < 128; n += 8) {
+    const int t = 128 * j + n;
+    float xk[P], xv[P];
+    float sk = 0.f, sv = 0.f;
+    if (t < T) {
+      const long long row = (static_cast<long long>(t) * a.n_kv_heads + kvh) * D + lane * P;
+      load_bf16_lane(static_cast<const uint16_t*>(a.k_src) + row, xk);
+      load_bf16_lane(static_cast<const uint16_t*>(a.v_src) + row, xv);
+      // (1) the int8 cache write (the fused producer's part)
+      const int bi = t / KVQ_BLOCK_SIZE;
+      const int page = bi < a.n_blocks_row ? a.block_table_row[bi] : -1;
+      if (page >= 0 && page < a.num_blocks) {
+        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        const int slot = t % KVQ_BLOCK_SIZE;
+        int8_t qc[P];
+        uint32_t packed[P / 4];
+        const float ck = quant_rule_warp(xk, qc);
+        pack_codes(qc, packed);
+        store_k_codes<D>(a.k, ph, slot, lane, packed);
+        const float cv = quant_rule_warp(xv, qc);
+        store_v_codes<D>(a.v, ph, slot, lane, qc);
+        if (lane == 0) {
+          a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = ck;
+          a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = cv;
+        }
+      } else if (lane == 0) {
+        set_status(a.status, KVQ_DEV_BAD_BLOCK);
+      }
+      // (2) fp16 operands
+      float mk = 0.f, mv = 0.f;
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        mk = fmaxf(mk, fabsf(xk[e]));
+        mv = fmaxf(mv, fabsf(xv[e]));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, off));
+        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, off));
+      }
+      float tk, tv;
+      pow2_scales(mk, tk, sk);
+      pow2_scales(mv, tv, sv);
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        xk[e] *= tk;
+        xv[e] *= tv;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < P; ++e) xk[e] = xv[e] = 0.f;
+    }
+    uint32_t hk[P / 2], hv[P / 2];
+    to_f16_pairs(xk, 1.0f, hk);
+    to_f16_pairs(xv, 1.0f, hv);
+    // K piece d / 64, row n, 16-byte chunk (d % 64) / 8 (this lane's P dims start at d = lane * P)
+    const int d0 = lane * P;
+    uint8_t* kp = kdst + (d0 / 64) * kPieceBytes + tc::sw128_off(n, (d0 % 64) / 8) + (d0 % 8) * 2;
+    if constexpr (P == 8) *reinterpret_cast<uint4*>(kp) = make_uint4(hk[0], hk[1], hk[2], hk[3]);
+    else *reinterpret_cast<uint2*>(kp) = make_uint2(hk[0], hk[1]);
+    if constexpr (P == 8) *reinterpret_cast<uint4*>(vs + n * D + d0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    else *reinterpret_cast<uint2*>(vs + n * D + d0) = make_uint2(hv[0], hv[1]);
+    if (lane == 0) {
+      a.skw[tile * 128 + n] = sk;
+      a.svw[tile * 128 + n] = sv;
+    }
+  }
+  __syncthreads();
+  // V pieces: piece kh * (D/128) + dh holds keys 64 kh .. 64 kh + 63 (8 chunks of 8 keys) of dims
+  // 128 dh .. 128 dh + 127 (rows); item = (piece, dim row, chunk)
+  for (int it = tid; it < 16 * D; it += 256) {
+    const int c = it & 7, d = (it >> 3) & 127, pc = it >> 10;
+    const int kh = pc / (D / 128), dh = pc % (D / 128);
+    const int dim = 128 * dh + d, key0 = 64 * kh + 8 * c;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = static_cast<uint32_t>(vs[(key0 + 2 * e) * D + dim]) |
+             (static_cast<uint32_t>(vs[(key0 + 2 * e + 1) * D + dim]) << 16);
+    *reinterpret_cast<uint4*>(vdst + pc * kPieceBytes + tc::sw128_off(d, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  grid_dep_trigger();
+}
+
 // ============================================================================ warp-specialised prefill
 // One CTA per (128 query rows, query head), 18 warps:
 //   warps 0-15  softmax: thread (row r, part p = warp / 4) owns keys 32p .. 32p+31 of row r's S
@@ -418,7 +566,6 @@ constexpr int kBarDrain = kBarQFull + 1;
 
 constexpr int kSoftmaxThreads = 512;
 constexpr int kMmaWarp = kSoftmaxThreads / 32;
-constexpr int kProducerWarp = kMmaWarp + 1;
 constexpr int kPrefillThreads = kSoftmaxThreads + 64;
 
 // Bounded wait that also gives up as soon as another thread of the CTA has given up.
@@ -474,7 +621,10 @@ __device__ __forceinline__ float max4_col(const float* p, int row) {
 
 }  // namespace
 
-template <int D>
+// HP: the first chunk in high precision (fp16 Q with a power-of-two scale per row, the
+// chunk's K/V as fp16 pieces with power-of-two scales per key, P as fp16 w / max w per tile)
+// in place of the int8 Q, K/V and P codes; everything else is the same kernel.
+template <int D, bool HP>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(PrefillArgs a) {
   using L = PrefillTmaSmem<D>;
   constexpr int OCOLS = D / 4;   // O columns per softmax thread
@@ -532,17 +682,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     const bool row_real = q0 + row < T;
     const int pos_r = a.history_len + q0 + row;
     {
-      // Q: this thread's D/4 codes of its row, widened to fp16 pairs into tensor memory, the A
-      // operand of QK (lane = row, dim d in column kQCol + d / 2, even dims in the low half)
+      // Q: this thread's D/4 dims of its row as fp16 pairs into tensor memory, the A operand of
+      // QK (lane = row, dim d in column kQCol + d / 2, even dims in the low half): the int8
+      // codes widened, or (HP) the fp16 row as it is
       const int8_t* src = a.q_codes + (static_cast<long long>(q0 + row) * Hq + h) * D;
+      const uint16_t* src_h = a.q_f16 + (static_cast<long long>(q0 + row) * Hq + h) * D;
       uint32_t qw[D / 8];
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
         const int c16 = part * NP + i;
-        int4 raw = make_int4(0, 0, 0, 0);
-        if (row_real) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
-        uint4 c0, c1;
-        widen16(raw, c0, c1);
+        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
+        if constexpr (HP) {
+          if (row_real) {
+            c0 = __ldg(reinterpret_cast<const uint4*>(src_h + 16 * c16));
+            c1 = __ldg(reinterpret_cast<const uint4*>(src_h + 16 * c16 + 8));
+          }
+        } else {
+          int4 raw = make_int4(0, 0, 0, 0);
+          if (row_real) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
+          widen16(raw, c0, c1);
+        }
         qw[8 * i + 0] = c0.x;
         qw[8 * i + 1] = c0.y;
         qw[8 * i + 2] = c0.z;
@@ -663,8 +822,28 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       // decisions in all four parts of the row)
       float f = 1.0f;
       bool codes_on = wmax_row > 0.0f;
-      const float ps_new = __fdiv_rn(wmax_row, 127.0f);
-      if (!started) {
+      const float ps_new = HP ? wmax_row : __fdiv_rn(wmax_row, 127.0f);
+      if constexpr (HP) {
+        // fp16 P needs no per-tile unit: O's unit ps_ref only grows (to a tile whose largest
+        // weight exceeds it), and a tile below it goes in as w / ps_ref <= 1, so O never grows.
+        // ps_ref stays a normal number: it starts at a tile holding the running maximum (a
+        // weight p * sV with p = 1), and it only decays (by alpha < 1) on a tile that holds a new
+        // maximum, whose own weight then bounds it from below.
+        if (!started) {
+          if (codes_on) {
+            started = true;
+            ps_ref = wmax_row;
+          }
+        } else {
+          const float dec = ps_ref * alpha;
+          if (wmax_row > dec) {
+            f = dec / wmax_row;
+            ps_ref = wmax_row;
+          } else {
+            ps_ref = dec;
+          }
+        }
+      } else if (!started) {
         if (codes_on) {
           started = true;
           ps_ref = ps_new;
@@ -681,15 +860,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       } else {
         ps_ref *= alpha;
       }
-      // c = rint(w * r) with one rounding, as the low byte of fma(w, r, 1.5 * 2^23) (w <= wmax
-      // keeps c in [0, 127]; r = 0 gives c = 0); two codes per 32-bit column
-      const float rr = codes_on ? __fdiv_rn(127.0f, wmax_row) : 0.0f;
       uint32_t pk[16];
-      const f2 r2 = mk2(rr, rr), mg = mk2(kMagic, kMagic);
+      if constexpr (HP) {
+        // P = w / ps_ref in [0, 1] as fp16 (round to nearest), two per 32-bit column
+        const float rr = (codes_on && ps_ref > 0.0f) ? __fdiv_rn(1.0f, ps_ref) : 0.0f;
+        const f2 r2 = mk2(rr, rr);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const f2 c = fma2(mk2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), r2, mg);
-        pk[e] = __byte_perm(__float_as_uint(lo2(c)), __float_as_uint(hi2(c)), 0x5410u);
+        for (int e = 0; e < 16; ++e) {
+          const f2 c = mul2(mk2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), r2);
+          pk[e] = pack_half2(lo2(c), hi2(c));
+        }
+      } else {
+        // c = rint(w * r) with one rounding, as the low byte of fma(w, r, 1.5 * 2^23) (w <= wmax
+        // keeps c in [0, 127]; r = 0 gives c = 0); two codes per 32-bit column
+        const float rr = codes_on ? __fdiv_rn(127.0f, wmax_row) : 0.0f;
+        const f2 r2 = mk2(rr, rr), mg = mk2(kMagic, kMagic);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const f2 c = fma2(mk2(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), r2, mg);
+          pk[e] = __byte_perm(__float_as_uint(lo2(c)), __float_as_uint(hi2(c)), 0x5410u);
+        }
       }
       // O must hold PV_{j-1} before it is rescaled (and P_{j-1} must be consumed: it is)
       if (j > 0) {
@@ -726,7 +916,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       tc::fence_before_sync();
       mbar_arrive(&bars[kBarPFull]);
     }
-    // ---- epilogue: out = O * 2^24 * ps_ref / l (l summed over the four parts)
+    // ---- epilogue: out = O * 2^24 * ps_ref / l (l summed over the four parts; HP: no 2^24)
     if (!*abort_flag) {
       wait_or_abort(&bars[kBarPvDone], (n_tiles - 1) & 1, a.status, abort_flag);
       tc::fence_after_sync();
@@ -734,7 +924,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     red_max[part * 128 + row] = l_part;
     named_bar(gbar, 128);
     const float l = (red_max[row] + red_max[128 + row]) + (red_max[256 + row] + red_max[384 + row]);
-    const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
+    const float sc = ((started && l > 0.0f) ? ps_ref / l : 0.0f) * (HP ? 1.0f : 16777216.0f);
 #pragma unroll
     for (int c = 0; c < OCOLS / 32; ++c) {
       uint32_t o[32];
@@ -745,8 +935,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(dst + e) = make_float4(
-              __uint_as_float(o[e]) * 16777216.0f * sc, __uint_as_float(o[e + 1]) * 16777216.0f * sc,
-              __uint_as_float(o[e + 2]) * 16777216.0f * sc, __uint_as_float(o[e + 3]) * 16777216.0f * sc);
+              __uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
+              __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -947,11 +1137,12 @@ __global__ void __launch_bounds__(128, 1) prefill_qk_debug_kernel(PrefillArgs a)
 // (each part starting on a 1024-byte boundary of the workspace).
 static long long round1k(long long x) { return (x + 1023) / 1024 * 1024; }
 
-PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim) {
+PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim,
+                                   int q_elem_bytes) {
   PrefillWorkspace w{};
   w.n_kv_tiles = static_cast<int>((static_cast<long long>(history_len) + n_tokens + 127) / 128);
   const long long tiles = static_cast<long long>(n_kv_heads) * w.n_kv_tiles;
-  w.off_q_scales = round1k(static_cast<long long>(n_tokens) * n_q_heads * head_dim);
+  w.off_q_scales = round1k(static_cast<long long>(n_tokens) * n_q_heads * head_dim * q_elem_bytes);
   w.off_kw = w.off_q_scales + round1k(static_cast<long long>(n_tokens) * n_q_heads * 4);
   w.off_vw = w.off_kw + tiles * 128 * head_dim * 2;
   w.off_skw = w.off_vw + tiles * 128 * head_dim * 2;
@@ -970,19 +1161,41 @@ cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D>
-static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
+template <int D, bool HP>
+static cudaError_t launch_attention(const PrefillArgs& a, cudaStream_t stream) {
   using L = PrefillTmaSmem<D>;
-  cudaError_t e = launch_pdl(kv_widen_kernel<D>, dim3(a.n_kv_tiles, a.n_kv_heads), dim3(256), 0, stream, a);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(prefill_tma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  cudaError_t e = cudaFuncSetAttribute(prefill_tma_kernel<D, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid((a.n_tokens + 127) / 128, a.n_q_heads);
-  return launch_pdl(prefill_tma_kernel<D>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
+  return launch_pdl(prefill_tma_kernel<D, HP>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
+}
+
+template <int D>
+static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
+  cudaError_t e = launch_pdl(kv_widen_kernel<D>, dim3(a.n_kv_tiles, a.n_kv_heads), dim3(256), 0, stream, a);
+  if (e != cudaSuccess) return e;
+  return launch_attention<D, false>(a, stream);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   return a.head_dim == 256 ? launch_prefill_d<256>(a, stream) : launch_prefill_d<128>(a, stream);
+}
+
+template <int D>
+static cudaError_t launch_prefill_first_d(const PrefillArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.n_tokens) * a.n_q_heads;
+  cudaError_t e = launch_pdl(q_pack_f16_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, stream, a);
+  if (e != cudaSuccess) return e;
+  const size_t vs_bytes = 128 * D * 2;
+  e = cudaFuncSetAttribute(first_pack_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(vs_bytes));
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(first_pack_kernel<D>, dim3(a.n_kv_tiles, a.n_kv_heads), dim3(256), vs_bytes, stream, a);
+  if (e != cudaSuccess) return e;
+  return launch_attention<D, true>(a, stream);
+}
+
+cudaError_t launch_prefill_first(const PrefillArgs& a, cudaStream_t stream) {
+  return a.head_dim == 256 ? launch_prefill_first_d<256>(a, stream) : launch_prefill_first_d<128>(a, stream);
 }
 
 template <int D>

@@ -76,6 +76,9 @@ def lib():
                                              ctypes.POINTER(_DecodeOpts), vp]
         L.kvq_decode_step_int8kv.argtypes = [cp, vp, vp, vp, i32, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
                                              ctypes.POINTER(_DecodeOpts), vp]
+        L.kvq_prefill_first_workspace_bytes.restype = sz
+        L.kvq_prefill_first_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        L.kvq_attn_prefill_first_bf16.argtypes = [cp, vp, vp, vp, i32, i32, vp, i32, f32, vp, vp, sz, vp]
         L.kvq_prefill_workspace_bytes.restype = sz
         L.kvq_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
         L.kvq_attn_prefill_int8.argtypes = [cp, vp, i32, i32, i32, vp, i32, f32, vp, vp, sz, vp]
@@ -280,6 +283,27 @@ def kvq_attn_decode_int8kv_noalloc(cache, q, block_table, ctx_lens, max_ctx, sof
 
 def kvq_prefill_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, history_len, head_dim):
     return int(lib().kvq_prefill_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, history_len, head_dim))
+
+
+def kvq_prefill_first_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, head_dim):
+    return int(lib().kvq_prefill_first_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, head_dim))
+
+
+def kvq_attn_prefill_first_bf16(cache, q, k_new, v_new, block_table_row, softmax_scale, out=None, workspace=None,
+                                stream=None):
+    """The first prefill chunk: q bf16 [T][Hq][D], k_new / v_new bf16 [T][Hkv][D] (positions 0..T-1,
+    written into the cache as int8); returns the high-precision causal attention, fp32 [T][Hq][D]."""
+    T, Hq, D = q.shape
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(kvq_prefill_first_workspace_bytes(T, Hq, cache.n_kv_heads, D), dtype=torch.uint8,
+                                device=q.device)
+    c = cache.struct()
+    _check("kvq_attn_prefill_first_bf16", lib().kvq_attn_prefill_first_bf16(
+        ctypes.byref(c), _p(q), _p(k_new), _p(v_new), T, Hq, _p(block_table_row), int(block_table_row.numel()),
+        float(softmax_scale), _p(out), _p(workspace), workspace.numel(), _stream(stream)))
+    return out
 
 
 def kvq_attn_prefill_int8(cache, q, history_len, block_table_row, softmax_scale, out=None,

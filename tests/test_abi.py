@@ -52,6 +52,12 @@ def test_host_helpers_without_gpu():
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 30720, 256) == (
         2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4)
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, -1, 256) == 0
+    # first chunk: fp16 Q (2 bytes per element) | Q scales | fp16 K and V pieces of the chunk's tiles | scales
+    tiles1 = 4 * ((4096 + 127) // 128)
+    q16 = 4096 * 24 * 256 * 2
+    assert k.kvq_prefill_first_workspace_bytes(4096, 24, 4, 256) == (
+        q16 + 4096 * 24 * 4 + 2 * tiles1 * 128 * 256 * 2 + 2 * tiles1 * 128 * 4)
+    assert k.kvq_prefill_first_workspace_bytes(4096, 24, 4, 192) == 0
     # sparse: one gather record (K row | V row | 2 scales | valid | pad) per page, KV head and slot
     assert k.kvq_sparse_workspace_bytes(2048, 1, 256) == 2048 * 16 * (2 * 256 + 16)
     assert k.kvq_sparse_workspace_bytes(100, 2, 128) == 100 * 2 * 16 * (2 * 128 + 16)
