@@ -685,19 +685,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       // Q: this thread's D/4 dims of its row as fp16 pairs into tensor memory, the A operand of
       // QK (lane = row, dim d in column kQCol + d / 2, even dims in the low half): the int8
       // codes widened, or (HP) the fp16 row as it is
-      const int8_t* src = a.q_codes + (static_cast<long long>(q0 + row) * Hq + h) * D;
-      const uint16_t* src_h = a.q_f16 + (static_cast<long long>(q0 + row) * Hq + h) * D;
       uint32_t qw[D / 8];
 #pragma unroll
       for (int i = 0; i < NP; ++i) {
         const int c16 = part * NP + i;
-        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
+        uint4 c0, c1;
         if constexpr (HP) {
+          const uint16_t* src_h = a.q_f16 + (static_cast<long long>(q0 + row) * Hq + h) * D;
+          c0 = make_uint4(0, 0, 0, 0);
+          c1 = make_uint4(0, 0, 0, 0);
           if (row_real) {
             c0 = __ldg(reinterpret_cast<const uint4*>(src_h + 16 * c16));
             c1 = __ldg(reinterpret_cast<const uint4*>(src_h + 16 * c16 + 8));
           }
         } else {
+          const int8_t* src = a.q_codes + (static_cast<long long>(q0 + row) * Hq + h) * D;
           int4 raw = make_int4(0, 0, 0, 0);
           if (row_real) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
           widen16(raw, c0, c1);
@@ -924,7 +926,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     red_max[part * 128 + row] = l_part;
     named_bar(gbar, 128);
     const float l = (red_max[row] + red_max[128 + row]) + (red_max[256 + row] + red_max[384 + row]);
-    const float sc = ((started && l > 0.0f) ? ps_ref / l : 0.0f) * (HP ? 1.0f : 16777216.0f);
+    const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
+    constexpr float kOUnit = HP ? 1.0f : 16777216.0f;  // the P codes' 2^-24 unit (int8 path)
 #pragma unroll
     for (int c = 0; c < OCOLS / 32; ++c) {
       uint32_t o[32];
@@ -935,8 +938,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
 #pragma unroll
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(dst + e) = make_float4(
-              __uint_as_float(o[e]) * sc, __uint_as_float(o[e + 1]) * sc,
-              __uint_as_float(o[e + 2]) * sc, __uint_as_float(o[e + 3]) * sc);
+              __uint_as_float(o[e]) * kOUnit * sc, __uint_as_float(o[e + 1]) * kOUnit * sc,
+              __uint_as_float(o[e + 2]) * kOUnit * sc, __uint_as_float(o[e + 3]) * kOUnit * sc);
       }
     }
   } else if (warp == kMmaWarp) {
