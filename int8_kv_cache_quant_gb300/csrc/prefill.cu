@@ -640,8 +640,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offFlag + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int h = blockIdx.y;
-  const int q0 = blockIdx.x * 128;
+  // longest first: block l takes query tile n_qt - 1 - l / Hq of head l % Hq, so the CTAs with the
+  // most key tiles start in the first wave and the short ones fill the last
+  const int n_qt = (a.n_tokens + 127) / 128;
+  const int h = static_cast<int>(blockIdx.x % a.n_q_heads);
+  const int q0 = (n_qt - 1 - static_cast<int>(blockIdx.x / a.n_q_heads)) * 128;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, kvh = h / G;
   const int T = a.n_tokens;
   const int n_keys = a.history_len + T;
@@ -1169,7 +1172,7 @@ static cudaError_t launch_attention(const PrefillArgs& a, cudaStream_t stream) {
   using L = PrefillTmaSmem<D>;
   cudaError_t e = cudaFuncSetAttribute(prefill_tma_kernel<D, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.n_tokens + 127) / 128, a.n_q_heads);
+  dim3 grid(((a.n_tokens + 127) / 128) * a.n_q_heads);
   return launch_pdl(prefill_tma_kernel<D, HP>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
 }
 
