@@ -7,11 +7,12 @@
 // §2.3 (K in 16-element head-dimension chunks with the tokens of a chunk adjacent, V
 // token-contiguous per dimension).
 //
-// Mapping: one warp per (token, KV head, K|V) row.  The row (head_dim bf16 values) is read
-// with one vector load per lane and quantised by the warp (quant_rule.cuh: warp-shuffle amax,
-// IEEE fp32 divisions, round to nearest even), so the codes and scales are bit-identical to
-// the reference rule.  K codes go out as 8- or 4-byte stores into the [chunk][slot][16] rows;
-// V codes are one byte per dimension into [dim][slot].
+// Mapping: a block per (16 consecutive tokens, KV head), a warp per token row.  The row
+// (head_dim bf16 values) is read with one vector load per lane and quantised by the warp
+// (quant_rule.cuh: warp-shuffle amax, IEEE fp32 divisions, round to nearest even), so the codes
+// and scales are bit-identical to the reference rule.  K codes go out as 8- or 4-byte stores
+// into the [chunk][slot][16] rows; V codes go through shared memory so that a page filled by 16
+// tokens of the block is written dim by dim in 16-byte stores.
 #include <cuda_bf16.h>
 
 #include "kvq_dev.cuh"
@@ -20,64 +21,103 @@
 
 namespace kvq {
 
+// One block per (group of 16 consecutive input tokens, KV head); warp w quantises the K and V
+// rows of token w of the group.  K codes go straight to their slots (8- or 4-byte
+// stores into the [chunk][slot][16] rows).  V codes are staged in shared memory: when the 16
+// tokens fill one page in slot order (a prefill chunk aligned to a page), each head dimension's
+// 16 slots leave as one 16-byte store into the page's [dim][slot] block; otherwise (decode
+// steps, scattered or unaligned tokens) each code leaves as a single byte, as its row dictates.
+constexpr int kGroup = 16;
+
 template <int D>
-__global__ void __launch_bounds__(256) quant_write_kernel(QuantWriteArgs a) {
-  constexpr int kPerLane = D / 32;  // 8 (D = 256) or 4 (D = 128) values per lane
-  const int lane = threadIdx.x & 31;
-  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-  const int H = a.n_kv_heads;
-  const long long n_rows = static_cast<long long>(a.n_tokens) * H * 2;
-  if (row >= n_rows) return;
-  const int is_v = static_cast<int>(row & 1);
-  const long long th = row >> 1;
-  const int tok = static_cast<int>(th / H);
-  const int h = static_cast<int>(th % H);
+__global__ void __launch_bounds__(kGroup * 32) quant_write_kernel(QuantWriteArgs a) {
+  constexpr int P = D / 32;  // 8 (D = 256) or 4 (D = 128) values per lane
+  __shared__ __align__(16) int8_t vs[kGroup][D];
+  __shared__ long long tok_ph[kGroup];  // page * n_kv_heads + head, -1: not written
+  __shared__ int tok_slot[kGroup];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g0 = blockIdx.x * kGroup, h = blockIdx.y, H = a.n_kv_heads;
 
   grid_dep_wait();     // the new rows may come from the previous kernel of the stream
   grid_dep_trigger();  // the attention kernel may start launching; it waits for this grid
-  const int seq = a.seq_idx[tok];
-  const int pos = a.pos[tok];
-  if (seq < 0 || seq >= a.num_seqs) {
-    if (lane == 0) set_status(a.status, KVQ_DEV_BAD_SEQ);
-    return;
+  {
+    const int k = warp;  // one token per warp
+    const int tok = g0 + k;
+    long long ph = -1;
+    int slot = 0;
+    if (tok < a.n_tokens) {
+      const int seq = a.seq_idx[tok];
+      const int pos = a.pos[tok];
+      if (seq < 0 || seq >= a.num_seqs) {
+        if (lane == 0) set_status(a.status, KVQ_DEV_BAD_SEQ);
+      } else if (pos < 0 || pos / KVQ_BLOCK_SIZE >= a.max_blocks_per_seq) {
+        if (lane == 0) set_status(a.status, KVQ_DEV_BAD_POS);
+      } else {
+        const int page = a.block_table[static_cast<long long>(seq) * a.max_blocks_per_seq + pos / KVQ_BLOCK_SIZE];
+        if (page < 0 || page >= a.num_blocks) {
+          if (lane == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
+        } else {
+          ph = static_cast<long long>(page) * H + h;
+          slot = pos % KVQ_BLOCK_SIZE;
+        }
+      }
+    }
+    if (lane == 0) {
+      tok_ph[k] = ph;
+      tok_slot[k] = slot;
+    }
+    if (ph >= 0) {  // warp-uniform
+      const long long row = (static_cast<long long>(tok) * H + h) * D + lane * P;
+      float xk[P], xv[P];
+      load_bf16_lane(static_cast<const uint16_t*>(a.k_new) + row, xk);
+      load_bf16_lane(static_cast<const uint16_t*>(a.v_new) + row, xv);
+      int8_t q[P];
+      uint32_t packed[P / 4];
+      const float sk = quant_rule_warp(xk, q);
+      pack_codes(q, packed);
+      store_k_codes<D>(a.k, ph, slot, lane, packed);
+      const float sv = quant_rule_warp(xv, q);
+      pack_codes(q, packed);
+      if constexpr (P == 8) *reinterpret_cast<uint2*>(&vs[k][lane * P]) = make_uint2(packed[0], packed[1]);
+      else *reinterpret_cast<uint32_t*>(&vs[k][lane * P]) = packed[0];
+      if (lane == 0) {
+        a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = sk;
+        a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = sv;
+      }
+    }
   }
-  if (pos < 0 || pos / KVQ_BLOCK_SIZE >= a.max_blocks_per_seq) {
-    if (lane == 0) set_status(a.status, KVQ_DEV_BAD_POS);
-    return;
-  }
-  const int page = a.block_table[static_cast<long long>(seq) * a.max_blocks_per_seq + pos / KVQ_BLOCK_SIZE];
-  if (page < 0 || page >= a.num_blocks) {
-    if (lane == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
-    return;
-  }
-  const int slot = pos % KVQ_BLOCK_SIZE;
-
-  const uint16_t* src = static_cast<const uint16_t*>(is_v ? a.v_new : a.k_new) +
-                        (static_cast<long long>(tok) * H + h) * D + lane * kPerLane;
-  float x[kPerLane];
-  load_bf16_lane(src, x);
-  int8_t q[kPerLane];
-  const float scale = quant_rule_warp(x, q);
-
-  const long long ph = static_cast<long long>(page) * H + h;
-  if (!is_v) {
-    uint32_t packed[kPerLane / 4];
-    pack_codes(q, packed);
-    store_k_codes<D>(a.k, ph, slot, lane, packed);
-    if (lane == 0) a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
+  __syncthreads();
+  // one page in slot order?
+  bool full = true;
+#pragma unroll
+  for (int k = 0; k < kGroup; ++k) full = full && tok_ph[k] == tok_ph[0] && tok_slot[k] == k;
+  full = full && tok_ph[0] >= 0;
+  if (full) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        w[q4] = static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4][d])) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4 + 1][d])) << 8) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4 + 2][d])) << 16) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4 + 3][d])) << 24);
+      *reinterpret_cast<uint4*>(a.v + (tok_ph[0] * D + d) * KVQ_BLOCK_SIZE) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
   } else {
-    store_v_codes<D>(a.v, ph, slot, lane, q);
-    if (lane == 0) a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
+    for (int it = threadIdx.x; it < kGroup * D; it += blockDim.x) {
+      const int k = it / D, d = it % D;
+      const long long ph = tok_ph[k];
+      if (ph >= 0) a.v[(ph * D + d) * KVQ_BLOCK_SIZE + tok_slot[k]] = vs[k][d];
+    }
   }
 }
 
 cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(a.n_tokens) * a.n_kv_heads * 2;
-  const int warps_per_block = 8;
-  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (a.head_dim == 256) return launch_pdl(quant_write_kernel<256>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
-  return launch_pdl(quant_write_kernel<128>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
+  const long long groups = (static_cast<long long>(a.n_tokens) + kGroup - 1) / kGroup;
+  if (groups > 0x7fffffffLL || a.n_kv_heads > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(groups), a.n_kv_heads);
+  if (a.head_dim == 256) return launch_pdl(quant_write_kernel<256>, grid, dim3(kGroup * 32), 0, stream, a);
+  return launch_pdl(quant_write_kernel<128>, grid, dim3(kGroup * 32), 0, stream, a);
 }
 
 // ============================================================================ fused producer
@@ -88,114 +128,160 @@ cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream) {
 //   dim i < r/2 (partner i + r/2):      out = fma(x_i, c_i, -(x_{i+r/2} * s_i))
 //   dim i + r/2 (partner i):            out = fma(x_{i+r/2}, c_i, x_i * s_i)
 // in fp32 with exactly these roundings, then the quantisation rule of quant_write_kernel on the
-// fp32 row.  One warp per (token, row) with rows = the token's Hq query heads, then Hkv K heads,
-// then Hkv V heads; lane l holds dims l*P .. l*P+P-1 (P = D/32), so the partner of a dim is the
-// same element of lane l +- (r/2)/P (r/2 is a multiple of P).
+// fp32 row.  A warp per (token, row); lane l holds dims l*P .. l*P+P-1 (P = D/32), so the partner
+// of a dim is the same element of lane l +- (r/2)/P (r/2 is a multiple of P).
+// The rotation of this lane's P elements of a Q or K row at position p (rotate-half form above).
+template <int P>
+__device__ __forceinline__ void rope_lane(float (&x)[P], const RopeQuantArgs& a, int p, int lane) {
+  const int half = a.rotary_dim / 2, shift = half / P;
+  const int d0 = lane * P;
+  const bool first = d0 < half, rotated = d0 < a.rotary_dim;
+  const int partner = rotated ? (first ? lane + shift : lane - shift) : lane;
+  const float* cs = a.cos_sin + static_cast<long long>(p) * a.rotary_dim;
+  const int fi = first ? d0 : d0 - half;  // frequency index of this lane's first dim
+#pragma unroll
+  for (int e = 0; e < P; ++e) {
+    const float other = __shfl_sync(0xffffffffu, x[e], partner);
+    if (rotated) {
+      const float c = __ldg(cs + fi + e), sn = __ldg(cs + half + fi + e);
+      x[e] = first ? __fmaf_rn(x[e], c, -__fmul_rn(other, sn)) : __fmaf_rn(x[e], c, __fmul_rn(other, sn));
+    }
+  }
+}
+
+// One block per (group of 16 consecutive tokens, head slot r): r < Hq is query head r (Q outputs),
+// r >= Hq is KV head r - Hq (the K row rotated into its cache slot, the V row staged in shared
+// memory and written page-wise as in quant_write_kernel).  Warp w takes token w.
 template <int D>
-__global__ void __launch_bounds__(256) rope_quant_write_kernel(RopeQuantArgs a) {
+__global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuantArgs a) {
   constexpr int P = D / 32;
-  const int lane = threadIdx.x & 31;
+  __shared__ __align__(16) int8_t vs[kGroup][D];
+  __shared__ long long tok_ph[kGroup];
+  __shared__ int tok_slot[kGroup];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hq = a.q ? a.n_q_heads : 0, H = a.kv.n_kv_heads;
-  const int rows_per_token = Hq + 2 * H;
-  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
-  if (row >= static_cast<long long>(a.kv.n_tokens) * rows_per_token) return;
-  const int tok = static_cast<int>(row / rows_per_token);
-  const int r = static_cast<int>(row % rows_per_token);
-  const int kind = r < Hq ? 0 : (r < Hq + H ? 1 : 2);  // 0 Q, 1 K, 2 V
-  const int h = kind == 0 ? r : (kind == 1 ? r - Hq : r - Hq - H);
+  const int g0 = blockIdx.x * kGroup, r = blockIdx.y;
+  const bool is_q = r < Hq;
+  const int h = is_q ? r : r - Hq;
 
   grid_dep_wait();     // the rows may come from the previous kernel of the stream
   grid_dep_trigger();  // the attention kernel may start launching; it waits for this grid
-  const int p = a.kv.pos[tok];
-  const bool pos_ok = p >= 0 && p < a.max_pos;
-
-  const uint16_t* src = kind == 0 ? static_cast<const uint16_t*>(a.q) + (static_cast<long long>(tok) * Hq + h) * D
-                        : static_cast<const uint16_t*>(kind == 1 ? a.kv.k_new : a.kv.v_new) +
-                              (static_cast<long long>(tok) * H + h) * D;
-  src += lane * P;
-  float x[P];
-  load_bf16_lane(src, x);
-  // ---- RoPE (Q and K; the warp takes the branch together: kind is uniform)
-  if (kind != 2 && pos_ok) {
-    const int half = a.rotary_dim / 2, shift = half / P;
-    const int d0 = lane * P;
-    const bool first = d0 < half, rotated = d0 < a.rotary_dim;
-    const int partner = rotated ? (first ? lane + shift : lane - shift) : lane;
-    const float* cs = a.cos_sin + static_cast<long long>(p) * a.rotary_dim;
-    const int fi = first ? d0 : d0 - half;  // frequency index of this lane's first dim
+  {
+    const int k = warp;  // one token per warp
+    const int tok = g0 + k;
+    long long ph = -1;
+    int slot = 0;
+    if (tok < a.kv.n_tokens) {
+      const int p = a.kv.pos[tok];
+      const bool pos_ok = p >= 0 && p < a.max_pos;
+      if (is_q) {
+        // ---- Q row: rotate, quantise, codes + scale + rotated bf16 row
+        float x[P];
+        load_bf16_lane(static_cast<const uint16_t*>(a.q) + (static_cast<long long>(tok) * Hq + h) * D + lane * P, x);
+        if (pos_ok) {
+          rope_lane(x, a, p, lane);
+        } else {
 #pragma unroll
-    for (int e = 0; e < P; ++e) {
-      const float other = __shfl_sync(0xffffffffu, x[e], partner);
-      if (rotated) {
-        const float c = __ldg(cs + fi + e), sn = __ldg(cs + half + fi + e);
-        x[e] = first ? __fmaf_rn(x[e], c, -__fmul_rn(other, sn)) : __fmaf_rn(x[e], c, __fmul_rn(other, sn));
+          for (int e = 0; e < P; ++e) x[e] = 0.0f;
+        }
+        int8_t qc[P];
+        uint32_t packed[P / 4];
+        const float scale = quant_rule_warp(x, qc);
+        pack_codes(qc, packed);
+        const long long u = static_cast<long long>(tok) * Hq + h;
+        if (a.q_codes) {
+          int8_t* dst = a.q_codes + u * D + lane * P;
+          if constexpr (P == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+          else *reinterpret_cast<uint32_t*>(dst) = packed[0];
+        }
+        if (a.q_scales && lane == 0) a.q_scales[u] = scale;
+        if (a.q_rot) {
+          uint32_t b[P / 2];
+#pragma unroll
+          for (int i = 0; i < P / 2; ++i) {
+            const __nv_bfloat162 v2 = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+            b[i] = *reinterpret_cast<const uint32_t*>(&v2);
+          }
+          uint16_t* dst = a.q_rot + u * D + lane * P;
+          if constexpr (P == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(b[0], b[1], b[2], b[3]);
+          else *reinterpret_cast<uint2*>(dst) = make_uint2(b[0], b[1]);
+        }
+      } else {
+        // ---- K and V rows of KV head h into the token's slot
+        const int seq = a.kv.seq_idx[tok];
+        if (!pos_ok || p / KVQ_BLOCK_SIZE >= a.kv.max_blocks_per_seq) {
+          if (lane == 0) set_status(a.kv.status, KVQ_DEV_BAD_POS);
+        } else if (seq < 0 || seq >= a.kv.num_seqs) {
+          if (lane == 0) set_status(a.kv.status, KVQ_DEV_BAD_SEQ);
+        } else {
+          const int page = a.kv.block_table[static_cast<long long>(seq) * a.kv.max_blocks_per_seq + p / KVQ_BLOCK_SIZE];
+          if (page < 0 || page >= a.kv.num_blocks) {
+            if (lane == 0) set_status(a.kv.status, KVQ_DEV_BAD_BLOCK);
+          } else {
+            ph = static_cast<long long>(page) * H + h;
+            slot = p % KVQ_BLOCK_SIZE;
+          }
+        }
+        if (ph >= 0) {  // warp-uniform
+          const long long row = (static_cast<long long>(tok) * H + h) * D + lane * P;
+          float xk[P], xv[P];
+          load_bf16_lane(static_cast<const uint16_t*>(a.kv.k_new) + row, xk);
+          load_bf16_lane(static_cast<const uint16_t*>(a.kv.v_new) + row, xv);
+          rope_lane(xk, a, p, lane);
+          int8_t qc[P];
+          uint32_t packed[P / 4];
+          const float sk = quant_rule_warp(xk, qc);
+          pack_codes(qc, packed);
+          store_k_codes<D>(a.kv.k, ph, slot, lane, packed);
+          const float sv = quant_rule_warp(xv, qc);
+          pack_codes(qc, packed);
+          if constexpr (P == 8) *reinterpret_cast<uint2*>(&vs[k][lane * P]) = make_uint2(packed[0], packed[1]);
+          else *reinterpret_cast<uint32_t*>(&vs[k][lane * P]) = packed[0];
+          if (lane == 0) {
+            a.kv.k_scale[ph * KVQ_BLOCK_SIZE + slot] = sk;
+            a.kv.v_scale[ph * KVQ_BLOCK_SIZE + slot] = sv;
+          }
+        }
       }
     }
-  }
-  if (!pos_ok) {
-#pragma unroll
-    for (int e = 0; e < P; ++e) x[e] = 0.0f;
-  }
-  // ---- the quantisation rule (as quant_write_kernel)
-  int8_t qc[P];
-  const float scale = quant_rule_warp(x, qc);
-  uint32_t packed[P / 4];
-  pack_codes(qc, packed);
-
-  if (kind == 0) {
-    const long long u = static_cast<long long>(tok) * Hq + h;
-    if (a.q_codes) {
-      int8_t* dst = a.q_codes + u * D + lane * P;
-      if constexpr (P == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-      else *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    if (lane == 0) {
+      tok_ph[k] = ph;
+      tok_slot[k] = slot;
     }
-    if (a.q_scales && lane == 0) a.q_scales[u] = scale;
-    if (a.q_rot) {
-      uint32_t b[P / 2];
+  }
+  if (is_q) return;  // block-uniform
+  __syncthreads();
+  bool full = true;
 #pragma unroll
-      for (int i = 0; i < P / 2; ++i) {
-        const __nv_bfloat162 v2 = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-        b[i] = *reinterpret_cast<const uint32_t*>(&v2);
-      }
-      uint16_t* dst = a.q_rot + u * D + lane * P;
-      if constexpr (P == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(b[0], b[1], b[2], b[3]);
-      else *reinterpret_cast<uint2*>(dst) = make_uint2(b[0], b[1]);
+  for (int k = 0; k < kGroup; ++k) full = full && tok_ph[k] == tok_ph[0] && tok_slot[k] == k;
+  full = full && tok_ph[0] >= 0;
+  if (full) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        w[q4] = static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4][d])) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4 + 1][d])) << 8) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4 + 2][d])) << 16) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vs[4 * q4 + 3][d])) << 24);
+      *reinterpret_cast<uint4*>(a.kv.v + (tok_ph[0] * D + d) * KVQ_BLOCK_SIZE) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    return;
-  }
-  // ---- K or V row into the token's slot
-  const int seq = a.kv.seq_idx[tok];
-  if (!pos_ok || p / KVQ_BLOCK_SIZE >= a.kv.max_blocks_per_seq) {
-    if (lane == 0) set_status(a.kv.status, KVQ_DEV_BAD_POS);
-    return;
-  }
-  if (seq < 0 || seq >= a.kv.num_seqs) {
-    if (lane == 0) set_status(a.kv.status, KVQ_DEV_BAD_SEQ);
-    return;
-  }
-  const int page = a.kv.block_table[static_cast<long long>(seq) * a.kv.max_blocks_per_seq + p / KVQ_BLOCK_SIZE];
-  if (page < 0 || page >= a.kv.num_blocks) {
-    if (lane == 0) set_status(a.kv.status, KVQ_DEV_BAD_BLOCK);
-    return;
-  }
-  const int slot = p % KVQ_BLOCK_SIZE;
-  const long long ph = static_cast<long long>(page) * H + h;
-  if (kind == 1) {
-    store_k_codes<D>(a.kv.k, ph, slot, lane, packed);
-    if (lane == 0) a.kv.k_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
   } else {
-    store_v_codes<D>(a.kv.v, ph, slot, lane, qc);
-    if (lane == 0) a.kv.v_scale[ph * KVQ_BLOCK_SIZE + slot] = scale;
+    for (int it = threadIdx.x; it < kGroup * D; it += blockDim.x) {
+      const int k = it / D, d = it % D;
+      const long long ph = tok_ph[k];
+      if (ph >= 0) a.kv.v[(ph * D + d) * KVQ_BLOCK_SIZE + tok_slot[k]] = vs[k][d];
+    }
   }
 }
 
 cudaError_t launch_rope_quant_write(const RopeQuantArgs& a, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(a.kv.n_tokens) * ((a.q ? a.n_q_heads : 0) + 2 * a.kv.n_kv_heads);
-  const long long blocks = (rows + 7) / 8;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (a.kv.head_dim == 256)
-    return launch_pdl(rope_quant_write_kernel<256>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
-  return launch_pdl(rope_quant_write_kernel<128>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, a);
+  const long long groups = (static_cast<long long>(a.kv.n_tokens) + kGroup - 1) / kGroup;
+  const int slots = (a.q ? a.n_q_heads : 0) + a.kv.n_kv_heads;
+  if (groups > 0x7fffffffLL || slots > 65535) return cudaErrorInvalidConfiguration;
+  const dim3 grid(static_cast<unsigned>(groups), slots);
+  if (a.kv.head_dim == 256) return launch_pdl(rope_quant_write_kernel<256>, grid, dim3(kGroup * 32), 0, stream, a);
+  return launch_pdl(rope_quant_write_kernel<128>, grid, dim3(kGroup * 32), 0, stream, a);
 }
 
 }  // namespace kvq
