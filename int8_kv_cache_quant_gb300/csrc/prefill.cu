@@ -406,25 +406,37 @@ __global__ void __launch_bounds__(256) q_pack_f16_kernel(PrefillArgs a) {
   if (lane == 0) a.q_scales[row] = back;
 }
 
-// One CTA per (128-key tile j, KV head): one warp per token row of the chunk.  Each K and V row is
-// (1) quantised by the kvq_quant_write rule into its cache slot (position t = 128 j + n of the
-// sequence whose block-table row is given), and (2) turned into fp16 with its power-of-two scale,
-// K straight into the tile's operand pieces (row = key), V through shared memory, whose
-// transpose (rows = dims) then goes out in 16-byte chunks: the layout kv_widen_kernel writes.
+// One CTA per (16 keys of the chunk's 128-key tiles, KV head), one warp per key t: its K and V
+// rows are (1) quantised by the kvq_quant_write rule into the cache slot of position t (V codes
+// staged so that a full page leaves in 16-byte stores), and (2) turned into fp16 with their
+// power-of-two scales: K straight into row t % 128 of its tile's operand pieces, V through
+// shared memory into the group's two 8-key chunks of each dimension row (rows = dims): the
+// layout kv_widen_kernel writes.  Keys from the chunk's end to the end of its last tile get zero
+// rows and zero scales (the attention multiplies masked keys' V by zero, so those rows must not
+// hold stale NaN bits).
+constexpr int kPackGroup = 16;
+
 template <int D>
-__global__ void __launch_bounds__(256) first_pack_kernel(PrefillArgs a) {
+__global__ void __launch_bounds__(kPackGroup * 32) first_pack_kernel(PrefillArgs a) {
   constexpr int P = D / 32;
-  extern __shared__ __align__(16) uint16_t vs[];  // [128 keys][D] fp16
-  const int j = blockIdx.x, kvh = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  __shared__ __align__(16) int8_t vq[kPackGroup][D];    // V codes for the cache
+  __shared__ __align__(16) uint16_t vh[kPackGroup][D];  // V as fp16 for the pieces
+  __shared__ long long tok_ph[kPackGroup];
+  __shared__ int tok_slot[kPackGroup];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g0 = blockIdx.x * kPackGroup, kvh = blockIdx.y;
   const int T = a.n_tokens;
+  const int j = g0 / 128;  // tile of this group
   const long long tile = static_cast<long long>(kvh) * a.n_kv_tiles + j;
   uint8_t* kdst = a.kw + tile * (D / 64) * kPieceBytes;
   uint8_t* vdst = a.vw + tile * (D / 64) * kPieceBytes;
   grid_dep_wait();  // Q packing and the chunk's rows come from the preceding kernels
-  for (int n = warp; n < 128; n += 8) {
-    const int t = 128 * j + n;
+  {
+    const int k = warp, t = g0 + k, n = t % 128;
     float xk[P], xv[P];
     float sk = 0.f, sv = 0.f;
+    long long ph = -1;
+    int slot = 0;
     if (t < T) {
       const long long row = (static_cast<long long>(t) * a.n_kv_heads + kvh) * D + lane * P;
       load_bf16_lane(static_cast<const uint16_t*>(a.k_src) + row, xk);
@@ -433,15 +445,17 @@ __global__ void __launch_bounds__(256) first_pack_kernel(PrefillArgs a) {
       const int bi = t / KVQ_BLOCK_SIZE;
       const int page = bi < a.n_blocks_row ? a.block_table_row[bi] : -1;
       if (page >= 0 && page < a.num_blocks) {
-        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
-        const int slot = t % KVQ_BLOCK_SIZE;
+        ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        slot = t % KVQ_BLOCK_SIZE;
         int8_t qc[P];
         uint32_t packed[P / 4];
         const float ck = quant_rule_warp(xk, qc);
         pack_codes(qc, packed);
         store_k_codes<D>(a.k, ph, slot, lane, packed);
         const float cv = quant_rule_warp(xv, qc);
-        store_v_codes<D>(a.v, ph, slot, lane, qc);
+        pack_codes(qc, packed);
+        if constexpr (P == 8) *reinterpret_cast<uint2*>(&vq[k][lane * P]) = make_uint2(packed[0], packed[1]);
+        else *reinterpret_cast<uint32_t*>(&vq[k][lane * P]) = packed[0];
         if (lane == 0) {
           a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = ck;
           a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = cv;
@@ -473,6 +487,10 @@ __global__ void __launch_bounds__(256) first_pack_kernel(PrefillArgs a) {
 #pragma unroll
       for (int e = 0; e < P; ++e) xk[e] = xv[e] = 0.f;
     }
+    if (lane == 0) {
+      tok_ph[k] = ph;
+      tok_slot[k] = slot;
+    }
     uint32_t hk[P / 2], hv[P / 2];
     to_f16_pairs(xk, 1.0f, hk);
     to_f16_pairs(xv, 1.0f, hv);
@@ -481,26 +499,47 @@ __global__ void __launch_bounds__(256) first_pack_kernel(PrefillArgs a) {
     uint8_t* kp = kdst + (d0 / 64) * kPieceBytes + tc::sw128_off(n, (d0 % 64) / 8) + (d0 % 8) * 2;
     if constexpr (P == 8) *reinterpret_cast<uint4*>(kp) = make_uint4(hk[0], hk[1], hk[2], hk[3]);
     else *reinterpret_cast<uint2*>(kp) = make_uint2(hk[0], hk[1]);
-    if constexpr (P == 8) *reinterpret_cast<uint4*>(vs + n * D + d0) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-    else *reinterpret_cast<uint2*>(vs + n * D + d0) = make_uint2(hv[0], hv[1]);
+    if constexpr (P == 8) *reinterpret_cast<uint4*>(&vh[k][d0]) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+    else *reinterpret_cast<uint2*>(&vh[k][d0]) = make_uint2(hv[0], hv[1]);
     if (lane == 0) {
       a.skw[tile * 128 + n] = sk;
       a.svw[tile * 128 + n] = sv;
     }
   }
   __syncthreads();
-  // V pieces: piece kh * (D/128) + dh holds keys 64 kh .. 64 kh + 63 (8 chunks of 8 keys) of dims
-  // 128 dh .. 128 dh + 127 (rows); item = (piece, dim row, chunk)
-  for (int it = tid; it < 16 * D; it += 256) {
-    const int c = it & 7, d = (it >> 3) & 127, pc = it >> 10;
-    const int kh = pc / (D / 128), dh = pc % (D / 128);
-    const int dim = 128 * dh + d, key0 = 64 * kh + 8 * c;
+  // V codes into the cache: one 16-byte store per dimension when the 16 keys fill a page in order
+  bool full = true;
+#pragma unroll
+  for (int k = 0; k < kPackGroup; ++k) full = full && tok_ph[k] == tok_ph[0] && tok_slot[k] == k;
+  full = full && tok_ph[0] >= 0;
+  if (full) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        w[q4] = static_cast<uint32_t>(static_cast<uint8_t>(vq[4 * q4][d])) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vq[4 * q4 + 1][d])) << 8) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vq[4 * q4 + 2][d])) << 16) |
+                (static_cast<uint32_t>(static_cast<uint8_t>(vq[4 * q4 + 3][d])) << 24);
+      *reinterpret_cast<uint4*>(a.v + (tok_ph[0] * D + d) * KVQ_BLOCK_SIZE) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    for (int it = threadIdx.x; it < kPackGroup * D; it += blockDim.x) {
+      const int k = it / D, d = it % D;
+      const long long ph = tok_ph[k];
+      if (ph >= 0) a.v[(ph * D + d) * KVQ_BLOCK_SIZE + tok_slot[k]] = vq[k][d];
+    }
+  }
+  // V pieces: this group's keys are 8-key chunks c0 and c0 + 1 of key half kh; item = (dim, chunk)
+  const int kh = (g0 % 128) / 64, c0 = (g0 % 64) / 8;
+  for (int it = threadIdx.x; it < 2 * D; it += blockDim.x) {
+    const int d = it >> 1, cc = it & 1;
+    const int pc = kh * (D / 128) + d / 128;
     uint32_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-      w[e] = static_cast<uint32_t>(vs[(key0 + 2 * e) * D + dim]) |
-             (static_cast<uint32_t>(vs[(key0 + 2 * e + 1) * D + dim]) << 16);
-    *reinterpret_cast<uint4*>(vdst + pc * kPieceBytes + tc::sw128_off(d, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      w[e] = static_cast<uint32_t>(vh[8 * cc + 2 * e][d]) | (static_cast<uint32_t>(vh[8 * cc + 2 * e + 1][d]) << 16);
+    *reinterpret_cast<uint4*>(vdst + pc * kPieceBytes + tc::sw128_off(d % 128, c0 + cc)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   grid_dep_trigger();
 }
@@ -1192,10 +1231,8 @@ static cudaError_t launch_prefill_first_d(const PrefillArgs& a, cudaStream_t str
   const long long rows = static_cast<long long>(a.n_tokens) * a.n_q_heads;
   cudaError_t e = launch_pdl(q_pack_f16_kernel<D>, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, stream, a);
   if (e != cudaSuccess) return e;
-  const size_t vs_bytes = 128 * D * 2;
-  e = cudaFuncSetAttribute(first_pack_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(vs_bytes));
-  if (e != cudaSuccess) return e;
-  e = launch_pdl(first_pack_kernel<D>, dim3(a.n_kv_tiles, a.n_kv_heads), dim3(256), vs_bytes, stream, a);
+  e = launch_pdl(first_pack_kernel<D>, dim3(a.n_kv_tiles * (128 / kPackGroup), a.n_kv_heads), dim3(kPackGroup * 32), 0,
+                 stream, a);
   if (e != cudaSuccess) return e;
   return launch_attention<D, true>(a, stream);
 }
