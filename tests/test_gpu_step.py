@@ -109,3 +109,32 @@ def test_step_with_short_context_writes_nothing_and_flags(kvq):
     assert np.array_equal(after_v[pages1], before_v[pages1])
     p0 = w["block_table"][0][39 // 16]
     assert not np.array_equal(after_k[p0], before_k[p0])
+
+
+def test_decode_b64_fused_step_full_sampled(kvq, oracle):
+    """decode_b64 at full size (64 sequences, ctx up to 16384, 32/8 heads, head_dim 128) through
+    the fused step, as bench.py times it: a fresh new token per sequence is written by stage 1;
+    the pages holding them match the oracle's writer bit for bit, and sampled outputs match FP64."""
+    from helpers import gpu_cache_from, sample_units
+    w = W.make("decode_b64")
+    cache, bt = gpu_cache_from(w, kvq)
+    rng = np.random.default_rng(730)
+    kn = W.normal_bf16(rng, (w["batch"], w["hkv"], w["d"]))
+    vn = W.normal_bf16(rng, (w["batch"], w["hkv"], w["d"]))
+    out = kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(kn), to_bf16_tensor(vn), to_bf16_tensor(w["q"]), bt,
+                                     to_i32(w["ctx_lens"]), w["max_ctx"], w["softmax_scale"]).cpu().numpy()
+    assert kvq.kvq_device_status() == 0
+    hc = host_cache_from(w, oracle)
+    oracle.kv_quant_write(hc, kn, vn, w["new_seq"], w["new_pos"], w["block_table"])
+    pages = w["block_table"][w["new_seq"], w["new_pos"] // 16]
+    for name in ("k", "v", "k_scale", "v_scale"):
+        got = getattr(cache, name)[torch_index(pages)].cpu().numpy()
+        assert np.array_equal(got.view(np.uint8), getattr(hc, name)[pages].view(np.uint8)), name
+    units = sample_units(w["batch"], w["hq"], 96, seed=731)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], units=units)
+    assert norm_max_err(out.reshape(-1, w["d"])[units], ref) <= DESIGN_TOL
+
+
+def torch_index(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).cuda()
