@@ -137,7 +137,9 @@ int kvq_rope_quant_write(const kvq_cache* cache, const void* q, int32_t n_q_head
 typedef struct kvq_decode_opts {
   int32_t split_rows;      /* keys per split in the split route, a multiple of 16; 0 -> sized to
                             * the GPU by kvq_decode_auto_split_rows */
-  int32_t route_threshold; /* max_ctx <= threshold -> single-CTA route; 0 -> 2048 ([DOT4] route table) */
+  int32_t route_threshold; /* > 0: max_ctx <= threshold -> single-CTA route ([DOT4] route table
+                            * uses 2048); 0 -> automatic: the split route whenever the split size
+                            * leaves more than one split of max_ctx, else the single-CTA route */
   int32_t force_route;     /* 0 auto, 1 single CTA per (sequence, KV head), 2 split-K */
   /* Optional profiling hooks: two cudaEvent_t (as void*) recorded on `stream` right before
    * and right after the stage-1 (K/V streaming) kernel launch; NULL to skip. */
@@ -147,7 +149,8 @@ typedef struct kvq_decode_opts {
 
 /* Workspace (bytes) the split route of kvq_attn_decode_int8kv needs; 0 when the call
  * will take the single-CTA route.  With opts->split_rows == 0 it is the bound for the
- * smallest split the automatic rule can choose (256 keys), so it does not depend on the GPU. */
+ * smallest split the automatic rule can choose (256 keys), so it does not depend on the GPU
+ * (and with the automatic route it is nonzero whenever max_ctx exceeds that split). */
 size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_ctx,
                                   int32_t head_dim, const kvq_decode_opts* opts);
 
@@ -157,11 +160,13 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
  *   out[b][h][:] = sum_t softmax_t(s) * v^[t],   s[t] = softmax_scale * q[b][h] . k^[t],
  *   k^[t] = k_code[t] * k_scale[t] (per token and KV head), same for v^, t < ctx_lens[b],
  *   KV head of query head h = h / (n_q_heads / n_kv_heads) (GQA).
- * The int8 codes are consumed directly; no dequantised copy is written.  Route: when
- * max_ctx <= route_threshold one CTA per (sequence, KV head) walks all keys; otherwise
- * stage 1 runs one CTA per (split_rows-key split, KV head, sequence) and writes a
- * partial (max, sum, acc[head_dim]) per query head, and stage 2 merges the partials
- * with the log-sum-exp rule.
+ * The int8 codes are consumed directly; no dequantised copy is written.  Routes: one CTA per
+ * (sequence, KV head) walks all keys (single-CTA route), or stage 1 runs one CTA per
+ * (split_rows-key split, KV head, sequence) and writes a partial (max, sum, acc[head_dim]) per
+ * query head, and stage 2 merges the partials with the log-sum-exp rule (split route).  The
+ * default (route_threshold 0) takes the split route whenever the split size leaves more than
+ * one split: on a GPU that one CTA per (sequence, KV head) does not fill, splitting even a
+ * 1024-key context is faster ([DOT4]'s table switches at 2048 keys for a smaller GPU).
  *   q          : device bf16 [batch][n_q_heads][head_dim]
  *   block_table: device int32 [batch][max_blocks_per_seq]
  *   ctx_lens   : device int32 [batch], each in [0, max_ctx]; ctx 0 gives zeros

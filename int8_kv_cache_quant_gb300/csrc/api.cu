@@ -47,7 +47,7 @@ int check_cache(const kvq_cache* c) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
 kvq_decode_opts decode_defaults(const kvq_decode_opts* o) {
-  kvq_decode_opts r = {0, 2048, 0, nullptr, nullptr};  // split_rows 0: sized to the GPU
+  kvq_decode_opts r = {0, 0, 0, nullptr, nullptr};  // split_rows 0: sized to the GPU; route 0: automatic
   if (o) {
     if (o->split_rows > 0) r.split_rows = o->split_rows;
     if (o->route_threshold > 0) r.route_threshold = o->route_threshold;
@@ -166,10 +166,18 @@ int kvq_rope_quant_write(const kvq_cache* cache, const void* q, int32_t n_q_head
   return cuda_status(kvq::launch_rope_quant_write(r, static_cast<cudaStream_t>(stream)));
 }
 
+// Smallest split the automatic rule chooses: the workspace bound when split_rows is 0.
+constexpr int kAutoSplitMinRows = 16 * KVQ_BLOCK_SIZE;
+
+// Whether the split route may be taken, from host arguments alone (sizes the workspace).  The
+// automatic route splits only when the split size leaves more than one split, and the automatic
+// split size is never below kAutoSplitMinRows keys.
 static bool decode_split_route(const kvq_decode_opts& o, int32_t max_ctx) {
   if (o.force_route == 1) return false;
   if (o.force_route == 2) return true;
-  return max_ctx > o.route_threshold;
+  if (o.route_threshold > 0) return max_ctx > o.route_threshold;
+  const int rows = o.split_rows > 0 ? o.split_rows : kAutoSplitMinRows;
+  return max_ctx > rows;
 }
 
 int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t head_dim, int32_t max_ctx,
@@ -188,9 +196,6 @@ int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t he
   }
   return static_cast<int32_t>(split_pages * KVQ_BLOCK_SIZE);
 }
-
-// Smallest split the automatic rule chooses: the workspace bound when split_rows is 0.
-constexpr int kAutoSplitMinRows = 16 * KVQ_BLOCK_SIZE;
 
 static int device_sm_count() {
   static std::mutex mu;
@@ -243,13 +248,15 @@ static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_
   kvq_decode_opts o = decode_defaults(opts);
   if (o.split_rows % KVQ_BLOCK_SIZE != 0 || o.force_route < 0 || o.force_route > 2) return KVQ_ERR_INVALID_ARG;
   const int mc = max_ctx > 0 ? max_ctx : 1;
-  const bool split = decode_split_route(o, mc);
+  bool split = decode_split_route(o, mc);
   if (split && !workspace) return KVQ_ERR_WORKSPACE;
   if (split && o.split_rows == 0) {
     const int sms = device_sm_count();
     if (sms <= 0) return KVQ_ERR_CUDA;
     o.split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, cache->head_dim, mc, sms);
   }
+  // automatic route: one split would be the single-CTA route plus a merge
+  if (split && o.force_route == 0 && o.route_threshold == 0 && mc <= o.split_rows) split = false;
   kvq::DecodeArgs a{};
   a.k = cache->k;
   a.v = cache->v;

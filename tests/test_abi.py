@@ -41,7 +41,12 @@ def test_host_helpers_without_gpu():
     assert k.kvq_decode_auto_split_rows(1, 1, 256, 1 << 20, 152) == 1712
     assert k.kvq_decode_auto_split_rows(0, 4, 256, 4096, 152) == 0
     assert k.kvq_decode_auto_split_rows(1, 4, 192, 4096, 152) == 0
-    assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 0  # single-CTA route
+    # automatic route: one split (ctx within the smallest automatic split) is the single-CTA
+    # route; beyond it the split route may be taken
+    assert k.kvq_decode_workspace_bytes(1, 24, 256, 256) == 0
+    assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 4 * 24 * 256 * 4 + 4 * 24 * 16
+    # the pages' threshold route: ctx <= 2048 takes the single-CTA route
+    assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256, route_threshold=2048) == 0
     # verify: the decode workspace of batch * n_rows query rows
     assert k.kvq_verify_workspace_bytes(2, 4, 24, 32768, 256, split_rows=512) == \
         k.kvq_decode_workspace_bytes(8, 24, 32768, 256, split_rows=512)
