@@ -376,14 +376,21 @@ def bench_extra(args, local, hbm, tflops, only=None):
         flush.fill_(i & 0xFF)
         sweep.sum()
 
-    def timed(fn, reps):
+    def timed(fn, reps, cold=True):
+        """Median event time of one call; L2 flushed before each (cold) or still holding the
+        previous call's inputs (warm: a ~50 us sleep kernel between that call and the timed
+        one keeps the host's launches ahead of the GPU, so the events see device time only)."""
         for _ in range(3):
             cold_l2(1)
             fn()
         torch.cuda.synchronize()
         ms = []
         for i in range(reps):
-            cold_l2(i)
+            if cold:
+                cold_l2(i)
+            else:
+                fn()
+                torch.cuda._sleep(100000)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(s)
             fn()
@@ -398,7 +405,7 @@ def bench_extra(args, local, hbm, tflops, only=None):
     def want(name):
         return only is None or only == name
 
-    # decode_1k: single-CTA route, launch/latency bound
+    # decode_1k: launch/latency bound
     if want("decode_1k"):
         res.update(_extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps or 50))
     if want("decode_b64"):
@@ -425,9 +432,47 @@ def _extra_decode_1k(kvq, W, bf16, i32, timed, dev, reps):
     kvq.kvq_quant_write(cache, bf16(w["k_fill"]), bf16(w["v_fill"]), i32(w["fill_seq"]), i32(w["fill_pos"]), bt)
     q, ctx = bf16(w["q"]), i32(w["ctx_lens"])
     out = torch.empty((1, w["hq"], w["d"]), dtype=torch.float32, device=dev)
-    ms = timed(lambda: kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out), reps)
+    ws = torch.empty(max(1, kvq.kvq_decode_workspace_bytes(1, w["hq"], w["max_ctx"], w["d"])), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out, workspace=ws)
+    split = kvq.kvq_decode_auto_split_rows(1, w["hkv"], w["d"], w["max_ctx"],
+                                           torch.cuda.get_device_properties(dev).multi_processor_count)
+    ms = timed(call, reps)
+    ms_warm = timed(call, reps, cold=False)
+    # the same call recorded once in a CUDA graph and replayed (no per-call host work)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    ms_graph = timed(g.replay, reps)
+    ms_graph_warm = timed(g.replay, reps, cold=False)
+
+    def back_to_back(fn, n=200):
+        # n calls issued as fast as the host can: host-bound unless each call is cheap to launch
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(n):
+            fn()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) / n
+    b2b, b2b_graph = back_to_back(call), back_to_back(g.replay)
     kvb = w["max_ctx"] * (2 * w["hkv"] * w["d"] + 8 * w["hkv"])
-    res["decode_1k"] = {"us_per_call": round(ms * 1e3, 2), "kv_GBps": round(kvb / ms / 1e6, 1)}
+    res["decode_1k"] = {"us_per_call": round(ms * 1e3, 2), "kv_GBps": round(kvb / ms / 1e6, 1),
+                        "us_per_call_warm_l2": round(ms_warm * 1e3, 2),
+                        "us_per_call_graph": round(ms_graph * 1e3, 2),
+                        "us_per_call_graph_warm_l2": round(ms_graph_warm * 1e3, 2),
+                        "us_per_call_back_to_back": round(b2b * 1e3, 2),
+                        "us_per_call_back_to_back_graph": round(b2b_graph * 1e3, 2),
+                        "gpu_launches_per_call": 2 if split < w["max_ctx"] else 1}
     return res
 
 

@@ -290,10 +290,23 @@ int kvq_decode_step_int8kv(const kvq_cache* cache, const void* k_new, const void
  * history_len keys: the int8 Q codes and their fp32 scales, and the K/V codes of every
  * (KV head, 128-key tile) of the history_len + n_tokens keys widened once to fp16 in the
  * attention kernel's shared-memory operand layout (2 * 2 * head_dim bytes per key and KV
- * head), with the tiles' key and value scales.  0 if an argument is not positive
+ * head), with the tiles' key and value scales.  With history_len >= 128, also room for the
+ * key-range split (kvq_prefill_split_tiles): per unit of 128 query rows and one query head,
+ * 128 rows of head_dim + 2 floats and two counters.  0 if an argument is not positive
  * (history_len may be 0). */
 size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads,
                                    int32_t history_len, int32_t head_dim);
+
+/*
+ * kvq_prefill_split_tiles — the key-range split kvq_attn_prefill_int8 uses at this shape on a
+ * GPU with n_sms SMs: 0 (each unit of 128 query rows and one query head is one CTA over all
+ * its keys), or r > 0 (each unit runs as two CTAs: a lead segment over key tiles [0, js) and a
+ * tail over [js, n_tiles), js = min(n_tiles - r, history_len / 128); the tails fill the SMs
+ * that the last wave of lead segments leaves idle, and the segment that finishes second
+ * merges the two partial softmax results).  Chosen by simulating the dispatch of the CTAs
+ * onto one slot per SM; never > 0 when history_len < 128.  Host only, no device call.
+ */
+int32_t kvq_prefill_split_tiles(int32_t n_tokens, int32_t n_q_heads, int32_t history_len, int32_t n_sms);
 
 /*
  * kvq_attn_prefill_int8 — a chunk of n_tokens causal queries of one sequence against

@@ -363,9 +363,20 @@ static kvq::PrefillArgs prefill_args(const kvq_cache* cache, const void* q, int3
     a.vw = reinterpret_cast<uint8_t*>(base + w.off_vw);
     a.skw = reinterpret_cast<float*>(base + w.off_skw);
     a.svw = reinterpret_cast<float*>(base + w.off_svw);
+    if (w.can_split) {
+      a.part = reinterpret_cast<float*>(base + w.off_part);
+      a.part_ml = reinterpret_cast<float*>(base + w.off_part_ml);
+      a.part_cnt = reinterpret_cast<unsigned int*>(base + w.off_part_flags);
+      a.part_ready = a.part_cnt + static_cast<long long>((n_tokens + 127) / 128) * n_q_heads;
+      a.split_tail = kvq::prefill_split_tail(n_tokens, n_q_heads, history_len, device_sm_count());
+    }
   }
   a.status = status_ptr();
   return a;
+}
+
+int32_t kvq_prefill_split_tiles(int32_t n_tokens, int32_t n_q_heads, int32_t history_len, int32_t n_sms) {
+  return kvq::prefill_split_tail(n_tokens, n_q_heads, history_len, n_sms);
 }
 
 int kvq_attn_prefill_int8(const kvq_cache* cache, const void* q, int32_t n_tokens, int32_t n_q_heads,

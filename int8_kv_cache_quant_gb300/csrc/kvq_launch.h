@@ -121,16 +121,32 @@ struct PrefillArgs {
   float* skw;        // [Hkv][n_kv_tiles][128]
   float* svw;        // [Hkv][n_kv_tiles][128]
   unsigned int* status;
+  // key-range split (int8 path): with split_tail > 0 each unit (128 query rows, query head) runs
+  // as two CTAs, a lead segment (key tiles [0, js)) and a tail segment (tiles [js, n_tiles)),
+  // js = min(n_tiles - split_tail, history_len / 128); whichever finishes first leaves its
+  // numerator and (m, l) in part / part_ml, and the other merges them into out
+  int split_tail;
+  float* part;               // workspace fp32 [units][128][D]
+  float* part_ml;            // workspace fp32 [units][128][2]
+  unsigned int* part_cnt;    // workspace [units]: segments arrived (zeroed by the widen pass)
+  unsigned int* part_ready;  // workspace [units]: the first segment's values are written
   // debug QK tile (kvq_debug_prefill_qk_int32)
   int dbg_q_head, dbg_q0, dbg_k0, dbg_nk;
   int32_t* dbg_s_out;
 };
 struct PrefillWorkspace {
   int n_kv_tiles;
-  long long off_q_scales, off_kw, off_vw, off_skw, off_svw, bytes;
+  long long off_q_scales, off_kw, off_vw, off_skw, off_svw;
+  long long off_part, off_part_ml, off_part_flags;  // only when the key range may be split
+  bool can_split;
+  long long bytes;
 };
 PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim,
                                    int q_elem_bytes = 1);
+// Tail length (in 128-key tiles) of the key-range split of the int8 prefill at this shape on
+// n_sms SMs, 0 for no split: the choice that minimises the modelled finish time of the
+// longest-first dispatch (one attention CTA per SM).
+int prefill_split_tail(int n_tokens, int n_q_heads, int history_len, int n_sms);
 cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
 // first chunk: Q to fp16, the chunk's K/V into the cache and into fp16 operand pieces, then the

@@ -22,6 +22,10 @@
 //   holds sum_tiles (ps_tile / ps_ref) * PV_tile).
 // * Every P-code decision is the page's fp32 sequence with a specified exp2 (exp2_det) and the
 //   running maximum after each 128-key tile, so the codes are reproducible off the GPU.
+#include <algorithm>
+#include <functional>
+#include <vector>
+
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
 #include "quant_rule.cuh"
@@ -304,6 +308,15 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
       }
     }
     page_s[tid] = page;
+  }
+  if (a.split_tail > 0 && j == 0 && kvh == 0) {
+    // the attention's split units meet through these counters: zero them before the trigger
+    // below lets the attention grid read them
+    const int n_units = ((a.n_tokens + 127) / 128) * a.n_q_heads;
+    for (int u = tid; u < n_units; u += 256) {
+      a.part_cnt[u] = 0u;
+      a.part_ready[u] = 0u;
+    }
   }
   __syncthreads();
   const long long tile = static_cast<long long>(kvh) * a.n_kv_tiles + j;
@@ -648,6 +661,25 @@ __device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
   return r != 0;
 }
 
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Bounded wait for a flag that another CTA of the same grid sets.  The prefill waits only on a
+// CTA that has already announced itself in its epilogue, so the flag comes within microseconds.
+__device__ __forceinline__ void wait_flag(const unsigned int* flag, unsigned int* status) {
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(flag) == 0u) {
+    if (clock64() - t0 > kWaitBudgetCycles) {
+      set_status(status, KVQ_DEV_TIMEOUT);
+      return;
+    }
+    __nanosleep(64);
+  }
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -679,17 +711,37 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offFlag + 4);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // longest first: block l takes query tile n_qt - 1 - l / Hq of head l % Hq, so the CTAs with the
-  // most key tiles start in the first wave and the short ones fill the last
+  // longest first: unit u takes query tile n_qt - 1 - u / Hq of head u % Hq, so the CTAs with the
+  // most key tiles start in the first wave and the short ones fill the last.  With the key range
+  // split, blocks [0, n_units) run the units' lead segments and blocks [n_units, 2 n_units) their
+  // (short) tail segments, which fill the SMs the last wave of lead segments leaves idle.
   const int n_qt = (a.n_tokens + 127) / 128;
-  const int h = static_cast<int>(blockIdx.x % a.n_q_heads);
-  const int q0 = (n_qt - 1 - static_cast<int>(blockIdx.x / a.n_q_heads)) * 128;
+  const int n_units = n_qt * a.n_q_heads;
+  const bool split = !HP && a.split_tail > 0;
+  const bool tail_seg = split && static_cast<int>(blockIdx.x) >= n_units;
+  const int unit = tail_seg ? static_cast<int>(blockIdx.x) - n_units : static_cast<int>(blockIdx.x);
+  const int h = unit % a.n_q_heads;
+  const int q0 = (n_qt - 1 - unit / a.n_q_heads) * 128;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, kvh = h / G;
   const int T = a.n_tokens;
   const int n_keys = a.history_len + T;
   const int last_pos = a.history_len + min(q0 + 127, T - 1);
-  const int n_tiles = last_pos / 128 + 1;
-  const long long tile0 = static_cast<long long>(kvh) * a.n_kv_tiles;  // first tile of this head
+  // key tiles [j_begin, j_begin + nt) of this CTA.  The tail starts at a tile no later than the
+  // last one inside the history, so its first tile holds a key that every row of the unit sees
+  // (the running maximum starts finite in both segments); the host keeps js >= 1.
+  int j_begin = 0, nt = last_pos / 128 + 1;
+  if (split) {
+    const int js = min(nt - a.split_tail, a.history_len / 128);
+    if (tail_seg) {
+      j_begin = js;
+      nt -= js;
+    } else {
+      nt = js;
+    }
+  }
+  // first tile of this head and segment: the producer's loads count from here, while the
+  // barrier phases and buffers count the segment's own tiles from 0
+  const long long tile0 = static_cast<long long>(kvh) * a.n_kv_tiles + j_begin;
 
   grid_dep_wait();  // Q codes, widened K/V and scales come from the preceding kernels
   if (warp == kMmaWarp) tc::tmem_alloc(tmem_slot, L::kTmemCols);
@@ -722,7 +774,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int gbar = 1 + (warp & 3);  // named barrier of the four warps on these lanes
     const bool row_real = q0 + row < T;
-    const int pos_r = a.history_len + q0 + row;
+    // the row's position and the key count, counted from this CTA's first key
+    const int pos_r = a.history_len + q0 + row - 128 * j_begin;
+    const int n_keys_seg = n_keys - 128 * j_begin;
     {
       // Q: this thread's D/4 dims of its row as fp16 pairs into tensor memory, the A operand of
       // QK (lane = row, dim d in column kQCol + d / 2, even dims in the low half): the int8
@@ -780,7 +834,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     float* red_max = red;             // exchange 1: [part][row]
     float* red_wmax = red + 4 * 128;  // exchange 2
     bool failed = false;  // a wait of this thread gave up; the group leaves together below
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; j < nt; ++j) {
       const int b = j & 1, sb = j & (kScaleBufs - 1);
       failed |= !wait_or_abort(&bars[kBarS0], j & 1, a.status, abort_flag);
       tc::fence_after_sync();
@@ -793,7 +847,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       const float4* sk_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 0) * 128 + 32 * part);
       const float4* sv_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 1) * 128 + 32 * part);
       // visible keys of this row in this tile, counted from the start of this thread's part
-      const int lim = min(min(pos_r - 128 * j + 1, n_keys - 128 * j), 128) - 32 * part;
+      const int lim = min(min(pos_r - 128 * j + 1, n_keys_seg - 128 * j), 128) - 32 * part;
       float ym0 = -INFINITY, ym1 = -INFINITY;
 #pragma unroll
       for (int n = 0; n < 32; n += 4) {
@@ -821,11 +875,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       tc::fence_before_sync();
       if (named_bar_or(gbar, 128, failed)) break;  // the four parts of these rows leave together
       tc::fence_after_sync();
-      const float m_new = fmaxf(m, __fmul_rn(max4_col(red_max, row), a_row));
+      // the tile's own maximum (fmaxf turns the NaN of a fully masked row times a zero a_row
+      // into -inf) and the running maximum
+      const float m_tile = fmaxf(__fmul_rn(max4_col(red_max, row), a_row), -INFINITY);
+      const float m_new = fmaxf(m, m_tile);
       const float alpha = (m == -INFINITY) ? 0.0f : fast_exp2(m - m_new);
+      // int8: p is taken relative to the tile's own maximum, so the P codes rint(127 w / max w)
+      // are decided from the tile alone, whichever tiles came before it in this CTA (the key
+      // range may be split between CTAs); beta = 2^(m_tile - m_new) moves the tile's P scale
+      // and sum of p onto the running maximum.  The first-chunk path keeps p relative to the
+      // running maximum (its P unit only grows).
+      const float m_ref = HP ? m_new : m_tile;
+      const float beta = HP ? 1.0f : (m_tile == -INFINITY ? 0.0f : fast_exp2(m_tile - m_new));
       f2 psum = mk2(0.0f, 0.0f);
       float wm0 = 0.0f, wm1 = 0.0f;
-      const f2 a2 = mk2(a_row, a_row), nm2 = mk2(-m_new, -m_new);
+      const f2 a2 = mk2(a_row, a_row), nm2 = mk2(-m_ref, -m_ref);
       // p of the four keys n .. n+3, w = p * sV back into sv, and the running sums; masked keys
       // (only on tiles that carry them: the diagonal and past the context) get p = 0
       auto pass2_step = [&](int n, bool masked) {
@@ -855,7 +919,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       }
       const float wmax = fmaxf(wm0, wm1);
       mbar_arrive(&bars[kBarSclFree + sb]);  // this tile's scales are no longer read
-      l_part = l_part * alpha + (lo2(psum) + hi2(psum));
+      l_part = l_part * alpha + (lo2(psum) + hi2(psum)) * beta;
       m = m_new;
       red_wmax[part * 128 + row] = wmax;
       tc::fence_before_sync();
@@ -866,7 +930,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       // decisions in all four parts of the row)
       float f = 1.0f;
       bool codes_on = wmax_row > 0.0f;
-      const float ps_new = HP ? wmax_row : __fdiv_rn(wmax_row, 127.0f);
+      const float ps_new = HP ? wmax_row : __fdiv_rn(wmax_row, 127.0f) * beta;
       if constexpr (HP) {
         // fp16 P needs no per-tile unit: O's unit ps_ref only grows (to a tile whose largest
         // weight exceeds it), and a tile below it goes in as w / ps_ref <= 1, so O never grows.
@@ -962,26 +1026,96 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     }
     // ---- epilogue: out = O * 2^24 * ps_ref / l (l summed over the four parts; HP: no 2^24)
     if (!*abort_flag) {
-      wait_or_abort(&bars[kBarPvDone], (n_tiles - 1) & 1, a.status, abort_flag);
+      wait_or_abort(&bars[kBarPvDone], (nt - 1) & 1, a.status, abort_flag);
       tc::fence_after_sync();
     }
     red_max[part * 128 + row] = l_part;
     named_bar(gbar, 128);
     const float l = (red_max[row] + red_max[128 + row]) + (red_max[256 + row] + red_max[384 + row]);
-    const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
     constexpr float kOUnit = HP ? 1.0f : 16777216.0f;  // the P codes' 2^-24 unit (int8 path)
+    float* dst_row = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + part * OCOLS;
+    if (!split) {
+      const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
 #pragma unroll
-    for (int c = 0; c < OCOLS / 32; ++c) {
-      uint32_t o[32];
-      tc::ld_32x32b_x32(tm_o + 32 * c, o);
-      tc::wait_ld();
-      if (row_real) {
-        float* dst = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + part * OCOLS + 32 * c;
+      for (int c = 0; c < OCOLS / 32; ++c) {
+        uint32_t o[32];
+        tc::ld_32x32b_x32(tm_o + 32 * c, o);
+        tc::wait_ld();
+        if (row_real) {
+          float* dst = dst_row + 32 * c;
 #pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          *reinterpret_cast<float4*>(dst + e) = make_float4(
-              __uint_as_float(o[e]) * kOUnit * sc, __uint_as_float(o[e + 1]) * kOUnit * sc,
-              __uint_as_float(o[e + 2]) * kOUnit * sc, __uint_as_float(o[e + 3]) * kOUnit * sc);
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + e) = make_float4(
+                __uint_as_float(o[e]) * kOUnit * sc, __uint_as_float(o[e + 1]) * kOUnit * sc,
+                __uint_as_float(o[e + 2]) * kOUnit * sc, __uint_as_float(o[e + 3]) * kOUnit * sc);
+        }
+      }
+    } else {
+      // The unit's two segments meet here.  The first to arrive leaves its numerator
+      // n = O * 2^24 * ps_ref and its (m, l) in the workspace and publishes them; the second
+      // moves both onto the larger maximum M (s = 2^(m - M)) and writes
+      // out = (n1 s1 + n2 s2) / (l1 s1 + l2 s2).
+      volatile unsigned int* arrive_s = reinterpret_cast<volatile unsigned int*>(sm + L::offFlag + 8);
+      if (tid == 0) *arrive_s = atomicAdd(a.part_cnt + unit, 1u);
+      named_bar(5, kSoftmaxThreads);
+      const bool second = *arrive_s != 0u;
+      const long long prow = static_cast<long long>(unit) * 128 + row;
+      float* num = a.part + prow * D + part * OCOLS;
+      const float own = started ? ps_ref * kOUnit : 0.0f;
+      if (!second) {
+#pragma unroll
+        for (int c = 0; c < OCOLS / 32; ++c) {
+          uint32_t o[32];
+          tc::ld_32x32b_x32(tm_o + 32 * c, o);
+          tc::wait_ld();
+          if (row_real) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(num + 32 * c + e) =
+                  make_float4(__uint_as_float(o[e]) * own, __uint_as_float(o[e + 1]) * own,
+                              __uint_as_float(o[e + 2]) * own, __uint_as_float(o[e + 3]) * own);
+          }
+        }
+        if (row_real && part == 0) {
+          a.part_ml[2 * prow] = m;
+          a.part_ml[2 * prow + 1] = l;
+        }
+        __threadfence();
+        named_bar(5, kSoftmaxThreads);
+        if (tid == 0) {
+          __threadfence();
+          atomicExch(a.part_ready + unit, 1u);
+        }
+      } else {
+        if (tid == 0) wait_flag(a.part_ready + unit, a.status);
+        named_bar(5, kSoftmaxThreads);
+        __threadfence();
+        float m2 = -INFINITY, l2 = 0.0f;
+        if (row_real) {
+          m2 = __ldcg(a.part_ml + 2 * prow);
+          l2 = __ldcg(a.part_ml + 2 * prow + 1);
+        }
+        const float mx = fmaxf(m, m2);
+        const float s1 = (m == -INFINITY) ? 0.0f : exp2f(m - mx);
+        const float s2 = (m2 == -INFINITY) ? 0.0f : exp2f(m2 - mx);
+        const float lt = l * s1 + l2 * s2;
+        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+        const float c1 = own * s1 * inv, c2 = s2 * inv;
+#pragma unroll
+        for (int c = 0; c < OCOLS / 32; ++c) {
+          uint32_t o[32];
+          tc::ld_32x32b_x32(tm_o + 32 * c, o);
+          tc::wait_ld();
+          if (row_real) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 n2 = __ldcg(reinterpret_cast<const float4*>(num + 32 * c + e));
+              *reinterpret_cast<float4*>(dst_row + 32 * c + e) = make_float4(
+                  __uint_as_float(o[e]) * c1 + n2.x * c2, __uint_as_float(o[e + 1]) * c1 + n2.y * c2,
+                  __uint_as_float(o[e + 2]) * c1 + n2.z * c2, __uint_as_float(o[e + 3]) * c1 + n2.w * c2);
+            }
+          }
+        }
       }
     }
   } else if (warp == kMmaWarp) {
@@ -994,8 +1128,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     int slot = 0;
     uint32_t ph = 0;
     bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag));
-    for (int j = 0; ok && j <= n_tiles; ++j) {
-      if (j < n_tiles) {
+    for (int j = 0; ok && j <= nt; ++j) {
+      if (j < nt) {
         // S is single-buffered: QK_j overwrites it once every softmax thread has loaded S_{j-1}
         if (j >= 1) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarS0 + 1], (j - 1) & 1, a.status, abort_flag));
         for (int qa = 0; ok && qa < NP; ++qa) {
@@ -1085,8 +1219,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       bulk_g2s(scale_s + sb * 256 + 128, a.svw + (tile0 + j) * 128, 512, &bars[kBarSclFull + sb]);
       ++scl_loads;
     };
-    for (int j = 0; ok && j <= n_tiles; ++j) {
-      if (j < n_tiles) {
+    for (int j = 0; ok && j <= nt; ++j) {
+      if (j < nt) {
         const uint8_t* kt = a.kw + (tile0 + j) * NP * kPieceBytes;
         for (int qa = 0; ok && qa < NP; ++qa) push(kt + qa * kPieceBytes);
         if (ok) push_scales(j);
@@ -1178,8 +1312,10 @@ __global__ void __launch_bounds__(128, 1) prefill_qk_debug_kernel(PrefillArgs a)
 }
 
 // ============================================================================ launchers
-// Workspace: int8 Q codes | Q scales | widened K tiles | widened V tiles | K scales | V scales
-// (each part starting on a 1024-byte boundary of the workspace).
+// Workspace: int8 Q codes | Q scales | widened K tiles | widened V tiles | K scales | V scales,
+// and for an int8 chunk with at least one full tile of history (whose key range may be split)
+// the split units' numerators | (m, l) | arrival counters and ready flags (each part starting on
+// a 1024-byte boundary of the workspace).
 static long long round1k(long long x) { return (x + 1023) / 1024 * 1024; }
 
 PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim,
@@ -1193,7 +1329,61 @@ PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, 
   w.off_skw = w.off_vw + tiles * 128 * head_dim * 2;
   w.off_svw = w.off_skw + tiles * 128 * 4;
   w.bytes = w.off_svw + tiles * 128 * 4;
+  w.can_split = q_elem_bytes == 1 && history_len >= 128;
+  if (w.can_split) {
+    const long long units = static_cast<long long>((n_tokens + 127) / 128) * n_q_heads;
+    w.off_part = round1k(w.bytes);
+    w.off_part_ml = w.off_part + round1k(units * 128 * head_dim * 4);
+    w.off_part_flags = w.off_part_ml + round1k(units * 128 * 2 * 4);
+    w.bytes = w.off_part_flags + units * 2 * 4;
+  }
   return w;
+}
+
+// The split choice models the attention grid as list scheduling in block order onto one CTA
+// slot per SM (the hardware hands the next block to the first SM that frees): a CTA costs its
+// key tiles plus a fixed start-up and epilogue cost, and a split segment also pays for writing
+// or reading the partial result.  Costs are in units of one key tile's time; the two constants
+// were fitted to the measured call time of a 2048-query chunk after 30720 keys (24 query /
+// 4 KV heads, head_dim 256) on 152 SMs at tail lengths 0, 16, 24, 32 and 48 tiles (within
+// 0.5% at each).
+int prefill_split_tail(int n_tokens, int n_q_heads, int history_len, int n_sms) {
+  if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 128 || n_sms <= 0) return 0;
+  const int n_qt = (n_tokens + 127) / 128;
+  const long long units = static_cast<long long>(n_qt) * n_q_heads;
+  if (units > 16384) return 0;  // many waves: the last one is a small share of the call
+  constexpr double kCtaCost = 8.0, kCombineCost = 3.0;
+  const int h_tiles = history_len / 128;
+  auto tiles_of = [&](int qt) { return (history_len + std::min(128 * qt + 127, n_tokens - 1)) / 128 + 1; };
+  std::vector<double> slots;
+  auto makespan = [&](int r) {
+    slots.assign(static_cast<size_t>(n_sms), 0.0);  // a min-heap of the SMs' free times
+    auto run = [&](double cost) {
+      std::pop_heap(slots.begin(), slots.end(), std::greater<double>());
+      slots.back() += cost;
+      std::push_heap(slots.begin(), slots.end(), std::greater<double>());
+    };
+    for (int seg = 0; seg < (r > 0 ? 2 : 1); ++seg)
+      for (long long u = 0; u < units; ++u) {
+        const int n = tiles_of(n_qt - 1 - static_cast<int>(u / n_q_heads));
+        const int js = std::min(n - r, h_tiles);
+        const int len = r == 0 ? n : (seg == 0 ? js : n - js);
+        run(len + kCtaCost + (r > 0 ? kCombineCost : 0.0));
+      }
+    return *std::max_element(slots.begin(), slots.end());
+  };
+  const int max_r = tiles_of(0) - 1;  // every lead segment keeps at least one tile
+  double best = makespan(0);
+  int best_r = 0;
+  for (int r : {8, 16, 24, 32, 48, 64, 96, 128}) {
+    if (r > max_r) break;
+    const double m = makespan(r);
+    if (m < best) {
+      best = m;
+      best_r = r;
+    }
+  }
+  return best_r;
 }
 
 cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
@@ -1211,7 +1401,7 @@ static cudaError_t launch_attention(const PrefillArgs& a, cudaStream_t stream) {
   using L = PrefillTmaSmem<D>;
   cudaError_t e = cudaFuncSetAttribute(prefill_tma_kernel<D, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  dim3 grid(((a.n_tokens + 127) / 128) * a.n_q_heads);
+  dim3 grid(((a.n_tokens + 127) / 128) * a.n_q_heads * (!HP && a.split_tail > 0 ? 2 : 1));
   return launch_pdl(prefill_tma_kernel<D, HP>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
 }
 

@@ -65,6 +65,8 @@ def lib():
         L.kvq_decode_workspace_bytes.restype = sz
         L.kvq_decode_auto_split_rows.restype = i32
         L.kvq_decode_auto_split_rows.argtypes = [i32, i32, i32, i32, i32]
+        L.kvq_prefill_split_tiles.restype = i32
+        L.kvq_prefill_split_tiles.argtypes = [i32, i32, i32, i32]
         L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
         L.kvq_attn_decode_int8kv.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
                                              ctypes.POINTER(_DecodeOpts), vp]
@@ -181,6 +183,10 @@ def _decode_opts(split_rows, route_threshold, force_route, events=None):
 
 def kvq_decode_auto_split_rows(batch, n_kv_heads, head_dim, max_ctx, n_sms):
     return int(lib().kvq_decode_auto_split_rows(batch, n_kv_heads, head_dim, max_ctx, n_sms))
+
+
+def kvq_prefill_split_tiles(n_tokens, n_q_heads, history_len, n_sms):
+    return int(lib().kvq_prefill_split_tiles(n_tokens, n_q_heads, history_len, n_sms))
 
 
 def kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx, head_dim, split_rows=0,

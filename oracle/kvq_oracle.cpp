@@ -572,22 +572,26 @@ void oracle_prefill_qk_int32(const int8_t* q_codes, int32_t n_tokens, int32_t n_
 }
 
 // Part B, prefill chunk with the int8 arithmetic of [DCU] §1.3 / §3.3, the page's
-// fragment code taken step by step in fp32 with an online running maximum:
+// fragment code taken step by step in fp32:
 //   Q codes by B1 per (token, query head);  S_t = sum_d q8 k8 (exact integer);
 //   a = sQ * c2 (c2 = softmax_scale * log2 e);  y_t = S_t * sK_t  (log2-domain score a*y_t);
-//   tiles of `pv_tile` keys at absolute multiples of pv_tile, taken in increasing order,
-//   over the visible keys of the tile:
-//     m_j = max(m_{j-1}, (max_t y_t) * a)                 online running maximum
-//     p_t = exp2_det(fma(y_t, a, -m_j))                   p relative to m_j
+//   tiles of `pv_tile` keys at absolute multiples of pv_tile, over the visible keys of the
+//   tile:
+//     t_j = (max_t y_t) * a                               the tile's own maximum
+//     p_t = exp2_det(fma(y_t, a, -t_j))                   p relative to t_j
 //     w_t = p_t * sV_t                                   sV folded into the weight
 //     r_j = 127 / max_t w_t;  c_t = rint(w_t * r_j) in [0, 127] (one rounding, fma)
 //     numerator_j = ps_j * sum_t c_t v8_t with ps_j = max_t w_t / 127, sum exact
-//   out = sum_j numerator_j 2^{m_j - M} / sum_j (sum_t p_t) 2^{m_j - M}, M the last m_j,
-//   this final combination in double.  l sums the unquantised p.
+//   out = sum_j numerator_j 2^{t_j - M} / sum_j (sum_t p_t) 2^{t_j - M}, M the row maximum,
+//   this final combination in double (accumulated with an online maximum, exact in double).
+//   l sums the unquantised p.
 // Readings (the page is silent): one P scale per (query row, tile); tiles aligned at
-// absolute key positions and walked in increasing order in one online softmax (§3.2);
-// l from the unquantised weights; exp by exp2_det so that both sides decide each code
-// with the same fp32 operations.  q_codes_out ([n_tokens][n_q_heads][D]) and q_scales_out
+// absolute key positions; l from the unquantised weights; exp by exp2_det so that both
+// sides decide each code with the same fp32 operations.  The page takes p relative to the
+// online running maximum; the maximum cancels in w / max w, so the codes are the same in
+// exact arithmetic, and taking the fp32 decision relative to the tile's own maximum makes
+// each tile's codes a function of that tile alone (independent of the order in which the
+// tiles are visited, or of how the key range is divided between workers).  q_codes_out ([n_tokens][n_q_heads][D]) and q_scales_out
 // ([n_tokens][n_q_heads]) may be null; they are written for every token and head.
 void oracle_prefill_int8_emul(const oracle_cache* cache, const uint16_t* q, int32_t n_tokens,
                               int32_t n_q_heads, int32_t history, const int32_t* bt_row,
@@ -632,9 +636,16 @@ void oracle_prefill_int8_emul(const oracle_cache* cache, const uint16_t* q, int3
         y[t - t0] = static_cast<float>(acc) * c.k_scale[scale_offset(c, s.page, kvh, s.slot)];
         ymax = std::max(ymax, y[t - t0]);
       }
-      float m_new = std::max(m, ymax * a);
+      // The tile's codes c = rint(127 w / max w) do not depend on the maximum that p is taken
+      // relative to (it cancels in w / max w); the fp32 decisions are taken relative to the
+      // tile's own maximum t = max(y) * a, so each tile's codes follow from the tile alone.
+      // beta = 2^(t - m) then moves the tile's P scale and its sum of p onto the running
+      // maximum m (in double).
+      const float m_tile = ymax * a;
+      float m_new = std::max(m, m_tile);
       // rescale what was accumulated relative to the previous maximum (exact in double)
       double alpha = (m == -INFINITY) ? 0.0 : std::exp2(static_cast<double>(m) - m_new);
+      const double beta = std::exp2(static_cast<double>(m_tile) - m_new);
       l *= alpha;
       for (int d = 0; d < D; ++d) num[d] *= alpha;
       m = m_new;
@@ -642,12 +653,12 @@ void oracle_prefill_int8_emul(const oracle_cache* cache, const uint16_t* q, int3
       double psum = 0.0;
       for (int t = t0; t < t1; ++t) {
         Slot s = locate(c, bt_row, t);
-        p[t - t0] = exp2_det(std::fma(y[t - t0], a, -m));
+        p[t - t0] = exp2_det(std::fma(y[t - t0], a, -m_tile));
         psum += p[t - t0];
         w[t - t0] = p[t - t0] * c.v_scale[scale_offset(c, s.page, kvh, s.slot)];
         wmax = std::max(wmax, w[t - t0]);
       }
-      l += psum;
+      l += psum * beta;
       if (!(wmax > 0.0f)) continue;  // every weight of the tile is zero: codes all zero
       const float r = 127.0f / wmax;
       std::fill(tile_sum.begin(), tile_sum.end(), 0);
@@ -660,7 +671,7 @@ void oracle_prefill_int8_emul(const oracle_cache* cache, const uint16_t* q, int3
         Slot s = locate(c, bt_row, t);
         for (int d = 0; d < D; ++d) tile_sum[d] += ci * c.v[v_offset(c, s.page, kvh, d, s.slot)];
       }
-      double ps = static_cast<double>(wmax) / 127.0;
+      double ps = static_cast<double>(wmax) / 127.0 * beta;
       for (int d = 0; d < D; ++d) num[d] += ps * static_cast<double>(tile_sum[d]);
     }
     double* o = out + j * D;

@@ -53,9 +53,24 @@ def test_host_helpers_without_gpu():
     assert k.kvq_verify_workspace_bytes(2, 0, 24, 32768, 256) == 0
     # prefill: Q codes | Q scales | widened K and V of 256 tiles x 4 KV heads (2 bytes per code) |
     # their key and value scales
+    # | with a full tile of history, room for the key-range split: per unit (16 query tiles x 24
+    # heads) 128 rows of numerators and (m, l), and two counters
     tiles = 4 * ((30720 + 2048 + 127) // 128)
+    units = 16 * 24
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 30720, 256) == (
+        2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4
+        + units * 128 * 256 * 4 + units * 128 * 2 * 4 + units * 2 * 4)
+    tiles = 4 * ((100 + 2048 + 127) // 128)  # history below one tile: no split region
+    assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 100, 256) == (
         2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4)
+    # the split choice (host-only simulation of the dispatch onto one CTA per SM)
+    assert k.kvq_prefill_split_tiles(2048, 24, 30720, 152) == 24
+    assert k.kvq_prefill_split_tiles(2048, 24, 100, 152) == 0       # no full tile of history
+    assert k.kvq_prefill_split_tiles(1, 24, 30000, 152) == 128      # 24 one-tile-row units
+    assert k.kvq_prefill_split_tiles(130, 6, 200, 152) == 0         # too few tiles to split
+    assert k.kvq_prefill_split_tiles(4096, 24, 4096, 152) == 0      # five waves: the split does not pay
+    assert k.kvq_prefill_split_tiles(0, 24, 30720, 152) == 0
+    assert k.kvq_prefill_split_tiles(2048, 24, 30720, 0) == 0
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, -1, 256) == 0
     # first chunk: fp16 Q (2 bytes per element) | Q scales | fp16 K and V pieces of the chunk's tiles | scales
     tiles1 = 4 * ((4096 + 127) // 128)

@@ -92,10 +92,39 @@ def test_prefill_outlier_keys_and_wide_scores(kvq, oracle):
     assert norm_max_err(got, emul) <= DESIGN_TOL
 
 
+def _n_sms():
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("history,T,d,hq,hkv,wide", [
+    (1200, 1024, 256, 6, 1, False),  # long units: tails start at the history's last full tile
+    (2000, 1, 128, 24, 4, False),    # a one-token chunk: 24 units become 48 CTAs
+    (5000, 700, 128, 32, 8, False),
+    (3000, 300, 256, 12, 2, True),   # outlier keys and a large scale: segment maxima far apart
+])
+def test_prefill_key_range_split(kvq, oracle, history, T, d, hq, hkv, wide):
+    """Shapes whose units run as a lead and a tail segment on this GPU (the second segment to
+    finish merges the two partial softmax results): against the int8 emulation."""
+    assert kvq.kvq_prefill_split_tiles(T, hq, history, _n_sms()) > 0
+    w = _case(760 + history + T, history=history, T=T, hq=hq, hkv=hkv, d=d,
+              **({"k_outlier_p": 0.02} if wide else {}))
+    if wide:
+        w["softmax_scale"] = 0.4
+    got = _prefill(kvq, w)
+    hc = host_cache_from(w, oracle)
+    emul = oracle.prefill_int8_emul(hc, w["q"], history, w["block_table"][0], w["softmax_scale"])
+    err = norm_max_err(got, emul)
+    print("split prefill h=%d T=%d: vs emulation %.3g" % (history, T, err))
+    assert err <= GATE and err <= DESIGN_TOL, err
+    assert kvq.kvq_device_status() == 0
+
+
 def test_prefill_32k_full_sampled(kvq, oracle):
     """Workload prefill_32k at full size (2048 queries after 30720 history, 24/4 heads,
-    head_dim 256, shuffled pages) in the benchmark's launch configuration; sampled
-    (token, head) outputs against the int8 emulation."""
+    head_dim 256, shuffled pages) in the benchmark's launch configuration (on 152 SMs its
+    units are split into lead and tail segments); sampled (token, head) outputs against the
+    int8 emulation."""
     w = W.make("prefill_32k")
     got = _prefill(kvq, w)
     hc = host_cache_from(w, oracle)
