@@ -112,6 +112,28 @@ def test_decode_32k_full(kvq, oracle):
     assert err <= GATE and err <= DESIGN_TOL
 
 
+def test_decode_128k_fused_step(kvq, oracle):
+    """A 131072-token context (the decode_32k geometry, four times longer: 272 MB of K/V) through
+    the fused step, which writes the newest token inside stage 1: every output against FP64,
+    and the rewritten token's codes and scales against the oracle's quantiser."""
+    w = W.make("decode_32k", seed=1300, ctx=131072)
+    cache, bt = gpu_cache_from(w, kvq)
+    kvq.kvq_quant_write(cache, to_bf16_tensor(np.zeros_like(w["k_new"])), to_bf16_tensor(np.zeros_like(w["v_new"])),
+                        to_i32(w["new_seq"]), to_i32(w["new_pos"]), bt)  # the step must write these rows
+    out = kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(w["k_new"]), to_bf16_tensor(w["v_new"]),
+                                     to_bf16_tensor(w["q"]), bt, to_i32(w["ctx_lens"]), w["max_ctx"],
+                                     w["softmax_scale"]).cpu().numpy()
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    err = norm_max_err(out, ref)
+    print("decode 128k fused step normalised max err", err)
+    assert err <= GATE and err <= DESIGN_TOL
+    page = int(w["block_table"][0][(131072 - 1) // 16])
+    assert np.array_equal(cache.k[page].cpu().numpy(), hc.k[page])
+    assert np.array_equal(cache.v_scale[page].cpu().numpy().view(np.uint32), hc.v_scale[page].view(np.uint32))
+    assert kvq.kvq_device_status() == 0
+
+
 def test_decode_b64_full_sampled(kvq, oracle):
     """Workload decode_b64 at full size (64 sequences, ctx up to 16384, head_dim 128) with the
     step's kv_quant_write of one new token per sequence; sampled (sequence, head) outputs."""

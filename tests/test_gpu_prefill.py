@@ -137,3 +137,19 @@ def test_prefill_32k_full_sampled(kvq, oracle):
     err = norm_max_err(g, emul)
     print("prefill_32k sampled: vs emulation %.3g, vs FP64 %.3g" % (err, norm_max_err(g, ref)))
     assert err <= GATE and err <= DESIGN_TOL
+
+
+def test_prefill_long_history_sampled(kvq, oracle):
+    """2048 queries after 122880 history keys (the prefill_32k geometry at four times the
+    context: 976 key tiles per head), split into lead and tail segments on this GPU; sampled
+    (token, head) outputs against the int8 emulation."""
+    w = W.make("prefill_32k", seed=1310, history=122880)
+    got = _prefill(kvq, w)
+    hc = host_cache_from(w, oracle)
+    units = sample_units(w["n_tokens"], w["hq"], 24, seed=1311)
+    emul = oracle.prefill_int8_emul(hc, w["q"], w["history"], w["block_table"][0], w["softmax_scale"],
+                                    units=units)
+    err = norm_max_err(got.reshape(-1, w["d"])[units], emul)
+    print("prefill 2048 @ 125k sampled: vs emulation %.3g" % err)
+    assert err <= GATE and err <= DESIGN_TOL
+    assert kvq.kvq_device_status() == 0
