@@ -278,42 +278,69 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     ms_step_max = max_over_ranks(ms_step, world)
     kv_bytes = max_ctx * (2 * Hkv * D + 2 * Hkv * 4)  # 2080 B per token at 4 x 256
 
-    # end to end through the public API with host buffers: H2D of the step's inputs from
-    # pinned memory, the step, D2H of the result, all inside the events
-    # the step's inputs (Q, the new K and V rows) staged in one pinned host buffer, so that one
-    # host-to-device copy carries them; the call reads 16-byte-aligned views of its device copy
-    parts = [np.ascontiguousarray(w[name]).view(np.int16).ravel() for name in ("q", "k_new", "v_new")]
-    in_h = torch.from_numpy(np.concatenate(parts)).pin_memory()
-    in_d = torch.empty_like(in_h, device=dev)
-    nq_el, nk_el = parts[0].size, parts[1].size
+    # End to end through the public API with host buffers.  On GB300 the kernels read and write
+    # page-locked host memory across the coherent host link, so the step takes its inputs (Q,
+    # the new K and V rows) from pinned host buffers and writes its result into one (zero-copy):
+    # the transfers run inside the call, overlapped with the K/V stream.  The timed steps cycle
+    # through NSET buffer sets with different query rows, and afterwards every set's host result
+    # is checked bit for bit against the same step with device buffers.  The same step with
+    # explicit copies (one H2D of a staged input buffer, the call, one D2H of the result) is
+    # timed as well.
+    NSET = 4
+    rng_e = np.random.default_rng(4242)
+    sets = []
+    for i in range(NSET):
+        qi = w["q"] if i == 0 else W.normal_bf16(rng_e, w["q"].shape)
+        parts = [np.ascontiguousarray(x).view(np.int16).ravel() for x in (qi, w["k_new"], w["v_new"])]
+        buf = torch.from_numpy(np.concatenate(parts)).pin_memory()
+        nq_el, nk_el = parts[0].size, parts[1].size
+        views = (buf[:nq_el].view(torch.bfloat16).view(1, Hq, D),
+                 buf[nq_el:nq_el + nk_el].view(torch.bfloat16).view(1, Hkv, D),
+                 buf[nq_el + nk_el:].view(torch.bfloat16).view(1, Hkv, D))
+        sets.append((buf, views, torch.empty((1, Hq, D), dtype=torch.float32).pin_memory()))
+    h2d = sets[0][0].numel() * 2
+    d2h = sets[0][2].numel() * 4
+
+    def e2e_step(i):
+        _, (qh, knh, vnh), oh = sets[i % NSET]
+        kvq.kvq_decode_step_int8kv(cache, knh, vnh, qh, bt, ctx, max_ctx, w["softmax_scale"], out=oh, workspace=ws)
+
+    in_d = torch.empty_like(sets[0][0], device=dev)
     q_d = in_d[:nq_el].view(torch.bfloat16).view(1, Hq, D)
     kn_d = in_d[nq_el:nq_el + nk_el].view(torch.bfloat16).view(1, Hkv, D)
     vn_d = in_d[nq_el + nk_el:].view(torch.bfloat16).view(1, Hkv, D)
-    out_h = torch.empty((1, Hq, D), dtype=torch.float32).pin_memory()
-    h2d = in_h.numel() * 2
-    d2h = out_h.numel() * 4
+    out_copy_h = torch.empty((1, Hq, D), dtype=torch.float32).pin_memory()
 
-    def e2e_step():
-        in_d.copy_(in_h, non_blocking=True)
+    def e2e_copy_step(i):
+        in_d.copy_(sets[i % NSET][0], non_blocking=True)
         kvq.kvq_decode_step_int8kv(cache, kn_d, vn_d, q_d, bt, ctx, max_ctx, w["softmax_scale"], out=out,
                                    workspace=ws)
-        out_h.copy_(out, non_blocking=True)
+        out_copy_h.copy_(out, non_blocking=True)
 
-    for _ in range(3):
-        cold_l2(2)
-        e2e_step()
-    torch.cuda.synchronize()
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    for i in range(K):
-        cold_l2(i)
-        e0[i].record(s)
-        e2e_step()
-        e1[i].record(s)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(e0, e1)), world)
-    got = out_h.numpy().copy()
-    assert np.isfinite(got).all()
+    def time_e2e(fn):
+        for i in range(3):
+            cold_l2(2)
+            fn(i)
+        torch.cuda.synchronize()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            cold_l2(i)
+            e0[i].record(s)
+            fn(i)
+            e1[i].record(s)
+        torch.cuda.synchronize()
+        return max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in zip(e0, e1)), world)
+
+    e2e_ms = time_e2e(e2e_step)
+    e2e_copy_ms = time_e2e(e2e_copy_step)
+    for i in range(NSET):  # each set's host result against the step with device buffers
+        in_d.copy_(sets[i][0])
+        kvq.kvq_decode_step_int8kv(cache, kn_d, vn_d, q_d, bt, ctx, max_ctx, w["softmax_scale"], out=out,
+                                   workspace=ws)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy().view(np.uint32), sets[i][2].numpy().view(np.uint32)), i
+    assert kvq.kvq_device_status() == 0
 
     hbm, _, peak_kind = load_peaks()
     kern_avg = statistics.mean(kern_ms)
@@ -345,7 +372,13 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                      "kernel": "decode_stage1_kernel<256,warps=8,DEPTH=3,split,fused write>", "peak_kind": peak_kind,
                      "kernel_us": round(kern_avg * 1e3, 2)},
         "e2e": {"value": round(aggregate_gbs(kv_bytes, e2e_ms, world), 2), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "transfer": "zero-copy: the step's kernels read Q and the new K/V rows from, and write the "
+                            "result into, page-locked host memory over the coherent host link; %d host "
+                            "buffer sets with different queries, each result checked bit for bit" % NSET,
+                "with_copies": {"value": round(aggregate_gbs(kv_bytes, e2e_copy_ms, world), 2),
+                                "ms_per_step": round(e2e_copy_ms, 5),
+                                "transfer": "one H2D copy of the staged inputs, the call, one D2H copy"}},
         "gpu_launches": 2 * K,
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 4),

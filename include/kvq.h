@@ -16,6 +16,15 @@
  *   - Every pointer argument named as "device" is device memory of the current CUDA
  *     device, owned by the caller.  The library allocates nothing, keeps no per-call
  *     state and never synchronises, except kvq_device_status().
+ *   - Zero-copy host buffers: the decode calls (kvq_attn_decode_int8kv,
+ *     kvq_attn_verify_int8kv, kvq_decode_step_int8kv) also take q, k_new, v_new and out in
+ *     page-locked host memory mapped into the device's address space (cudaHostAlloc, or
+ *     cudaHostRegister with the mapped flag, under unified addressing: the pointer the host
+ *     uses is the one the device uses).  The kernels then read the step's inputs and write
+ *     its result across the host link themselves, overlapped with the K/V stream, so a
+ *     step needs no separate host-device copies.  kvq_device_accessible() tells such a
+ *     pointer from pageable host memory, which a kernel cannot read: the library cannot
+ *     detect that case on the device, so a caller that may hold either checks first.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - bf16 tensors are passed as raw 16-bit patterns (const void*).
  *   - Outputs of the attention calls are fp32 (a bf16 output would add up to 2^-9
@@ -64,6 +73,13 @@ typedef enum kvq_status {
   KVQ_ERR_WORKSPACE = 4,   /* workspace missing or smaller than the *_workspace_bytes size */
   KVQ_ERR_CUDA = 5         /* a launch failed (cudaGetLastError after the launch) */
 } kvq_status;
+
+/*
+ * kvq_device_accessible — 1 when p can be dereferenced by the kernels of the current device:
+ * device memory, managed memory, or page-locked host memory whose device address is p itself;
+ * 0 otherwise (NULL, pageable host memory, no device).  Host only, no synchronisation.
+ */
+int32_t kvq_device_accessible(const void* p);
 
 /* Device status bits (sticky until read by kvq_device_status). */
 #define KVQ_DEV_BAD_BLOCK 0x1u /* a block-table entry is outside [0, num_blocks) */

@@ -7,6 +7,6 @@ from .kvq import (KVCache, KvqError, kvq_attn_decode_int8kv, kvq_attn_decode_int
                   kvq_attn_prefill_first_bf16, kvq_attn_prefill_int8, kvq_attn_prefill_int8_qcodes, kvq_rope_quant_write,
                   kvq_attn_sparse_int8kv, kvq_attn_verify_int8kv, kvq_debug_prefill_q_codes, kvq_debug_prefill_qk_int32,
                   kvq_decode_auto_split_rows, kvq_decode_step_int8kv, kvq_decode_workspace_bytes, kvq_device_status,
-                  kvq_prefill_split_tiles,
+                  kvq_prefill_split_tiles, kvq_device_accessible,
                   kvq_prefill_first_workspace_bytes, kvq_prefill_workspace_bytes, kvq_sparse_workspace_bytes, kvq_verify_workspace_bytes,
                   kvq_quant_write, kvq_version, lib)

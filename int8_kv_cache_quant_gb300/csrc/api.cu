@@ -375,6 +375,17 @@ static kvq::PrefillArgs prefill_args(const kvq_cache* cache, const void* q, int3
   return a;
 }
 
+int32_t kvq_device_accessible(const void* p) {
+  if (!p) return 0;
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    (void)cudaGetLastError();  // not a sticky error: clear it so the caller's next check is clean
+    return 0;
+  }
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) return 1;
+  return attr.type == cudaMemoryTypeHost && attr.devicePointer == p ? 1 : 0;
+}
+
 int32_t kvq_prefill_split_tiles(int32_t n_tokens, int32_t n_q_heads, int32_t history_len, int32_t n_sms) {
   return kvq::prefill_split_tail(n_tokens, n_q_heads, history_len, n_sms);
 }

@@ -66,6 +66,8 @@ def lib():
         L.kvq_decode_auto_split_rows.restype = i32
         L.kvq_decode_auto_split_rows.argtypes = [i32, i32, i32, i32, i32]
         L.kvq_prefill_split_tiles.restype = i32
+        L.kvq_device_accessible.restype = i32
+        L.kvq_device_accessible.argtypes = [ctypes.c_void_p]
         L.kvq_prefill_split_tiles.argtypes = [i32, i32, i32, i32]
         L.kvq_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, ctypes.POINTER(_DecodeOpts)]
         L.kvq_attn_decode_int8kv.argtypes = [cp, vp, i32, i32, vp, i32, vp, i32, f32, vp, vp, sz,
@@ -105,6 +107,26 @@ def _p(t):
 def _check(fn, status):
     if status != 0:
         raise KvqError(fn, status)
+
+
+def kvq_device_accessible(t):
+    """True when the kernels can dereference tensor t's storage (device memory, or page-locked
+    host memory mapped into the device's address space)."""
+    return bool(lib().kvq_device_accessible(ctypes.c_void_p(t.data_ptr())))
+
+
+def _host_ok(fn, *tensors):
+    """Host tensors passed to a decode call must be mapped page-locked memory (zero-copy): the
+    kernels read and write them across the host link.  Anything else is refused before launch."""
+    for t in tensors:
+        if t is not None and t.device.type == "cpu" and not kvq_device_accessible(t):
+            raise ValueError(fn + ": a host tensor must be page-locked memory mapped into the device's "
+                             "address space (e.g. tensor.pin_memory())")
+
+
+def _new_out(shape, q):
+    # a host q (zero-copy) gets its result in page-locked host memory too
+    return torch.empty(shape, dtype=torch.float32, device=q.device, pin_memory=q.device.type == "cpu")
 
 
 class KVCache:
@@ -209,11 +231,12 @@ def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
     pair of torch.cuda.Event recorded around the stage-1 kernel (profiling)."""
     B, Hq, D = q.shape
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+        out = _new_out((B, Hq, D), q)
+    _host_ok("kvq_attn_decode_int8kv", q, out)
     o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
     need = int(lib().kvq_decode_workspace_bytes(B, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=cache.k.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = cache.struct()
     _check("kvq_attn_decode_int8kv", lib().kvq_attn_decode_int8kv(
@@ -230,11 +253,12 @@ def kvq_attn_verify_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
     keys t < ctx_lens[b] - nq + 1 + i.  Returns out fp32 [B][nq][Hq][D]."""
     B, nq, Hq, D = q.shape
     if out is None:
-        out = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=q.device)
+        out = _new_out((B, nq, Hq, D), q)
+    _host_ok("kvq_attn_verify_int8kv", q, out)
     o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
     need = int(lib().kvq_verify_workspace_bytes(B, nq, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=cache.k.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = cache.struct()
     _check("kvq_attn_verify_int8kv", lib().kvq_attn_verify_int8kv(
@@ -256,18 +280,22 @@ def kvq_decode_step_int8kv(cache, k_new, v_new, q, block_table, ctx_lens, max_ct
         q, k_new, v_new = q[:, None], k_new[:, None], v_new[:, None]
     B, nq, Hq, D = q.shape
     if out is None:
-        out = torch.empty((B, nq, Hq, D), dtype=torch.float32, device=q.device)
+        out = _new_out((B, nq, Hq, D), q)
+        ret = out[:, 0] if squeeze else out
+    else:
+        ret = out  # the caller's buffer, in the caller's shape ([B][Hq][D] for the one-token step)
+    _host_ok("kvq_decode_step_int8kv", q, k_new, v_new, out)
     o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
     need = int(lib().kvq_verify_workspace_bytes(B, nq, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
     if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=cache.k.device)
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = cache.struct()
     _check("kvq_decode_step_int8kv", lib().kvq_decode_step_int8kv(
         ctypes.byref(c), _p(k_new), _p(v_new), _p(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]),
         _p(ctx_lens), int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
-    return out[:, 0] if squeeze else out
+    return ret
 
 
 NOALLOC_SCRATCH_BYTES = 4 << 20

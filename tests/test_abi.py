@@ -28,6 +28,12 @@ def test_host_helpers_without_gpu():
     L = k.lib()
     assert L.kvq_version() == 1
     assert L.kvq_status_string(4) == b"workspace missing or too small"
+    # pageable host memory (and NULL) is never reported as device-accessible
+    import ctypes
+    import numpy as np
+    buf = np.zeros(64, np.uint8)
+    assert L.kvq_device_accessible(ctypes.c_void_p(buf.ctypes.data)) == 0
+    assert L.kvq_device_accessible(None) == 0
     # workspace sizes are pure host arithmetic
     # automatic split size: the workspace is the bound for its smallest split (256 keys)
     assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 128 * 24 * 256 * 4 + 128 * 24 * 16
