@@ -1033,90 +1033,121 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     named_bar(gbar, 128);
     const float l = (red_max[row] + red_max[128 + row]) + (red_max[256 + row] + red_max[384 + row]);
     constexpr float kOUnit = HP ? 1.0f : 16777216.0f;  // the P codes' 2^-24 unit (int8 path)
-    float* dst_row = a.out + (static_cast<long long>(q0 + row) * Hq + h) * D + part * OCOLS;
-    if (!split) {
-      const float sc = (started && l > 0.0f) ? ps_ref / l : 0.0f;
+    // The result tile goes out through shared memory: each thread puts its row's D/4 columns
+    // into a staging tile (the P tiles and the ring, idle once the last PV is done; rows padded
+    // by 16 bytes so that a warp's 32 rows hit distinct banks), then each warp copies whole rows
+    // with 512-byte coalesced accesses.  Stored straight from registers, every warp store would
+    // touch 32 rows a head-row stride apart.
+    constexpr int kStageStride = D + 4;
+    static_assert(128 * kStageStride * 4 <= L::offScale - L::offP, "the staging tile fits in the P tiles and the ring");
+    float* stage = reinterpret_cast<float*>(sm + L::offP);
+    float* my = stage + row * kStageStride + part * OCOLS;
+    volatile unsigned int* bcast = reinterpret_cast<volatile unsigned int*>(sm + L::offFlag + 8);
+    // After an abort the producer may still have copies landing in the ring: no staging then
+    // (the status word already reports the failure).  One decision for all 512 threads.
+    if (tid == 0) bcast[0] = *abort_flag ? 2u : (split ? atomicAdd(a.part_cnt + unit, 1u) : 0u);
+    tc::fence_proxy_async_smem();  // the tensor core's reads of these bytes come before our writes
+    named_bar(5, kSoftmaxThreads);
+    const unsigned int decision = bcast[0];
+    auto stage_o = [&](float scale) {
 #pragma unroll
       for (int c = 0; c < OCOLS / 32; ++c) {
         uint32_t o[32];
         tc::ld_32x32b_x32(tm_o + 32 * c, o);
         tc::wait_ld();
-        if (row_real) {
-          float* dst = dst_row + 32 * c;
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + e) = make_float4(
-                __uint_as_float(o[e]) * kOUnit * sc, __uint_as_float(o[e + 1]) * kOUnit * sc,
-                __uint_as_float(o[e + 2]) * kOUnit * sc, __uint_as_float(o[e + 3]) * kOUnit * sc);
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(my + 32 * c + e) =
+              make_float4(__uint_as_float(o[e]) * scale, __uint_as_float(o[e + 1]) * scale,
+                          __uint_as_float(o[e + 2]) * scale, __uint_as_float(o[e + 3]) * scale);
+      }
+    };
+    // warp w moves staged rows 8w .. 8w + 7 (those below n_rows) to dst0 + row * dst_stride
+    auto store_rows = [&](float* dst0, long long dst_stride, int n_rows) {
+#pragma unroll 1
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = warp * 8 + rr;
+        if (r < n_rows) {
+          const float4* src = reinterpret_cast<const float4*>(stage + r * kStageStride);
+          float4* dst = reinterpret_cast<float4*>(dst0 + r * dst_stride);
+#pragma unroll
+          for (int i = lane; i < D / 4; i += 32) dst[i] = src[i];
         }
+      }
+    };
+    float* out0 = a.out + (static_cast<long long>(q0) * Hq + h) * D;
+    const int n_real = min(128, T - q0);
+    if (decision == 2u) {
+      // aborted: nothing is written
+    } else if (!split) {
+      stage_o((started && l > 0.0f) ? ps_ref / l * kOUnit : 0.0f);
+      named_bar(5, kSoftmaxThreads);
+      store_rows(out0, static_cast<long long>(Hq) * D, n_real);
+    } else if (decision == 0u) {
+      // The unit's two segments meet here, and this one arrived first: it leaves its numerator
+      // n = O * 2^24 * ps_ref and its (m, l) in the workspace and publishes them.
+      const long long prow = static_cast<long long>(unit) * 128 + row;
+      stage_o(started ? ps_ref * kOUnit : 0.0f);
+      if (part == 0) {
+        a.part_ml[2 * prow] = m;
+        a.part_ml[2 * prow + 1] = l;
+      }
+      named_bar(5, kSoftmaxThreads);
+      store_rows(a.part + static_cast<long long>(unit) * 128 * D, D, 128);
+      __threadfence();
+      named_bar(5, kSoftmaxThreads);
+      if (tid == 0) {
+        __threadfence();
+        atomicExch(a.part_ready + unit, 1u);
       }
     } else {
-      // The unit's two segments meet here.  The first to arrive leaves its numerator
-      // n = O * 2^24 * ps_ref and its (m, l) in the workspace and publishes them; the second
-      // moves both onto the larger maximum M (s = 2^(m - M)) and writes
-      // out = (n1 s1 + n2 s2) / (l1 s1 + l2 s2).
-      volatile unsigned int* arrive_s = reinterpret_cast<volatile unsigned int*>(sm + L::offFlag + 8);
-      if (tid == 0) *arrive_s = atomicAdd(a.part_cnt + unit, 1u);
-      named_bar(5, kSoftmaxThreads);
-      const bool second = *arrive_s != 0u;
+      // The second segment: moves both numerators onto the larger maximum M (s = 2^(m - M)) and
+      // writes out = (n_lead s_lead + n_tail s_tail) / (l_lead s_lead + l_tail s_tail).  The
+      // terms are taken in lead, tail order whichever segment arrived second, and this segment's
+      // own n is rounded exactly as the first one's was, so the result does not depend on the
+      // order in which the two segments finished.
       const long long prow = static_cast<long long>(unit) * 128 + row;
-      float* num = a.part + prow * D + part * OCOLS;
+      if (tid == 0) wait_flag(a.part_ready + unit, a.status);
+      named_bar(5, kSoftmaxThreads);
+      __threadfence();
+#pragma unroll 1
+      for (int rr = 0; rr < 8; ++rr) {  // the first segment's numerator rows, coalesced, into the stage
+        const int r = warp * 8 + rr;
+        const float4* src = reinterpret_cast<const float4*>(a.part + (static_cast<long long>(unit) * 128 + r) * D);
+        float4* dst = reinterpret_cast<float4*>(stage + r * kStageStride);
+#pragma unroll
+        for (int i = lane; i < D / 4; i += 32) dst[i] = __ldcg(src + i);
+      }
+      const float m2 = __ldcg(a.part_ml + 2 * prow), l2 = __ldcg(a.part_ml + 2 * prow + 1);
+      named_bar(5, kSoftmaxThreads);
+      const float m_lead = tail_seg ? m2 : m, m_tail = tail_seg ? m : m2;
+      const float l_lead = tail_seg ? l2 : l, l_tail = tail_seg ? l : l2;
+      const float mx = fmaxf(m_lead, m_tail);
+      const float s_lead = (m_lead == -INFINITY) ? 0.0f : exp2f(m_lead - mx);
+      const float s_tail = (m_tail == -INFINITY) ? 0.0f : exp2f(m_tail - mx);
+      const float lt = __fadd_rn(__fmul_rn(l_lead, s_lead), __fmul_rn(l_tail, s_tail));
+      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
       const float own = started ? ps_ref * kOUnit : 0.0f;
-      if (!second) {
+      auto comb = [&](float o_bits_f, float n_other) {
+        const float n_own = __fmul_rn(o_bits_f, own);
+        const float nl = tail_seg ? n_other : n_own, ntl = tail_seg ? n_own : n_other;
+        return __fmul_rn(__fadd_rn(__fmul_rn(nl, s_lead), __fmul_rn(ntl, s_tail)), inv);
+      };
 #pragma unroll
-        for (int c = 0; c < OCOLS / 32; ++c) {
-          uint32_t o[32];
-          tc::ld_32x32b_x32(tm_o + 32 * c, o);
-          tc::wait_ld();
-          if (row_real) {
+      for (int c = 0; c < OCOLS / 32; ++c) {
+        uint32_t o[32];
+        tc::ld_32x32b_x32(tm_o + 32 * c, o);
+        tc::wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(num + 32 * c + e) =
-                  make_float4(__uint_as_float(o[e]) * own, __uint_as_float(o[e + 1]) * own,
-                              __uint_as_float(o[e + 2]) * own, __uint_as_float(o[e + 3]) * own);
-          }
-        }
-        if (row_real && part == 0) {
-          a.part_ml[2 * prow] = m;
-          a.part_ml[2 * prow + 1] = l;
-        }
-        __threadfence();
-        named_bar(5, kSoftmaxThreads);
-        if (tid == 0) {
-          __threadfence();
-          atomicExch(a.part_ready + unit, 1u);
-        }
-      } else {
-        if (tid == 0) wait_flag(a.part_ready + unit, a.status);
-        named_bar(5, kSoftmaxThreads);
-        __threadfence();
-        float m2 = -INFINITY, l2 = 0.0f;
-        if (row_real) {
-          m2 = __ldcg(a.part_ml + 2 * prow);
-          l2 = __ldcg(a.part_ml + 2 * prow + 1);
-        }
-        const float mx = fmaxf(m, m2);
-        const float s1 = (m == -INFINITY) ? 0.0f : exp2f(m - mx);
-        const float s2 = (m2 == -INFINITY) ? 0.0f : exp2f(m2 - mx);
-        const float lt = l * s1 + l2 * s2;
-        const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-        const float c1 = own * s1 * inv, c2 = s2 * inv;
-#pragma unroll
-        for (int c = 0; c < OCOLS / 32; ++c) {
-          uint32_t o[32];
-          tc::ld_32x32b_x32(tm_o + 32 * c, o);
-          tc::wait_ld();
-          if (row_real) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const float4 n2 = __ldcg(reinterpret_cast<const float4*>(num + 32 * c + e));
-              *reinterpret_cast<float4*>(dst_row + 32 * c + e) = make_float4(
-                  __uint_as_float(o[e]) * c1 + n2.x * c2, __uint_as_float(o[e + 1]) * c1 + n2.y * c2,
-                  __uint_as_float(o[e + 2]) * c1 + n2.z * c2, __uint_as_float(o[e + 3]) * c1 + n2.w * c2);
-            }
-          }
+        for (int e = 0; e < 32; e += 4) {
+          float4* sp = reinterpret_cast<float4*>(my + 32 * c + e);
+          const float4 n2 = *sp;
+          *sp = make_float4(comb(__uint_as_float(o[e]), n2.x), comb(__uint_as_float(o[e + 1]), n2.y),
+                            comb(__uint_as_float(o[e + 2]), n2.z), comb(__uint_as_float(o[e + 3]), n2.w));
         }
       }
+      named_bar(5, kSoftmaxThreads);
+      store_rows(out0, static_cast<long long>(Hq) * D, n_real);
     }
   } else if (warp == kMmaWarp) {
     // ================================================================ MMA issue (the whole warp
@@ -1345,14 +1376,15 @@ PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, 
 // key tiles plus a fixed start-up and epilogue cost, and a split segment also pays for writing
 // or reading the partial result.  Costs are in units of one key tile's time; the two constants
 // were fitted to the measured call time of a 2048-query chunk after 30720 keys (24 query /
-// 4 KV heads, head_dim 256) on 152 SMs at tail lengths 0, 16, 24, 32 and 48 tiles (within
-// 0.5% at each).
+// 4 KV heads, head_dim 256) on 152 SMs at tail lengths 0, 16, 24, 32, 40, 48 and 64 tiles
+// (within 0.5% at each), and agree with per-CTA timestamps (about 5 tiles of start-up and
+// epilogue per CTA).
 int prefill_split_tail(int n_tokens, int n_q_heads, int history_len, int n_sms) {
   if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 128 || n_sms <= 0) return 0;
   const int n_qt = (n_tokens + 127) / 128;
   const long long units = static_cast<long long>(n_qt) * n_q_heads;
   if (units > 16384) return 0;  // many waves: the last one is a small share of the call
-  constexpr double kCtaCost = 8.0, kCombineCost = 3.0;
+  constexpr double kCtaCost = 6.0, kCombineCost = 1.0;
   const int h_tiles = history_len / 128;
   auto tiles_of = [&](int qt) { return (history_len + std::min(128 * qt + 127, n_tokens - 1)) / 128 + 1; };
   std::vector<double> slots;

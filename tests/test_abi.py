@@ -70,7 +70,7 @@ def test_host_helpers_without_gpu():
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 100, 256) == (
         2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4)
     # the split choice (host-only simulation of the dispatch onto one CTA per SM)
-    assert k.kvq_prefill_split_tiles(2048, 24, 30720, 152) == 24
+    assert k.kvq_prefill_split_tiles(2048, 24, 30720, 152) == 32
     assert k.kvq_prefill_split_tiles(2048, 24, 100, 152) == 0       # no full tile of history
     assert k.kvq_prefill_split_tiles(1, 24, 30000, 152) == 128      # 24 one-tile-row units
     assert k.kvq_prefill_split_tiles(130, 6, 200, 152) == 0         # too few tiles to split
