@@ -754,8 +754,17 @@ def cpu_baseline_for_line(budget_s=12.0):
         if time.perf_counter() - t > budget_s or n >= 64:
             break
     dt = (time.perf_counter() - t) / n
+    # one core: a few query heads single-threaded, scaled to a full call (every head costs the same)
+    k1 = 4
+    t1 = time.perf_counter()
+    oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], units=units[:k1],
+                      n_threads=1)
+    dt1 = (time.perf_counter() - t1) * w["hq"] / k1
     return {"value": round(kv_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": "%d full decode_32k calls (all 24 query heads, FP64 Part A), %.1f s" % (n, dt * n)}
+            "sample": "%d full decode_32k calls (all 24 query heads, FP64 Part A), %.1f s" % (n, dt * n),
+            "one_core": {"value": round(kv_bytes / dt1 / 1e9, 4), "unit": "GB/s", "cores": 1,
+                         "sample": "%d of %d query heads of one decode_32k call, single-threaded, scaled to the "
+                                   "full call" % (k1, w["hq"])}}
 
 
 def main():
