@@ -322,10 +322,12 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
   const long long tile = static_cast<long long>(kvh) * a.n_kv_tiles + j;
   uint8_t* kdst = a.kw + tile * (D / 64) * kPieceBytes;
   uint8_t* vdst = a.vw + tile * (D / 64) * kPieceBytes;
-  // K: item i = (16-dim chunk c16 = i / 128, key n = i % 128); one key's chunk is 16 bytes of
-  // the [page][head][D/16][slot][16] cache block.
+  // K: item i = (key n, 16-dim chunk c16); one key's chunk is 16 bytes of the
+  // [page][head][D/16][slot][16] cache block.  The four chunks that fill one 128-byte row of a
+  // piece (c16 = 4a .. 4a + 3 for key n) go to four adjacent lanes, so a warp's stores cover
+  // whole rows (8 keys x 128 bytes) and its loads four 128-byte runs.
   for (int i = tid; i < 128 * (D / 16); i += 256) {
-    const int n = i & 127, c16 = i >> 7;
+    const int n = (i >> 2) & 127, c16 = ((i >> 9) << 2) | (i & 3);
     const int page = page_s[n >> 4];
     int4 raw = make_int4(0, 0, 0, 0);
     if (page >= 0 && 128 * j + n < n_keys)
@@ -338,11 +340,13 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(PrefillArgs a) {
     sts128(piece + tc::sw128_off(n, cc), c0);  // global stores (same helper, generic address)
     sts128(piece + tc::sw128_off(n, cc + 1), c1);
   }
-  // V: item i = (page pl = i / D, dim d = i % D); the 16 keys of page pl for dim d are 16
-  // bytes of the [page][head][D][slot] cache block.  Keys past the context carry whatever the
-  // slot holds: their P codes are zero, and int8 codes are finite, so they add nothing.
+  // V: item i = (dim d, page pl); the 16 keys of page pl for dim d are 16 bytes of the
+  // [page][head][D][slot] cache block.  The four pages that fill one 128-byte row of a piece
+  // (pl = 4b .. 4b + 3 for dim d) go to four adjacent lanes.  Keys past the context carry
+  // whatever the slot holds: their P codes are zero, and int8 codes are finite, so they add
+  // nothing.
   for (int i = tid; i < 8 * D; i += 256) {
-    const int d = i % D, pl = i / D;
+    const int pl = ((i / (4 * D)) << 2) | (i & 3), d = (i >> 2) % D;
     const int page = page_s[pl];
     int4 raw = make_int4(0, 0, 0, 0);
     if (page >= 0)
