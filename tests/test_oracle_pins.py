@@ -440,6 +440,34 @@ def test_int8_emul_tiles_are_aligned_at_absolute_multiples_of_128(oracle):
     assert np.abs(b96 - a).max() > 1e-4
 
 
+def test_int8_emul_tile_order_does_not_change_the_codes(oracle):
+    # Rows that see every history key attend over the same (key, value) set whichever order
+    # the history's 128-key tiles come in.  Each tile's P codes are decided from the tile
+    # alone (relative to its own maximum score), so exchanging two whole tiles leaves every
+    # code, and the output up to double rounding, unchanged.  Decided relative to the
+    # running maximum instead, the fp32 codes would differ in near-tie cases (a rounding flip
+    # moves a row by ~1e-3 of the output RMS), so this pins the decision basis.
+    rng = np.random.default_rng(17)
+    hist, T, H, G, D = 512, 64, 2, 4, 128
+    ctx = hist + T
+    k = W.normal_bf16(rng, (ctx, H, D), 0.01)
+    v = W.normal_bf16(rng, (ctx, H, D))
+    q = W.normal_bf16(rng, (T, H * G, D))
+    perm = np.arange(ctx)
+    perm[0:128], perm[256:384] = np.arange(256, 384), np.arange(0, 128)  # tiles 0 and 2 exchanged
+    c1, table = make_cache(oracle, k, v)
+    c2, _ = make_cache(oracle, k[perm], v[perm])
+    a = oracle.prefill_int8_emul(c1, q, hist, table, 0.3)
+    b = oracle.prefill_int8_emul(c2, q, hist, table, 0.3)
+    rms = np.sqrt((a ** 2).mean())
+    assert np.abs(a - b).max() <= 1e-12 * rms
+    # and the exchange is real: a row at position 300 sees only part of tile 2, so its
+    # visible key set, and its output, change
+    a1 = oracle.prefill_int8_emul(c1, q[:1], 300, table, 0.3)
+    b1 = oracle.prefill_int8_emul(c2, q[:1], 300, table, 0.3)
+    assert np.abs(a1 - b1).max() > 1e-3 * rms
+
+
 def test_int8_emul_error_within_p_quantisation_bound(oracle):
     # Q chosen exactly representable by its codes (amax = 127/128, values on the 2^-7
     # grid), so the scores of Part A and Part B agree; the only difference is the
