@@ -78,8 +78,6 @@ struct PrefillSmem {
   static constexpr int offTmem = offBar + 16;  // TMEM base address
   static constexpr int kBytes = offTmem + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
-  static constexpr uint32_t kTmemCols = (D == 256) ? 512 : 256;
-  static constexpr uint32_t kOCol = (D == 256) ? 256 : 128;  // O after S (128 columns)
 };
 
 constexpr float kLog2eP = 1.44269504088896341f;
@@ -96,18 +94,19 @@ __device__ __forceinline__ f2 mk2(float x, float y) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(x), "f"(y));
   return r;
 }
+// one half of a pair: the unpacking mov names both halves and the other one is dropped
+#pragma nv_diag_suppress 550
 __device__ __forceinline__ float lo2(f2 a) {
   float x, y;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(a.v));
-  (void)y;
   return x;
 }
 __device__ __forceinline__ float hi2(f2 a) {
   float x, y;
   asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(a.v));
-  (void)x;
   return y;
 }
+#pragma nv_diag_default 550
 __device__ __forceinline__ f2 add2(f2 a, f2 b) {
   f2 r;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
