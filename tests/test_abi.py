@@ -77,6 +77,18 @@ def test_host_helpers_without_gpu():
     assert k.kvq_prefill_split_tiles(4096, 24, 4096, 152) == 0      # five waves: the split does not pay
     assert k.kvq_prefill_split_tiles(0, 24, 30720, 152) == 0
     assert k.kvq_prefill_split_tiles(2048, 24, 30720, 0) == 0
+    # the kernel's preconditions for any split it is given: a full tile of history, and a lead
+    # segment of at least one tile in every unit (r < the shortest unit's tile count)
+    import numpy as np
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        T = int(rng.integers(1, 9000))
+        hq = int(rng.choice([1, 4, 6, 8, 12, 24, 32, 64]))
+        hist = int(rng.integers(0, 140000))
+        sms = int(rng.choice([1, 8, 132, 148, 152]))
+        r = k.kvq_prefill_split_tiles(T, hq, hist, sms)
+        shortest = (hist + min(127, T - 1)) // 128 + 1
+        assert r == 0 or (hist >= 128 and 1 <= r < shortest), (T, hq, hist, sms, r)
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, -1, 256) == 0
     # first chunk: fp16 Q (2 bytes per element) | Q scales | fp16 K and V pieces of the chunk's tiles | scales
     tiles1 = 4 * ((4096 + 127) // 128)

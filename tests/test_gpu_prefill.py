@@ -1,6 +1,6 @@
 """kvq_attn_prefill_int8 on the GPU against the oracle's int8 emulation.
 
-Gates (the benchmark spec): Q codes and the int32 QK score tiles bit-exact; outputs within 2e-3
+Gates: Q codes and the int32 QK score tiles bit-exact; outputs within 2e-3
 normalised max-abs of the int8-emulated output.  The P-code decisions are taken with the
 same fp32 operations on both sides, so the expected difference is only the fp32 vs double
 accumulation of l and of the numerator (~1e-6); DESIGN_TOL = 1e-4 catches regressions.
