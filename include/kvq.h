@@ -306,10 +306,10 @@ int kvq_decode_step_int8kv(const kvq_cache* cache, const void* k_new, const void
  * history_len keys: the int8 Q codes and their fp32 scales, and the K/V codes of every
  * (KV head, 128-key tile) of the history_len + n_tokens keys widened once to fp16 in the
  * attention kernel's shared-memory operand layout (2 * 2 * head_dim bytes per key and KV
- * head), with the tiles' key and value scales.  With history_len >= 128, also room for the
- * key-range split (kvq_prefill_split_tiles): per unit of 128 query rows and one query head,
- * 128 rows of head_dim + 2 floats and two counters.  0 if an argument is not positive
- * (history_len may be 0). */
+ * head), with the tiles' key and value scales.  With history_len >= 128 and at most 16384
+ * units of 128 query rows and one query head, also room for the key-range split
+ * (kvq_prefill_split_tiles): per unit, 128 rows of head_dim + 2 floats and two counters (more
+ * units never split).  0 if an argument is not positive (history_len may be 0). */
 size_t kvq_prefill_workspace_bytes(int32_t n_tokens, int32_t n_q_heads, int32_t n_kv_heads,
                                    int32_t history_len, int32_t head_dim);
 

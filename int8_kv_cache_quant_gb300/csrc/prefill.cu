@@ -1321,6 +1321,10 @@ __global__ void __launch_bounds__(128, 1) prefill_qk_debug_kernel(PrefillArgs a)
 // a 1024-byte boundary of the workspace).
 static long long round1k(long long x) { return (x + 1023) / 1024 * 1024; }
 
+// Above this many units (128 query rows x one query head) the last wave is a small share of the
+// call and the key range is never split, so no workspace is reserved for it either.
+constexpr long long kMaxSplitUnits = 16384;
+
 PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, int history_len, int head_dim,
                                    int q_elem_bytes) {
   PrefillWorkspace w{};
@@ -1332,9 +1336,9 @@ PrefillWorkspace prefill_workspace(int n_tokens, int n_q_heads, int n_kv_heads, 
   w.off_skw = w.off_vw + tiles * 128 * head_dim * 2;
   w.off_svw = w.off_skw + tiles * 128 * 4;
   w.bytes = w.off_svw + tiles * 128 * 4;
-  w.can_split = q_elem_bytes == 1 && history_len >= 128;
+  const long long units = static_cast<long long>((n_tokens + 127) / 128) * n_q_heads;
+  w.can_split = q_elem_bytes == 1 && history_len >= 128 && units <= kMaxSplitUnits;
   if (w.can_split) {
-    const long long units = static_cast<long long>((n_tokens + 127) / 128) * n_q_heads;
     w.off_part = round1k(w.bytes);
     w.off_part_ml = w.off_part + round1k(units * 128 * head_dim * 4);
     w.off_part_flags = w.off_part_ml + round1k(units * 128 * 2 * 4);
@@ -1355,7 +1359,7 @@ int prefill_split_tail(int n_tokens, int n_q_heads, int history_len, int n_sms) 
   if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 128 || n_sms <= 0) return 0;
   const int n_qt = (n_tokens + 127) / 128;
   const long long units = static_cast<long long>(n_qt) * n_q_heads;
-  if (units > 16384) return 0;  // many waves: the last one is a small share of the call
+  if (units > kMaxSplitUnits) return 0;
   constexpr double kCtaCost = 6.0, kCombineCost = 1.0;
   const int h_tiles = history_len / 128;
   auto tiles_of = [&](int qt) { return (history_len + std::min(128 * qt + 127, n_tokens - 1)) / 128 + 1; };

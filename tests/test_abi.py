@@ -69,6 +69,11 @@ def test_host_helpers_without_gpu():
     tiles = 4 * ((100 + 2048 + 127) // 128)  # history below one tile: no split region
     assert k.kvq_prefill_workspace_bytes(2048, 24, 4, 100, 256) == (
         2048 * 24 * 256 + 2048 * 24 * 4 + 2 * tiles * 128 * 256 * 2 + 2 * tiles * 128 * 4)
+    # more than 16384 units (here 512 query tiles x 64 heads) never split: no split region
+    tiles = 8 * ((4096 + 65536 + 127) // 128)
+    assert k.kvq_prefill_workspace_bytes(65536, 64, 8, 4096, 128) == (
+        65536 * 64 * 128 + 65536 * 64 * 4 + 2 * tiles * 128 * 128 * 2 + 2 * tiles * 128 * 4)
+    assert k.kvq_prefill_split_tiles(65536, 64, 4096, 152) == 0
     # the split choice (host-only simulation of the dispatch onto one CTA per SM)
     assert k.kvq_prefill_split_tiles(2048, 24, 30720, 152) == 32
     assert k.kvq_prefill_split_tiles(2048, 24, 100, 152) == 0       # no full tile of history
