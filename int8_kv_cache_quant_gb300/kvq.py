@@ -101,7 +101,24 @@ def _stream(stream):
 
 
 def _p(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    """Device pointer of a CUDA tensor.  Anything else is refused before any launch: a kernel
+    handed a host pointer would fault."""
+    if t is None:
+        return None
+    if t.device.type != "cuda":
+        raise ValueError("the library takes CUDA tensors here (got a %s tensor)" % t.device.type)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _hp(t):
+    """Pointer for the decode calls' zero-copy arguments (q, k_new, v_new, out): a CUDA tensor,
+    or page-locked host memory mapped into the device's address space."""
+    if t is None:
+        return None
+    if t.device.type != "cuda" and not kvq_device_accessible(t):
+        raise ValueError("a host tensor must be page-locked memory mapped into the device's address space "
+                         "(e.g. tensor.pin_memory())")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _check(fn, status):
@@ -240,8 +257,8 @@ def kvq_attn_decode_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = cache.struct()
     _check("kvq_attn_decode_int8kv", lib().kvq_attn_decode_int8kv(
-        ctypes.byref(c), _p(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
-        int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
+        ctypes.byref(c), _hp(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), float(softmax_scale), _hp(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
     return out
 
@@ -262,8 +279,8 @@ def kvq_attn_verify_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = cache.struct()
     _check("kvq_attn_verify_int8kv", lib().kvq_attn_verify_int8kv(
-        ctypes.byref(c), _p(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
-        int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
+        ctypes.byref(c), _hp(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), float(softmax_scale), _hp(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
     return out
 
@@ -292,8 +309,8 @@ def kvq_decode_step_int8kv(cache, k_new, v_new, q, block_table, ctx_lens, max_ct
     wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     c = cache.struct()
     _check("kvq_decode_step_int8kv", lib().kvq_decode_step_int8kv(
-        ctypes.byref(c), _p(k_new), _p(v_new), _p(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]),
-        _p(ctx_lens), int(max_ctx), float(softmax_scale), _p(out), _p(workspace), wbytes, ctypes.byref(o),
+        ctypes.byref(c), _hp(k_new), _hp(v_new), _hp(q), B, nq, Hq, _p(block_table), int(block_table.shape[1]),
+        _p(ctx_lens), int(max_ctx), float(softmax_scale), _hp(out), _p(workspace), wbytes, ctypes.byref(o),
         _stream(stream)))
     return ret
 

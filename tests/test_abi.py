@@ -141,3 +141,23 @@ def test_invalid_arguments_rejected_before_launch():
     for bad in (0.0, -0.5, float("inf"), float("nan")):
         assert L.kvq_attn_prefill_int8(ctypes.byref(c), 16, 16, 8, 0, 16, 1, bad, 16, 16, 1 << 30,
                                        None) == 1
+
+
+def test_host_tensors_refused_before_launch():
+    import pytest
+    # a kernel handed a pageable host pointer would fault, so the binding refuses CPU tensors
+    # (outside the decode calls' zero-copy arguments, which must be mapped page-locked memory)
+    import numpy as np
+    import torch
+
+    import int8_kv_cache_quant_gb300 as k
+    cache = k.KVCache(4, 1, 128, device="cpu")
+    rows = torch.zeros((2, 1, 128), dtype=torch.bfloat16)
+    idx = torch.zeros(2, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        k.kvq_quant_write(cache, rows, rows, idx, idx, torch.zeros((1, 4), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        k.kvq.kvq_attn_prefill_int8(cache, rows.view(2, 1, 128), 0, torch.zeros(4, dtype=torch.int32), 0.1,
+                                    out=torch.zeros((2, 1, 128)), workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+    # a pageable tensor is not device-accessible
+    assert not k.kvq_device_accessible(torch.from_numpy(np.zeros(16, np.float32)))
