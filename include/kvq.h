@@ -336,6 +336,12 @@ int32_t kvq_prefill_split_tiles(int32_t n_tokens, int32_t n_q_heads, int32_t his
  *   w = p * v_scale[t]; per (query row, KVQ_PV_TILE keys at absolute multiples of 128):
  *   ps = max w / 127, c = rint(w / ps) in [0, 127];
  *   out = (sum over tiles of ps * sum_t c * v_code[t]) / l.
+ * The running maximum cancels in w / ps, so the codes are decided in fp32 relative to the
+ * tile's own maximum score (exp2 by a fixed polynomial, the same steps as the reference
+ * implementation's); the running maximum only rescales ps and the tile's sum of p.  Each
+ * tile's codes therefore depend on that tile alone, and the call may split a unit's key range
+ * between two CTAs (kvq_prefill_split_tiles) without changing any code; the result does not
+ * depend on which CTA finishes first, and the workspace's contents on entry do not matter.
  * The integer contractions run on the tensor cores with int8 codes widened to
  * integer-valued fp16 (exact: every partial sum is an integer below 2^24).  The chunk's
  * own K/V must already be in the cache (kvq_quant_write).
