@@ -337,8 +337,8 @@ int32_t kvq_prefill_split_tiles(int32_t n_tokens, int32_t n_q_heads, int32_t his
  *   ps = max w / 127, c = rint(w / ps) in [0, 127];
  *   out = (sum over tiles of ps * sum_t c * v_code[t]) / l.
  * The running maximum cancels in w / ps, so the codes are decided in fp32 relative to the
- * tile's own maximum score (exp2 by a fixed polynomial, the same steps as the reference
- * implementation's); the running maximum only rescales ps and the tile's sum of p.  Each
+ * tile's own maximum score (exp2 by a fixed polynomial, so that a CPU implementation can
+ * reproduce every decision); the running maximum only rescales ps and the tile's sum of p.  Each
  * tile's codes therefore depend on that tile alone, and the call may split a unit's key range
  * between two CTAs (kvq_prefill_split_tiles) without changing any code; the result does not
  * depend on which CTA finishes first, and the workspace's contents on entry do not matter.
