@@ -534,10 +534,12 @@ def _extra_decode_b64(kvq, W, bf16, i32, timed, dev, reps, hbm):
         kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out=out, workspace=ws)
     ms = timed(step, reps)
     ms_unfused = timed(step_unfused, reps)
+    ms_write = timed(lambda: kvq.kvq_quant_write(cache, kn, vn, ns, npos, bt), reps)
     kvb = int(w["ctx_lens"].astype(np.int64).sum()) * w["hkv"] * (2 * D + 8)
     res["decode_b64"] = {"us_per_step": round(ms * 1e3, 2), "kv_bytes": kvb, "kv_GBps": round(kvb / ms / 1e6, 1),
                          "frac_of_hbm_peak": round(kvb / ms / 1e6 / hbm, 4),
                          "us_per_step_unfused": round(ms_unfused * 1e3, 2),
+                         "us_quant_write": round(ms_write * 1e3, 2),
                          "step": "kvq_decode_step_int8kv: 64 new tokens written inside decode stage 1 (split route)"}
     return res
 
