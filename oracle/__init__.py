@@ -48,6 +48,7 @@ def _load():
         lib.oracle_prefill_first_f64.argtypes = [vp, vp, vp, i32, i32, i32, i32, f64, vp, i32, vp, i32]
         lib.oracle_prefill_ref_f64.argtypes = [vp, vp, i32, i32, i32, vp, f64, vp, i32, vp, i32]
         lib.oracle_prefill_qk_int32.argtypes = [vp, i32, i32, vp, vp, i32, i32, i32, i32, i32, vp]
+        lib.oracle_prefill_qdeq_f64.argtypes = [vp, vp, i32, i32, i32, vp, f64, i32, vp, i32, vp, vp, vp, i32]
         lib.oracle_prefill_int8_emul.argtypes = [vp, vp, i32, i32, i32, vp, ctypes.c_float, i32,
                                                  vp, i32, vp, vp, vp, i32]
         lib.oracle_exp2_det.restype = ctypes.c_float
@@ -207,6 +208,23 @@ def prefill_ref_f64(cache, q, history, bt_row, scale, units=None, n_threads=0):
     _load().oracle_prefill_ref_f64(ctypes.byref(s), _ptr(q), T, Hq, int(history), _ptr(bt),
                                    float(scale), _ptr(u), nu, _ptr(out), n_threads)
     return out
+
+
+def prefill_qdeq_f64(cache, q, history, bt_row, scale, pv_tile=PV_TILE, units=None, n_threads=0):
+    """The method's prefill with exact softmax: Q quantised to its codes and dequantised,
+    FP64 attention, no P quantisation.  Returns (out, bound, mag), each float64 [T][Hq][D] (or
+    [n_units][D]): bound is the largest change the per-tile P re-quantisation can make to each
+    output element, mag = sum_t p_t |v^_t| / l (the scale of fp32 rounding effects)."""
+    q = _c(q, np.uint16)
+    bt = _c(bt_row, np.int32)
+    T, Hq, D = q.shape
+    u, nu = _units_arg(units)
+    shape = (T, Hq, D) if u is None else (nu, D)
+    out, bound, mag = (np.zeros(shape, np.float64) for _ in range(3))
+    s = cache.struct()
+    _load().oracle_prefill_qdeq_f64(ctypes.byref(s), _ptr(q), T, Hq, int(history), _ptr(bt), float(scale),
+                                    int(pv_tile), _ptr(u), nu, _ptr(out), _ptr(bound), _ptr(mag), n_threads)
+    return out, bound, mag
 
 
 def prefill_first_f64(q, k, v, scale, units=None, n_threads=0):

@@ -548,6 +548,80 @@ void oracle_prefill_ref_f64(const oracle_cache* cache, const uint16_t* q, int32_
   });
 }
 
+// The method's prefill with exact softmax arithmetic ([DCU] §1.3, §3.3; §2.1 for Q): Q is
+// quantised per (token, query head) by B1 and enters as its dequantised value
+// q^ = q_code * sQ; the attention is then the plain definition in double,
+//   s_t = scale * (q^ . k^_t),  p_t = exp(s_t - max s),  l = sum_t p_t,
+//   out[d] = sum_t p_t v^_t[d] / l,
+// with no P quantisation.  Beside it, per output element, the largest change that the
+// per-tile P re-quantisation of the method can make to it:
+//   w_t = p_t * sV_t;  per tile of pv_tile keys at absolute multiples of pv_tile,
+//   ps_j = max_{t in tile} w_t / 127;  the code of w_t is rint(w_t / ps_j), so ps_j * code
+//   differs from w_t by at most ps_j / 2, and by exactly w_t when w_t < ps_j / 2 (code 0);
+//   the numerator multiplies that difference by the integer v8_t[d]:
+//   bound[d] = sum_t min(w_t, ps_{j(t)} / 2) * |v8_t[d]| / l,
+// and mag[d] = sum_t p_t |v^_t[d]| / l, the scale of the output's own rounding errors (an
+// implementation whose weights carry a relative error e moves the output by at most about
+// e * mag[d]).  bound and mag may be null.
+void oracle_prefill_qdeq_f64(const oracle_cache* cache, const uint16_t* q, int32_t n_tokens, int32_t n_q_heads,
+                             int32_t history, const int32_t* bt_row, double scale, int32_t pv_tile,
+                             const int64_t* units, int32_t n_units, double* out, double* bound, double* mag,
+                             int32_t n_threads) {
+  const oracle_cache& c = *cache;
+  const int D = c.head_dim, G = n_q_heads / c.n_kv_heads;
+  int64_t n = units ? n_units : static_cast<int64_t>(n_tokens) * n_q_heads;
+  parallel_for(n, n_threads, [&](int64_t j) {
+    int64_t u = unit_at(units, j);
+    int i = static_cast<int>(u / n_q_heads), h = static_cast<int>(u % n_q_heads);
+    int kvh = h / G;
+    std::vector<int8_t> q8(D);
+    float sq;
+    quant_row(q + u * D, D, q8.data(), &sq);
+    std::vector<double> qd(D);
+    for (int d = 0; d < D; ++d) qd[d] = static_cast<double>(q8[d]) * static_cast<double>(sq);
+    const int nk = history + i + 1;
+    std::vector<double> s(nk), kd(D), vd(D);
+    double m = -INFINITY;
+    for (int t = 0; t < nk; ++t) {
+      load_kv(c, bt_row, t, kvh, kd, vd);
+      double dot = 0.0;
+      for (int d = 0; d < D; ++d) dot += qd[d] * kd[d];
+      s[t] = scale * dot;
+      m = std::max(m, s[t]);
+    }
+    double l = 0.0;
+    std::vector<double> o(D, 0.0), b(D, 0.0), a(D, 0.0), p(pv_tile), w(pv_tile);
+    for (int t0 = 0; t0 < nk; t0 += pv_tile) {
+      const int t1 = std::min(nk, t0 + pv_tile);
+      double wmax = 0.0;
+      for (int t = t0; t < t1; ++t) {
+        Slot sl = locate(c, bt_row, t);
+        p[t - t0] = std::exp(s[t] - m);
+        w[t - t0] = p[t - t0] * c.v_scale[scale_offset(c, sl.page, kvh, sl.slot)];
+        wmax = std::max(wmax, w[t - t0]);
+      }
+      const double half_ps = (wmax / 127.0) / 2.0;
+      for (int t = t0; t < t1; ++t) {
+        Slot sl = locate(c, bt_row, t);
+        const double sv = c.v_scale[scale_offset(c, sl.page, kvh, sl.slot)];
+        const double e = std::min(w[t - t0], half_ps);
+        l += p[t - t0];
+        for (int d = 0; d < D; ++d) {
+          const double v8 = c.v[v_offset(c, sl.page, kvh, d, sl.slot)];
+          o[d] += p[t - t0] * (v8 * sv);
+          a[d] += p[t - t0] * std::fabs(v8 * sv);
+          b[d] += e * std::fabs(v8);
+        }
+      }
+    }
+    for (int d = 0; d < D; ++d) {
+      out[j * D + d] = o[d] / l;
+      if (bound) bound[j * D + d] = b[d] / l;
+      if (mag) mag[j * D + d] = a[d] / l;
+    }
+  });
+}
+
 // B2: exact integer QK for one window, no mask: s_out[r][j] = sum_d q8[q0+r][h][d] *
 // k8[k0+j][h/G][d] for r < nq, j < nk; rows at or past n_tokens give 0.
 void oracle_prefill_qk_int32(const int8_t* q_codes, int32_t n_tokens, int32_t n_q_heads,

@@ -508,6 +508,88 @@ def test_int8_emul_error_within_p_quantisation_bound(oracle):
     assert np.abs(b - a).max() / rms < 0.1
 
 
+# --------------------------------------------------------------------------- prefill, Q dequantised (FP64)
+
+def test_qdeq_equals_part_a_when_q_is_exactly_its_codes(oracle):
+    # Q rows on the 2^-7 grid with amax 127/128 are exactly code * scale (scale = 1/128), so
+    # the Q-dequantised reference must equal Part A over the bf16 Q.
+    rng = np.random.default_rng(21)
+    hist, T, H, D, Hq = 200, 20, 2, 128, 4
+    k = W.normal_bf16(rng, (hist + T, H, D))
+    v = W.normal_bf16(rng, (hist + T, H, D))
+    c, table = make_cache(oracle, k, v)
+    qi = rng.integers(-127, 128, size=(T, Hq, D))
+    qi[:, :, 3] = -127
+    q = bf16(qi.astype(np.float32) / 128.0)
+    a = oracle.prefill_ref_f64(c, q, hist, table, 0.2)
+    b, bound, mag = oracle.prefill_qdeq_f64(c, q, hist, table, 0.2)
+    assert np.abs(a - b).max() <= 1e-12 * np.abs(a).max()
+    # mag bounds |out| (triangle inequality), bound is positive and far below mag
+    assert np.all(np.abs(b) <= mag * (1 + 1e-12))
+    assert np.all(bound > 0) and np.all(bound <= mag)
+
+
+def test_qdeq_single_key_closed_form(oracle):
+    # Row 0 of a chunk with no history sees key 0 alone: p = 1, l = 1, out = v^_0, and the
+    # bound is (sV / 127) / 2 * |v8_0| = |v^_0| / 254, mag = |v^_0|.
+    rng = np.random.default_rng(22)
+    D = 256
+    k = W.normal_bf16(rng, (3, 1, D))
+    v = W.normal_bf16(rng, (3, 1, D))
+    c, table = make_cache(oracle, k, v)
+    q = W.normal_bf16(rng, (3, 2, D))
+    out, bound, mag = oracle.prefill_qdeq_f64(c, q, 0, table, 1 / 16)
+    vc, vs = oracle.quant_rows(v)
+    v0 = vc[0, 0].astype(np.float64) * np.float64(vs[0, 0])
+    for h in range(2):
+        assert np.array_equal(out[0, h], v0)
+        assert np.allclose(bound[0, h], np.abs(v0) / 254, rtol=1e-15, atol=0)
+        assert np.array_equal(mag[0, h], np.abs(v0))
+
+
+def test_qdeq_bound_is_per_tile_at_absolute_multiples_of_128(oracle):
+    # Zero K rows give every key the same score (p = 1, l = n).  Keys of tile 0 (positions
+    # 0..127) get V rows of amax 1 (sV = 1/127), keys of tile 1 amax 64: each tile's P scale is
+    # its own sV / 127, every weight of a tile is 127 of its P scale (min(w, ps / 2) = ps / 2), so
+    # bound = (sum_tiles sV_tile * sum_{t in tile} |v8_t|) / (254 n).  One scale for the whole
+    # row, or tiles counted from the row's first key, would give another number.
+    rng = np.random.default_rng(23)
+    hist, T, D = 150, 2, 128
+    n = hist + T
+    k = np.zeros((n, 1, D), np.uint16)
+    vf = rng.uniform(-1, 1, size=(n, 1, D)).astype(np.float32)
+    vf[:, 0, 0] = 1.0
+    vf[128:] *= 64.0
+    v = bf16(vf)
+    c, table = make_cache(oracle, k, v)
+    q = W.normal_bf16(rng, (T, 1, D))
+    out, bound, _ = oracle.prefill_qdeq_f64(c, q, hist, table, 0.1)
+    vc, vs = oracle.quant_rows(v)
+    assert vs[0, 0] == np.float32(1 / 127) and vs[130, 0] == np.float32(64 / 127)
+    for i in range(T):
+        nk = hist + i + 1
+        expect = (np.float64(vs[0, 0]) * np.abs(vc[:128, 0].astype(np.float64)).sum(axis=0) +
+                  np.float64(vs[128, 0]) * np.abs(vc[128:nk, 0].astype(np.float64)).sum(axis=0)) / (254 * nk)
+        assert np.allclose(bound[i, 0], expect, rtol=1e-12, atol=0)
+        vhat = vc[:nk, 0].astype(np.float64) * vs[:nk, 0, None].astype(np.float64)
+        assert np.allclose(out[i, 0], vhat.mean(axis=0), rtol=1e-12, atol=1e-15)
+
+
+def test_int8_emul_within_the_qdeq_bound(oracle):
+    # Part B differs from the Q-dequantised reference only by the per-tile P rounding (and
+    # fp32 arithmetic): every element within bound + 2e-5 * mag, on N(0,1) inputs with a ragged
+    # last tile, and on K outliers with a large softmax scale (tiles with very different P
+    # scales).
+    for seed, hist, T, outl, scale in ((24, 300, 40, 0.0, 1 / np.sqrt(128)), (25, 900, 20, 0.02, 0.4)):
+        w, c = _prefill_case(oracle, seed, history=hist, T=T, hq=4, hkv=2, d=128, k_outlier_p=outl)
+        emul = oracle.prefill_int8_emul(c, w["q"], hist, w["block_table"][0], scale)
+        ref, bound, mag = oracle.prefill_qdeq_f64(c, w["q"], hist, w["block_table"][0], scale)
+        excess = np.abs(emul - ref) - (bound + 2e-5 * mag)
+        assert excess.max() <= 0, excess.max()
+        # the bound is not vacuous: the method's error reaches a visible share of it
+        assert (np.abs(emul - ref) / bound).max() > 0.1
+
+
 def test_int8_emul_uniform_v_close_to_v(oracle):
     rng = np.random.default_rng(10)
     hist, T, D = 140, 12, 128
