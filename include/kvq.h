@@ -185,7 +185,9 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
  * 1024-key context is faster ([DOT4]'s table switches at 2048 keys for a smaller GPU).
  *   q          : device bf16 [batch][n_q_heads][head_dim]
  *   block_table: device int32 [batch][max_blocks_per_seq]
- *   ctx_lens   : device int32 [batch], each in [0, max_ctx]; ctx 0 gives zeros
+ *   ctx_lens   : device int32 [batch], each in [0, max_ctx]; ctx 0 gives zeros; a ctx above
+ *                max_ctx (or above what the sequence's block-table row maps) is clamped to it on
+ *                both routes and sets KVQ_DEV_BAD_POS
  *   max_ctx    : host upper bound of ctx_lens (sizes the grid and the workspace)
  *   out        : device fp32 [batch][n_q_heads][head_dim]
  *   workspace  : device, >= kvq_decode_workspace_bytes(...), 16-byte aligned; its
@@ -224,11 +226,13 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
  *   Same arguments and results as kvq_attn_decode_int8kv, without workspace / workspace_bytes:
  *   the split-K partials live in a fixed scratch array of KVQ_NOALLOC_SCRATCH_BYTES bytes
  *   inside the library, which every GPU that loads the library holds until the process exits.
- *   The call allocates nothing.  A problem whose split route needs more than
- *   KVQ_NOALLOC_SCRATCH_BYTES (see kvq_decode_workspace_bytes) is rejected with
- *   KVQ_ERR_WORKSPACE before any launch.
+ *   The call allocates nothing.  A problem whose partials, at the split size the call takes
+ *   (kvq_decode_auto_split_rows for this GPU unless opts sets split_rows), need more than
+ *   KVQ_NOALLOC_SCRATCH_BYTES is rejected with KVQ_ERR_WORKSPACE before any launch.
  *   The first call on a device looks up the scratch array's device address for that device
- *   (a one-time host-side set-up); make that first call before any stream capture.
+ *   (a one-time host-side set-up); make that first call before any stream capture.  The
+ *   address, like the device status word's, stays valid for the life of the device's context:
+ *   after a cudaDeviceReset the library must be unloaded and loaded again.
  *   All calls share the one array: calls that overlap on the GPU (different streams, or
  *   different host threads on one device) race and corrupt each other's results.  The
  *   array keeps the last call's contents; every call writes the partials it reads, so
@@ -434,24 +438,60 @@ int kvq_attn_prefill_first_bf16(const kvq_cache* cache, const void* q, const voi
                                 size_t workspace_bytes, void* stream);
 
 /*
- * Test entry points of the prefill path (same device code as kvq_attn_prefill_int8).
+ * Test entry points of the prefill path (the same device code as kvq_attn_prefill_int8).
  * kvq_debug_prefill_q_codes: the per-(token, query head) Q quantisation step alone.
  *   q: device bf16 [n_tokens][n_q_heads][head_dim]; q_codes: device int8, same shape;
  *   q_scales: device fp32 [n_tokens][n_q_heads].
- * kvq_debug_prefill_qk_int32: the tensor-core QK tile alone, no mask: for query rows
- *   q0 .. q0+127 of query head q_head and keys k0 .. k0+nk-1 (k0 and nk multiples of
- *   128) writes the exact integer S[row][key] to s_out (device int32 [128][nk]); rows
- *   at or past n_tokens are written as 0.
- *   q_codes: device int8 [n_tokens][n_q_heads][head_dim] (from kvq_debug_prefill_q_codes).
+ * kvq_debug_prefill_qk_int32: kvq_attn_prefill_int8_qcodes (the whole call: the widening pre-pass
+ *   and the production attention kernel, writing `out`), compiled with one addition: as its softmax
+ *   threads load the integer scores S of the unit (query rows q0 .. q0+127 of query head q_head)
+ *   from tensor memory, the ones of keys k0 .. k0+nk-1 are also written, before any masking, to
+ *   s_out (device int32 [128][nk]): S[row][key] = sum_d q_code[q0+row][q_head][d] * k_code[key][d]
+ *   ([DCU] §1.3, §3.3: Score = MMA_int8(Q, K^T) with an int32 accumulator).  Rows at or past
+ *   n_tokens and keys at or past history_len + n_tokens are 0 (their operands are zero).
+ *   q0 is a multiple of 128 below n_tokens; k0 and nk are multiples of 128 and the window lies in
+ *   the key tiles the unit computes: k0 + nk <= 128 * ((history_len + min(q0 + 127, n_tokens - 1))
+ *   / 128 + 1).  split_tiles: -1 for the key-range split the call would choose on this GPU, 0 for
+ *   none, r > 0 to force a tail segment of r key tiles (KVQ_ERR_INVALID_ARG when the shape cannot
+ *   split: history_len < 128, or r would leave a lead segment empty).  Other arguments and the
+ *   workspace as kvq_attn_prefill_int8_qcodes.
  */
 int kvq_debug_prefill_q_codes(const void* q, int32_t n_tokens, int32_t n_q_heads,
                               int32_t head_dim, int8_t* q_codes, float* q_scales,
                               void* stream);
-int kvq_debug_prefill_qk_int32(const kvq_cache* cache, const int8_t* q_codes,
-                               int32_t n_tokens, int32_t n_q_heads,
-                               const int32_t* block_table_row, int32_t n_blocks_row,
-                               int32_t q_head, int32_t q0, int32_t k0, int32_t nk,
-                               int32_t* s_out, void* stream);
+int kvq_debug_prefill_qk_int32(const kvq_cache* cache, const int8_t* q_codes, const float* q_scales,
+                               int32_t n_tokens, int32_t n_q_heads, int32_t history_len,
+                               const int32_t* block_table_row, int32_t n_blocks_row, float softmax_scale,
+                               int32_t split_tiles, int32_t q_head, int32_t q0, int32_t k0, int32_t nk,
+                               int32_t* s_out, float* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * kvq_debug_stream_floor — measurement entry point: the K/V stream of kvq_attn_decode_int8kv's
+ * split route (stage 1) alone.  It launches the same grid (one CTA per (split, KV head, sequence)),
+ * the same eight warps with their three-stage shared-memory rings and the same bulk copies of the
+ * same pages (K, V and both scale runs of every (page, KV head) below ctx_lens[b]), waits for each
+ * copy and computes nothing.  Its duration is the cost of streaming one decode call's K/V by
+ * itself on this GPU, launch and ramp-up included: the floor the attention's stage 1 is measured
+ * against.  split_rows: 0 for the size kvq_attn_decode_int8kv would choose, else a multiple of 16.
+ * Arguments otherwise as kvq_attn_decode_int8kv; writes nothing but the device status word.
+ */
+int kvq_debug_stream_floor(const kvq_cache* cache, int32_t batch, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t max_ctx, int32_t split_rows,
+                           void* stream);
+
+/*
+ * kvq_debug_fault_inject — test entry point of the failure path: every bounded wait of the decode
+ * and prefill kernels launched after this call gives up after wait_budget_cycles SM clock cycles
+ * (<= 0: the default, about 2 s), and with mode 1 the first team of decode stage-1 CTA 0 does not
+ * issue the copy of its second page, with mode 2 the producer of prefill attention CTA 0 does not
+ * issue its fourth piece (mode 0: no injection).  No copy is left in flight: the consumer's wait
+ * runs out, the kernel sets KVQ_DEV_TIMEOUT, waits (bounded) for the copies it did issue, drops
+ * that CTA's result (decode single route: zero output rows; split route: an empty partial that the
+ * merge skips; prefill: the unit's output rows are not written) and returns; the device stays
+ * usable.  Process-wide, host only; kvq_debug_fault_inject(0, 0) restores the defaults.
+ * KVQ_ERR_INVALID_ARG for an unknown mode.
+ */
+int kvq_debug_fault_inject(int32_t mode, int64_t wait_budget_cycles);
 
 /* Synchronises `stream`, then returns the device status bits of the current device in
  * *flags_out and clears them.  Returns KVQ_ERR_CUDA if the stream reports an error. */

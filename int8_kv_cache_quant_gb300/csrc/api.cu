@@ -2,11 +2,13 @@
 // Every entry point checks its arguments before launching anything, allocates nothing and
 // never synchronises (except kvq_device_status).
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 
 #include "kvq.h"
+#include "kvq_dev.cuh"
 #include "kvq_launch.h"
 
 namespace {
@@ -60,7 +62,17 @@ kvq_decode_opts decode_defaults(const kvq_decode_opts* o) {
 
 constexpr int kMaxSplits = 16384;
 
+// Test-only fault injection (kvq_debug_fault_inject): the mode and the wait budget that the
+// kernels launched from now on receive.
+std::atomic<int> g_fault_mode{0};
+std::atomic<long long> g_wait_budget{kvq::kWaitBudgetCycles};
+
 }  // namespace
+
+namespace kvq {
+int debug_fault_mode() { return g_fault_mode.load(std::memory_order_relaxed); }
+long long debug_wait_budget() { return g_wait_budget.load(std::memory_order_relaxed); }
+}  // namespace kvq
 
 extern "C" {
 
@@ -76,6 +88,13 @@ const char* kvq_status_string(int s) {
     case KVQ_ERR_CUDA: return "CUDA launch or runtime error";
     default: return "unknown status";
   }
+}
+
+int kvq_debug_fault_inject(int32_t mode, int64_t wait_budget_cycles) {
+  if (mode < 0 || mode > 2) return KVQ_ERR_INVALID_ARG;
+  g_wait_budget.store(wait_budget_cycles > 0 ? static_cast<long long>(wait_budget_cycles) : kvq::kWaitBudgetCycles);
+  g_fault_mode.store(mode);
+  return KVQ_OK;
 }
 
 int kvq_device_status(uint32_t* flags_out, void* stream) {
@@ -226,6 +245,40 @@ size_t kvq_verify_workspace_bytes(int32_t batch, int32_t n_rows, int32_t n_q_hea
   return kvq_decode_workspace_bytes(batch * n_rows, n_q_heads, max_ctx, head_dim, opts);
 }
 
+}  // extern "C"
+
+namespace kvq {
+int decode_plan(const kvq_cache* cache, int32_t batch, int32_t nq, int32_t n_q_heads, int32_t max_ctx,
+                const kvq_decode_opts* opts, DecodePlan* plan) {
+  if (!cache || batch <= 0 || nq <= 0 || n_q_heads <= 0 || cache->n_kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  if (cache->head_dim != 128 && cache->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  kvq_decode_opts o = decode_defaults(opts);
+  if (o.split_rows % KVQ_BLOCK_SIZE != 0 || o.force_route < 0 || o.force_route > 2) return KVQ_ERR_INVALID_ARG;
+  const int mc = max_ctx > 0 ? max_ctx : 1;
+  bool split = decode_split_route(o, mc);
+  if (split && o.split_rows == 0) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return KVQ_ERR_CUDA;
+    o.split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, cache->head_dim, mc, sms);
+  }
+  // automatic route: one split would be the single-CTA route plus a merge
+  if (split && o.force_route == 0 && o.route_threshold == 0 && mc <= o.split_rows) split = false;
+  plan->split = split;
+  plan->split_rows = o.split_rows;
+  plan->n_split = 1;
+  plan->bytes = 0;
+  if (split) {
+    const long long n_split = (static_cast<long long>(mc) + o.split_rows - 1) / o.split_rows;
+    if (n_split > kMaxSplits) return KVQ_ERR_UNSUPPORTED;
+    plan->n_split = static_cast<int>(n_split);
+    plan->bytes = decode_workspace_bytes(batch * nq, n_q_heads, mc, cache->head_dim, o.split_rows);
+  }
+  return KVQ_OK;
+}
+}  // namespace kvq
+
+extern "C" {
+
 // Decode with nq query rows per sequence (nq = 1: plain decode); with k_new / v_new, the fused
 // step that first writes each sequence's nq newest tokens into the cache.
 static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_new, const void* q, int32_t batch,
@@ -245,18 +298,15 @@ static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_
   if (G > 8 || static_cast<long long>(G) * nq > KVQ_VERIFY_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
   if (!aligned4(block_table) || !aligned4(ctx_lens)) return KVQ_ERR_MISALIGNED;
-  kvq_decode_opts o = decode_defaults(opts);
-  if (o.split_rows % KVQ_BLOCK_SIZE != 0 || o.force_route < 0 || o.force_route > 2) return KVQ_ERR_INVALID_ARG;
   const int mc = max_ctx > 0 ? max_ctx : 1;
-  bool split = decode_split_route(o, mc);
-  if (split && !workspace) return KVQ_ERR_WORKSPACE;
-  if (split && o.split_rows == 0) {
-    const int sms = device_sm_count();
-    if (sms <= 0) return KVQ_ERR_CUDA;
-    o.split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, cache->head_dim, mc, sms);
-  }
-  // automatic route: one split would be the single-CTA route plus a merge
-  if (split && o.force_route == 0 && o.route_threshold == 0 && mc <= o.split_rows) split = false;
+  const kvq_decode_opts o = decode_defaults(opts);
+  if (o.split_rows % KVQ_BLOCK_SIZE != 0 || o.force_route < 0 || o.force_route > 2) return KVQ_ERR_INVALID_ARG;
+  // the workspace rule is pure host arithmetic (kvq_decode_workspace_bytes), checked before the GPU is asked
+  if (decode_split_route(o, mc) && !workspace) return KVQ_ERR_WORKSPACE;
+  kvq::DecodePlan plan;
+  st = kvq::decode_plan(cache, batch, nq, n_q_heads, mc, opts, &plan);
+  if (st != KVQ_OK) return st;
+  const bool split = plan.split;
   kvq::DecodeArgs a{};
   a.k = cache->k;
   a.v = cache->v;
@@ -277,15 +327,15 @@ static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_
   a.k_new = k_new;
   a.v_new = v_new;
   a.out = out;
-  a.split_rows = o.split_rows;
+  a.split_rows = plan.split_rows;
   a.status = status_ptr();
   a.ev_begin = static_cast<cudaEvent_t>(o.stage1_event_begin);
   a.ev_end = static_cast<cudaEvent_t>(o.stage1_event_end);
+  a.wait_budget = kvq::debug_wait_budget();
+  a.fault = kvq::debug_fault_mode();
   if (split) {
-    const long long n_split = (static_cast<long long>(mc) + o.split_rows - 1) / o.split_rows;
-    if (n_split > kMaxSplits) return KVQ_ERR_UNSUPPORTED;
-    const size_t need = kvq::decode_workspace_bytes(batch * nq, n_q_heads, mc, cache->head_dim, o.split_rows);
-    if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+    const long long n_split = plan.n_split;
+    if (!workspace || workspace_bytes < plan.bytes) return KVQ_ERR_WORKSPACE;
     if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
     a.n_split = static_cast<int>(n_split);
     const long long units = static_cast<long long>(batch) * nq * n_q_heads * n_split;
@@ -372,6 +422,8 @@ static kvq::PrefillArgs prefill_args(const kvq_cache* cache, const void* q, int3
     }
   }
   a.status = status_ptr();
+  a.wait_budget = kvq::debug_wait_budget();
+  a.fault = kvq::debug_fault_mode();
   return a;
 }
 
@@ -524,6 +576,42 @@ int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_quer
   return cuda_status(kvq::launch_sparse(a, static_cast<cudaStream_t>(stream)));
 }
 
+int kvq_debug_stream_floor(const kvq_cache* cache, int32_t batch, const int32_t* block_table,
+                           int32_t max_blocks_per_seq, const int32_t* ctx_lens, int32_t max_ctx, int32_t split_rows,
+                           void* stream) {
+  int st = check_cache(cache);
+  if (st != KVQ_OK) return st;
+  if (!block_table || !ctx_lens || batch <= 0 || batch > 65535 || max_blocks_per_seq <= 0 || max_ctx <= 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (split_rows < 0 || split_rows % KVQ_BLOCK_SIZE != 0) return KVQ_ERR_INVALID_ARG;
+  if (!aligned4(block_table) || !aligned4(ctx_lens)) return KVQ_ERR_MISALIGNED;
+  if (split_rows == 0) {
+    const int sms = device_sm_count();
+    if (sms <= 0) return KVQ_ERR_CUDA;
+    split_rows = kvq_decode_auto_split_rows(batch, cache->n_kv_heads, cache->head_dim, max_ctx, sms);
+  }
+  const long long n_split = (static_cast<long long>(max_ctx) + split_rows - 1) / split_rows;
+  if (n_split > kMaxSplits) return KVQ_ERR_UNSUPPORTED;
+  kvq::DecodeArgs a{};
+  a.k = cache->k;
+  a.v = cache->v;
+  a.k_scale = cache->k_scale;
+  a.v_scale = cache->v_scale;
+  a.num_blocks = cache->num_blocks;
+  a.n_kv_heads = cache->n_kv_heads;
+  a.head_dim = cache->head_dim;
+  a.batch = batch;
+  a.block_table = block_table;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.ctx_lens = ctx_lens;
+  a.max_ctx = max_ctx;
+  a.split_rows = split_rows;
+  a.n_split = static_cast<int>(n_split);
+  a.status = status_ptr();
+  a.wait_budget = kvq::debug_wait_budget();
+  return cuda_status(kvq::launch_stream_floor(a, static_cast<cudaStream_t>(stream)));
+}
+
 int kvq_debug_prefill_q_codes(const void* q, int32_t n_tokens, int32_t n_q_heads, int32_t head_dim,
                               int8_t* q_codes, float* q_scales, void* stream) {
   if (!q || !q_codes || !q_scales || n_tokens <= 0 || n_q_heads <= 0) return KVQ_ERR_INVALID_ARG;
@@ -540,24 +628,42 @@ int kvq_debug_prefill_q_codes(const void* q, int32_t n_tokens, int32_t n_q_heads
   return cuda_status(kvq::launch_prefill_q_quant(a, static_cast<cudaStream_t>(stream)));
 }
 
-int kvq_debug_prefill_qk_int32(const kvq_cache* cache, const int8_t* q_codes, int32_t n_tokens,
-                               int32_t n_q_heads, const int32_t* block_table_row, int32_t n_blocks_row,
-                               int32_t q_head, int32_t q0, int32_t k0, int32_t nk, int32_t* s_out,
-                               void* stream) {
+int kvq_debug_prefill_qk_int32(const kvq_cache* cache, const int8_t* q_codes, const float* q_scales,
+                               int32_t n_tokens, int32_t n_q_heads, int32_t history_len,
+                               const int32_t* block_table_row, int32_t n_blocks_row, float softmax_scale,
+                               int32_t split_tiles, int32_t q_head, int32_t q0, int32_t k0, int32_t nk,
+                               int32_t* s_out, float* out, void* workspace, size_t workspace_bytes, void* stream) {
   int st = check_cache(cache);
   if (st != KVQ_OK) return st;
-  if (!q_codes || !block_table_row || !s_out) return KVQ_ERR_INVALID_ARG;
-  if (n_tokens <= 0 || n_q_heads <= 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
+  if (!q_codes || !q_scales || !block_table_row || !s_out || !out) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens <= 0 || n_q_heads <= 0 || history_len < 0 || n_blocks_row <= 0) return KVQ_ERR_INVALID_ARG;
   if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
-  if (q_head < 0 || q_head >= n_q_heads || q0 < 0 || q0 >= n_tokens) return KVQ_ERR_INVALID_ARG;
-  if (k0 < 0 || nk <= 0 || k0 % 128 != 0 || nk % 128 != 0) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<long long>(k0) + nk > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
+  if (!(softmax_scale > 0.0f) || !std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(history_len) + n_tokens > static_cast<long long>(n_blocks_row) * KVQ_BLOCK_SIZE)
     return KVQ_ERR_INVALID_ARG;
-  if (!aligned16(q_codes) || !aligned16(s_out) || !aligned4(block_table_row)) return KVQ_ERR_MISALIGNED;
-  kvq::PrefillArgs a = prefill_args(cache, nullptr, n_tokens, n_q_heads, 0, block_table_row, n_blocks_row,
-                                    1.0f, nullptr, nullptr);
+  // the window: one unit (query tile q0 / 128 of q_head) and whole key tiles it computes
+  if (q_head < 0 || q_head >= n_q_heads || q0 < 0 || q0 >= n_tokens || q0 % 128 != 0) return KVQ_ERR_INVALID_ARG;
+  const long long unit_tiles = (static_cast<long long>(history_len) + std::min(q0 + 127, n_tokens - 1)) / 128 + 1;
+  if (k0 < 0 || nk <= 0 || k0 % 128 != 0 || nk % 128 != 0 || k0 + static_cast<long long>(nk) > 128 * unit_tiles)
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(q_codes) || !aligned4(q_scales) || !aligned16(out) || !aligned16(s_out) || !aligned4(block_table_row))
+    return KVQ_ERR_MISALIGNED;
+  const size_t need = kvq_prefill_workspace_bytes(n_tokens, n_q_heads, cache->n_kv_heads, history_len,
+                                                  cache->head_dim);
+  if (!workspace || workspace_bytes < need) return KVQ_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return KVQ_ERR_MISALIGNED;
+  kvq::PrefillArgs a = prefill_args(cache, nullptr, n_tokens, n_q_heads, history_len, block_table_row,
+                                    n_blocks_row, softmax_scale, out, workspace);
+  if (split_tiles >= 0) {
+    // a forced split: every lead segment keeps at least one tile, as the automatic choice does
+    const long long shortest = (static_cast<long long>(history_len) + std::min(127, n_tokens - 1)) / 128 + 1;
+    const bool can = kvq::prefill_workspace(n_tokens, n_q_heads, cache->n_kv_heads, history_len, cache->head_dim)
+                         .can_split;
+    if (split_tiles > 0 && (!can || split_tiles > shortest - 1)) return KVQ_ERR_INVALID_ARG;
+    a.split_tail = split_tiles;
+  }
   a.q_codes = const_cast<int8_t*>(q_codes);
-  a.q_scales = nullptr;
+  a.q_scales = const_cast<float*>(q_scales);
   a.dbg_q_head = q_head;
   a.dbg_q0 = q0;
   a.dbg_k0 = k0;

@@ -80,7 +80,8 @@ struct DecodeSmem {
   static constexpr int kBarOffset = kQOffset + kQBytes;           // full [team][DEPTH], then empty [team][DEPTH]
   static constexpr int kFlagOffset = kBarOffset + (NT > 1 ? 2 : 1) * kStages * 8;  // page-ok flags [team][DEPTH]
   static constexpr int kCqOffset = kFlagOffset + kStages * 4;     // score factor per row
-  static constexpr int kTotal = kCqOffset + kRows * 4;
+  static constexpr int kFailOffset = kCqOffset + kRows * 4;       // a warp's bounded wait ran out
+  static constexpr int kTotal = kFailOffset + 16;
   static constexpr int kMergeBytes = (kWarps * 8 * (D + 4) + kWarps * 8 * 4 + kWarps * 8 + kRows * 4) * 4;
   static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the ring");
   static_assert(kWarps >= 8 && kWarps <= 16, "8..16 warps");
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   uint64_t* empty = full + L::kStages;
   int* stage_ok = reinterpret_cast<int*>(smem + L::kFlagOffset);
   float* cq_s = reinterpret_cast<float*>(smem + L::kCqOffset);
+  volatile int* cta_failed = reinterpret_cast<volatile int*>(smem + L::kFailOffset);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int p = warp / NT;   // team: takes whole pages
@@ -164,7 +166,35 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
     if (nt == 0 && first < a.max_blocks_per_seq) pg = __ldg(bt + p + lane * NTEAM);
   }
   int ctx = a.ctx_lens[b];
-  const int cap = a.max_blocks_per_seq * KVQ_BLOCK_SIZE;
+  // The query rows are requested next, ahead of every page copy: a load issued after the first
+  // copies queues behind tens of megabytes of them, and no page can be used before Q is set up
+  // (which would leave the copies' slots full and HBM idle once they have landed).  Warp w holds
+  // rows w, w + NW, ... of the Q^T set-up below.
+  constexpr int PER = D / 32;  // dims per lane
+  constexpr int kQPerWarp = (L::kRows + NW - 1) / NW;
+  uint4 qraw[kQPerWarp];
+#pragma unroll
+  for (int i = 0; i < kQPerWarp; ++i) {
+    const int h = warp + i * NW;
+    const bool real = h < R;
+    const int qi = (MROW && real) ? h / G : 0, hh = !MROW ? h : real ? h % G : 0;
+    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) +
+                           ((static_cast<long long>(b) * nq + qi) * Hq + kvh * G + hh) * D + lane * PER;
+    qraw[i] = make_uint4(0, 0, 0, 0);
+    if (real) {
+      if constexpr (PER == 8) {
+        qraw[i] = __ldg(reinterpret_cast<const uint4*>(qrow));
+      } else {
+        const uint2 r2 = __ldg(reinterpret_cast<const uint2*>(qrow));
+        qraw[i].x = r2.x;
+        qraw[i].y = r2.y;
+      }
+    }
+  }
+  // keys this call may read: what the block-table row maps, and the host's bound max_ctx (the
+  // split route's grid and workspace are sized by it); a longer ctx is clamped to it, on both
+  // routes, and reported
+  const int cap = min(a.max_blocks_per_seq * KVQ_BLOCK_SIZE, a.max_ctx);
   // fused step: the new tokens are written only when their positions are all mapped
   const bool write_new = WRITE && a.k_new != nullptr && ctx >= nq && ctx <= cap;
   if (ctx > cap || (WRITE && a.k_new != nullptr && ctx < nq)) {
@@ -204,6 +234,7 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
       mbar_init(&full[s], 1);
       if (NT > 1) mbar_init(&empty[s], NT);
     }
+    *cta_failed = 0;
     mbar_fence_init();
   }
   __syncthreads();  // the barriers are initialised before any copy completes on them
@@ -218,6 +249,10 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   // (lane i <-> page k = wb + i)
   int wb = 0;
   if (lane >= npp) pg = -1;
+  int n_issued = 0;  // pages of the team whose copies the issuing warp has issued
+  // test-only fault injection: the first team of CTA 0 leaves its second page un-issued (no copy
+  // in flight, its full barrier never completes), so its bounded waits run out
+  const bool skip_one = a.fault == 1 && p == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
   // the issuing warp, collectively: issue the copy of the team's page k into its slot
   auto issue = [&](int k) {
     while (k >= wb + 32) {
@@ -225,7 +260,8 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
       pg = (wb + lane < npp) ? __ldg(bt + p + (wb + lane) * NTEAM) : -1;
     }
     const int page = __shfl_sync(0xffffffffu, pg, k - wb);
-    if (lane == 0) {
+    ++n_issued;
+    if (lane == 0 && !(skip_one && k == 1)) {
       const int s = k % DEPTH;
       const bool ok = page >= 0 && page < a.num_blocks;
       pok[s] = ok ? 1 : 0;
@@ -268,7 +304,8 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
       }
     }
   };
-  // The first copies go out before Q is prepared, so their HBM latency overlaps it.
+  // The first copies go out before Q is set up (its rows were requested first), so their HBM
+  // latency overlaps the set-up.
   if (nt == 0) {
     write_team_pages(true);
     for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
@@ -280,31 +317,18 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   // chunk j (16 dims) is two 8 x 8 b16 matrices, rows = query rows, whose columns are the
   // k-slots of the MMA: slots (2c, 2c+1) carry dims (4c, 4c+1) and slots (2c+8, 2c+9) carry
   // dims (4c+2, 4c+3).
-  for (int h = warp; h < L::kRows; h += NW) {
-    const bool real = h < R;
-    const int qi = (MROW && real) ? h / G : 0, hh = !MROW ? h : real ? h % G : 0;
+#pragma unroll
+  for (int iq = 0; iq < kQPerWarp; ++iq) {
+    const int h = warp + iq * NW;
+    if (h >= L::kRows) break;
     uint8_t* q_tile = q_s + (h >> 3) * (D * 16);
     const int hr = h & 7;
-    constexpr int PER = D / 32;  // dims per lane
     float x[PER];
-    const uint16_t* qrow = static_cast<const uint16_t*>(a.q) +
-                           ((static_cast<long long>(b) * nq + qi) * Hq + kvh * G + hh) * D + lane * PER;
-    if constexpr (PER == 8) {
-      const uint4 raw = real ? __ldg(reinterpret_cast<const uint4*>(qrow)) : make_uint4(0, 0, 0, 0);
-      const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    const uint32_t w4[4] = {qraw[iq].x, qraw[iq].y, qraw[iq].z, qraw[iq].w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[2 * i] = __uint_as_float(w4[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-      }
-    } else {
-      const uint2 raw = real ? __ldg(reinterpret_cast<const uint2*>(qrow)) : make_uint2(0, 0);
-      const uint32_t w2[2] = {raw.x, raw.y};
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        x[2 * i] = __uint_as_float(w2[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w2[i] & 0xFFFF0000u);
-      }
+    for (int i = 0; i < PER / 2; ++i) {
+      x[2 * i] = __uint_as_float(w4[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
     }
     float amax = 0.f;
 #pragma unroll
@@ -353,9 +377,10 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   const uint32_t selA = (c < 2) ? kSelB01 : kSelB23;
   const uint32_t selB = (c < 2) ? kSelB23 : kSelB01;
 
+  int k_fail = npp;  // the page whose wait ran out (npp: none)
   for (int k = 0; k < npp; ++k) {
     const int s = k % DEPTH;
-    const bool got = mbar_wait(&pfull[s], (k / DEPTH) & 1, a.status);
+    const bool got = mbar_wait(&pfull[s], (k / DEPTH) & 1, a.status, a.wait_budget);
     uint8_t* st = pring + s * L::kStageBytes;
     const uint32_t kbase = smem_u32(st);
     const uint32_t vbase = kbase + KB;
@@ -376,7 +401,10 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
       i8x4_to_h2x2(r3, kSelB01, kSelB23, a1, a3);
       mma_f16_16816(sb, a0, a1, a2, a3, q2, q3);
     }
-    if (!__all_sync(0xffffffffu, got)) break;  // the warp leaves together
+    if (!__all_sync(0xffffffffu, got)) {  // the warp leaves together
+      k_fail = k;
+      break;
+    }
     const float S[4] = {sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]};
 
     // ---- online softmax
@@ -454,10 +482,21 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
       if (nt == 0 && k + DEPTH < npp) {
         // every warp of the team has read the slot (the (k / DEPTH)-th phase of its empty barrier)
         bool freed = true;
-        if (lane == 0) freed = mbar_wait(&pempty[s], (k / DEPTH) & 1, a.status);
+        if (lane == 0) freed = mbar_wait(&pempty[s], (k / DEPTH) & 1, a.status, a.wait_budget);
         if (__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) issue(k + DEPTH);
       }
     }
+  }
+  if (k_fail < npp) {
+    // A wait ran out: the CTA's result is dropped (below).  The issuing warp first waits, again
+    // with the budget, for the copies it issued past that page, so that none lands in shared
+    // memory after the ring is reused or the CTA exits.
+    if (lane == 0) {
+      *cta_failed = 1;
+      if (nt == 0)
+        for (int kk = k_fail; kk < n_issued; ++kk) mbar_wait(&pfull[kk % DEPTH], (kk / DEPTH) & 1, a.status, a.wait_budget);
+    }
+    __syncwarp();
   }
   // l over all tokens of the warp for heads 2c, 2c + 1
 #pragma unroll
@@ -469,6 +508,28 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   // ------------------------------------------------------------ merge the warps
   grid_dep_trigger();  // the stage-2 merge may start launching
   __syncthreads();  // every issued copy was waited for by its warp: the ring is free
+  if (*cta_failed) {
+    // a bounded wait ran out (KVQ_DEV_TIMEOUT is set): this range contributes nothing; the single
+    // route writes zeros, a split writes an empty partial that the merge skips
+    for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
+      const int hh = idx / D, d = idx % D;
+      const long long orow = MROW ? (static_cast<long long>(b) * nq + hh / G) * Hq + kvh * G + hh % G
+                                  : static_cast<long long>(b) * Hq + kvh * G + hh;
+      if (SPLIT) {
+        const long long pu = orow * a.n_split + blockIdx.x;
+        a.part_acc[pu * D + d] = 0.0f;
+        if (d == 0) {
+          a.part_stats[pu * 4 + 0] = -INFINITY;
+          a.part_stats[pu * 4 + 1] = -INFINITY;
+          a.part_stats[pu * 4 + 2] = 0.0f;
+          a.part_stats[pu * 4 + 3] = 0.0f;
+        }
+      } else {
+        a.out[orow * D + d] = 0.0f;
+      }
+    }
+    return;
+  }
   constexpr int RS = D + 4;                                     // padded row: no bank conflicts
   // slot of (team, row r) = team * 8 NT + r = warp * 8 + (r mod 8) for the warp holding r
   float* mo = reinterpret_cast<float*>(smem);                   // [NW][8][RS]
@@ -537,6 +598,89 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   }
 }
 
+// The K/V stream of the stage-1 kernel alone (measurement entry point kvq_debug_stream_floor): the
+// same grid, the same eight warps with their three-stage rings, the same bulk copies of the same
+// pages in the same order, and no arithmetic.  Its duration is what streaming one launch's pages
+// costs on this GPU by itself (launch, ramp-up and tail included), the floor of stage 1.
+template <int D>
+__global__ void __launch_bounds__(256, D == 128 ? 2 : 1) decode_stream_kernel(DecodeArgs a) {
+  constexpr int NTEAM = 8, DEPTH = 3;
+  using L = DecodeSmem<D, 1, NTEAM, DEPTH>;
+  constexpr int KB = L::kKvBytes;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  grid_dep_wait();
+  const int t_begin = static_cast<int>(blockIdx.x) * a.split_rows;
+  const int32_t* bt = a.block_table + static_cast<long long>(b) * a.max_blocks_per_seq + t_begin / KVQ_BLOCK_SIZE;
+  int pg = -1;
+  if (t_begin / KVQ_BLOCK_SIZE + warp + lane * NTEAM < a.max_blocks_per_seq) pg = __ldg(bt + warp + lane * NTEAM);
+  const int ctx = max(0, min(a.ctx_lens[b], min(a.max_blocks_per_seq * KVQ_BLOCK_SIZE, a.max_ctx)));
+  const int t_end = min(ctx, t_begin + a.split_rows);
+  const int n_pages = (t_end > t_begin) ? (t_end - t_begin + KVQ_BLOCK_SIZE - 1) / KVQ_BLOCK_SIZE : 0;
+  if (n_pages == 0) return;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < L::kStages; ++st) mbar_init(&full[st], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const int npp = (warp < n_pages) ? (n_pages - warp + NTEAM - 1) / NTEAM : 0;
+  uint64_t* pfull = full + warp * DEPTH;
+  uint8_t* pring = smem + warp * DEPTH * L::kStageBytes;
+  if (lane >= npp) pg = -1;
+  int wb = 0, n_issued = 0;
+  auto issue = [&](int k) {
+    while (k >= wb + 32) {
+      wb += 32;
+      pg = (wb + lane < npp) ? __ldg(bt + warp + (wb + lane) * NTEAM) : -1;
+    }
+    const int page = __shfl_sync(0xffffffffu, pg, k - wb);
+    ++n_issued;
+    if (lane == 0) {
+      const int st = k % DEPTH;
+      if (page >= 0 && page < a.num_blocks) {
+        uint8_t* dst = pring + st * L::kStageBytes;
+        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        mbar_arrive_expect_tx(&pfull[st], 2 * KB + 128);
+        bulk_g2s(dst, a.k + ph * KB, KB, &pfull[st]);
+        bulk_g2s(dst + KB, a.v + ph * KB, KB, &pfull[st]);
+        bulk_g2s(dst + 2 * KB, a.k_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[st]);
+        bulk_g2s(dst + 2 * KB + 64, a.v_scale + ph * KVQ_BLOCK_SIZE, 64, &pfull[st]);
+      } else {
+        set_status(a.status, KVQ_DEV_BAD_BLOCK);
+        mbar_arrive(&pfull[st]);
+      }
+    }
+  };
+  for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
+  for (int k = 0; k < npp; ++k) {
+    const bool got = mbar_wait(&pfull[k % DEPTH], (k / DEPTH) & 1, a.status, a.wait_budget);
+    if (!__all_sync(0xffffffffu, got)) {
+      // the copies issued past this page land before the CTA exits
+      if (lane == 0)
+        for (int kk = k; kk < n_issued; ++kk) mbar_wait(&pfull[kk % DEPTH], (kk / DEPTH) & 1, a.status, a.wait_budget);
+      __syncwarp();
+      break;
+    }
+    if (k + DEPTH < npp) issue(k + DEPTH);
+  }
+}
+
+cudaError_t launch_stream_floor(const DecodeArgs& a, cudaStream_t stream) {
+  dim3 grid(a.n_split, a.n_kv_heads, a.batch);
+  if (a.head_dim == 256) {
+    using L = DecodeSmem<256, 1, 8, 3>;
+    cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(decode_stream_kernel<256>, grid, dim3(256), L::kTotal, stream, a);
+  }
+  using L = DecodeSmem<128, 1, 8, 3>;
+  cudaError_t e = cudaFuncSetAttribute(decode_stream_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_stream_kernel<128>, grid, dim3(256), L::kTotal, stream, a);
+}
+
 // Stage 2: log-sum-exp merge of the splits of one (sequence, query row, query head).
 //   M_s = max m_s, M_z = max m_z;  l = sum l_s 2^{m_s - M_s};  o = sum acc_s 2^{m_z - M_z};
 //   out = o 2^{M_z - M_s} / l.  The per-split weights are computed once into shared memory
@@ -573,7 +717,7 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
   float4 st0 = make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
   if (tid < a.n_split) st0 = reinterpret_cast<const float4*>(stats)[tid];
   int ctx = a.ctx_lens[b];
-  ctx = max(0, min(ctx, a.max_blocks_per_seq * KVQ_BLOCK_SIZE));
+  ctx = max(0, min(ctx, min(a.max_blocks_per_seq * KVQ_BLOCK_SIZE, a.max_ctx)));
   const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
 
   float Ms = tid < n ? st0.x : -INFINITY, Mz = tid < n ? st0.y : -INFINITY;

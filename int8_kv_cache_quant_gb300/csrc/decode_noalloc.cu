@@ -48,17 +48,17 @@ extern "C" int kvq_attn_decode_int8kv_noalloc(const kvq_cache* cache, const void
                                               int32_t max_blocks_per_seq, const int32_t* ctx_lens,
                                               int32_t max_ctx, float softmax_scale, float* out,
                                               const kvq_decode_opts* opts, void* stream) {
-  // Same validation and kernels as kvq_attn_decode_int8kv; only the workspace differs.
-  const size_t need = kvq_decode_workspace_bytes(batch, n_q_heads, max_ctx > 0 ? max_ctx : 1,
-                                                 cache ? cache->head_dim : 0, opts);
-  if (need > static_cast<size_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_WORKSPACE;
+  // Same validation and kernels as kvq_attn_decode_int8kv; only the workspace differs.  The
+  // limit applies to the partials of the split this call actually takes (the automatic split
+  // size of this GPU unless opts sets one), not to the bound kvq_decode_workspace_bytes states.
+  if (!cache) return KVQ_ERR_INVALID_ARG;
+  kvq::DecodePlan plan;
+  const int st0 = kvq::decode_plan(cache, batch, 1, n_q_heads, max_ctx > 0 ? max_ctx : 1, opts, &plan);
+  if (st0 != KVQ_OK) return st0;
+  if (plan.bytes > static_cast<size_t>(KVQ_NOALLOC_SCRATCH_BYTES)) return KVQ_ERR_WORKSPACE;
   void* ws = nullptr;
-  size_t ws_bytes = 0;
-  if (need > 0) {
-    const int st = scratch_ptr(&ws);
-    if (st != KVQ_OK) return st;
-    ws_bytes = KVQ_NOALLOC_SCRATCH_BYTES;
-  }
+  const int st = scratch_ptr(&ws);
+  if (st != KVQ_OK) return st;
   return kvq_attn_decode_int8kv(cache, q, batch, n_q_heads, block_table, max_blocks_per_seq, ctx_lens,
-                                max_ctx, softmax_scale, out, ws, ws_bytes, opts, stream);
+                                max_ctx, softmax_scale, out, ws, KVQ_NOALLOC_SCRATCH_BYTES, opts, stream);
 }

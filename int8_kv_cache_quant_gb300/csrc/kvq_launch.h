@@ -69,10 +69,28 @@ struct DecodeArgs {
   unsigned int* status;
   cudaEvent_t ev_begin;  // optional events around the stage-1 launch
   cudaEvent_t ev_end;
+  // bounded waits: budget in SM clock cycles; fault: test-only injection (kvq_debug_fault_inject),
+  // 1 = CTA 0's first team does not issue the copy of its second page
+  long long wait_budget;
+  int fault;
 };
 enum class DecodeRoute { kSingle = 1, kSplit = 2 };
+// Test-only fault injection and wait budget of the kernels launched next (kvq_debug_fault_inject).
+int debug_fault_mode();
+long long debug_wait_budget();
 size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_dim, int split_rows);
+// The route, split size and workspace bytes a decode call with these (checked) arguments takes:
+// the automatic split size of this GPU when opts->split_rows is 0.  A kvq_status.
+struct DecodePlan {
+  bool split;
+  int split_rows, n_split;
+  size_t bytes;
+};
+int decode_plan(const kvq_cache* cache, int32_t batch, int32_t nq, int32_t n_q_heads, int32_t max_ctx,
+                const kvq_decode_opts* opts, DecodePlan* plan);
 cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream);
+// the stage-1 kernel's K/V stream alone, split route geometry (kvq_debug_stream_floor)
+cudaError_t launch_stream_floor(const DecodeArgs& a, cudaStream_t stream);
 
 struct SparseArgs {
   const int8_t* k;
@@ -133,6 +151,10 @@ struct PrefillArgs {
   // debug QK tile (kvq_debug_prefill_qk_int32)
   int dbg_q_head, dbg_q0, dbg_k0, dbg_nk;
   int32_t* dbg_s_out;
+  // bounded waits: budget in SM clock cycles; fault: test-only injection (kvq_debug_fault_inject),
+  // 2 = the producer of attention CTA 0 does not issue its fourth piece copy
+  long long wait_budget;
+  int fault;
 };
 struct PrefillWorkspace {
   int n_kv_tiles;

@@ -8,20 +8,27 @@
 // V) * p_scale), §2.1 (Q quantised per (token, head) by the same absmax rule).
 //
 // GB300 design.
-// * sm_103a has no tcgen05 kind::i8, so the int8 codes are widened to integer-valued fp16 in
-//   shared memory and the contractions use tcgen05.mma kind::f16 with fp32 accumulators in
-//   tensor memory.  This is exact: every QK partial sum is an integer of magnitude at most
-//   256 * 127 * 127 < 2^24, every per-tile PV sum at most 128 * 127 * 127 < 2^24.
-// * One CTA per (128 query rows, query head).  Q (128 x D), the K tile (128 keys x D) and the
-//   V tile (D x 128 keys) live in shared memory in the K-major 128-byte-swizzle layout; S
-//   (128 x 128, two buffers), the P codes (fp16, over the first half of their S buffer) and O
-//   (128 x D) live in tensor memory.
-// * Two softmax threads share query row r (tensor-memory lane r), one per half of the key
-//   tile: they read their S halves, run the online softmax and the per-tile P re-quantisation,
-//   write their P codes, and rescale their halves of the O row when the P scale changes (O
-//   holds sum_tiles (ps_tile / ps_ref) * PV_tile).
-// * Every P-code decision is the page's fp32 sequence with a specified exp2 (exp2_det) and the
-//   running maximum after each 128-key tile, so the codes are reproducible off the GPU.
+// * sm_103a has no tcgen05 kind::i8, so the int8 codes are widened to integer-valued fp16 and
+//   the contractions use tcgen05.mma kind::f16 with fp32 accumulators in tensor memory.  This
+//   is exact: every QK partial sum is an integer of magnitude at most 256 * 127 * 127 < 2^24,
+//   every per-tile PV sum at most 128 * 127 * 127 < 2^24.
+// * Three kernels per call, chained by programmatic dependent launch: Q codes (q_quant_kernel),
+//   a pre-pass that widens each (KV head, 128-key tile) of the cache once into the exact byte
+//   image of the attention kernel's shared-memory operands (kv_widen_kernel), and the attention
+//   (prefill_tma_kernel).
+// * Attention: one CTA per (128 query rows, query head), longest units first.  A producer lane
+//   brings the widened K and V pieces through a ring of 16 KB shared-memory slots by bulk copy;
+//   one MMA warp issues QK (A = Q, held in tensor memory as fp16 pairs, B = a K piece) into a
+//   single S buffer, and PV (A = the P codes in shared memory, B = V pieces) into O in tensor
+//   memory.  16 softmax warps, four threads per query row (each owns 32 keys of the tile and a
+//   quarter of the O columns), load S into registers, free the S buffer, and run the online
+//   softmax and the per-tile P re-quantisation.
+// * Every P-code decision is taken in fp32 relative to the tile's own maximum score, with a
+//   specified exp2 (exp2_det), so the codes of a tile depend on that tile alone and are
+//   reproducible off the GPU; the running maximum only rescales the tile's P scale and sum.
+// * A unit's key range may run as two CTAs (a lead and a tail segment); the segment that
+//   finishes second merges the two partial results, in an order that does not depend on which
+//   finished first.
 #include <algorithm>
 #include <functional>
 #include <vector>
@@ -59,26 +66,6 @@ __global__ void __launch_bounds__(256) q_quant_kernel(PrefillArgs a) {
 }
 
 namespace {
-
-// ============================================================================ layout
-template <int D>
-struct PrefillSmem {
-  static constexpr int kQ = 128 * D * 2;   // Q tile: 128 rows x D, fp16
-  static constexpr int kK = 128 * D * 2;   // K tile: 128 keys x D
-  static constexpr int kV = D * 128 * 2;   // V tile: D rows x 128 keys
-  static constexpr int kP = 128 * 128 * 2; // P tile: 128 rows x 128 keys
-  static constexpr int offQ = 0;
-  static constexpr int offK = offQ + kQ;
-  static constexpr int offV = offK + kK;
-  static constexpr int offP = offV + kV;
-  static constexpr int offSK = offP + kP;      // float[128] key scales of the tile
-  static constexpr int offSV = offSK + 512;    // float[128] value scales
-  static constexpr int offPage = offSV + 512;  // int[8] pages of the tile (-1 = none)
-  static constexpr int offBar = offPage + 64;  // mbarriers: QK done, PV done
-  static constexpr int offTmem = offBar + 16;  // TMEM base address
-  static constexpr int kBytes = offTmem + 16;
-  static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024 bytes
-};
 
 constexpr float kLog2eP = 1.44269504088896341f;
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
@@ -130,8 +117,9 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
 
 // The specified exp2 of the P-code decisions (the same function, step for step, as the CPU
 // reference): the argument clamped to [-125, 125] (fmaxf / fminf: NaN becomes -125), Cody-Waite
-// reduction x = n + f with n = rint(x), 2^f by the degree-4 polynomial with constant term 1
-// fitted to the minimax relative error of 2^f on [-1/2, 1/2] (Horner, fp32 fma), times 2^n.
+// reduction x = n + f with n = rint(x), 2^f by the degree-4 polynomial with constant term 1 whose
+// other coefficients minimise the largest relative error of 2^f on [-1/2, 1/2] (2.82e-6; Horner,
+// fp32 fma), times 2^n.
 // Here on a pair, the same operations per element, for arguments x <= 0 up to one rounding (the
 // attention kernels pass x = fma(y, a, -m) with m >= fl(ymax * a) >= fl(y * a) and a >= 0, so
 // the clamp at +125 never acts and is left out): n = rint(x) through the 1.5 * 2^23 magic sum t,
@@ -144,9 +132,9 @@ __device__ __forceinline__ f2 exp2_det2(f2 xin) {
   const f2 t = add2(x, magic);
   const f2 n = sub2(t, magic);
   const f2 f = sub2(x, n);
-  f2 p = fma2(mk2(0.00966636837f, 0.00966636837f), f, mk2(0.0559219755f, 0.0559219755f));
-  p = fma2(p, f, mk2(0.240223497f, 0.240223497f));
-  p = fma2(p, f, mk2(0.693121016f, 0.693121016f));
+  f2 p = fma2(mk2(0.00958285294f, 0.00958285294f), f, mk2(0.0559064262f, 0.0559064262f));
+  p = fma2(p, f, mk2(0.240240991f, 0.240240991f));
+  p = fma2(p, f, mk2(0.693124175f, 0.693124175f));
   p = fma2(p, f, mk2(1.0f, 1.0f));
   const uint32_t r0 = __float_as_uint(lo2(p)) + (__float_as_uint(lo2(t)) << 23);
   const uint32_t r1 = __float_as_uint(hi2(p)) + (__float_as_uint(hi2(t)) << 23);
@@ -171,72 +159,6 @@ __device__ __forceinline__ void widen16(const int4 raw, uint4& c0, uint4& c1) {
 }
 
 __device__ __forceinline__ void sts128(uint8_t* p, const uint4& v) { *reinterpret_cast<uint4*>(p) = v; }
-
-// Q tile: rows q0 .. q0+127 of query head h; row r -> tile row r.  K-block stride 128 * 128 B.
-template <int D>
-__device__ void load_q_tile(uint8_t* qs, const int8_t* q_codes, int T, int Hq, int h, int q0, int tid) {
-  const int r = tid;
-  const bool ok = q0 + r < T;
-  const int8_t* src = q_codes + (static_cast<long long>(q0 + r) * Hq + h) * D;
-#pragma unroll 4
-  for (int c16 = 0; c16 < D / 16; ++c16) {
-    int4 raw = make_int4(0, 0, 0, 0);
-    if (ok) raw = __ldg(reinterpret_cast<const int4*>(src + 16 * c16));
-    uint4 c0, c1;
-    widen16(raw, c0, c1);
-    uint8_t* blk = qs + (c16 >> 2) * (128 * 128);
-    const int cc = (c16 & 3) * 2;
-    sts128(blk + tc::sw128_off(r, cc), c0);
-    sts128(blk + tc::sw128_off(r, cc + 1), c1);
-  }
-}
-
-// K tile j (keys 128j .. 128j+127) of KV head kvh; key n -> tile row n.  Also the tile's key
-// and value scales and its 8 page numbers.  Keys at or past `n_keys` (and keys on a bad page)
-// are zero.
-template <int D>
-__device__ void load_k_tile(uint8_t* ks, float* sk_s, float* sv_s, int* page_s, const PrefillArgs& a, int kvh,
-                            int j, int n_keys, int tid) {
-  const int n = tid;
-  const int t = 128 * j + n;
-  int page = -1;
-  if (t < n_keys) {
-    const int bi = t / KVQ_BLOCK_SIZE;
-    if (bi < a.n_blocks_row) page = a.block_table_row[bi];
-    if (page < 0 || page >= a.num_blocks) {
-      if ((t & 15) == 0) set_status(a.status, KVQ_DEV_BAD_BLOCK);
-      page = -1;
-    }
-  }
-  if ((n & 15) == 0) page_s[n >> 4] = page;
-  const long long ph = static_cast<long long>(page < 0 ? 0 : page) * a.n_kv_heads + kvh;
-  const int slot = t & 15;
-  sk_s[n] = page >= 0 ? a.k_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
-  sv_s[n] = page >= 0 ? a.v_scale[ph * KVQ_BLOCK_SIZE + slot] : 0.0f;
-  const int8_t* src = a.k + ph * D * KVQ_BLOCK_SIZE + slot * 16;
-#pragma unroll 4
-  for (int c16 = 0; c16 < D / 16; ++c16) {
-    int4 raw = make_int4(0, 0, 0, 0);
-    if (page >= 0) raw = __ldg(reinterpret_cast<const int4*>(src + c16 * 256));
-    uint4 c0, c1;
-    widen16(raw, c0, c1);
-    uint8_t* blk = ks + (c16 >> 2) * (128 * 128);
-    const int cc = (c16 & 3) * 2;
-    sts128(blk + tc::sw128_off(n, cc), c0);
-    sts128(blk + tc::sw128_off(n, cc + 1), c1);
-  }
-}
-
-// S = Q K^T over the head dimension (M = 128 rows, N = 128 keys, K = D), one thread.
-template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t qs, uint32_t ks, uint32_t tmem_s) {
-  constexpr uint32_t idesc = tc::idesc_f16_f32(128, 128);
-#pragma unroll
-  for (int k = 0; k < D / 16; ++k) {
-    const uint32_t off = (k >> 2) * (128 * 128) + (k & 3) * 32;
-    tc::mma_f16_ss(tmem_s, tc::sdesc_sw128(qs + off), tc::sdesc_sw128(ks + off), idesc, k > 0 ? 1u : 0u);
-  }
-}
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
   const uint32_t s = smem_u32(p);
@@ -594,12 +516,12 @@ constexpr int kPrefillThreads = kSoftmaxThreads + 64;
 
 // Bounded wait that also gives up as soon as another thread of the CTA has given up.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned int* status,
-                                              volatile int* abort_flag) {
+                                              volatile int* abort_flag, long long budget) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       set_status(status, KVQ_DEV_TIMEOUT);
       *abort_flag = 1;
       return false;
@@ -641,10 +563,10 @@ __device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
 
 // Bounded wait for a flag that another CTA of the same grid sets.  The prefill waits only on a
 // CTA that has already announced itself in its epilogue, so the flag comes within microseconds.
-__device__ __forceinline__ void wait_flag(const unsigned int* flag, unsigned int* status) {
+__device__ __forceinline__ void wait_flag(const unsigned int* flag, unsigned int* status, long long budget) {
   const long long t0 = clock64();
   while (ld_acquire_gpu(flag) == 0u) {
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       set_status(status, KVQ_DEV_TIMEOUT);
       return;
     }
@@ -667,7 +589,10 @@ __device__ __forceinline__ float max4_col(const float* p, int row) {
 // HP: the first chunk in high precision (fp16 Q with a power-of-two scale per row, the
 // chunk's K/V as fp16 pieces with power-of-two scales per key, P as fp16 w / max w per tile)
 // in place of the int8 Q, K/V and P codes; everything else is the same kernel.
-template <int D, bool HP>
+// DBG (test entry point kvq_debug_prefill_qk_int32): the same int8 kernel, which also copies
+// the raw integer scores S of the requested (query head, query tile, key window) out of tensor
+// memory as each softmax thread loads them; nothing else changes.
+template <int D, bool HP, bool DBG = false>
 __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(PrefillArgs a) {
   using L = PrefillTmaSmem<D>;
   constexpr int OCOLS = D / 4;   // O columns per softmax thread
@@ -808,12 +733,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     bool failed = false;  // a wait of this thread gave up; the group leaves together below
     for (int j = 0; j < nt; ++j) {
       const int b = j & 1, sb = j & (kScaleBufs - 1);
-      failed |= !wait_or_abort(&bars[kBarS0], j & 1, a.status, abort_flag);
+      failed |= !wait_or_abort(&bars[kBarS0], j & 1, a.status, abort_flag, a.wait_budget);
       tc::fence_after_sync();
       uint32_t sv[32];
       tc::ld_32x32b_x32(tmem + lane_base + 32 * part, sv);
-      failed |= !wait_or_abort(&bars[kBarSclFull + sb], (j / kScaleBufs) & 1, a.status, abort_flag);
+      failed |= !wait_or_abort(&bars[kBarSclFull + sb], (j / kScaleBufs) & 1, a.status, abort_flag, a.wait_budget);
       tc::wait_ld();
+      if constexpr (DBG) {
+        // this thread's 32 scores of key tile j_begin + j, when the tile lies in the window
+        const int k_abs = 128 * (j_begin + j);
+        if (h == a.dbg_q_head && q0 == a.dbg_q0 && k_abs >= a.dbg_k0 && k_abs < a.dbg_k0 + a.dbg_nk) {
+          int32_t* dst = a.dbg_s_out + static_cast<long long>(row) * a.dbg_nk + (k_abs - a.dbg_k0) + 32 * part;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<int4*>(dst + e) =
+                make_int4(__float2int_rn(__uint_as_float(sv[e])), __float2int_rn(__uint_as_float(sv[e + 1])),
+                          __float2int_rn(__uint_as_float(sv[e + 2])), __float2int_rn(__uint_as_float(sv[e + 3])));
+        }
+      }
       tc::fence_before_sync();
       mbar_arrive(&bars[kBarS0 + 1]);  // S_j is in registers: the next QK may overwrite it
       const float4* sk_t = reinterpret_cast<const float4*>(scale_s + (sb * 2 + 0) * 128 + 32 * part);
@@ -963,7 +900,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       }
       // O must hold PV_{j-1} before it is rescaled (and P_{j-1} must be consumed: it is)
       if (j > 0) {
-        failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag);
+        failed |= !wait_or_abort(&bars[kBarPvDone], (j - 1) & 1, a.status, abort_flag, a.wait_budget);
         tc::fence_after_sync();
       }
       {
@@ -998,7 +935,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     }
     // ---- epilogue: out = O * 2^24 * ps_ref / l (l summed over the four parts; HP: no 2^24)
     if (!*abort_flag) {
-      wait_or_abort(&bars[kBarPvDone], (nt - 1) & 1, a.status, abort_flag);
+      wait_or_abort(&bars[kBarPvDone], (nt - 1) & 1, a.status, abort_flag, a.wait_budget);
       tc::fence_after_sync();
     }
     red_max[part * 128 + row] = l_part;
@@ -1079,7 +1016,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
       // own n is rounded exactly as the first one's was, so the result does not depend on the
       // order in which the two segments finished.
       const long long prow = static_cast<long long>(unit) * 128 + row;
-      if (tid == 0) wait_flag(a.part_ready + unit, a.status);
+      if (tid == 0) wait_flag(a.part_ready + unit, a.status, a.wait_budget);
       named_bar(5, kSoftmaxThreads);
       __threadfence();
 #pragma unroll 1
@@ -1130,13 +1067,13 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     const uint32_t tm_o = tmem + L::kOCol;
     int slot = 0;
     uint32_t ph = 0;
-    bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag));
+    bool ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarQFull], 0, a.status, abort_flag, a.wait_budget));
     for (int j = 0; ok && j <= nt; ++j) {
       if (j < nt) {
         // S is single-buffered: QK_j overwrites it once every softmax thread has loaded S_{j-1}
-        if (j >= 1) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarS0 + 1], (j - 1) & 1, a.status, abort_flag));
+        if (j >= 1) ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarS0 + 1], (j - 1) & 1, a.status, abort_flag, a.wait_budget));
         for (int qa = 0; ok && qa < NP; ++qa) {
-          ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag));
+          ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag, a.wait_budget));
           if (!ok) break;
           if (elect_one()) {
             tc::fence_after_sync();
@@ -1159,11 +1096,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
         // slots, so one N = D MMA per k-step covers all of O.
         const int jp = j - 1, bp = jp & 1;
         constexpr uint32_t idesc_pv = tc::idesc_f16_f32(128, D);
-        ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag));
+        ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarPFull], jp & 1, a.status, abort_flag, a.wait_budget));
         for (int kh = 0; ok && kh < 2; ++kh) {
           const int s0 = slot;
           for (int dh = 0; ok && dh < D / 128; ++dh) {
-            ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag));
+            ok = __all_sync(0xffffffffu, wait_or_abort(&bars[kBarFull + slot], ph, a.status, abort_flag, a.wait_budget));
             if (++slot == kRingSlots) {
               slot = 0;
               ph ^= 1u;
@@ -1188,7 +1125,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     // every MMA this warp issued has completed before the CTA releases tensor memory
     if (elect_one()) {
       tc::commit(&bars[kBarDrain]);
-      mbar_wait(&bars[kBarDrain], 0, a.status);
+      mbar_wait(&bars[kBarDrain], 0, a.status, a.wait_budget);
     }
     __syncwarp();
   } else if (lane == 0) {
@@ -1196,13 +1133,18 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     int slot = 0, fills = 0;
     uint32_t ph = 0;
     bool ok = true;
+    // test-only fault injection: CTA 0 leaves its fourth piece un-issued (no copy in flight, its
+    // full barrier never completes), so the MMA warp's bounded wait on it runs out
+    const bool skip_one = a.fault == 2 && blockIdx.x == 0;
     auto push = [&](const uint8_t* src) {
-      if (fills >= kRingSlots && !wait_or_abort(&bars[kBarEmpty + slot], ph ^ 1u, a.status, abort_flag)) {
+      if (fills >= kRingSlots && !wait_or_abort(&bars[kBarEmpty + slot], ph ^ 1u, a.status, abort_flag, a.wait_budget)) {
         ok = false;
         return;
       }
-      mbar_arrive_expect_tx(&bars[kBarFull + slot], kPieceBytes);
-      bulk_g2s(ring + slot * kPieceBytes, src, kPieceBytes, &bars[kBarFull + slot]);
+      if (!(skip_one && fills == 3)) {
+        mbar_arrive_expect_tx(&bars[kBarFull + slot], kPieceBytes);
+        bulk_g2s(ring + slot * kPieceBytes, src, kPieceBytes, &bars[kBarFull + slot]);
+      }
       ++fills;
       if (++slot == kRingSlots) {
         slot = 0;
@@ -1213,7 +1155,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     auto push_scales = [&](int j) {
       const int sb = j & (kScaleBufs - 1);
       if (j >= kScaleBufs &&
-          !wait_or_abort(&bars[kBarSclFree + sb], ((j - kScaleBufs) / kScaleBufs) & 1, a.status, abort_flag)) {
+          !wait_or_abort(&bars[kBarSclFree + sb], ((j - kScaleBufs) / kScaleBufs) & 1, a.status, abort_flag, a.wait_budget)) {
         ok = false;
         return;
       }
@@ -1236,9 +1178,9 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
     // Copies still in flight (only after an abort) land before the CTA exits: wait for the
     // last fill of every slot and the last load of every scale buffer.
     for (int i = (fills > kRingSlots ? fills - kRingSlots : 0); i < fills; ++i)
-      mbar_wait(&bars[kBarFull + i % kRingSlots], (i / kRingSlots) & 1, a.status);
+      mbar_wait(&bars[kBarFull + i % kRingSlots], (i / kRingSlots) & 1, a.status, a.wait_budget);
     for (int i = (scl_loads > kScaleBufs ? scl_loads - kScaleBufs : 0); i < scl_loads; ++i)
-      mbar_wait(&bars[kBarSclFull + i % kScaleBufs], (i / kScaleBufs) & 1, a.status);
+      mbar_wait(&bars[kBarSclFull + i % kScaleBufs], (i / kScaleBufs) & 1, a.status, a.wait_budget);
   }
 
   tc::fence_before_sync();
@@ -1246,71 +1188,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_tma_kernel(Prefill
   if (warp == kMmaWarp) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, L::kTmemCols);
-  }
-}
-
-// ============================================================================ debug QK tile
-// The prefill kernel's QK path alone: S for query rows q0 .. q0+127 of dbg_q_head against the
-// 128 keys of tile (dbg_k0 / 128 + blockIdx.x), written as exact int32.
-template <int D>
-__global__ void __launch_bounds__(128, 1) prefill_qk_debug_kernel(PrefillArgs a) {
-  using L = PrefillSmem<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  uint8_t* qs = sm + L::offQ;
-  uint8_t* ks = sm + L::offK;
-  float* sk_s = reinterpret_cast<float*>(sm + L::offSK);
-  float* sv_s = reinterpret_cast<float*>(sm + L::offSV);
-  int* page_s = reinterpret_cast<int*>(sm + L::offPage);
-  uint64_t* bar_qk = reinterpret_cast<uint64_t*>(sm + L::offBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::offTmem);
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads, h = a.dbg_q_head, kvh = h / G;
-  const int j = a.dbg_k0 / 128 + blockIdx.x;
-
-  if (warp == 0) tc::tmem_alloc(tmem_slot, 128);
-  if (tid == 0) {
-    mbar_init(bar_qk, 1);
-    mbar_fence_init();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *tmem_slot;
-
-  load_q_tile<D>(qs, a.q_codes, a.n_tokens, Hq, h, a.dbg_q0, tid);
-  load_k_tile<D>(ks, sk_s, sv_s, page_s, a, kvh, j, a.n_blocks_row * KVQ_BLOCK_SIZE, tid);
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  if (tid == 0) {
-    tc::fence_after_sync();
-    issue_qk<D>(smem_u32(qs), smem_u32(ks), tmem);
-    tc::commit(bar_qk);
-  }
-  const bool ok = mbar_wait(bar_qk, 0, a.status);
-  tc::fence_after_sync();
-  const bool row_real = a.dbg_q0 + tid < a.n_tokens;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t s[32];
-    tc::ld_32x32b_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * c, s);
-    tc::wait_ld();
-    int32_t* dst = a.dbg_s_out + static_cast<long long>(tid) * a.dbg_nk + 128 * blockIdx.x + 32 * c;
-#pragma unroll
-    for (int e = 0; e < 32; e += 4) {
-      int4 v = make_int4(0, 0, 0, 0);
-      if (row_real && ok)
-        v = make_int4(__float2int_rn(__uint_as_float(s[e])), __float2int_rn(__uint_as_float(s[e + 1])),
-                      __float2int_rn(__uint_as_float(s[e + 2])), __float2int_rn(__uint_as_float(s[e + 3])));
-      *reinterpret_cast<int4*>(dst + e) = v;
-    }
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  if (warp == 0) {
-    tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 128);
   }
 }
 
@@ -1404,24 +1281,29 @@ cudaError_t launch_prefill_q_quant(const PrefillArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-template <int D, bool HP>
+template <int D, bool HP, bool DBG = false>
 static cudaError_t launch_attention(const PrefillArgs& a, cudaStream_t stream) {
   using L = PrefillTmaSmem<D>;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tma_kernel<D, HP>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  auto kern = prefill_tma_kernel<D, HP, DBG>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   dim3 grid(((a.n_tokens + 127) / 128) * a.n_q_heads * (!HP && a.split_tail > 0 ? 2 : 1));
-  return launch_pdl(prefill_tma_kernel<D, HP>, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
+  return launch_pdl(kern, grid, dim3(kPrefillThreads), L::kAlloc, stream, a);
 }
 
-template <int D>
+template <int D, bool DBG>
 static cudaError_t launch_prefill_d(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = launch_pdl(kv_widen_kernel<D>, dim3(a.n_kv_tiles, a.n_kv_heads), dim3(256), 0, stream, a);
   if (e != cudaSuccess) return e;
-  return launch_attention<D, false>(a, stream);
+  return launch_attention<D, false, DBG>(a, stream);
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  return a.head_dim == 256 ? launch_prefill_d<256>(a, stream) : launch_prefill_d<128>(a, stream);
+  return a.head_dim == 256 ? launch_prefill_d<256, false>(a, stream) : launch_prefill_d<128, false>(a, stream);
+}
+
+cudaError_t launch_prefill_qk_debug(const PrefillArgs& a, cudaStream_t stream) {
+  return a.head_dim == 256 ? launch_prefill_d<256, true>(a, stream) : launch_prefill_d<128, true>(a, stream);
 }
 
 template <int D>
@@ -1437,20 +1319,6 @@ static cudaError_t launch_prefill_first_d(const PrefillArgs& a, cudaStream_t str
 
 cudaError_t launch_prefill_first(const PrefillArgs& a, cudaStream_t stream) {
   return a.head_dim == 256 ? launch_prefill_first_d<256>(a, stream) : launch_prefill_first_d<128>(a, stream);
-}
-
-template <int D>
-static cudaError_t launch_qk_debug_d(const PrefillArgs& a, cudaStream_t stream) {
-  using L = PrefillSmem<D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_qk_debug_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-  if (e != cudaSuccess) return e;
-  prefill_qk_debug_kernel<D><<<a.dbg_nk / 128, 128, L::kAlloc, stream>>>(a);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_prefill_qk_debug(const PrefillArgs& a, cudaStream_t stream) {
-  return a.head_dim == 256 ? launch_qk_debug_d<256>(a, stream) : launch_qk_debug_d<128>(a, stream);
 }
 
 }  // namespace kvq

@@ -90,7 +90,10 @@ def lib():
         L.kvq_sparse_workspace_bytes.restype = sz
         L.kvq_sparse_workspace_bytes.argtypes = [i32, i32, i32]
         L.kvq_debug_prefill_q_codes.argtypes = [vp, i32, i32, i32, vp, vp, vp]
-        L.kvq_debug_prefill_qk_int32.argtypes = [cp, vp, i32, i32, vp, i32, i32, i32, i32, i32, vp, vp]
+        L.kvq_debug_fault_inject.argtypes = [i32, ctypes.c_int64]
+        L.kvq_debug_stream_floor.argtypes = [cp, i32, vp, i32, vp, i32, i32, vp]
+        L.kvq_debug_prefill_qk_int32.argtypes = [cp, vp, vp, i32, i32, i32, vp, i32, f32, i32, i32, i32, i32, i32,
+                                                 vp, vp, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -162,9 +165,10 @@ class KVCache:
         self.v_scale = torch.zeros_like(self.k_scale)
 
     def struct(self):
-        return _Cache(self.k.data_ptr(), self.v.data_ptr(), self.k_scale.data_ptr(),
-                      self.v_scale.data_ptr(), self.num_blocks, BLOCK_SIZE, self.n_kv_heads,
-                      self.head_dim)
+        # every cache tensor goes through _p: a cache left in host memory is refused before any
+        # launch (a kernel handed its pageable pointers would fault)
+        ptrs = [_p(t).value for t in (self.k, self.v, self.k_scale, self.v_scale)]
+        return _Cache(*ptrs, self.num_blocks, BLOCK_SIZE, self.n_kv_heads, self.head_dim)
 
 
 def kvq_version():
@@ -324,12 +328,20 @@ def kvq_attn_decode_int8kv_noalloc(cache, q, block_table, ctx_lens, max_ctx, sof
     the split-K partials live in a fixed scratch array inside the library.  `out` (fp32
     [B][Hq][D]) must be provided by the caller; nothing is allocated here."""
     B, Hq, D = q.shape
+    _host_ok("kvq_attn_decode_int8kv_noalloc", q, out)
     o = _decode_opts(split_rows, route_threshold, force_route)
     c = cache.struct()
     _check("kvq_attn_decode_int8kv_noalloc", lib().kvq_attn_decode_int8kv_noalloc(
-        ctypes.byref(c), _p(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
-        int(max_ctx), float(softmax_scale), _p(out), ctypes.byref(o), _stream(stream)))
+        ctypes.byref(c), _hp(q), B, Hq, _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), float(softmax_scale), _hp(out), ctypes.byref(o), _stream(stream)))
     return out
+
+
+def kvq_debug_fault_inject(mode, wait_budget_cycles=0):
+    """Test entry point of the failure path (see kvq.h): mode 0 none, 1 a decode stage-1 copy left
+    un-issued, 2 a prefill piece left un-issued; every bounded wait gives up after
+    wait_budget_cycles (<= 0: the default)."""
+    _check("kvq_debug_fault_inject", lib().kvq_debug_fault_inject(int(mode), int(wait_budget_cycles)))
 
 
 def kvq_prefill_workspace_bytes(n_tokens, n_q_heads, n_kv_heads, history_len, head_dim):
@@ -423,12 +435,30 @@ def kvq_debug_prefill_q_codes(q, stream=None):
     return codes, scales
 
 
-def kvq_debug_prefill_qk_int32(cache, q_codes, block_table_row, q_head, q0, k0, nk, stream=None):
-    """Tensor-core QK tile alone: int32 [128][nk] for query rows q0..q0+127, keys k0..k0+nk-1."""
+def kvq_debug_prefill_qk_int32(cache, q_codes, q_scales, history_len, block_table_row, softmax_scale, q_head, q0,
+                               k0, nk, split_tiles=-1, out=None, workspace=None, stream=None):
+    """The production prefill (kvq_attn_prefill_int8_qcodes) that also exports the integer QK scores
+    of one unit: returns (S int32 [128][nk] for query rows q0..q0+127 of q_head and keys
+    k0..k0+nk-1, out fp32 [T][Hq][D]).  split_tiles: -1 the call's own key-range split, 0 none,
+    r > 0 a forced tail of r key tiles."""
     T, Hq, D = q_codes.shape
     s = torch.empty((128, nk), dtype=torch.int32, device=q_codes.device)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.float32, device=q_codes.device)
+    need = kvq_prefill_workspace_bytes(T, Hq, cache.n_kv_heads, int(history_len), D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_codes.device)
     c = cache.struct()
     _check("kvq_debug_prefill_qk_int32", lib().kvq_debug_prefill_qk_int32(
-        ctypes.byref(c), _p(q_codes), T, Hq, _p(block_table_row), int(block_table_row.numel()),
-        int(q_head), int(q0), int(k0), int(nk), _p(s), _stream(stream)))
-    return s
+        ctypes.byref(c), _p(q_codes), _p(q_scales), T, Hq, int(history_len), _p(block_table_row),
+        int(block_table_row.numel()), float(softmax_scale), int(split_tiles), int(q_head), int(q0), int(k0), int(nk),
+        _p(s), _p(out), _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return s, out
+
+
+def kvq_debug_stream_floor(cache, block_table, ctx_lens, max_ctx, split_rows=0, stream=None):
+    """The K/V stream of decode stage 1 alone (same grid, rings and copies, no arithmetic)."""
+    c = cache.struct()
+    _check("kvq_debug_stream_floor", lib().kvq_debug_stream_floor(
+        ctypes.byref(c), int(block_table.shape[0]), _p(block_table), int(block_table.shape[1]), _p(ctx_lens),
+        int(max_ctx), int(split_rows), _stream(stream)))

@@ -169,8 +169,9 @@ void rope_row(float* x, const float* cs, int r) {
 // Deterministic base-2 exponential shared, as a specification, by the oracle and the
 // CUDA prefill kernel (each has its own code): the argument is clamped to [-125, 125] (with the
 // fmax / fmin rule, so NaN becomes -125), then Cody-Waite range reduction x = n + f with
-// n = rint(x), f in [-1/2, 1/2], 2^f by a degree-4 polynomial with constant term 1, fitted to
-// the minimax relative error of 2^f on [-1/2, 1/2], in Horner form with fp32 fma, and scaling
+// n = rint(x), f in [-1/2, 1/2], 2^f by a degree-4 polynomial with constant term 1 whose other
+// four coefficients minimise the largest relative error of 2^f on [-1/2, 1/2] (2.82e-6; found,
+// and rounded to fp32, by oracle/fit_exp2_poly.py), in Horner form with fp32 fma, and scaling
 // by 2^n.  Relative error against 2^x is below 3.6e-6 on [-125, 125] (fit error plus fp32
 // rounding); integers are exact (f = 0 gives p = 1); below -125 the result is 2^-125.  It
 // exists so that the P-code decisions below are the same fp32 decisions on both sides.
@@ -180,9 +181,9 @@ float exp2_det(float x) {
   float t = x + magic;
   float n = t - magic;
   float f = x - n;
-  float p = std::fma(0.00966636837f, f, 0.0559219755f);
-  p = std::fma(p, f, 0.240223497f);
-  p = std::fma(p, f, 0.693121016f);
+  float p = std::fma(0.00958285294f, f, 0.0559064262f);
+  p = std::fma(p, f, 0.240240991f);
+  p = std::fma(p, f, 0.693124175f);
   p = std::fma(p, f, 1.0f);
   int ni = static_cast<int>(n);
   uint32_t bits = static_cast<uint32_t>(ni + 127) << 23;

@@ -159,5 +159,8 @@ def test_host_tensors_refused_before_launch():
     with pytest.raises(ValueError):
         k.kvq.kvq_attn_prefill_int8(cache, rows.view(2, 1, 128), 0, torch.zeros(4, dtype=torch.int32), 0.1,
                                     out=torch.zeros((2, 1, 128)), workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+    # the cache itself: its four tensors are checked like every other argument
+    with pytest.raises(ValueError):
+        cache.struct()
     # a pageable tensor is not device-accessible
     assert not k.kvq_device_accessible(torch.from_numpy(np.zeros(16, np.float32)))

@@ -101,8 +101,9 @@ def test_decode_1k_full(kvq, oracle):
 
 
 def test_decode_32k_full(kvq, oracle):
-    """Workload decode_32k at full size in the benchmark's launch configuration (split-K,
-    512-key splits, shuffled pages, K outliers): every output against FP64."""
+    """Workload decode_32k at full size at the split size its configuration states (split-K with
+    512-key splits, shuffled pages, K outliers; the benchmark's own call, the fused step with the
+    automatic split, is checked in full in test_gpu_step.py): every output against FP64."""
     w = W.make("decode_32k")
     got, _, _ = _run(kvq, w, split_rows=w["split_rows"])
     hc = host_cache_from(w, oracle)
@@ -156,3 +157,21 @@ def test_decode_b64_full_sampled(kvq, oracle):
     print("decode_b64 normalised max err (sampled)", err)
     assert err <= GATE and err <= DESIGN_TOL
     del torch
+
+
+def test_ctx_above_max_ctx_is_clamped_and_reported(kvq, oracle):
+    """A ctx_lens entry above the host bound max_ctx (but within the pages its block-table row
+    maps) breaks the call's contract: both routes clamp it to max_ctx, set KVQ_DEV_BAD_POS, and
+    agree with the FP64 reference over max_ctx keys."""
+    w = W.make("decode_32k", seed=1400, batch=2, ctx=1000, hq=8, hkv=2, d=128)
+    cache, bt = gpu_cache_from(w, kvq)
+    hc = host_cache_from(w, oracle)
+    max_ctx = 900
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], np.full(2, max_ctx, np.int32), w["softmax_scale"])
+    q, ctx = to_bf16_tensor(w["q"]), to_i32(w["ctx_lens"])
+    kvq.kvq_device_status()
+    for route in (1, 2):
+        got = kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, max_ctx, w["softmax_scale"], force_route=route,
+                                         split_rows=256).cpu().numpy()
+        assert kvq.kvq_device_status() & kvq.kvq.DEV_BAD_POS, route
+        assert norm_max_err(got, ref) <= DESIGN_TOL, route

@@ -70,8 +70,10 @@ def test_step_writes_and_attends(kvq, oracle, nq, d, hq, hkv, route):
 
 
 def test_one_token_step_3d_and_decode_32k_shape(kvq, oracle):
-    """The headline step's shape (ctx 32768, 24/4, head_dim 256, automatic split): the new token
-    is the last of the last split."""
+    """The benchmark's call in full: the fused step at workload decode_32k (ctx 32768, 24/4,
+    head_dim 256, shuffled pages, K outliers) with the automatic split and no option set, the new
+    token the last of the last split.  The rewritten cache bit for bit, and all 24 heads against
+    FP64."""
     w = W.make("decode_32k")
     cache, bt = _cache_without_new(kvq, w)
     kn, vn = _new_rows(w)
@@ -85,9 +87,10 @@ def test_one_token_step_3d_and_decode_32k_shape(kvq, oracle):
     dec = kvq.kvq_attn_decode_int8kv(cache, to_bf16_tensor(w["q"]), bt, to_i32(w["ctx_lens"]), w["max_ctx"],
                                      w["softmax_scale"]).cpu().numpy()
     assert np.array_equal(out, dec)
-    units = np.array([0, 5, 11, 17, 23], np.int64)
-    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"], units=units)
-    assert norm_max_err(out.reshape(-1, w["d"])[units], ref) <= DESIGN_TOL
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    err = norm_max_err(out, ref)
+    print("decode_32k fused step (automatic split), all heads: normalised max err", err)
+    assert err <= DESIGN_TOL
 
 
 def test_step_with_short_context_writes_nothing_and_flags(kvq):

@@ -82,3 +82,21 @@ def test_pageable_host_memory_is_refused(kvq):
         kvq.kvq_attn_decode_int8kv(cache, q_pageable, bt, to_i32(w["ctx_lens"]), w["max_ctx"], w["softmax_scale"])
     torch.cuda.synchronize()
     assert kvq.kvq_device_status() == 0
+
+
+def test_host_cache_with_device_inputs_refused():
+    """A cache left in host memory is refused before launch even when every other argument is a
+    device tensor (the decode calls accept mapped host memory for q and out only)."""
+    import torch
+
+    import int8_kv_cache_quant_gb300 as kvq
+    cache = kvq.KVCache(4, 1, 128, device="cpu")
+    q = torch.zeros((1, 2, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    ctx = torch.ones(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, 64, 0.1)
+    rows = torch.zeros((1, 1, 128), dtype=torch.bfloat16, device="cuda")
+    idx = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        kvq.kvq_quant_write(cache, rows, rows, idx, idx, bt)

@@ -606,6 +606,22 @@ def test_int8_emul_uniform_v_close_to_v(oracle):
     assert np.allclose(b, vhat[None, None, :], rtol=1 / 200, atol=1e-12)
 
 
+def test_exp2_det_coefficients_are_the_minimax_fit(oracle):
+    # The polynomial's four coefficients are the ones the committed Remez fit produces (rounded to
+    # fp32): the fit is the minimax relative error of 2^f on [-1/2, 1/2] with constant term 1.
+    from oracle import fit_exp2_poly as fit
+    c, err = fit.remez()
+    assert 2.7e-6 < err < 2.9e-6
+    src = open(os.path.join(os.path.dirname(GOLDEN), "..", "oracle", "kvq_oracle.cpp")).read()
+    body = src[src.index("float exp2_det(float x) {"):]
+    body = body[:body.index("\n}\n")]
+    for ci in np.asarray(c, np.float32):
+        assert ("%.9gf" % ci) in body, ci
+    # and the fitted polynomial's error, exactly evaluated, is its minimax value
+    grid = np.linspace(-0.5, 0.5, 100001)
+    assert np.abs(fit._err(np.asarray(c, np.float32).astype(np.float64), grid)).max() < 2.9e-6
+
+
 def test_exp2_det_against_exp2(oracle):
     import math
     xs = np.concatenate([np.linspace(-124.9, 0.0, 20001), -np.arange(0, 125, dtype=np.float64),

@@ -55,3 +55,25 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     with pytest.raises(kvq.KvqError) as e:
         kvq.kvq_attn_decode_int8kv_noalloc(cache, q, bt, ctx, 65536, 0.1, out)
     assert e.value.status == 4
+
+
+def test_noalloc_limit_applies_to_the_split_it_takes():
+    """A shape whose partials at the smallest automatic split (the bound kvq_decode_workspace_bytes
+    states) exceed the scratch array, but whose partials at the split size this GPU takes fit:
+    accepted, and equal to the regular entry point's result."""
+    import torch
+
+    import int8_kv_cache_quant_gb300 as kvq
+    kvq.lib()
+    w = W.make("decode_32k", seed=903, batch=1, ctx=32768, hq=48, hkv=6, d=256)
+    assert kvq.kvq_decode_workspace_bytes(1, 48, 32768, 256) > kvq.kvq.NOALLOC_SCRATCH_BYTES
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    split = kvq.kvq_decode_auto_split_rows(1, 6, 256, 32768, sms)
+    assert kvq.kvq_decode_workspace_bytes(1, 48, 32768, 256, split_rows=split) <= kvq.kvq.NOALLOC_SCRATCH_BYTES
+    cache, bt = gpu_cache_from(w, kvq)
+    q, ctx = to_bf16_tensor(w["q"]), to_i32(w["ctx_lens"])
+    ref = kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"]).cpu().numpy()
+    out = torch.full((1, 48, 256), float("nan"), dtype=torch.float32, device="cuda")
+    kvq.kvq_attn_decode_int8kv_noalloc(cache, q, bt, ctx, w["max_ctx"], w["softmax_scale"], out)
+    assert norm_max_err(out.cpu().numpy(), ref) <= DESIGN_TOL
+    assert kvq.kvq_device_status() == 0
