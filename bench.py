@@ -3,9 +3,10 @@
 A step of the headline workload (decode_32k: one sequence, ctx 32768, 24 query / 4 KV heads,
 head_dim 256, int8 K/V in 16-token pages behind a shuffled block table, K outliers) is one
 pass of the decode path: kv_quant_write of the step's new token, then split-K decode over
-the whole context (split-K with the library's split size for this GPU, stage 1 + merge).  value = K/V bytes the step reads
-(2080 B per token) / device time of the step, in GB/s, with the L2 flushed (256 MB write)
-before every timed step, outside its events.
+the whole context (split-K with the library's split size for this GPU: stage 1, then the merge).
+value = K/V bytes the step reads
+(2080 B per token) / device time of the step, in GB/s, with the L2 flushed (256 MB write, then a
+256 MB read of another buffer) before every timed step, outside its events.
 
 Prints one JSON line.  --impl reference times the CPU oracle (the plain reference) on the
 host cores on a bounded sample of the same workload.  Under torchrun (N > 1) every rank runs
@@ -32,10 +33,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel (dram__bytes_read.sum + dram__bytes_write.sum), and the SHA-256 prefix of the kernel's
 # sources at that capture.  Once the sources differ, the figure no longer describes the kernel
 # and the line reports null.
-STAGE1_TRAFFIC_BYTES = 68237824 + 128000
+STAGE1_TRAFFIC_BYTES = 68242688 + 143872
 STAGE1_TRAFFIC_SOURCES = ("int8_kv_cache_quant_gb300/csrc/decode.cu", "int8_kv_cache_quant_gb300/csrc/kvq_dev.cuh",
                           "int8_kv_cache_quant_gb300/csrc/quant_rule.cuh")
-STAGE1_TRAFFIC_SHA = "c19f57ad1cb4481d"
+STAGE1_TRAFFIC_SHA = "0e06a5e3bc4a683e"
 
 
 def stage1_traffic():
@@ -207,9 +208,13 @@ def bench_decode_32k(args, world, rank, local, extra_out):
 
     def cold_l2(i):
         # write 256 MB (> the 129 MB L2), then read another 256 MB so that the L2 holds clean
-        # lines of an unrelated buffer: the timed step then starts cold and pays no write-back
+        # lines of an unrelated buffer: the timed step then starts cold and pays no write-back.
+        # A ~30 us device sleep follows, so that the host has queued the step's launches before
+        # the GPU reaches the start event: the events then time device work, not the host's
+        # argument marshalling (e2e below is the figure with the host in it).
         flush.fill_(i & 0xFF)
         sweep.sum()
+        torch.cuda._sleep(60000)
 
     def step(ev=None):
         # the fused step: stage 1 writes the new token into its page, then attends
@@ -274,6 +279,46 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         ev3[i].record(s)
     torch.cuda.synchronize()
     step_ms_unfused = statistics.mean(a.elapsed_time(b) for a, b in zip(ev2, ev3))
+    # kernels one step launches (stage 1 and the merge on the split route)
+    import ctypes
+    n_launch = ctypes.c_int32(0)
+    kvq.kvq_decode_step_int8kv(cache, k_new, v_new, q, bt, ctx, max_ctx, w["softmax_scale"], out=out, workspace=ws,
+                               launches=n_launch)
+    torch.cuda.synchronize()
+    launches_per_step = int(n_launch.value)
+
+    def time_events(fn, with_stage1=False):
+        t_all, t_s1 = [], []
+        for i in range(K):
+            cold_l2(i)
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            if with_stage1:
+                e[2].record(s)
+                e[3].record(s)
+            e[0].record(s)
+            fn((e[2], e[3]) if with_stage1 else None)
+            e[1].record(s)
+            torch.cuda.synchronize()
+            t_all.append(e[0].elapsed_time(e[1]))
+            if with_stage1:
+                t_s1.append(e[2].elapsed_time(e[3]))
+        return statistics.mean(t_all), (statistics.mean(t_s1) if with_stage1 else None)
+
+    # The stream floor: decode stage 1's grid, rings and bulk copies of the same pages, with no
+    # arithmetic (kvq_debug_stream_floor), timed like the step.
+    floor_ms, _ = time_events(lambda ev: kvq.kvq_debug_stream_floor(cache, bt, ctx, max_ctx))
+    # The stated configuration's 512-key splits (64 splits x 4 KV heads = 256 CTAs, two waves:
+    # the split route then ends in the separate merge kernel), beside the automatic split above.
+    ws512 = torch.empty(kvq.kvq_decode_workspace_bytes(1, Hq, max_ctx, D, split_rows=512), dtype=torch.uint8,
+                        device=dev)
+
+    def step512(ev):
+        kvq.kvq_decode_step_int8kv(cache, k_new, v_new, q, bt, ctx, max_ctx, w["softmax_scale"], out=out,
+                                   workspace=ws512, split_rows=512, stage1_events=ev)
+    step512(None)
+    torch.cuda.synchronize()
+    ms512, _ = time_events(step512)
+    _, s1_512 = time_events(step512, with_stage1=True)
     ms_step = statistics.mean(step_ms)
     ms_step_max = max_over_ranks(ms_step, world)
     kv_bytes = max_ctx * (2 * Hkv * D + 2 * Hkv * 4)  # 2080 B per token at 4 x 256
@@ -318,6 +363,8 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         out_copy_h.copy_(out, non_blocking=True)
 
     def time_e2e(fn):
+        # no device sleep here: the host's work of each call (argument checks and marshalling)
+        # stays inside the timed region
         for i in range(3):
             cold_l2(2)
             fn(i)
@@ -325,7 +372,8 @@ def bench_decode_32k(args, world, rank, local, extra_out):
         e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         for i in range(K):
-            cold_l2(i)
+            flush.fill_(i & 0xFF)
+            sweep.sum()
             e0[i].record(s)
             fn(i)
             e1[i].record(s)
@@ -335,6 +383,8 @@ def bench_decode_32k(args, world, rank, local, extra_out):
     e2e_ms = time_e2e(e2e_step)
     e2e_copy_ms = time_e2e(e2e_copy_step)
     for i in range(NSET):  # each set's host result against the step with device buffers
+        e2e_step(i)
+        torch.cuda.synchronize()
         in_d.copy_(sets[i][0])
         kvq.kvq_decode_step_int8kv(cache, kn_d, vn_d, q_d, bt, ctx, max_ctx, w["softmax_scale"], out=out,
                                    workspace=ws)
@@ -379,7 +429,18 @@ def bench_decode_32k(args, world, rank, local, extra_out):
                 "with_copies": {"value": round(aggregate_gbs(kv_bytes, e2e_copy_ms, world), 2),
                                 "ms_per_step": round(e2e_copy_ms, 5),
                                 "transfer": "one H2D copy of the staged inputs, the call, one D2H copy"}},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches_per_step * K,
+        "launches_per_step": launches_per_step,
+        "stream_floor": {"us": round(floor_ms * 1e3, 2), "GBps": round(kv_bytes / (floor_ms * 1e-3) / 1e9, 1),
+                         "frac": round(kv_bytes / (floor_ms * 1e-3) / 1e9 / hbm, 4),
+                         "what": "kvq_debug_stream_floor: stage 1's grid, rings and bulk copies of the same 68 MB "
+                                 "of pages, no arithmetic, timed like the step (cold L2, CUDA events)",
+                         "stage1_over_floor": round(kern_avg / floor_ms, 3)},
+        "split_512": {"split_rows": 512, "us_per_step": round(ms512 * 1e3, 2),
+                      "GBps": round(kv_bytes / (ms512 * 1e-3) / 1e9, 1),
+                      "stage1_us": round(s1_512 * 1e3, 2),
+                      "stage1_frac": round(kv_bytes / (s1_512 * 1e-3) / 1e9 / hbm, 4),
+                      "what": "the stated 512-key splits: 256 stage-1 CTAs in two waves, then the merge kernel"},
         "clocks": clk.summary(),
         "wall_s_timed_region": round(t_wall, 4),
     }
@@ -408,6 +469,7 @@ def bench_extra(args, local, hbm, tflops, only=None):
     def cold_l2(i):
         flush.fill_(i & 0xFF)
         sweep.sum()
+        torch.cuda._sleep(60000)  # the host's launches get ahead of the GPU (device-only timing)
 
     def timed(fn, reps, cold=True):
         """Median event time of one call; L2 flushed before each (cold) or still holding the

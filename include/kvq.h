@@ -161,6 +161,9 @@ typedef struct kvq_decode_opts {
    * and right after the stage-1 (K/V streaming) kernel launch; NULL to skip. */
   void* stage1_event_begin;
   void* stage1_event_end;
+  /* Optional: receives the number of kernels the call launched (1: the single-CTA route; 2: the
+   * split route's stage 1 and its merge).  NULL to skip. */
+  int32_t* launches;
 } kvq_decode_opts;
 
 /* Workspace (bytes) the split route of kvq_attn_decode_int8kv needs; 0 when the call

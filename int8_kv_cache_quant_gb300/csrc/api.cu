@@ -49,13 +49,14 @@ int check_cache(const kvq_cache* c) {
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
 kvq_decode_opts decode_defaults(const kvq_decode_opts* o) {
-  kvq_decode_opts r = {0, 0, 0, nullptr, nullptr};  // split_rows 0: sized to the GPU; route 0: automatic
+  kvq_decode_opts r = {0, 0, 0, nullptr, nullptr, nullptr};  // split_rows 0: sized to the GPU; route 0: automatic
   if (o) {
     if (o->split_rows > 0) r.split_rows = o->split_rows;
     if (o->route_threshold > 0) r.route_threshold = o->route_threshold;
     r.force_route = o->force_route;
     r.stage1_event_begin = o->stage1_event_begin;
     r.stage1_event_end = o->stage1_event_end;
+    r.launches = o->launches;
   }
   return r;
 }
@@ -342,10 +343,16 @@ static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_
     const long long acc_bytes = ((units * cache->head_dim * 4 + 255) / 256) * 256;
     a.part_acc = static_cast<float*>(workspace);
     a.part_stats = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_bytes);
-    return cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSplit, static_cast<cudaStream_t>(stream)));
+    int launched = 0;
+    const int rc = cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSplit, static_cast<cudaStream_t>(stream), &launched));
+    if (o.launches) *o.launches = launched;
+    return rc;
   }
   a.n_split = 1;
-  return cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSingle, static_cast<cudaStream_t>(stream)));
+  int launched = 0;
+  const int rc = cuda_status(kvq::launch_decode(a, kvq::DecodeRoute::kSingle, static_cast<cudaStream_t>(stream), &launched));
+  if (o.launches) *o.launches = launched;
+  return rc;
 }
 
 int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_q_heads,

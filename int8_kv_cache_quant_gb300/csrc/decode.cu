@@ -851,7 +851,8 @@ static cudaError_t launch_stage1_rows(const DecodeArgs& a, dim3 grid, cudaStream
   }
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream, int* launched) {
+  *launched = route == DecodeRoute::kSingle ? 1 : 2;
   if (route == DecodeRoute::kSingle) {
     dim3 grid(1, a.n_kv_heads, a.batch);
     if (a.head_dim == 256) return launch_stage1_rows<256, false>(a, grid, stream);

@@ -88,7 +88,7 @@ struct DecodePlan {
 };
 int decode_plan(const kvq_cache* cache, int32_t batch, int32_t nq, int32_t n_q_heads, int32_t max_ctx,
                 const kvq_decode_opts* opts, DecodePlan* plan);
-cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t stream, int* launched);
 // the stage-1 kernel's K/V stream alone, split route geometry (kvq_debug_stream_floor)
 cudaError_t launch_stream_floor(const DecodeArgs& a, cudaStream_t stream);
 

@@ -38,7 +38,7 @@ class _Cache(ctypes.Structure):
 class _DecodeOpts(ctypes.Structure):
     _fields_ = [("split_rows", ctypes.c_int32), ("route_threshold", ctypes.c_int32),
                 ("force_route", ctypes.c_int32), ("stage1_event_begin", ctypes.c_void_p),
-                ("stage1_event_end", ctypes.c_void_p)]
+                ("stage1_event_end", ctypes.c_void_p), ("launches", ctypes.POINTER(ctypes.c_int32))]
 
 
 _lib = None
@@ -217,11 +217,12 @@ def kvq_rope_quant_write(cache, q, k_new, v_new, seq_idx, pos, block_table, cos_
     return q_codes, q_scales, q_rot
 
 
-def _decode_opts(split_rows, route_threshold, force_route, events=None):
+def _decode_opts(split_rows, route_threshold, force_route, events=None, launches=None):
     ev0 = ev1 = None
     if events is not None:
         ev0, ev1 = (ctypes.c_void_p(e.cuda_event) for e in events)
-    return _DecodeOpts(int(split_rows), int(route_threshold), int(force_route), ev0, ev1)
+    return _DecodeOpts(int(split_rows), int(route_threshold), int(force_route), ev0, ev1,
+                       ctypes.pointer(launches) if launches is not None else None)
 
 
 def kvq_decode_auto_split_rows(batch, n_kv_heads, head_dim, max_ctx, n_sms):
@@ -291,7 +292,7 @@ def kvq_attn_verify_int8kv(cache, q, block_table, ctx_lens, max_ctx, softmax_sca
 
 def kvq_decode_step_int8kv(cache, k_new, v_new, q, block_table, ctx_lens, max_ctx, softmax_scale, out=None,
                            workspace=None, split_rows=0, route_threshold=0, force_route=0,
-                           stream=None, stage1_events=None):
+                           stream=None, stage1_events=None, launches=None):
     """One decode step: write each sequence's nq newest tokens (k_new / v_new bf16
     [B][nq][Hkv][D], positions ctx_lens[b] - nq + j) into the cache, then attend with their
     query rows q bf16 [B][nq][Hq][D].  A 3-D q ([B][Hq][D]) with 3-D k_new / v_new
@@ -306,7 +307,7 @@ def kvq_decode_step_int8kv(cache, k_new, v_new, q, block_table, ctx_lens, max_ct
     else:
         ret = out  # the caller's buffer, in the caller's shape ([B][Hq][D] for the one-token step)
     _host_ok("kvq_decode_step_int8kv", q, k_new, v_new, out)
-    o = _decode_opts(split_rows, route_threshold, force_route, stage1_events)
+    o = _decode_opts(split_rows, route_threshold, force_route, stage1_events, launches)
     need = int(lib().kvq_verify_workspace_bytes(B, nq, Hq, max(1, int(max_ctx)), D, ctypes.byref(o)))
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=cache.k.device)
