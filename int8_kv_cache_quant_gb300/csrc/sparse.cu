@@ -164,15 +164,32 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, 2) sparse_kernel(SparseArgs a
   uint32_t* pmask = cmask + p * DEPTH;
   uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
 
+  // Cell positions of the team's tiles, loaded DEPTH tiles ahead of their copies (lane l < 16
+  // holds cell l of a tile; pos_q[k % DEPTH] holds tile k's): the tiles are issued in order, so
+  // the index load of tile k + DEPTH goes out right after tile k's copies and has DEPTH tiles of
+  // work to arrive, instead of stalling the issuing warp on a memory round trip every tile.
+  auto load_pos = [&](int k) {
+    const int cb = c_begin + (p + k * NTEAM) * kTile;
+    return (k < npp && lane < kTile && cb + lane < c_end) ? __ldg(a.cells + cb + lane) : -1;
+  };
+  int pos_q[DEPTH];
+#pragma unroll
+  for (int k = 0; k < DEPTH; ++k) pos_q[k] = nt == 0 ? load_pos(k) : -1;
   // the issuing warp, collectively: copy the records of tile k's cells into its slot (lane l < 16
   // copies cell l); cells outside the list or the mapped range are not copied and are masked
   auto issue = [&](int k) {
     const int s = k % DEPTH;
     const int cb = c_begin + (p + k * NTEAM) * kTile;
+    int pos = -1;
+#pragma unroll
+    for (int d = 0; d < DEPTH; ++d)
+      if (d == s) {
+        pos = pos_q[d];
+        pos_q[d] = load_pos(k + DEPTH);
+      }
     bool ok = false;
     long long rec = 0;
     if (lane < kTile && cb + lane < c_end) {
-      const int pos = a.cells[cb + lane];
       if (pos >= 0 && pos / KVQ_BLOCK_SIZE < a.n_blocks_row) {
         ok = true;
         rec = ((static_cast<long long>(pos / KVQ_BLOCK_SIZE) * a.n_kv_heads + kvh) * KVQ_BLOCK_SIZE +
