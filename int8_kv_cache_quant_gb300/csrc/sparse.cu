@@ -13,18 +13,11 @@
 //   head, slot): [K codes D][V codes D][k_scale][v_scale][valid][pad], 2D + 16 bytes.  Each
 //   selected cell is then one contiguous bulk copy, and the record stride (33 or 17 units of
 //   16 bytes) keeps the ldmatrix rows of 8 cells in 8 distinct bank groups.
-// * Attention.  As decode's stage 1 with cells for page slots: teams of NT warps (NT = ceil(G /
-//   8)) stream 16-cell tiles through DEPTH-stage rings of bulk copies on mbarriers; warp nt of
-//   a team holds query heads 8nt..8nt+7.  QK: S^T = K * Q^T on mma.sync m16n8k16 (cells on M,
-//   heads on N) with the int8 codes widened to integer-valued fp16 (exact).  PV: O^T += V^T * W
-//   with the V^T fragments taken straight from the token-major records by ldmatrix.trans: for an
-//   8-cell x 16-dim block a lane receives V[2c][2g], V[2c][2g+1], V[2c+1][2g], V[2c+1][2g+1]
-//   (c = lane % 4, g = lane / 4), and byte selectors (0, 2) / (1, 3) split that into the A
-//   fragments of an even-dimension and an odd-dimension M-tile.  W = p * sV is split into fp16
-//   hi + lo parts (two MMAs), and a second running maximum carries log2 sV, as in decode.
-// * Precision: fp32 accumulation throughout; the page's chunked fold ("summed from zero and
-//   folded with one fma") only changes fp32 rounding, and the tests hold the result to 1e-4 of
-//   the FP64 reference.
+// * Attention (sparse_chunk_kernel, below): one CTA of four warps per (query, KV head) walks the
+//   cells in 64-cell chunks with the page's blocked fold: the chunk's scores give the chunk
+//   maximum, the chunk's sums start from zero relative to the updated maximum, and they are folded
+//   into the running sums with one fma each.  QK and PV run on mma.sync with the int8 codes widened
+//   exactly to fp16 (each code once per query), the weights as fp16 hi + lo parts.
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
 
@@ -33,33 +26,12 @@ namespace kvq {
 namespace {
 
 constexpr float kLog2eS = 1.4426950408889634f;
-constexpr int kTile = 16;                 // cells per tile (M of the QK MMA, K of the PV MMA)
-constexpr float kLazyRescaleS = 8.0f;     // keep a running maximum until a tile exceeds it by 2^8
 
 template <int D>
 struct SparseRec {
   static constexpr int kBytes = 2 * D + 16;  // K | V | k_scale | v_scale | valid | pad
   static constexpr int kV = D;
   static constexpr int kScales = 2 * D;
-};
-
-template <int D, int NT, int NTEAM, int DEPTH>
-struct SparseSmem {
-  static constexpr int kWarps = NT * NTEAM;
-  static constexpr int kRows = NT * 8;
-  static constexpr int kStageBytes = kTile * SparseRec<D>::kBytes;
-  static constexpr int kStages = NTEAM * DEPTH;
-  static constexpr int kRingBytes = kStages * kStageBytes;
-  static constexpr int kQOffset = kRingBytes;
-  static constexpr int kQBytes = NT * D * 16;
-  static constexpr int kBarOffset = kQOffset + kQBytes;            // full [team][DEPTH], empty [team][DEPTH]
-  static constexpr int kMaskOffset = kBarOffset + 2 * kStages * 8;  // copied-cell mask per stage
-  static constexpr int kCqOffset = kMaskOffset + kStages * 4;
-  static constexpr int kTotal = kCqOffset + kRows * 4;
-  static constexpr int kMergeBytes = (kWarps * 8 * (D + 4) + kWarps * 8 * 4 + kWarps * 8 + kRows * 4) * 4;
-  static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the ring");
-  static_assert(kTotal <= 227 * 1024, "shared memory of one CTA");
-  static_assert(kQOffset % 16 == 0 && kBarOffset % 8 == 0, "ldmatrix / mbarrier alignment");
 };
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
@@ -118,78 +90,114 @@ __global__ void __launch_bounds__(256) sparse_prep_kernel(SparseArgs a) {
   }
 }
 
-// One CTA per (query, KV head): NTEAM teams of NT warps; team p takes tiles p, p + NTEAM, ... of
-// the query's cell list; warp nt of a team holds query heads 8 nt .. 8 nt + 7 of the group.
-template <int D, int NT, int NTEAM, int DEPTH>
-__global__ void __launch_bounds__(NT * NTEAM * 32, 2) sparse_kernel(SparseArgs a) {
-  using L = SparseSmem<D, NT, NTEAM, DEPTH>;
+// ============================================================================ chunked attention
+// [QSA] "Approach": the query's cells are walked in 64-cell chunks; each chunk's scores give the
+// chunk maximum, the running maximum moves to max(m, chunk max), the chunk's weights are summed
+// from zero relative to it (l_c, acc_c), and the chunk is folded into the running sums with one
+// fma each: l = fma(l, alpha, l_c), acc = fma(acc, alpha, acc_c), alpha = 2^(m_old - m_new).
+// One CTA of four warps per (query, KV head); chunk c sits in buffer c % NBUF.
+// * QK: warp w scores the chunk's cells 16 w .. 16 w + 15 against every head of the group (cells
+//   on M, heads on N of mma.sync m16n8k16, the int8 K codes widened once and used for each 8-head
+//   n-tile).  The four warps then agree on each head's chunk maximum through shared memory.
+// * Weights: warp w turns its cells' scores into W = 2^(z - m_z) (z = s + log2 sV: the second
+//   running maximum keeps W in [0, 1] whatever the V scales are) and l_c's part, and leaves W as
+//   fp16 hi + lo PV B-fragments in shared memory.
+// * PV: warp w multiplies all 64 weights into head dims w D/4 .. (w + 1) D/4 - 1 (dims on M via the
+//   ldmatrix.trans V^T fragments of the token-major records, the V codes widened once), from a
+//   zero chunk accumulator, and folds it into its running O^T.
+// Every K and V code is therefore widened once per query, and the four warps' accumulators are
+// disjoint: the CTA needs no merge at the end.
+template <int D, int NHT, int NBUF>
+struct ChunkSmem {
+  static constexpr int kCells = 64;
+  static constexpr int kBufBytes = kCells * SparseRec<D>::kBytes;
+  static constexpr int kQOffset = NBUF * kBufBytes;         // Q^T fragments, NHT n-tiles
+  static constexpr int kWOffset = kQOffset + NHT * D * 16;  // W fragments [tile][n-tile][4][32 lanes]
+  static constexpr int kRedOffset = kWOffset + 4 * NHT * 4 * 32 * 4;  // [3][warp][NHT * 8] floats
+  static constexpr int kCqOffset = kRedOffset + 3 * 4 * NHT * 8 * 4;
+  static constexpr int kMaskOffset = kCqOffset + NHT * 8 * 4;         // [NBUF][warp] copied-cell masks
+  static constexpr int kBarOffset = (kMaskOffset + NBUF * 4 * 4 + 7) / 8 * 8;  // full [NBUF], empty [NBUF]
+  static constexpr int kTotal = kBarOffset + 2 * NBUF * 8;
+  static_assert(kQOffset % 16 == 0 && kWOffset % 16 == 0, "ldmatrix alignment");
+  static_assert(kTotal <= 227 * 1024, "shared memory of one CTA");
+};
+
+// bar.sync on barrier 1 of the CTA's 128 threads, returning the OR of pred over them
+__device__ __forceinline__ bool chunk_bar_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.or.pred p, 1, 128, q;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void chunk_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <int D, int NHT, int NBUF>
+__global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(SparseArgs a) {
+  using L = ChunkSmem<D, NHT, NBUF>;
   using R = SparseRec<D>;
-  constexpr int NW = L::kWarps;
   constexpr int RB = R::kBytes;
-  constexpr int NMT = D / 16;  // 16-dim M-tiles of O^T
+  constexpr int NH = NHT * 8;     // heads of the group, padded to whole n-tiles
+  constexpr int NDB = D / 128;    // 32-dim blocks of a warp's quarter of the head dimension
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;
   uint8_t* q_s = smem + L::kQOffset;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
-  uint64_t* empty = full + L::kStages;
-  uint32_t* cmask = reinterpret_cast<uint32_t*>(smem + L::kMaskOffset);
+  uint32_t* wx = reinterpret_cast<uint32_t*>(smem + L::kWOffset);
+  float* red = reinterpret_cast<float*>(smem + L::kRedOffset);
   float* cq_s = reinterpret_cast<float*>(smem + L::kCqOffset);
+  uint32_t* cmask = reinterpret_cast<uint32_t*>(smem + L::kMaskOffset);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOffset);
+  uint64_t* empty = full + NBUF;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p = warp / NT, nt = warp % NT;
   const int i = blockIdx.x, kvh = blockIdx.y;
   const int Hq = a.n_q_heads, G = Hq / a.n_kv_heads;
 
   grid_dep_wait();  // the records come from the pre-pass
   const int c_begin = a.cell_offsets[i], c_end = a.cell_offsets[i + 1];
   const int n_cells = max(0, c_end - c_begin);
-  const int n_tiles = (n_cells + kTile - 1) / kTile;
-  if (n_tiles == 0) {
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x)
-      a.out[(static_cast<long long>(i) * Hq + kvh * G + e / D) * D + e % D] = 0.0f;
+  const int n_chunks = (n_cells + L::kCells - 1) / L::kCells;
+  float* out_q = a.out + (static_cast<long long>(i) * Hq + kvh * G) * D;
+  if (n_chunks == 0) {
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) out_q[e] = 0.0f;
     return;
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      if (NT > 1) mbar_init(&empty[s], NT);
+    for (int b = 0; b < NBUF; ++b) {
+      mbar_init(&full[b], 4);
+      mbar_init(&empty[b], 4);
     }
     mbar_fence_init();
   }
   __syncthreads();
 
-  const int npp = (p < n_tiles) ? (n_tiles - p + NTEAM - 1) / NTEAM : 0;  // tiles of this team
-  uint64_t* pfull = full + p * DEPTH;
-  uint64_t* pempty = empty + p * DEPTH;
-  uint32_t* pmask = cmask + p * DEPTH;
-  uint8_t* pring = ring + p * DEPTH * L::kStageBytes;
-
-  // Cell positions of the team's tiles, loaded DEPTH tiles ahead of their copies (lane l < 16
-  // holds cell l of a tile; pos_q[k % DEPTH] holds tile k's): the tiles are issued in order, so
-  // the index load of tile k + DEPTH goes out right after tile k's copies and has DEPTH tiles of
-  // work to arrive, instead of stalling the issuing warp on a memory round trip every tile.
-  auto load_pos = [&](int k) {
-    const int cb = c_begin + (p + k * NTEAM) * kTile;
-    return (k < npp && lane < kTile && cb + lane < c_end) ? __ldg(a.cells + cb + lane) : -1;
+  // Warp w copies cells 16 w + l (lane l < 16) of each chunk.  Their positions are loaded NBUF
+  // chunks ahead of the copies (pos_q[c % NBUF] holds chunk c's), so no copy waits on an index load.
+  auto load_pos = [&](int c) {
+    const int cell = c_begin + c * L::kCells + warp * 16 + lane;
+    return (c < n_chunks && lane < 16 && cell < c_end) ? __ldg(a.cells + cell) : -1;
   };
-  int pos_q[DEPTH];
+  int pos_q[NBUF];
 #pragma unroll
-  for (int k = 0; k < DEPTH; ++k) pos_q[k] = nt == 0 ? load_pos(k) : -1;
-  // the issuing warp, collectively: copy the records of tile k's cells into its slot (lane l < 16
-  // copies cell l); cells outside the list or the mapped range are not copied and are masked
-  auto issue = [&](int k) {
-    const int s = k % DEPTH;
-    const int cb = c_begin + (p + k * NTEAM) * kTile;
+  for (int b = 0; b < NBUF; ++b) pos_q[b] = load_pos(b);
+  int n_issued = 0;
+  auto issue = [&](int c) {
+    const int b = c % NBUF;
     int pos = -1;
 #pragma unroll
-    for (int d = 0; d < DEPTH; ++d)
-      if (d == s) {
+    for (int d = 0; d < NBUF; ++d)
+      if (d == b) {
         pos = pos_q[d];
-        pos_q[d] = load_pos(k + DEPTH);
+        pos_q[d] = load_pos(c + NBUF);
       }
+    const int cell = c_begin + c * L::kCells + warp * 16 + lane;
     bool ok = false;
     long long rec = 0;
-    if (lane < kTile && cb + lane < c_end) {
+    if (lane < 16 && cell < c_end) {
       if (pos >= 0 && pos / KVQ_BLOCK_SIZE < a.n_blocks_row) {
         ok = true;
         rec = ((static_cast<long long>(pos / KVQ_BLOCK_SIZE) * a.n_kv_heads + kvh) * KVQ_BLOCK_SIZE +
@@ -200,18 +208,18 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, 2) sparse_kernel(SparseArgs a
     }
     const uint32_t m = __ballot_sync(0xffffffffu, ok);
     if (lane == 0) {
-      pmask[s] = m;
+      cmask[b * 4 + warp] = m;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&pfull[s], __popc(m) * RB);
+      mbar_arrive_expect_tx(&full[b], __popc(m) * RB);
     }
     __syncwarp();
-    if (ok) bulk_g2s(pring + s * L::kStageBytes + lane * RB, a.records + rec, RB, &pfull[s]);
+    if (ok) bulk_g2s(ring + b * L::kBufBytes + (warp * 16 + lane) * RB, a.records + rec, RB, &full[b]);
+    ++n_issued;
   };
-  if (nt == 0)
-    for (int k = 0; k < min(DEPTH, npp); ++k) issue(k);
+  for (int c = 0; c < min(NBUF, n_chunks); ++c) issue(c);
 
   // ---- Q^T fragments (as decode): row r = head r of the group, fp16 q * 2^e per head
-  for (int h = warp; h < L::kRows; h += NW) {
+  for (int h = warp; h < NH; h += 4) {
     const bool real = h < G;
     uint8_t* q_tile = q_s + (h >> 3) * (D * 16);
     const int hr = h & 7;
@@ -254,196 +262,248 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, 2) sparse_kernel(SparseArgs a
   }
   __syncthreads();
 
-  const int g = lane >> 2, c = lane & 3;
-  float o_acc[NMT][4];
+  const int g = lane >> 2, c4 = lane & 3;
+  // running statistics of this thread's heads nt * 8 + 2 c4 + e (the same in all four warps)
+  float ms[NHT][2], mz[NHT][2], lsum[NHT][2], cq[NHT][2];
+  float o_acc[2 * NDB][NHT][4];
 #pragma unroll
-  for (int t = 0; t < NMT; ++t) o_acc[t][0] = o_acc[t][1] = o_acc[t][2] = o_acc[t][3] = 0.f;
-  float ms[2] = {-INFINITY, -INFINITY}, mz[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
-  const float cq0 = cq_s[nt * 8 + 2 * c], cq1 = cq_s[nt * 8 + 2 * c + 1];
+  for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      ms[nt][e] = -INFINITY;
+      mz[nt][e] = -INFINITY;
+      lsum[nt][e] = 0.f;
+      cq[nt][e] = cq_s[nt * 8 + 2 * c4 + e];
+    }
+#pragma unroll
+  for (int t = 0; t < 2 * NDB; ++t)
+#pragma unroll
+    for (int nt = 0; nt < NHT; ++nt) o_acc[t][nt][0] = o_acc[t][nt][1] = o_acc[t][nt][2] = o_acc[t][nt][3] = 0.f;
 
-  // per-lane ldmatrix offsets.  K: matrix mi = lane / 8 holds cells 8 (mi & 1) + r of dim chunk
-  // (mi >> 1) of the chunk pair; V (transposed load): cells 8 (mi >> 1) + r, dims 16 (mi & 1).
   const int mi = lane >> 3, r = lane & 7;
   const uint32_t k_lane_off = ((mi & 1) * 8 + r) * RB + (mi >> 1) * 16;
   const uint32_t v_lane_off = ((mi >> 1) * 8 + r) * RB + R::kV + (mi & 1) * 16;
-  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + nt * (D * 16) + mi * 128 + r * 16;
+  const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + mi * 128 + r * 16;
+  float* red_s = red;                  // [warp][NH] tile maxima of the scores
+  float* red_z = red + 4 * NH;         // [warp][NH] tile maxima of z
+  float* red_l = red + 8 * NH;         // [warp][NH] parts of l_c
 
-  int k = 0;
-  for (; k < npp; ++k) {
-    const int s = k % DEPTH;
-    const bool got = mbar_wait(&pfull[s], (k / DEPTH) & 1, a.status);
-    const uint8_t* st = pring + s * L::kStageBytes;
-    const uint32_t sbase = smem_u32(st);
+  int c = 0;
+  bool failed = false;
+  for (; c < n_chunks; ++c) {
+    const int b = c % NBUF;
+    const bool got = mbar_wait(&full[b], (c / NBUF) & 1, a.status, kWaitBudgetCycles);
+    const uint8_t* buf = ring + b * L::kBufBytes;
+    const uint32_t bbase = smem_u32(buf);
+    const uint32_t tbase = bbase + warp * 16 * RB;  // this warp's 16 cells
 
-    // ---- S^T = K * Q^T over the head dimension
-    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    // ---- S^T = K * Q^T for this warp's cells, every head
+    float S[NHT][4];
+    {
+      float sa[NHT][4], sb[NHT][4];
 #pragma unroll
-    for (int jj = 0; jj < D / 32; ++jj) {
-      uint32_t r0, r1, r2, r3, a0, a1, a2, a3, q0, q1, q2, q3;
-      ldsm_x4(sbase + jj * 32 + k_lane_off, r0, r1, r2, r3);
-      ldsm_x4(q_lane_off + jj * 512, q0, q1, q2, q3);
-      i8x4_to_h2x2(r0, kSelB01, kSelB23, a0, a2);
-      i8x4_to_h2x2(r1, kSelB01, kSelB23, a1, a3);
-      mma_f16_16816(sa, a0, a1, a2, a3, q0, q1);
-      i8x4_to_h2x2(r2, kSelB01, kSelB23, a0, a2);
-      i8x4_to_h2x2(r3, kSelB01, kSelB23, a1, a3);
-      mma_f16_16816(sb, a0, a1, a2, a3, q2, q3);
+      for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < D / 32; ++jj) {
+        uint32_t r0, r1, r2, r3, a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(tbase + jj * 32 + k_lane_off, r0, r1, r2, r3);
+        i8x4_to_h2x2(r0, kSelB01, kSelB23, a0, a2);
+        i8x4_to_h2x2(r1, kSelB01, kSelB23, a1, a3);
+        i8x4_to_h2x2(r2, kSelB01, kSelB23, b0, b2);
+        i8x4_to_h2x2(r3, kSelB01, kSelB23, b1, b3);
+#pragma unroll
+        for (int nt = 0; nt < NHT; ++nt) {
+          uint32_t q0, q1, q2, q3;
+          ldsm_x4(q_lane_off + nt * (D * 16) + jj * 512, q0, q1, q2, q3);
+          mma_f16_16816(sa[nt], a0, a1, a2, a3, q0, q1);
+          mma_f16_16816(sb[nt], b0, b1, b2, b3, q2, q3);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S[nt][e] = sa[nt][e] + sb[nt][e];
     }
-    if (!__all_sync(0xffffffffu, got)) break;
-    const float S[4] = {sa[0] + sb[0], sa[1] + sb[1], sa[2] + sb[2], sa[3] + sb[3]};
-
-    // ---- online softmax over the tile's cells g and g + 8
-    const uint32_t m = pmask[s];
-    const int4 t0 = *reinterpret_cast<const int4*>(st + g * RB + R::kScales);
-    const int4 t1 = *reinterpret_cast<const int4*>(st + (g + 8) * RB + R::kScales);
+    // ---- scores and this tile's maxima per head
+    const uint32_t m = cmask[b * 4 + warp];
+    const int4 t0 = *reinterpret_cast<const int4*>(buf + (warp * 16 + g) * RB + R::kScales);
+    const int4 t1 = *reinterpret_cast<const int4*>(buf + (warp * 16 + g + 8) * RB + R::kScales);
     const bool c0 = ((m >> g) & 1) != 0, c1 = ((m >> (g + 8)) & 1) != 0;
-    if ((c0 && t0.z == 0) || (c1 && t1.z == 0)) set_status(a.status, KVQ_DEV_BAD_BLOCK);
+    if (got && ((c0 && t0.z == 0) || (c1 && t1.z == 0))) set_status(a.status, KVQ_DEV_BAD_BLOCK);
     const bool v0 = c0 && t0.z != 0, v1 = c1 && t1.z != 0;
     const float sk0 = __int_as_float(t0.x), sk1 = __int_as_float(t1.x);
     const float lv0 = v0 ? fast_log2(__int_as_float(t0.y)) : -INFINITY;
     const float lv1 = v1 ? fast_log2(__int_as_float(t1.y)) : -INFINITY;
-    float w[2][2];
+    float sc[NHT][4], zc[NHT][4];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float cqe = e ? cq1 : cq0;
-      const float s0 = v0 ? S[e] * sk0 * cqe : -INFINITY;
-      const float s1 = v1 ? S[2 + e] * sk1 * cqe : -INFINITY;
-      const float z0 = s0 + lv0, z1 = s1 + lv1;
-      float tms = fmaxf(s0, s1), tmz = fmaxf(z0, z1);
+    for (int nt = 0; nt < NHT; ++nt)
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        tms = fmaxf(tms, __shfl_xor_sync(0xffffffffu, tms, off));
-        tmz = fmaxf(tmz, __shfl_xor_sync(0xffffffffu, tmz, off));
-      }
-      if (tms > ms[e] + kLazyRescaleS) {
-        lsum[e] *= (ms[e] == -INFINITY) ? 0.f : fast_exp2(ms[e] - tms);
-        ms[e] = tms;
-      }
-      if (tmz > mz[e] + kLazyRescaleS) {
-        const float az = (mz[e] == -INFINITY) ? 0.f : fast_exp2(mz[e] - tmz);
+      for (int e = 0; e < 2; ++e) {
+        sc[nt][e] = v0 ? S[nt][e] * sk0 * cq[nt][e] : -INFINITY;
+        sc[nt][2 + e] = v1 ? S[nt][2 + e] * sk1 * cq[nt][e] : -INFINITY;
+        zc[nt][e] = sc[nt][e] + lv0;
+        zc[nt][2 + e] = sc[nt][2 + e] + lv1;
+        float tms = fmaxf(sc[nt][e], sc[nt][2 + e]), tmz = fmaxf(zc[nt][e], zc[nt][2 + e]);
 #pragma unroll
-        for (int t = 0; t < NMT; ++t) {
-          o_acc[t][e] *= az;
-          o_acc[t][2 + e] *= az;
+        for (int off = 4; off < 32; off <<= 1) {
+          tms = fmaxf(tms, __shfl_xor_sync(0xffffffffu, tms, off));
+          tmz = fmaxf(tmz, __shfl_xor_sync(0xffffffffu, tmz, off));
         }
-        mz[e] = tmz;
+        if (g == 0) {
+          red_s[warp * NH + nt * 8 + 2 * c4 + e] = tms;
+          red_z[warp * NH + nt * 8 + 2 * c4 + e] = tmz;
+        }
       }
-      const float msr = (ms[e] == -INFINITY) ? 0.f : ms[e];
-      const float mzr = (mz[e] == -INFINITY) ? 0.f : mz[e];
-      lsum[e] += fast_exp2(s0 - msr) + fast_exp2(s1 - msr);
-      w[0][e] = fast_exp2(z0 - mzr);
-      w[1][e] = fast_exp2(z1 - mzr);
+    // every warp's maxima are in place, and every warp leaves together if a wait ran out
+    if (chunk_bar_or(!got)) {
+      failed = true;
+      break;
     }
-    // W fragments (cells on K, heads on N): hi + lo fp16 parts
-    const uint32_t h0 = pack_half2(w[0][0], w[0][1]);
-    const uint32_t h1 = pack_half2(w[1][0], w[1][1]);
-    const __half2 hh0 = *reinterpret_cast<const __half2*>(&h0);
-    const __half2 hh1 = *reinterpret_cast<const __half2*>(&h1);
-    const uint32_t l0 = pack_half2(w[0][0] - __low2float(hh0), w[0][1] - __high2float(hh0));
-    const uint32_t l1 = pack_half2(w[1][0] - __low2float(hh1), w[1][1] - __high2float(hh1));
-    const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
-    const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
-
-    // ---- O^T += V^T * W: per 32-dim block, an even-dimension and an odd-dimension M-tile
+    // ---- the chunk maximum, the weights relative to the updated maximum, l_c's part
+    float ms_new[NHT][2], mz_new[NHT][2];
+    uint32_t wf[NHT][4];
 #pragma unroll
-    for (int db = 0; db < D / 32; ++db) {
-      uint32_t r0, r1, r2, r3, e0, e1, e2, e3, o0, o1, o2, o3;
-      ldsm_x4_trans(sbase + v_lane_off + db * 32, r0, r1, r2, r3);
-      i8x4_to_h2x2(r0, kSelB02, kSelB13, e0, o0);  // cells 0..7, dims 32 db + 0..15
-      i8x4_to_h2x2(r1, kSelB02, kSelB13, e1, o1);  // cells 0..7, dims 32 db + 16..31
-      i8x4_to_h2x2(r2, kSelB02, kSelB13, e2, o2);  // cells 8..15, dims 32 db + 0..15
-      i8x4_to_h2x2(r3, kSelB02, kSelB13, e3, o3);  // cells 8..15, dims 32 db + 16..31
-      mma_f16_16816(o_acc[2 * db], e0, e1, e2, e3, bh0, bh1);
-      mma_f16_16816(o_acc[2 * db], e0, e1, e2, e3, bl0, bl1);
-      mma_f16_16816(o_acc[2 * db + 1], o0, o1, o2, o3, bh0, bh1);
-      mma_f16_16816(o_acc[2 * db + 1], o0, o1, o2, o3, bl0, bl1);
+    for (int nt = 0; nt < NHT; ++nt) {
+      float w[2][2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hd = nt * 8 + 2 * c4 + e;
+        float cs = red_s[hd], cz = red_z[hd];
+#pragma unroll
+        for (int q2 = 1; q2 < 4; ++q2) {
+          cs = fmaxf(cs, red_s[q2 * NH + hd]);
+          cz = fmaxf(cz, red_z[q2 * NH + hd]);
+        }
+        ms_new[nt][e] = fmaxf(ms[nt][e], cs);
+        mz_new[nt][e] = fmaxf(mz[nt][e], cz);
+        const float msr = ms_new[nt][e] == -INFINITY ? 0.f : ms_new[nt][e];
+        const float mzr = mz_new[nt][e] == -INFINITY ? 0.f : mz_new[nt][e];
+        float lp = fast_exp2(sc[nt][e] - msr) + fast_exp2(sc[nt][2 + e] - msr);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) lp += __shfl_xor_sync(0xffffffffu, lp, off);
+        if (g == 0) red_l[warp * NH + hd] = lp;
+        w[0][e] = fast_exp2(zc[nt][e] - mzr);      // cell g
+        w[1][e] = fast_exp2(zc[nt][2 + e] - mzr);  // cell g + 8
+      }
+      // W as fp16 hi + lo parts, transposed to the PV B layout (cells on K, heads on N)
+      const uint32_t h0 = pack_half2(w[0][0], w[0][1]);
+      const uint32_t h1 = pack_half2(w[1][0], w[1][1]);
+      const __half2 hh0 = *reinterpret_cast<const __half2*>(&h0);
+      const __half2 hh1 = *reinterpret_cast<const __half2*>(&h1);
+      const uint32_t l0 = pack_half2(w[0][0] - __low2float(hh0), w[0][1] - __high2float(hh0));
+      const uint32_t l1 = pack_half2(w[1][0] - __low2float(hh1), w[1][1] - __high2float(hh1));
+      wf[nt][0] = movmatrix_trans(h0);
+      wf[nt][1] = movmatrix_trans(h1);
+      wf[nt][2] = movmatrix_trans(l0);
+      wf[nt][3] = movmatrix_trans(l1);
     }
+#pragma unroll
+    for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) wx[((warp * NHT + nt) * 4 + q4) * 32 + lane] = wf[nt][q4];
+    chunk_bar();  // every warp's W fragments and l_c parts are in place
+    // ---- the fold of l: l = fma(l, alpha, l_c)
+#pragma unroll
+    for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int hd = nt * 8 + 2 * c4 + e;
+        const float lc = (red_l[hd] + red_l[NH + hd]) + (red_l[2 * NH + hd] + red_l[3 * NH + hd]);
+        const float al = ms[nt][e] == -INFINITY ? 0.f : fast_exp2(ms[nt][e] - ms_new[nt][e]);
+        lsum[nt][e] = fmaf(lsum[nt][e], al, lc);
+        ms[nt][e] = ms_new[nt][e];
+      }
+    // ---- acc_c = V^T W over the chunk's 64 cells for this warp's dims, from zero; then the fold
+    float acc_c[2 * NDB][NHT][4];
+#pragma unroll
+    for (int t = 0; t < 2 * NDB; ++t)
+#pragma unroll
+      for (int nt = 0; nt < NHT; ++nt) acc_c[t][nt][0] = acc_c[t][nt][1] = acc_c[t][nt][2] = acc_c[t][nt][3] = 0.f;
+#pragma unroll
+    for (int tile = 0; tile < 4; ++tile) {
+      uint32_t bf[NHT][4];
+#pragma unroll
+      for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) bf[nt][q4] = wx[((tile * NHT + nt) * 4 + q4) * 32 + lane];
+#pragma unroll
+      for (int db = 0; db < NDB; ++db) {
+        uint32_t r0, r1, r2, r3, e0, e1, e2, e3, o0, o1, o2, o3;
+        ldsm_x4_trans(bbase + tile * 16 * RB + v_lane_off + (warp * NDB + db) * 32, r0, r1, r2, r3);
+        i8x4_to_h2x2(r0, kSelB02, kSelB13, e0, o0);  // cells 0..7, dims + 0..15
+        i8x4_to_h2x2(r1, kSelB02, kSelB13, e1, o1);  // cells 0..7, dims + 16..31
+        i8x4_to_h2x2(r2, kSelB02, kSelB13, e2, o2);  // cells 8..15, dims + 0..15
+        i8x4_to_h2x2(r3, kSelB02, kSelB13, e3, o3);  // cells 8..15, dims + 16..31
+#pragma unroll
+        for (int nt = 0; nt < NHT; ++nt) {
+          mma_f16_16816(acc_c[2 * db][nt], e0, e1, e2, e3, bf[nt][0], bf[nt][1]);
+          mma_f16_16816(acc_c[2 * db][nt], e0, e1, e2, e3, bf[nt][2], bf[nt][3]);
+          mma_f16_16816(acc_c[2 * db + 1][nt], o0, o1, o2, o3, bf[nt][0], bf[nt][1]);
+          mma_f16_16816(acc_c[2 * db + 1][nt], o0, o1, o2, o3, bf[nt][2], bf[nt][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float al = mz[nt][e] == -INFINITY ? 0.f : fast_exp2(mz[nt][e] - mz_new[nt][e]);
+#pragma unroll
+        for (int t = 0; t < 2 * NDB; ++t) {
+          o_acc[t][nt][e] = fmaf(o_acc[t][nt][e], al, acc_c[t][nt][e]);
+          o_acc[t][nt][2 + e] = fmaf(o_acc[t][nt][2 + e], al, acc_c[t][nt][2 + e]);
+        }
+        mz[nt][e] = mz_new[nt][e];
+      }
+    // ---- this warp is done with the buffer: refill it with chunk c + NBUF once all four are
     __syncwarp();
-    if constexpr (NT == 1) {
-      if (k + DEPTH < npp) issue(k + DEPTH);
-    } else {
-      if (lane == 0) mbar_arrive(&pempty[s]);
-      if (nt == 0 && k + DEPTH < npp) {
-        bool freed = true;
-        if (lane == 0) freed = mbar_wait(&pempty[s], (k / DEPTH) & 1, a.status);
-        if (__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) issue(k + DEPTH);
+    if (lane == 0) mbar_arrive(&empty[b]);
+    if (c + NBUF < n_chunks) {
+      bool freed = true;
+      if (lane == 0) freed = mbar_wait(&empty[b], (c / NBUF) & 1, a.status, kWaitBudgetCycles);
+      if (__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) issue(c + NBUF);
+    }
+  }
+  if (failed) {
+    // a wait ran out (KVQ_DEV_TIMEOUT is set): the copies issued from this chunk on land before the
+    // CTA exits (bounded waits), and the query's rows are written as zeros
+    if (lane == 0)
+      for (int cc = c; cc < n_issued; ++cc) mbar_wait(&full[cc % NBUF], (cc / NBUF) & 1, a.status, kWaitBudgetCycles);
+    __syncwarp();
+    for (int e = lane; e < G * (D / 4); e += 32) out_q[(e / (D / 4)) * D + warp * (D / 4) + e % (D / 4)] = 0.0f;
+    return;
+  }
+  // ---- out = O 2^(m_z - m_s) / l for this warp's dims
+#pragma unroll
+  for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int hd = nt * 8 + 2 * c4 + e;
+      if (hd >= G) continue;
+      const float fin = (lsum[nt][e] > 0.f && mz[nt][e] != -INFINITY) ? fast_exp2(mz[nt][e] - ms[nt][e]) / lsum[nt][e] : 0.f;
+#pragma unroll
+      for (int t = 0; t < 2 * NDB; ++t) {
+        // M-tile t = 2 db + odd: row g <-> dim 32 db + odd + 2 g, row g + 8 <-> that + 16
+        const int d0 = warp * (D / 4) + (t >> 1) * 32 + (t & 1) + 2 * g;
+        out_q[hd * D + d0] = o_acc[t][nt][e] * fin;
+        out_q[hd * D + d0 + 16] = o_acc[t][nt][2 + e] * fin;
       }
     }
-  }
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) lsum[e] += __shfl_xor_sync(0xffffffffu, lsum[e], off);
-  }
-
-  // ------------------------------------------------------------ merge the teams
-  __syncthreads();  // every issued copy was waited for: the ring is free
-  constexpr int RS = D + 4;
-  float* mo = reinterpret_cast<float*>(smem);   // [NW][8][RS]
-  float* mstat = mo + NW * 8 * RS;              // [NW][8][4]
-  float* mw = mstat + NW * 8 * 4;               // [rows][NTEAM]
-  float* mfin = mw + NW * 8;                    // [rows][4]
-#pragma unroll
-  for (int t = 0; t < NMT; ++t) {
-    // M-tile t = 2 db + odd: row g <-> dim 32 db + odd + 2 g, row g + 8 <-> dim 32 db + 16 + odd + 2 g
-    const int d0 = (t >> 1) * 32 + (t & 1) + 2 * g;
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      mo[(warp * 8 + 2 * c + e) * RS + d0] = o_acc[t][e];
-      mo[(warp * 8 + 2 * c + e) * RS + d0 + 16] = o_acc[t][2 + e];
-    }
-  }
-  if (g == 0) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float* stt = mstat + (warp * 8 + 2 * c + e) * 4;
-      stt[0] = ms[e];
-      stt[1] = mz[e];
-      stt[2] = lsum[e];
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int hh = threadIdx.x;
-    float Ms = -INFINITY, Mz = -INFINITY;
-    for (int q2 = 0; q2 < NTEAM; ++q2) {
-      Ms = fmaxf(Ms, mstat[(q2 * L::kRows + hh) * 4 + 0]);
-      Mz = fmaxf(Mz, mstat[(q2 * L::kRows + hh) * 4 + 1]);
-    }
-    float lsum_all = 0.f;
-    for (int q2 = 0; q2 < NTEAM; ++q2) {
-      const float* stt = mstat + (q2 * L::kRows + hh) * 4;
-      if (Ms != -INFINITY && stt[0] != -INFINITY) lsum_all += stt[2] * fast_exp2(stt[0] - Ms);
-      mw[hh * NTEAM + q2] = (Mz != -INFINITY && stt[1] != -INFINITY) ? fast_exp2(stt[1] - Mz) : 0.f;
-    }
-    mfin[hh * 4 + 3] = (lsum_all > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / lsum_all : 0.f;
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int hh = idx / D, d = idx % D;
-    float o = 0.f;
-#pragma unroll
-    for (int q2 = 0; q2 < NTEAM; ++q2) o = fmaf(mo[(q2 * L::kRows + hh) * RS + d], mw[hh * NTEAM + q2], o);
-    a.out[(static_cast<long long>(i) * Hq + kvh * G + hh) * D + d] = o * mfin[hh * 4 + 3];
-  }
 }
 
 size_t sparse_workspace_bytes(int n_blocks_row, int n_kv_heads, int head_dim) {
   return static_cast<size_t>(n_blocks_row) * n_kv_heads * KVQ_BLOCK_SIZE * (2 * head_dim + 16);
 }
 
-template <int D, int NT>
-static cudaError_t launch_sparse_attn(const SparseArgs& a, cudaStream_t stream) {
-  // four teams, three stages each: two CTAs per SM, so one CTA's start-up and merge overlap
-  // the other's streaming (measured at sparse_32k: 0.668 ms, against 0.742 ms for one CTA of
-  // eight teams per SM and 0.77-1.07 ms for the other shapes tried)
-  constexpr int NTEAM = 4;
-  constexpr int DEPTH = 3;
-  using L = SparseSmem<D, NT, NTEAM, DEPTH>;
-  auto kern = sparse_kernel<D, NT, NTEAM, DEPTH>;
+template <int D, int NHT, int NBUF>
+static cudaError_t launch_sparse_chunk(const SparseArgs& a, cudaStream_t stream) {
+  using L = ChunkSmem<D, NHT, NBUF>;
+  auto kern = sparse_chunk_kernel<D, NHT, NBUF>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.n_queries, a.n_kv_heads), dim3(L::kWarps * 32), L::kTotal, stream, a);
+  return launch_pdl(kern, dim3(a.n_queries, a.n_kv_heads), dim3(128), L::kTotal, stream, a);
 }
 
 template <int D>
@@ -451,9 +511,11 @@ static cudaError_t launch_sparse_d(const SparseArgs& a, cudaStream_t stream) {
   sparse_prep_kernel<D><<<dim3(a.n_blocks_row, a.n_kv_heads), 256, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // One chunk buffer: four CTAs per SM at head_dim 256, whose copies and compute interleave
+  // (measured at sparse_32k: 0.527 ms, against 0.628 ms for two buffers and two CTAs per SM).
   const int G = a.n_q_heads / a.n_kv_heads;
-  if (G <= 8) return launch_sparse_attn<D, 1>(a, stream);
-  return launch_sparse_attn<D, 2>(a, stream);
+  if (G <= 8) return launch_sparse_chunk<D, 1, 1>(a, stream);
+  return launch_sparse_chunk<D, 2, 1>(a, stream);
 }
 
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream) {
