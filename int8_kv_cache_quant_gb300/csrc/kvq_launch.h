@@ -37,6 +37,7 @@ struct RopeQuantArgs {
   int8_t* q_codes;        // [T][Hq][D] or nullptr
   float* q_scales;        // [T][Hq] or nullptr
   uint16_t* q_rot;        // bf16 [T][Hq][D] or nullptr
+  int q_heads_per_warp;   // set by launch_rope_quant_write
 };
 cudaError_t launch_rope_quant_write(const RopeQuantArgs& a, cudaStream_t stream);
 

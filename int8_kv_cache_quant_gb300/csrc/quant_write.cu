@@ -128,8 +128,9 @@ cudaError_t launch_quant_write(const QuantWriteArgs& a, cudaStream_t stream) {
 //   dim i < r/2 (partner i + r/2):      out = fma(x_i, c_i, -(x_{i+r/2} * s_i))
 //   dim i + r/2 (partner i):            out = fma(x_{i+r/2}, c_i, x_i * s_i)
 // in fp32 with exactly these roundings, then the quantisation rule of quant_write_kernel on the
-// fp32 row.  A warp per (token, row); lane l holds dims l*P .. l*P+P-1 (P = D/32), so the partner
-// of a dim is the same element of lane l +- (r/2)/P (r/2 is a multiple of P).
+// fp32 row.  A warp per (token, K/V head), or per (token, group of q_heads_per_warp query heads);
+// lane l holds dims l*P .. l*P+P-1 (P = D/32), so the partner of a dim is the same element of lane
+// l +- (r/2)/P (r/2 is a multiple of P).
 // The rotation of this lane's P elements of a Q or K row at position p (rotate-half form above).
 template <int P>
 __device__ __forceinline__ void rope_lane(float (&x)[P], const RopeQuantArgs& a, int p, int lane) {
@@ -149,9 +150,89 @@ __device__ __forceinline__ void rope_lane(float (&x)[P], const RopeQuantArgs& a,
   }
 }
 
-// One block per (group of 16 consecutive tokens, head slot r): r < Hq is query head r (Q outputs),
-// r >= Hq is KV head r - Hq (the K row rotated into its cache slot, the V row staged in shared
-// memory and written page-wise as in quant_write_kernel).  Warp w takes token w.
+// The query side: warp w of a block takes token g0 + w and the block's q_heads_per_warp query
+// heads, loading its lane's table values once for all of them and each next row before it works on
+// the current one.
+template <int D>
+__device__ __forceinline__ void rope_q_rows(const RopeQuantArgs& a, int tok, int h0, int lane) {
+  constexpr int P = D / 32;
+  const int Hq = a.n_q_heads;
+  const int h1 = min(Hq, h0 + a.q_heads_per_warp);
+  const int p = a.kv.pos[tok];
+  const bool pos_ok = p >= 0 && p < a.max_pos;
+  const int half = a.rotary_dim / 2, shift = half / P;
+  const int d0 = lane * P;
+  const bool first = d0 < half, rotated = d0 < a.rotary_dim;
+  const int partner = rotated ? (first ? lane + shift : lane - shift) : lane;
+  float cf[P], sf[P];
+  if (pos_ok && rotated) {
+    const float* cs = a.cos_sin + static_cast<long long>(p) * a.rotary_dim + (first ? d0 : d0 - half);
+#pragma unroll
+    for (int e = 0; e < P; ++e) {
+      cf[e] = __ldg(cs + e);
+      sf[e] = __ldg(cs + half + e);
+    }
+  }
+  using Raw = typename std::conditional<P == 8, uint4, uint2>::type;
+  const uint16_t* qrow = static_cast<const uint16_t*>(a.q) + static_cast<long long>(tok) * Hq * D + d0;
+  Raw nxt = __ldg(reinterpret_cast<const Raw*>(qrow + h0 * D));
+  for (int h = h0; h < h1; ++h) {
+    const Raw raw = nxt;
+    if (h + 1 < h1) nxt = __ldg(reinterpret_cast<const Raw*>(qrow + (h + 1) * D));
+    float x[P];
+    {
+      uint32_t w[P / 2];
+      if constexpr (P == 8) {
+        w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
+      } else {
+        w[0] = raw.x; w[1] = raw.y;
+      }
+#pragma unroll
+      for (int i = 0; i < P / 2; ++i) {
+        x[2 * i] = __uint_as_float(w[i] << 16);
+        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+    // ---- rotate, quantise, codes + scale + rotated bf16 row
+    if (pos_ok) {
+#pragma unroll
+      for (int e = 0; e < P; ++e) {
+        const float other = __shfl_sync(0xffffffffu, x[e], partner);
+        if (rotated) x[e] = first ? __fmaf_rn(x[e], cf[e], -__fmul_rn(other, sf[e])) : __fmaf_rn(x[e], cf[e], __fmul_rn(other, sf[e]));
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < P; ++e) x[e] = 0.0f;
+    }
+    int8_t qc[P];
+    uint32_t packed[P / 4];
+    const float scale = quant_rule_warp(x, qc);
+    pack_codes(qc, packed);
+    const long long u = static_cast<long long>(tok) * Hq + h;
+    if (a.q_codes) {
+      int8_t* dst = a.q_codes + u * D + d0;
+      if constexpr (P == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+      else *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    }
+    if (a.q_scales && lane == 0) a.q_scales[u] = scale;
+    if (a.q_rot) {
+      uint32_t b[P / 2];
+#pragma unroll
+      for (int i = 0; i < P / 2; ++i) {
+        const __nv_bfloat162 v2 = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+        b[i] = *reinterpret_cast<const uint32_t*>(&v2);
+      }
+      uint16_t* dst = a.q_rot + u * D + d0;
+      if constexpr (P == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(b[0], b[1], b[2], b[3]);
+      else *reinterpret_cast<uint2*>(dst) = make_uint2(b[0], b[1]);
+    }
+  }
+}
+
+// One block per (group of 16 consecutive tokens, slot r): r < n_qg is the query heads
+// q_heads_per_warp * r .. (Q outputs), r >= n_qg is KV head r - n_qg (the K row rotated into its cache
+// slot, the V row staged in shared memory and written page-wise as in quant_write_kernel).  Warp w
+// takes token w.
 template <int D>
 __global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuantArgs a) {
   constexpr int P = D / 32;
@@ -159,13 +240,17 @@ __global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuant
   __shared__ long long tok_ph[kGroup];
   __shared__ int tok_slot[kGroup];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int Hq = a.q ? a.n_q_heads : 0, H = a.kv.n_kv_heads;
+  const int n_qg = a.q ? (a.n_q_heads + a.q_heads_per_warp - 1) / a.q_heads_per_warp : 0, H = a.kv.n_kv_heads;
   const int g0 = blockIdx.x * kGroup, r = blockIdx.y;
-  const bool is_q = r < Hq;
-  const int h = is_q ? r : r - Hq;
+  const bool is_q = r < n_qg;
+  const int h = is_q ? r : r - n_qg;
 
   grid_dep_wait();     // the rows may come from the previous kernel of the stream
   grid_dep_trigger();  // the attention kernel may start launching; it waits for this grid
+  if (is_q) {  // block-uniform; the query side has no block barrier
+    if (g0 + warp < a.kv.n_tokens) rope_q_rows<D>(a, g0 + warp, h * a.q_heads_per_warp, lane);
+    return;
+  }
   {
     const int k = warp;  // one token per warp
     const int tok = g0 + k;
@@ -174,39 +259,7 @@ __global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuant
     if (tok < a.kv.n_tokens) {
       const int p = a.kv.pos[tok];
       const bool pos_ok = p >= 0 && p < a.max_pos;
-      if (is_q) {
-        // ---- Q row: rotate, quantise, codes + scale + rotated bf16 row
-        float x[P];
-        load_bf16_lane(static_cast<const uint16_t*>(a.q) + (static_cast<long long>(tok) * Hq + h) * D + lane * P, x);
-        if (pos_ok) {
-          rope_lane(x, a, p, lane);
-        } else {
-#pragma unroll
-          for (int e = 0; e < P; ++e) x[e] = 0.0f;
-        }
-        int8_t qc[P];
-        uint32_t packed[P / 4];
-        const float scale = quant_rule_warp(x, qc);
-        pack_codes(qc, packed);
-        const long long u = static_cast<long long>(tok) * Hq + h;
-        if (a.q_codes) {
-          int8_t* dst = a.q_codes + u * D + lane * P;
-          if constexpr (P == 8) *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
-          else *reinterpret_cast<uint32_t*>(dst) = packed[0];
-        }
-        if (a.q_scales && lane == 0) a.q_scales[u] = scale;
-        if (a.q_rot) {
-          uint32_t b[P / 2];
-#pragma unroll
-          for (int i = 0; i < P / 2; ++i) {
-            const __nv_bfloat162 v2 = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
-            b[i] = *reinterpret_cast<const uint32_t*>(&v2);
-          }
-          uint16_t* dst = a.q_rot + u * D + lane * P;
-          if constexpr (P == 8) *reinterpret_cast<uint4*>(dst) = make_uint4(b[0], b[1], b[2], b[3]);
-          else *reinterpret_cast<uint2*>(dst) = make_uint2(b[0], b[1]);
-        }
-      } else {
+      {
         // ---- K and V rows of KV head h into the token's slot
         const int seq = a.kv.seq_idx[tok];
         if (!pos_ok || p / KVQ_BLOCK_SIZE >= a.kv.max_blocks_per_seq) {
@@ -249,7 +302,6 @@ __global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuant
       tok_slot[k] = slot;
     }
   }
-  if (is_q) return;  // block-uniform
   __syncthreads();
   bool full = true;
 #pragma unroll
@@ -275,9 +327,14 @@ __global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuant
   }
 }
 
-cudaError_t launch_rope_quant_write(const RopeQuantArgs& a, cudaStream_t stream) {
+cudaError_t launch_rope_quant_write(const RopeQuantArgs& a_in, cudaStream_t stream) {
+  RopeQuantArgs a = a_in;
+  // Many tokens: a warp takes several query heads of its token (the table row is read once for
+  // them and the next row's load overlaps the current row); few tokens: one head per warp, so
+  // that the rows still spread over the GPU.
+  a.q_heads_per_warp = a.kv.n_tokens >= 512 ? 8 : 1;
   const long long groups = (static_cast<long long>(a.kv.n_tokens) + kGroup - 1) / kGroup;
-  const int slots = (a.q ? a.n_q_heads : 0) + a.kv.n_kv_heads;
+  const int slots = (a.q ? (a.n_q_heads + a.q_heads_per_warp - 1) / a.q_heads_per_warp : 0) + a.kv.n_kv_heads;
   if (groups > 0x7fffffffLL || slots > 65535) return cudaErrorInvalidConfiguration;
   const dim3 grid(static_cast<unsigned>(groups), slots);
   if (a.kv.head_dim == 256) return launch_pdl(rope_quant_write_kernel<256>, grid, dim3(kGroup * 32), 0, stream, a);
