@@ -43,6 +43,8 @@
 //   proxy fence orders the generic stores before the copy's reads).  Only that warp's team
 //   reads the page, so no other CTA or launch has to wait for the write; the write sits in the
 //   CTA's prologue, off the page loop.
+#include <type_traits>
+
 #include "kvq_dev.cuh"
 #include "kvq_launch.h"
 #include "quant_rule.cuh"
@@ -204,7 +206,41 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   if (ctx < 0) ctx = 0;
   const int t_end = SPLIT ? min(ctx, t_begin + a.split_rows) : ctx;
   const int n_pages = (t_end > t_begin) ? (t_end - t_begin + KVQ_BLOCK_SIZE - 1) / KVQ_BLOCK_SIZE : 0;
-  if constexpr (WRITE) {
+  // One new token (plain decode, single-warp teams, head_dim 256): the owning warp requests the
+  // token's bf16 K/V rows now, quantises them after the Q set-up and stores the codes to the cache
+  // with no fence, and writes the same codes into its shared-memory copy of the page once that copy
+  // has landed (the copy may read the slot before or after the stores; the patch makes it right
+  // either way).  Nothing on the way to the page's copy waits for the write, which otherwise held
+  // the owning warp (the last CTA's) about 4 us behind the others.  At head_dim 128 (two CTAs per
+  // SM) the write before the copy measured faster, so it stays there.
+  constexpr bool PATCH = WRITE && !MROW && NT == 1 && D == 256;
+  using RowRaw = typename std::conditional<PATCH && PER == 8, uint4, uint2>::type;
+  int k_w = -1;  // PATCH: this warp's page index holding the new token, or -1
+  int pr_w = 0;
+  RowRaw raw_k{}, raw_v{};
+  if constexpr (PATCH) {
+    const int tok = ctx - 1;  // nq = 1: the new token's position
+    if (write_new && tok >= t_begin && tok < t_end) {
+      pr_w = (tok - t_begin) / KVQ_BLOCK_SIZE;
+      if (pr_w % NTEAM == p) {
+        k_w = pr_w / NTEAM;
+        const long long row = (static_cast<long long>(b) * a.n_kv_heads + kvh) * D + lane * PER;
+        // volatile: the loads go out here, ahead of the copies, not where their values are used
+        const uint16_t* pk = static_cast<const uint16_t*>(a.k_new) + row;
+        const uint16_t* pv = static_cast<const uint16_t*>(a.v_new) + row;
+        if constexpr (PER == 8) {
+          asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(raw_k.x), "=r"(raw_k.y), "=r"(raw_k.z), "=r"(raw_k.w) : "l"(pk));
+          asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(raw_v.x), "=r"(raw_v.y), "=r"(raw_v.z), "=r"(raw_v.w) : "l"(pv));
+        } else {
+          asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(raw_k.x), "=r"(raw_k.y) : "l"(pk));
+          asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(raw_v.x), "=r"(raw_v.y) : "l"(pv));
+        }
+      }
+    }
+  }
+  if constexpr (WRITE && !PATCH) {
     // fused step: warp 0 of a CTA whose range holds new tokens pulls their bf16 K/V rows into L2
     // now, so the write in the prologue below finds them there
     if (write_new && warp == 0) {
@@ -288,7 +324,7 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   // the empty barriers, and the issuing warp copies page k only after acquiring one of them.
   // The page loop has no write in it.
   auto write_team_pages = [&](bool first_batch) {
-    if constexpr (WRITE) {
+    if constexpr (WRITE && !PATCH) {
       if (!write_new) return;
       const int first_new = ctx - nq;
       const int lo_all = max(first_new, t_begin);
@@ -349,6 +385,50 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
   }
   __syncthreads();
   write_team_pages(false);
+  // PATCH: the new token's codes and scales, kept for the shared-memory patch
+  uint32_t kpk[PER / 4], vpk[PER / 4];
+  float w_sk = 0.f, w_sv = 0.f;
+  bool w_ok = false;
+  if constexpr (PATCH) {
+    if (k_w >= 0) {  // warp-uniform
+      float xk[PER], xv[PER];
+      {
+        uint32_t wk[PER / 2], wv[PER / 2];
+        if constexpr (PER == 8) {
+          wk[0] = raw_k.x; wk[1] = raw_k.y; wk[2] = raw_k.z; wk[3] = raw_k.w;
+          wv[0] = raw_v.x; wv[1] = raw_v.y; wv[2] = raw_v.z; wv[3] = raw_v.w;
+        } else {
+          wk[0] = raw_k.x; wk[1] = raw_k.y;
+          wv[0] = raw_v.x; wv[1] = raw_v.y;
+        }
+#pragma unroll
+        for (int i = 0; i < PER / 2; ++i) {
+          xk[2 * i] = __uint_as_float(wk[i] << 16);
+          xk[2 * i + 1] = __uint_as_float(wk[i] & 0xFFFF0000u);
+          xv[2 * i] = __uint_as_float(wv[i] << 16);
+          xv[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        }
+      }
+      int8_t qc[PER];
+      w_sk = quant_rule_warp(xk, qc);
+      pack_codes(qc, kpk);
+      w_sv = quant_rule_warp(xv, qc);
+      pack_codes(qc, vpk);
+      // the page: from the issuing window (page k <-> lane k) when it holds it
+      const int page = (k_w < 32) ? __shfl_sync(0xffffffffu, pg, k_w) : __ldg(bt + pr_w);
+      w_ok = page >= 0 && page < a.num_blocks;
+      if (w_ok) {
+        const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
+        const int slot = (ctx - 1) % KVQ_BLOCK_SIZE;
+        store_k_codes<D>(a.k, ph, slot, lane, kpk);
+        store_v_codes<D>(a.v, ph, slot, lane, qc);
+        if (lane == 0) {
+          a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = w_sk;
+          a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = w_sv;
+        }
+      }
+    }
+  }
 
 
   const int g = lane >> 2, c = lane & 3;
@@ -382,6 +462,26 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
     const int s = k % DEPTH;
     const bool got = mbar_wait(&pfull[s], (k / DEPTH) & 1, a.status, a.wait_budget);
     uint8_t* st = pring + s * L::kStageBytes;
+    if constexpr (PATCH) {
+      if (k == k_w) {  // warp-uniform: the new token's slot of this copy gets its codes
+        if (w_ok) {
+          const int slot = (ctx - 1) % KVQ_BLOCK_SIZE, d0 = lane * PER;
+          uint8_t* kd = st + ((d0 / 16) * KVQ_BLOCK_SIZE + slot) * 16 + (d0 % 16);
+          if constexpr (PER == 8) *reinterpret_cast<uint2*>(kd) = make_uint2(kpk[0], kpk[1]);
+          else *reinterpret_cast<uint32_t*>(kd) = kpk[0];
+#pragma unroll
+          for (int i = 0; i < PER; ++i)
+            st[KB + (d0 + i) * KVQ_BLOCK_SIZE + slot] = static_cast<uint8_t>((vpk[i / 4] >> (8 * (i % 4))) & 0xFFu);
+          if (lane == 0) {
+            reinterpret_cast<float*>(st + 2 * KB)[slot] = w_sk;
+            reinterpret_cast<float*>(st + 2 * KB + 64)[slot] = w_sv;
+          }
+          // a later copy into this slot comes after these generic writes
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
+        __syncwarp();
+      }
+    }
     const uint32_t kbase = smem_u32(st);
     const uint32_t vbase = kbase + KB;
     const float* sks = reinterpret_cast<const float*>(st + 2 * KB);
