@@ -483,15 +483,16 @@ int kvq_debug_stream_floor(const kvq_cache* cache, int32_t batch, const int32_t*
                            void* stream);
 
 /*
- * kvq_debug_fault_inject — test entry point of the failure path: every bounded wait of the decode
- * and prefill kernels launched after this call gives up after wait_budget_cycles SM clock cycles
- * (<= 0: the default, about 2 s), and with mode 1 the first team of decode stage-1 CTA 0 does not
- * issue the copy of its second page, with mode 2 the producer of prefill attention CTA 0 does not
- * issue its fourth piece (mode 0: no injection).  No copy is left in flight: the consumer's wait
- * runs out, the kernel sets KVQ_DEV_TIMEOUT, waits (bounded) for the copies it did issue, drops
- * that CTA's result (decode single route: zero output rows; split route: an empty partial that the
- * merge skips; prefill: the unit's output rows are not written) and returns; the device stays
- * usable.  Process-wide, host only; kvq_debug_fault_inject(0, 0) restores the defaults.
+ * kvq_debug_fault_inject — test entry point of the failure path: every bounded wait of the decode,
+ * prefill and sparse kernels launched after this call gives up after wait_budget_cycles SM clock
+ * cycles (<= 0: the default, about 2 s), and with mode 1 the first team of decode stage-1 CTA 0
+ * does not issue the copy of its second page, with mode 2 the producer of prefill attention CTA 0
+ * does not issue its fourth piece, with mode 3 the sparse CTA of (query 0, KV head 0) does not
+ * issue the copies of its second chunk (mode 0: no injection).  No copy is left in flight:
+ * the consumer's wait runs out, the kernel sets KVQ_DEV_TIMEOUT, waits (bounded) for the copies it
+ * did issue, drops that CTA's result (decode single route: zero output rows; split route: an empty
+ * partial that the merge skips; prefill: the unit's output rows are not written; sparse: the
+ * query's rows are zeros) and returns; the device stays usable.  Process-wide, host only; kvq_debug_fault_inject(0, 0) restores the defaults.
  * KVQ_ERR_INVALID_ARG for an unknown mode.
  */
 int kvq_debug_fault_inject(int32_t mode, int64_t wait_budget_cycles);

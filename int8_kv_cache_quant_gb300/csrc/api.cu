@@ -92,7 +92,7 @@ const char* kvq_status_string(int s) {
 }
 
 int kvq_debug_fault_inject(int32_t mode, int64_t wait_budget_cycles) {
-  if (mode < 0 || mode > 2) return KVQ_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return KVQ_ERR_INVALID_ARG;
   g_wait_budget.store(wait_budget_cycles > 0 ? static_cast<long long>(wait_budget_cycles) : kvq::kWaitBudgetCycles);
   g_fault_mode.store(mode);
   return KVQ_OK;
@@ -580,6 +580,8 @@ int kvq_attn_sparse_int8kv(const kvq_cache* cache, const void* q, int32_t n_quer
   a.out = out;
   a.records = static_cast<uint8_t*>(workspace);
   a.status = status_ptr();
+  a.wait_budget = kvq::debug_wait_budget();
+  a.fault = kvq::debug_fault_mode();
   return cuda_status(kvq::launch_sparse(a, static_cast<cudaStream_t>(stream)));
 }
 

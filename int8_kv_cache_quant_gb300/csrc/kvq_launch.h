@@ -109,6 +109,8 @@ struct SparseArgs {
   float* out;
   uint8_t* records;  // workspace: gather records [n_blocks_row][Hkv][16][2D + 16]
   unsigned int* status;
+  long long wait_budget;  // SM clock cycles a bounded wait may take
+  int fault;              // test-only fault injection (kvq_debug_fault_inject), 0: none
 };
 size_t sparse_workspace_bytes(int n_blocks_row, int n_kv_heads, int head_dim);
 cudaError_t launch_sparse(const SparseArgs& a, cudaStream_t stream);

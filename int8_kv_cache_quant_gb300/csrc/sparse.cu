@@ -136,7 +136,9 @@ __device__ __forceinline__ bool chunk_bar_or(bool pred) {
 
 __device__ __forceinline__ void chunk_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-template <int D, int NHT, int NBUF>
+// FI: the test-only fault injection and wait budget of kvq_debug_fault_inject are compiled in
+// (a separate instantiation, so that the production kernel keeps its registers).
+template <int D, int NHT, int NBUF, bool FI>
 __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(SparseArgs a) {
   using L = ChunkSmem<D, NHT, NBUF>;
   using R = SparseRec<D>;
@@ -185,6 +187,10 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
 #pragma unroll
   for (int b = 0; b < NBUF; ++b) pos_q[b] = load_pos(b);
   int n_issued = 0;
+  // test-only fault injection: the first CTA leaves chunk 1 un-issued (no copy and no arrival: the
+  // chunk's barrier never completes and nothing is in flight for it), so the bounded waits run out
+  const bool skip_one = FI && a.fault == 3 && blockIdx.x == 0 && blockIdx.y == 0;
+  const long long budget = FI ? a.wait_budget : kWaitBudgetCycles;
   auto issue = [&](int c) {
     const int b = c % NBUF;
     int pos = -1;
@@ -207,6 +213,10 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
       }
     }
     const uint32_t m = __ballot_sync(0xffffffffu, ok);
+    if (skip_one && c == 1) {
+      ++n_issued;
+      return;
+    }
     if (lane == 0) {
       cmask[b * 4 + warp] = m;
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
   bool failed = false;
   for (; c < n_chunks; ++c) {
     const int b = c % NBUF;
-    const bool got = mbar_wait(&full[b], (c / NBUF) & 1, a.status, kWaitBudgetCycles);
+    const bool got = mbar_wait(&full[b], (c / NBUF) & 1, a.status, budget);
     const uint8_t* buf = ring + b * L::kBufBytes;
     const uint32_t bbase = smem_u32(buf);
     const uint32_t tbase = bbase + warp * 16 * RB;  // this warp's 16 cells
@@ -462,7 +472,7 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
     if (lane == 0) mbar_arrive(&empty[b]);
     if (c + NBUF < n_chunks) {
       bool freed = true;
-      if (lane == 0) freed = mbar_wait(&empty[b], (c / NBUF) & 1, a.status, kWaitBudgetCycles);
+      if (lane == 0) freed = mbar_wait(&empty[b], (c / NBUF) & 1, a.status, budget);
       if (__shfl_sync(0xffffffffu, freed ? 1 : 0, 0)) issue(c + NBUF);
     }
   }
@@ -470,7 +480,7 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
     // a wait ran out (KVQ_DEV_TIMEOUT is set): the copies issued from this chunk on land before the
     // CTA exits (bounded waits), and the query's rows are written as zeros
     if (lane == 0)
-      for (int cc = c; cc < n_issued; ++cc) mbar_wait(&full[cc % NBUF], (cc / NBUF) & 1, a.status, kWaitBudgetCycles);
+      for (int cc = c; cc < n_issued; ++cc) mbar_wait(&full[cc % NBUF], (cc / NBUF) & 1, a.status, budget);
     __syncwarp();
     for (int e = lane; e < G * (D / 4); e += 32) out_q[(e / (D / 4)) * D + warp * (D / 4) + e % (D / 4)] = 0.0f;
     return;
@@ -500,7 +510,8 @@ size_t sparse_workspace_bytes(int n_blocks_row, int n_kv_heads, int head_dim) {
 template <int D, int NHT, int NBUF>
 static cudaError_t launch_sparse_chunk(const SparseArgs& a, cudaStream_t stream) {
   using L = ChunkSmem<D, NHT, NBUF>;
-  auto kern = sparse_chunk_kernel<D, NHT, NBUF>;
+  auto kern = (a.fault != 0 || a.wait_budget != kWaitBudgetCycles) ? sparse_chunk_kernel<D, NHT, NBUF, true>
+                                                                    : sparse_chunk_kernel<D, NHT, NBUF, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kTotal);
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3(a.n_queries, a.n_kv_heads), dim3(128), L::kTotal, stream, a);

@@ -96,3 +96,24 @@ def test_prefill_wait_runs_out_and_the_device_recovers(kvq, oracle):
 def test_fault_inject_rejects_unknown_modes(kvq):
     with pytest.raises(kvq.KvqError):
         kvq.kvq_debug_fault_inject(7, 0)
+
+
+def test_sparse_wait_runs_out_and_the_device_recovers(kvq, oracle):
+    w = W.make("sparse_32k", seed=1703, ctx=640, n_queries=6, hq=4, hkv=1, d=128, n_sample=300)
+    cache, bt = gpu_cache_from(w, kvq)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.sparse_f64(hc, w["q"], w["cell_offsets"], w["cells"], w["block_table"][0], w["softmax_scale"])
+    q, off, cells, row = to_bf16_tensor(w["q"]), to_i32(w["cell_offsets"]), to_i32(w["cells"]), to_i32(w["block_table"][0])
+    assert int(w["cell_offsets"][1]) > 64  # query 0 has a second chunk
+
+    def call():
+        return kvq.kvq_attn_sparse_int8kv(cache, q, off, cells, row, w["softmax_scale"]).cpu().numpy()
+
+    # the CTA of (query 0, KV head 0) leaves its second chunk un-issued: its rows are zeros
+    out, st = _run_injected(kvq, 3, call)
+    assert st & kvq.kvq.DEV_TIMEOUT, st
+    assert np.all(out[0] == 0)
+    assert norm_max_err(out[1:], ref[1:]) <= 1e-4
+    got = call()
+    assert norm_max_err(got, ref) <= 1e-4
+    assert kvq.kvq_device_status() == 0
