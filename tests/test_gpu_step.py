@@ -141,3 +141,49 @@ def test_decode_b64_fused_step_full_sampled(kvq, oracle):
 def torch_index(a):
     import torch
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).cuda()
+
+
+def test_one_token_step_far_into_a_warps_pages(kvq, oracle):
+    """Single route at head_dim 256 with a context long enough that the new token's page is
+    past the first 32 pages of its warp (the page id then comes from the block table, not the
+    warp's window): the rewritten cache bit for bit, the output against FP64 and bit-identical to
+    plain decode on the completed cache."""
+    w = W.make("decode_32k", seed=741, batch=1, ctx=6000, hq=24, hkv=4, d=256)
+    assert (w["ctx_lens"][0] - 1) // 16 // 8 >= 32
+    cache, bt = _cache_without_new(kvq, w)
+    kn, vn = _new_rows(w)
+    args = (bt, to_i32(w["ctx_lens"]), w["max_ctx"], w["softmax_scale"])
+    out = kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(kn[:, 0]), to_bf16_tensor(vn[:, 0]),
+                                     to_bf16_tensor(w["q"]), *args, force_route=1).cpu().numpy()
+    assert kvq.kvq_device_status() == 0
+    hc = host_cache_from(w, oracle)
+    _check_cache(cache, hc)
+    dec = kvq.kvq_attn_decode_int8kv(cache, to_bf16_tensor(w["q"]), *args, force_route=1).cpu().numpy()
+    assert np.array_equal(out, dec)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    assert norm_max_err(out, ref) <= DESIGN_TOL
+
+
+@pytest.mark.parametrize("route", [1, 2])
+def test_one_token_step_on_an_unmapped_page(kvq, route):
+    """The new token's page has no valid block-table entry: nothing is written, KVQ_DEV_BAD_BLOCK
+    is reported, and the output is that of plain decode, which skips the same page."""
+    import torch
+    w = W.make("decode_32k", seed=742, batch=1, ctx=3000, hq=24, hkv=4, d=256)
+    cache, _ = _cache_without_new(kvq, w)
+    table = w["block_table"].copy()
+    table[0, (w["ctx_lens"][0] - 1) // 16] = w["num_blocks"] + 5
+    bt = to_i32(table)
+    before = [t.clone() for t in (cache.k, cache.v, cache.k_scale, cache.v_scale)]
+    kn, vn = _new_rows(w)
+    args = (bt, to_i32(w["ctx_lens"]), w["max_ctx"], w["softmax_scale"])
+    out = kvq.kvq_decode_step_int8kv(cache, to_bf16_tensor(kn[:, 0]), to_bf16_tensor(vn[:, 0]),
+                                     to_bf16_tensor(w["q"]), *args, force_route=route, split_rows=512).cpu().numpy()
+    assert kvq.kvq_device_status() & 0x1  # KVQ_DEV_BAD_BLOCK
+    for t0, t1 in zip(before, (cache.k, cache.v, cache.k_scale, cache.v_scale)):
+        assert torch.equal(t0, t1)
+    dec = kvq.kvq_attn_decode_int8kv(cache, to_bf16_tensor(w["q"]), *args, force_route=route,
+                                     split_rows=512).cpu().numpy()
+    kvq.kvq_device_status()
+    assert np.isfinite(out).all()
+    assert np.array_equal(out, dec)
