@@ -36,7 +36,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 STAGE1_TRAFFIC_BYTES = 68230912 + 117248
 STAGE1_TRAFFIC_SOURCES = ("int8_kv_cache_quant_gb300/csrc/decode.cu", "int8_kv_cache_quant_gb300/csrc/kvq_dev.cuh",
                           "int8_kv_cache_quant_gb300/csrc/quant_rule.cuh")
-STAGE1_TRAFFIC_SHA = "66092b00dc4cc175"
+STAGE1_TRAFFIC_SHA = "3d9f61042a75f552"
 
 
 def stage1_traffic():

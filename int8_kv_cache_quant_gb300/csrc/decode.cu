@@ -42,7 +42,9 @@
 //   written into their page, before its bulk copy, by the warp that will issue that copy (a
 //   proxy fence orders the generic stores before the copy's reads).  Only that warp's team
 //   reads the page, so no other CTA or launch has to wait for the write; the write sits in the
-//   CTA's prologue, off the page loop.
+//   CTA's prologue, off the page loop.  One new token at head_dim 256: the owning warp stores the
+//   codes without waiting for them and writes them into its landed shared-memory copy of the
+//   page instead (see PATCH below).
 #include <type_traits>
 
 #include "kvq_dev.cuh"
