@@ -6,7 +6,8 @@
 // Method: "gfx936 DCU上实现INT8 KV与INT8 MMAC Attention推理优化" §2.1 (amax = max|x|,
 // scale = amax / 127, q = clamp(round(x / scale), -127, 127)) and §2.3 (K in 16-element
 // head-dimension chunks with the tokens of a chunk adjacent, V token-contiguous per dimension).
-// Every division is IEEE fp32 (__fdiv_rn) and rounding is to nearest even.
+// Scales are IEEE fp32 quotients (__fdiv_rn), codes the nearest-even rounding of the IEEE
+// quotient x / scale (computed through the reciprocal where that provably gives the same code).
 #pragma once
 
 #include <cstdint>
@@ -48,14 +49,34 @@ __device__ __forceinline__ float quant_rule_warp(const float (&x)[P], int8_t (&q
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   const float scale = __fdiv_rn(amax, 127.0f);
+  // code = rint(RN(x / scale)), taken as rint(y) with y = RN(x * RN(1 / scale)).  y lies within
+  // |x / scale| * 2^-23 (< 1.6e-5, since |x / scale| <= 127 (1 + 2^-23)) of the exact quotient and
+  // RN(x / scale) within 2^-18 of it, so the two round to the same integer unless y is within 2^-15
+  // of a half-integer; there (and where 1 / scale overflows) the IEEE division decides.
+  const float r = __fdiv_rn(1.0f, scale);
+  float c[P];
+  bool exact_needed = false;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
-    float c = 0.0f;
-    if (amax != 0.0f) {
-      c = rintf(__fdiv_rn(x[i], scale));
-      c = fminf(fmaxf(c, -127.0f), 127.0f);
+    const float y = __fmul_rn(x[i], r);
+    // y's signed distance to the half-integer above floor(y), within 2^-24 of the exact value
+    const float h = __fsub_rn(__fsub_rn(y, floorf(y)), 0.5f);
+    const bool fast = fabsf(h) >= 3.0517578125e-05f;           // false for NaN / inf
+    exact_needed |= !fast;
+    c[i] = rintf(y);
+  }
+  if (__any_sync(0xffffffffu, exact_needed && amax != 0.0f)) {
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      const float y = __fmul_rn(x[i], r);
+      const float h = __fsub_rn(__fsub_rn(y, floorf(y)), 0.5f);
+      if (!(fabsf(h) >= 3.0517578125e-05f)) c[i] = rintf(__fdiv_rn(x[i], scale));
     }
-    q[i] = static_cast<int8_t>(static_cast<int>(c));
+  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const float ci = amax != 0.0f ? fminf(fmaxf(c[i], -127.0f), 127.0f) : 0.0f;
+    q[i] = static_cast<int8_t>(static_cast<int>(ci));
   }
   return scale;
 }
