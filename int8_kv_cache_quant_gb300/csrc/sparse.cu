@@ -112,7 +112,7 @@ struct ChunkSmem {
   static constexpr int kCells = 64;
   static constexpr int kBufBytes = kCells * SparseRec<D>::kBytes;
   static constexpr int kQOffset = NBUF * kBufBytes;         // Q^T fragments, NHT n-tiles
-  static constexpr int kWOffset = kQOffset + NHT * D * 16;  // W fragments [tile][n-tile][4][32 lanes]
+  static constexpr int kWOffset = kQOffset + NHT * D * 16;  // W fragments [tile][n-tile][32 lanes] x 4 words
   static constexpr int kRedOffset = kWOffset + 4 * NHT * 4 * 32 * 4;  // [3][warp][NHT * 8] floats
   static constexpr int kCqOffset = kRedOffset + 3 * 4 * NHT * 8 * 4;
   static constexpr int kMaskOffset = kCqOffset + NHT * 8 * 4;         // [NBUF][warp] copied-cell masks
@@ -148,7 +148,7 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ring = smem;
   uint8_t* q_s = smem + L::kQOffset;
-  uint32_t* wx = reinterpret_cast<uint32_t*>(smem + L::kWOffset);
+  uint4* wx = reinterpret_cast<uint4*>(smem + L::kWOffset);
   float* red = reinterpret_cast<float*>(smem + L::kRedOffset);
   float* cq_s = reinterpret_cast<float*>(smem + L::kCqOffset);
   uint32_t* cmask = reinterpret_cast<uint32_t*>(smem + L::kMaskOffset);
@@ -410,9 +410,7 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
       wf[nt][3] = movmatrix_trans(l1);
     }
 #pragma unroll
-    for (int nt = 0; nt < NHT; ++nt)
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) wx[((warp * NHT + nt) * 4 + q4) * 32 + lane] = wf[nt][q4];
+    for (int nt = 0; nt < NHT; ++nt) wx[(warp * NHT + nt) * 32 + lane] = make_uint4(wf[nt][0], wf[nt][1], wf[nt][2], wf[nt][3]);
     chunk_bar();  // every warp's W fragments and l_c parts are in place
     // ---- the fold of l: l = fma(l, alpha, l_c)
 #pragma unroll
@@ -435,9 +433,13 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
     for (int tile = 0; tile < 4; ++tile) {
       uint32_t bf[NHT][4];
 #pragma unroll
-      for (int nt = 0; nt < NHT; ++nt)
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) bf[nt][q4] = wx[((tile * NHT + nt) * 4 + q4) * 32 + lane];
+      for (int nt = 0; nt < NHT; ++nt) {
+        const uint4 wv = wx[(tile * NHT + nt) * 32 + lane];
+        bf[nt][0] = wv.x;
+        bf[nt][1] = wv.y;
+        bf[nt][2] = wv.z;
+        bf[nt][3] = wv.w;
+      }
 #pragma unroll
       for (int db = 0; db < NDB; ++db) {
         uint32_t r0, r1, r2, r3, e0, e1, e2, e3, o0, o1, o2, o3;
