@@ -113,12 +113,12 @@ struct ChunkSmem {
   static constexpr int kBufBytes = kCells * SparseRec<D>::kBytes;
   static constexpr int kQOffset = NBUF * kBufBytes;         // Q^T fragments, NHT n-tiles
   static constexpr int kWOffset = kQOffset + NHT * D * 16;  // W fragments [tile][n-tile][32 lanes] x 4 words
-  static constexpr int kRedOffset = kWOffset + 4 * NHT * 4 * 32 * 4;  // [3][warp][NHT * 8] floats
+  static constexpr int kRedOffset = kWOffset + 4 * NHT * 4 * 32 * 4;  // [3][NHT * 8 heads][warp] floats
   static constexpr int kCqOffset = kRedOffset + 3 * 4 * NHT * 8 * 4;
   static constexpr int kMaskOffset = kCqOffset + NHT * 8 * 4;         // [NBUF][warp] copied-cell masks
   static constexpr int kBarOffset = (kMaskOffset + NBUF * 4 * 4 + 7) / 8 * 8;  // full [NBUF], empty [NBUF]
   static constexpr int kTotal = kBarOffset + 2 * NBUF * 8;
-  static_assert(kQOffset % 16 == 0 && kWOffset % 16 == 0, "ldmatrix alignment");
+  static_assert(kQOffset % 16 == 0 && kWOffset % 16 == 0 && kRedOffset % 16 == 0, "ldmatrix / vector alignment");
   static_assert(kTotal <= 227 * 1024, "shared memory of one CTA");
 };
 
@@ -294,9 +294,9 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
   const uint32_t k_lane_off = ((mi & 1) * 8 + r) * RB + (mi >> 1) * 16;
   const uint32_t v_lane_off = ((mi >> 1) * 8 + r) * RB + R::kV + (mi & 1) * 16;
   const uint32_t q_lane_off = static_cast<uint32_t>(smem_u32(q_s)) + mi * 128 + r * 16;
-  float* red_s = red;                  // [warp][NH] tile maxima of the scores
-  float* red_z = red + 4 * NH;         // [warp][NH] tile maxima of z
-  float* red_l = red + 8 * NH;         // [warp][NH] parts of l_c
+  float* red_s = red;                  // [NH][warp] chunk maxima of the scores
+  float* red_z = red + 4 * NH;         // [NH][warp] chunk maxima of z
+  float* red_l = red + 8 * NH;         // [NH][warp] parts of l_c
 
   int c = 0;
   bool failed = false;
@@ -362,8 +362,8 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
           tmz = fmaxf(tmz, __shfl_xor_sync(0xffffffffu, tmz, off));
         }
         if (g == 0) {
-          red_s[warp * NH + nt * 8 + 2 * c4 + e] = tms;
-          red_z[warp * NH + nt * 8 + 2 * c4 + e] = tmz;
+          red_s[(nt * 8 + 2 * c4 + e) * 4 + warp] = tms;
+          red_z[(nt * 8 + 2 * c4 + e) * 4 + warp] = tmz;
         }
       }
     // every warp's maxima are in place, and every warp leaves together if a wait ran out
@@ -380,12 +380,10 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int hd = nt * 8 + 2 * c4 + e;
-        float cs = red_s[hd], cz = red_z[hd];
-#pragma unroll
-        for (int q2 = 1; q2 < 4; ++q2) {
-          cs = fmaxf(cs, red_s[q2 * NH + hd]);
-          cz = fmaxf(cz, red_z[q2 * NH + hd]);
-        }
+        const float4 vs4 = *reinterpret_cast<const float4*>(red_s + hd * 4);
+        const float4 vz4 = *reinterpret_cast<const float4*>(red_z + hd * 4);
+        const float cs = fmaxf(fmaxf(vs4.x, vs4.y), fmaxf(vs4.z, vs4.w));
+        const float cz = fmaxf(fmaxf(vz4.x, vz4.y), fmaxf(vz4.z, vz4.w));
         ms_new[nt][e] = fmaxf(ms[nt][e], cs);
         mz_new[nt][e] = fmaxf(mz[nt][e], cz);
         const float msr = ms_new[nt][e] == -INFINITY ? 0.f : ms_new[nt][e];
@@ -393,7 +391,7 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
         float lp = fast_exp2(sc[nt][e] - msr) + fast_exp2(sc[nt][2 + e] - msr);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) lp += __shfl_xor_sync(0xffffffffu, lp, off);
-        if (g == 0) red_l[warp * NH + hd] = lp;
+        if (g == 0) red_l[hd * 4 + warp] = lp;
         w[0][e] = fast_exp2(zc[nt][e] - mzr);      // cell g
         w[1][e] = fast_exp2(zc[nt][2 + e] - mzr);  // cell g + 8
       }
@@ -418,7 +416,8 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int hd = nt * 8 + 2 * c4 + e;
-        const float lc = (red_l[hd] + red_l[NH + hd]) + (red_l[2 * NH + hd] + red_l[3 * NH + hd]);
+        const float4 vl4 = *reinterpret_cast<const float4*>(red_l + hd * 4);
+        const float lc = (vl4.x + vl4.y) + (vl4.z + vl4.w);
         const float al = ms[nt][e] == -INFINITY ? 0.f : fast_exp2(ms[nt][e] - ms_new[nt][e]);
         lsum[nt][e] = fmaf(lsum[nt][e], al, lc);
         ms[nt][e] = ms_new[nt][e];
