@@ -36,7 +36,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 STAGE1_TRAFFIC_BYTES = 68233728 + 125184
 STAGE1_TRAFFIC_SOURCES = ("int8_kv_cache_quant_gb300/csrc/decode.cu", "int8_kv_cache_quant_gb300/csrc/kvq_dev.cuh",
                           "int8_kv_cache_quant_gb300/csrc/quant_rule.cuh")
-STAGE1_TRAFFIC_SHA = "0965578520f7644f"
+STAGE1_TRAFFIC_SHA = "88a3b7518a689cda"
 
 
 def stage1_traffic():

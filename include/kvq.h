@@ -195,6 +195,7 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
  *   out        : device fp32 [batch][n_q_heads][head_dim]
  *   workspace  : device, >= kvq_decode_workspace_bytes(...), 16-byte aligned; its
  *                contents on entry do not matter
+ * The GQA group (n_q_heads / n_kv_heads) may be 1..16; a larger one is KVQ_ERR_UNSUPPORTED.
  */
 /*
  * kvq_decode_auto_split_rows — the split size the split route uses when opts->split_rows is
@@ -275,7 +276,7 @@ size_t kvq_verify_workspace_bytes(int32_t batch, int32_t n_rows, int32_t n_q_hea
  *   workspace  : >= kvq_verify_workspace_bytes(...), 16-byte aligned
  *   other arguments as kvq_attn_decode_int8kv.
  * KVQ_ERR_UNSUPPORTED when (n_q_heads / n_kv_heads) * n_rows > KVQ_VERIFY_MAX_ROWS, the GQA
- * group exceeds 8, or batch * n_rows > 65535.
+ * group exceeds 16, or batch * n_rows > 65535.
  */
 int kvq_attn_verify_int8kv(const kvq_cache* cache, const void* q, int32_t batch, int32_t n_rows,
                            int32_t n_q_heads, const int32_t* block_table, int32_t max_blocks_per_seq,

@@ -296,7 +296,7 @@ static int decode_rows(const kvq_cache* cache, const void* k_new, const void* v_
   if (static_cast<long long>(batch) * nq > 65535) return KVQ_ERR_UNSUPPORTED;
   if (n_q_heads % cache->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   const int G = n_q_heads / cache->n_kv_heads;
-  if (G > 8 || static_cast<long long>(G) * nq > KVQ_VERIFY_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
+  if (G > 16 || static_cast<long long>(G) * nq > KVQ_VERIFY_MAX_ROWS) return KVQ_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(out)) return KVQ_ERR_MISALIGNED;
   if (!aligned4(block_table) || !aligned4(ctx_lens)) return KVQ_ERR_MISALIGNED;
   const int mc = max_ctx > 0 ? max_ctx : 1;

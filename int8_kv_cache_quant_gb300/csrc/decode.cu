@@ -20,7 +20,8 @@
 //   CTA.
 // * QK and PV of a 16-token page run on the tensor cores (mma.sync m16n8k16, fp32
 //   accumulate) with the int8 codes widened to integer-valued fp16 in registers (exact:
-//   |code| <= 127).  S^T = K * Q^T puts the 16 tokens on M and the GQA group (<= 8 heads)
+//   |code| <= 127).  S^T = K * Q^T puts the 16 tokens on M and the GQA group (<= 8 heads; a
+//   larger group, up to 16, takes the rows path below with its heads as the rows)
 //   on N; O^T = V^T * W puts 16 head dimensions on M.  This keeps the FP32 pipe free: at
 //   GQA 6 x head_dim 256 a CUDA-core FMA decode needs ~11 us of FMA issue per 68 MB of
 //   K/V on GB300, more than the ~10 us the bytes take at the measured HBM rate.
@@ -937,7 +938,7 @@ static cudaError_t launch_stage1(const DecodeArgs& a, dim3 grid, cudaStream_t st
 
 template <int D, bool SPLIT>
 static cudaError_t launch_stage1_rows(const DecodeArgs& a, dim3 grid, cudaStream_t stream) {
-  if (a.nq == 1) {  // plain decode, or the fused one-token step
+  if (a.nq == 1 && a.n_q_heads / a.n_kv_heads <= 8) {  // plain decode, or the fused one-token step
     if (a.k_new) return launch_stage1<D, 1, SPLIT, false, true>(a, grid, stream);
     return launch_stage1<D, 1, SPLIT, false, false>(a, grid, stream);
   }

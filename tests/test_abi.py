@@ -118,10 +118,10 @@ def test_invalid_arguments_rejected_before_launch():
     assert L.kvq_quant_write(ctypes.byref(c), 16, 16, 1, 16, 16, 16, 1, 1, None) == 3
     c = k.kvq._Cache(16, 16, 16, 16, 4, 16, 4, 256)
     assert L.kvq_quant_write(ctypes.byref(c), None, 16, 1, 16, 16, 16, 1, 1, None) == 1
-    # decode: Hq not a multiple of Hkv; group above 8; workspace too small
+    # decode: Hq not a multiple of Hkv; group above 16; workspace too small
     assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 6, 16, 4, 16, 100, 1.0, 16, None, 0,
                                     None, None) == 1
-    assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 40, 16, 4, 16, 100, 1.0, 16, None, 0,
+    assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 68, 16, 4, 16, 100, 1.0, 16, None, 0,
                                     None, None) == 2
     assert L.kvq_attn_decode_int8kv(ctypes.byref(c), 16, 1, 8, 16, 4000, 16, 60000, 1.0, 16, None,
                                     0, None, None) == 4

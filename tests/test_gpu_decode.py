@@ -45,8 +45,11 @@ def test_small_contexts_both_routes(kvq, oracle, route, ctx):
     assert kvq.kvq_device_status() == 0
 
 
-@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 8, 1), (256, 16, 2), (128, 4, 4)])
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 8, 1), (256, 16, 2), (128, 4, 4),
+                                      (128, 32, 2), (256, 12, 1), (256, 16, 1)])
 def test_head_geometries(kvq, oracle, d, hq, hkv):
+    """GQA groups 1..8 take the one-row kernel; 12 and 16 take the rows kernel with the group's
+    heads as its rows (two 8-row n-tiles)."""
     w = W.make("decode_b64", seed=300 + hq, batch=5, ctx_range=(1, 1500), hq=hq, hkv=hkv, d=d)
     hc = host_cache_from(w, oracle)
     ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
@@ -175,3 +178,14 @@ def test_ctx_above_max_ctx_is_clamped_and_reported(kvq, oracle):
                                          split_rows=256).cpu().numpy()
         assert kvq.kvq_device_status() & kvq.kvq.DEV_BAD_POS, route
         assert norm_max_err(got, ref) <= DESIGN_TOL, route
+
+
+def test_gqa_group_above_16_is_refused(kvq):
+    import torch
+    cache = kvq.KVCache(4, 2, 128)
+    q = torch.zeros((1, 34, 128), dtype=torch.bfloat16, device="cuda")
+    bt = torch.zeros((1, 4), dtype=torch.int32, device="cuda")
+    ctx = torch.ones(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, 64, 0.1)
+    assert e.value.status == 2  # KVQ_ERR_UNSUPPORTED

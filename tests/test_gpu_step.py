@@ -49,7 +49,8 @@ def _check_cache(cache, hc):
 
 
 @pytest.mark.parametrize("nq,d,hq,hkv,route", [(1, 128, 32, 8, 2), (1, 256, 24, 4, 1), (1, 256, 24, 4, 2),
-                                               (4, 256, 24, 4, 2), (3, 128, 8, 2, 1), (6, 128, 16, 2, 2)])
+                                               (4, 256, 24, 4, 2), (3, 128, 8, 2, 1), (6, 128, 16, 2, 2),
+                                               (1, 256, 32, 2, 2), (3, 128, 32, 2, 1)])
 def test_step_writes_and_attends(kvq, oracle, nq, d, hq, hkv, route):
     w = W.make("decode_b64", seed=700 + nq + d + route, batch=5, ctx_range=(nq, 1500), hq=hq, hkv=hkv, d=d, nq=nq)
     cache, bt = _cache_without_new(kvq, w)
