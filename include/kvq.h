@@ -168,7 +168,7 @@ typedef struct kvq_decode_opts {
 
 /* Workspace (bytes) the split route of kvq_attn_decode_int8kv needs; 0 when the call
  * will take the single-CTA route.  With opts->split_rows == 0 it is the bound for the
- * smallest split the automatic rule can choose (256 keys), so it does not depend on the GPU
+ * smallest split the automatic rule can choose (64 keys), so it does not depend on the GPU
  * (and with the automatic route it is nonzero whenever max_ctx exceeds that split). */
 size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_ctx,
                                   int32_t head_dim, const kvq_decode_opts* opts);
@@ -205,7 +205,7 @@ size_t kvq_decode_workspace_bytes(int32_t batch, int32_t n_q_heads, int32_t max_
  *   If units * ceil(pages / 32) > 2 * slots (at 512-key splits the grid is over two waves),
  *   the split takes clamp(units * pages / (4 * slots), 32, 128) pages: longer splits amortise
  *   each CTA's start-up over more pages.
- *   Otherwise the split takes max(16, ceil(pages / floor(slots / units))) pages: the grid fills
+ *   Otherwise the split takes max(4, ceil(pages / floor(slots / units))) pages: the grid fills
  *   every SM in one wave.
  * Returns keys (pages * 16); 0 if an argument is not positive or head_dim is not 128 / 256.
  * The source pages use a fixed 512 ([DOT4] route table); any split size gives the same result
@@ -242,7 +242,7 @@ int kvq_attn_decode_int8kv(const kvq_cache* cache, const void* q, int32_t batch,
  *   array keeps the last call's contents; every call writes the partials it reads, so
  *   nothing in it has to start at zero.
  */
-#define KVQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define KVQ_NOALLOC_SCRATCH_BYTES (16u << 20)
 int kvq_attn_decode_int8kv_noalloc(const kvq_cache* cache, const void* q, int32_t batch,
                                    int32_t n_q_heads, const int32_t* block_table,
                                    int32_t max_blocks_per_seq, const int32_t* ctx_lens,

@@ -187,7 +187,7 @@ int kvq_rope_quant_write(const kvq_cache* cache, const void* q, int32_t n_q_head
 }
 
 // Smallest split the automatic rule chooses: the workspace bound when split_rows is 0.
-constexpr int kAutoSplitMinRows = 16 * KVQ_BLOCK_SIZE;
+constexpr int kAutoSplitMinRows = 4 * KVQ_BLOCK_SIZE;
 
 // Whether the split route may be taken, from host arguments alone (sizes the workspace).  The
 // automatic route splits only when the split size leaves more than one split, and the automatic
@@ -212,7 +212,7 @@ int32_t kvq_decode_auto_split_rows(int32_t batch, int32_t n_kv_heads, int32_t he
     split_pages = std::min(128LL, std::max(32LL, units * pages / (4 * slots)));
   } else {
     const long long per_unit = std::max(1LL, slots / units);
-    split_pages = std::max(16LL, (pages + per_unit - 1) / per_unit);
+    split_pages = std::max(4LL, (pages + per_unit - 1) / per_unit);
   }
   return static_cast<int32_t>(split_pages * KVQ_BLOCK_SIZE);
 }

@@ -320,7 +320,7 @@ def kvq_decode_step_int8kv(cache, k_new, v_new, q, block_table, ctx_lens, max_ct
     return ret
 
 
-NOALLOC_SCRATCH_BYTES = 4 << 20
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def kvq_attn_decode_int8kv_noalloc(cache, q, block_table, ctx_lens, max_ctx, softmax_scale, out,

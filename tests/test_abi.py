@@ -35,22 +35,23 @@ def test_host_helpers_without_gpu():
     assert L.kvq_device_accessible(ctypes.c_void_p(buf.ctypes.data)) == 0
     assert L.kvq_device_accessible(None) == 0
     # workspace sizes are pure host arithmetic
-    # automatic split size: the workspace is the bound for its smallest split (256 keys)
-    assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 128 * 24 * 256 * 4 + 128 * 24 * 16
+    # automatic split size: the workspace is the bound for its smallest split (64 keys)
+    assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256) == 512 * 24 * 256 * 4 + 512 * 24 * 16
     assert k.kvq_decode_workspace_bytes(1, 24, 32768, 256, split_rows=512) == 64 * 24 * 256 * 4 + 64 * 24 * 16
     # the automatic rule: one wave of resident CTAs (one per SM at head_dim 256, two at 128) for
-    # few (sequence, KV head) units, 2048-key splits for a large batch; never below 256 keys
+    # few (sequence, KV head) units, 2048-key splits for a large batch; never below 64 keys
     assert k.kvq_decode_auto_split_rows(1, 4, 256, 32768, 152) == 864   # 38 splits x 4 = 152 CTAs
     assert k.kvq_decode_auto_split_rows(1, 4, 128, 32768, 152) == 432   # 76 x 4 = 304 (two per SM)
     assert k.kvq_decode_auto_split_rows(64, 8, 128, 16384, 152) == 2048
-    assert k.kvq_decode_auto_split_rows(1, 4, 256, 4096, 152) == 256
+    assert k.kvq_decode_auto_split_rows(1, 4, 256, 4096, 152) == 112   # 37 splits x 4 = 148 CTAs
+    assert k.kvq_decode_auto_split_rows(1, 4, 256, 1024, 152) == 64    # 16 x 4: four pages per CTA
     assert k.kvq_decode_auto_split_rows(1, 1, 256, 1 << 20, 152) == 1712
     assert k.kvq_decode_auto_split_rows(0, 4, 256, 4096, 152) == 0
     assert k.kvq_decode_auto_split_rows(1, 4, 192, 4096, 152) == 0
     # automatic route: one split (ctx within the smallest automatic split) is the single-CTA
     # route; beyond it the split route may be taken
-    assert k.kvq_decode_workspace_bytes(1, 24, 256, 256) == 0
-    assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 4 * 24 * 256 * 4 + 4 * 24 * 16
+    assert k.kvq_decode_workspace_bytes(1, 24, 64, 256) == 0
+    assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256) == 16 * 24 * 256 * 4 + 16 * 24 * 16
     # the pages' threshold route: ctx <= 2048 takes the single-CTA route
     assert k.kvq_decode_workspace_bytes(1, 24, 1024, 256, route_threshold=2048) == 0
     # verify: the decode workspace of batch * n_rows query rows
