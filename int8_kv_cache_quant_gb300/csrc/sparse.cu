@@ -422,25 +422,35 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
         lsum[nt][e] = fmaf(lsum[nt][e], al, lc);
         ms[nt][e] = ms_new[nt][e];
       }
-    // ---- acc_c = V^T W over the chunk's 64 cells for this warp's dims, from zero; then the fold
-    float acc_c[2 * NDB][NHT][4];
+    // ---- acc_c = V^T W over the chunk's 64 cells for this warp's dims, from zero; then the fold.
+    // One 32-dim block at a time (its two m-tiles' chunk accumulators over the four 16-cell
+    // tiles, then their fold), so that only one block's accumulators are live.
+    float al[NHT][2];
 #pragma unroll
-    for (int t = 0; t < 2 * NDB; ++t)
+    for (int nt = 0; nt < NHT; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < NHT; ++nt) acc_c[t][nt][0] = acc_c[t][nt][1] = acc_c[t][nt][2] = acc_c[t][nt][3] = 0.f;
-#pragma unroll
-    for (int tile = 0; tile < 4; ++tile) {
-      uint32_t bf[NHT][4];
-#pragma unroll
-      for (int nt = 0; nt < NHT; ++nt) {
-        const uint4 wv = wx[(tile * NHT + nt) * 32 + lane];
-        bf[nt][0] = wv.x;
-        bf[nt][1] = wv.y;
-        bf[nt][2] = wv.z;
-        bf[nt][3] = wv.w;
+      for (int e = 0; e < 2; ++e) {
+        al[nt][e] = mz[nt][e] == -INFINITY ? 0.f : fast_exp2(mz[nt][e] - mz_new[nt][e]);
+        mz[nt][e] = mz_new[nt][e];
       }
 #pragma unroll
-      for (int db = 0; db < NDB; ++db) {
+    for (int db = 0; db < NDB; ++db) {
+      float acc_c[2][NHT][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NHT; ++nt) acc_c[t][nt][0] = acc_c[t][nt][1] = acc_c[t][nt][2] = acc_c[t][nt][3] = 0.f;
+#pragma unroll
+      for (int tile = 0; tile < 4; ++tile) {
+        uint32_t bf[NHT][4];
+#pragma unroll
+        for (int nt = 0; nt < NHT; ++nt) {
+          const uint4 wv = wx[(tile * NHT + nt) * 32 + lane];
+          bf[nt][0] = wv.x;
+          bf[nt][1] = wv.y;
+          bf[nt][2] = wv.z;
+          bf[nt][3] = wv.w;
+        }
         uint32_t r0, r1, r2, r3, e0, e1, e2, e3, o0, o1, o2, o3;
         ldsm_x4_trans(bbase + tile * 16 * RB + v_lane_off + (warp * NDB + db) * 32, r0, r1, r2, r3);
         i8x4_to_h2x2(r0, kSelB02, kSelB13, e0, o0);  // cells 0..7, dims + 0..15
@@ -449,25 +459,22 @@ __global__ void __launch_bounds__(128, NBUF == 1 ? 4 : 2) sparse_chunk_kernel(Sp
         i8x4_to_h2x2(r3, kSelB02, kSelB13, e3, o3);  // cells 8..15, dims + 16..31
 #pragma unroll
         for (int nt = 0; nt < NHT; ++nt) {
-          mma_f16_16816(acc_c[2 * db][nt], e0, e1, e2, e3, bf[nt][0], bf[nt][1]);
-          mma_f16_16816(acc_c[2 * db][nt], e0, e1, e2, e3, bf[nt][2], bf[nt][3]);
-          mma_f16_16816(acc_c[2 * db + 1][nt], o0, o1, o2, o3, bf[nt][0], bf[nt][1]);
-          mma_f16_16816(acc_c[2 * db + 1][nt], o0, o1, o2, o3, bf[nt][2], bf[nt][3]);
+          mma_f16_16816(acc_c[0][nt], e0, e1, e2, e3, bf[nt][0], bf[nt][1]);
+          mma_f16_16816(acc_c[0][nt], e0, e1, e2, e3, bf[nt][2], bf[nt][3]);
+          mma_f16_16816(acc_c[1][nt], o0, o1, o2, o3, bf[nt][0], bf[nt][1]);
+          mma_f16_16816(acc_c[1][nt], o0, o1, o2, o3, bf[nt][2], bf[nt][3]);
         }
       }
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NHT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            o_acc[2 * db + t][nt][e] = fmaf(o_acc[2 * db + t][nt][e], al[nt][e], acc_c[t][nt][e]);
+            o_acc[2 * db + t][nt][2 + e] = fmaf(o_acc[2 * db + t][nt][2 + e], al[nt][e], acc_c[t][nt][2 + e]);
+          }
     }
-#pragma unroll
-    for (int nt = 0; nt < NHT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float al = mz[nt][e] == -INFINITY ? 0.f : fast_exp2(mz[nt][e] - mz_new[nt][e]);
-#pragma unroll
-        for (int t = 0; t < 2 * NDB; ++t) {
-          o_acc[t][nt][e] = fmaf(o_acc[t][nt][e], al, acc_c[t][nt][e]);
-          o_acc[t][nt][2 + e] = fmaf(o_acc[t][nt][2 + e], al, acc_c[t][nt][2 + e]);
-        }
-        mz[nt][e] = mz_new[nt][e];
-      }
     // ---- this warp is done with the buffer: refill it with chunk c + NBUF once all four are
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[b]);
