@@ -912,6 +912,69 @@ __global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(DecodeArgs 
   }
 }
 
+// Stage 2 for many (query row, head) units with few splits each (a large batch): one warp per
+// unit, the splits' statistics in its lanes and their weights passed by shuffles, each lane
+// combining D / 32 head dimensions of every split.  No shared memory and no block barrier, and
+// a CTA of eight warps takes eight units, so the grid stays within a wave where the per-(unit,
+// 64-dim block) CTAs of decode_merge_kernel would take several.  The same rule as that kernel.
+constexpr int kMergeWarpMaxSplits = 32;
+
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_warp_kernel(DecodeArgs a) {
+  constexpr int PER = D / 32;  // dims per lane
+  const int lane = threadIdx.x & 31;
+  const int Hq = a.n_q_heads;
+  const long long unit = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);  // row * Hq + h
+  grid_dep_wait();  // the partials come from stage 1
+  if (unit >= static_cast<long long>(a.batch) * a.nq * Hq) return;  // warp-uniform
+  const int row = static_cast<int>(unit / Hq), b = row / a.nq;
+  int ctx = a.ctx_lens[b];
+  ctx = max(0, min(ctx, min(a.max_blocks_per_seq * KVQ_BLOCK_SIZE, a.max_ctx)));
+  const int n = min(a.n_split, (ctx + a.split_rows - 1) / a.split_rows);
+  const long long pu0 = unit * a.n_split;
+  float4 st = make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+  if (lane < n) st = reinterpret_cast<const float4*>(a.part_stats)[pu0 + lane];
+  float Ms = st.x, Mz = st.y;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    Ms = fmaxf(Ms, __shfl_xor_sync(0xffffffffu, Ms, off));
+    Mz = fmaxf(Mz, __shfl_xor_sync(0xffffffffu, Mz, off));
+  }
+  float l = (Ms != -INFINITY && st.x != -INFINITY) ? st.z * fast_exp2(st.x - Ms) : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+  const float wgt = (Mz != -INFINITY && st.y != -INFINITY) ? fast_exp2(st.y - Mz) : 0.f;  // split `lane`
+  float o[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) o[i] = 0.f;
+  const float* acc = a.part_acc + pu0 * D + lane * PER;
+  for (int s0 = 0; s0 < n; s0 += 8) {
+    float4 v[8][PER / 4];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (s0 + u < n)
+#pragma unroll
+        for (int i = 0; i < PER / 4; ++i) v[u][i] = *reinterpret_cast<const float4*>(acc + static_cast<long long>(s0 + u) * D + 4 * i);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wgt, (s0 + u) & 31);
+      if (s0 + u < n)
+#pragma unroll
+        for (int i = 0; i < PER / 4; ++i) {
+          o[4 * i + 0] = fmaf(v[u][i].x, w, o[4 * i + 0]);
+          o[4 * i + 1] = fmaf(v[u][i].y, w, o[4 * i + 1]);
+          o[4 * i + 2] = fmaf(v[u][i].z, w, o[4 * i + 2]);
+          o[4 * i + 3] = fmaf(v[u][i].w, w, o[4 * i + 3]);
+        }
+    }
+  }
+  const float sc = (l > 0.f && Mz != -INFINITY) ? fast_exp2(Mz - Ms) / l : 0.f;
+  float* dst = a.out + unit * D + lane * PER;
+#pragma unroll
+  for (int i = 0; i < PER / 4; ++i)
+    *reinterpret_cast<float4*>(dst + 4 * i) = make_float4(o[4 * i] * sc, o[4 * i + 1] * sc, o[4 * i + 2] * sc, o[4 * i + 3] * sc);
+}
+
 size_t decode_workspace_bytes(int batch, int n_q_heads, int max_ctx, int head_dim, int split_rows) {
   const long long n_split = (static_cast<long long>(max_ctx) + split_rows - 1) / split_rows;
   const long long units = static_cast<long long>(batch) * n_q_heads * n_split;
@@ -968,6 +1031,15 @@ cudaError_t launch_decode(const DecodeArgs& a, DecodeRoute route, cudaStream_t s
   else
     e = launch_stage1_rows<128, true>(a, grid, stream);
   if (e != cudaSuccess) return e;
+  const long long units = static_cast<long long>(a.batch) * a.nq * a.n_q_heads;
+  if (a.n_split <= kMergeWarpMaxSplits && units >= 512) {
+    // many units, few splits each: a warp per unit
+    const dim3 gw(static_cast<unsigned>((units + 7) / 8));
+    e = a.head_dim == 256 ? launch_pdl(decode_merge_warp_kernel<256>, gw, dim3(256), 0, stream, a)
+                          : launch_pdl(decode_merge_warp_kernel<128>, gw, dim3(256), 0, stream, a);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   const size_t wbytes = static_cast<size_t>(a.n_split) * sizeof(float);
   dim3 g2(a.n_q_heads, a.batch * a.nq, a.head_dim / kMergeCols);
   if (a.head_dim == 256) {

@@ -189,3 +189,17 @@ def test_gqa_group_above_16_is_refused(kvq):
     with pytest.raises(kvq.KvqError) as e:
         kvq.kvq_attn_decode_int8kv(cache, q, bt, ctx, 64, 0.1)
     assert e.value.status == 2  # KVQ_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_many_units_few_splits_merge(kvq, oracle, d):
+    """A batch with many (sequence, query head) units and a few splits each takes the
+    warp-per-unit merge: against FP64, and ctx 0 rows give zeros."""
+    w = W.make("decode_b64", seed=330 + d, batch=24, ctx_range=(300, 2000), hq=24, hkv=4, d=d)
+    w["ctx_lens"][3] = 0
+    got, _, _ = _run(kvq, w, force_route=2, split_rows=256)
+    hc = host_cache_from(w, oracle)
+    ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
+    assert np.all(got[3] == 0)
+    assert norm_max_err(got, ref) <= DESIGN_TOL
+    assert kvq.kvq_device_status() == 0
