@@ -76,8 +76,10 @@ __global__ void __launch_bounds__(256) sparse_prep_kernel(SparseArgs a) {
   }
   __syncthreads();
   if (t < D) {
-    // V of slot s, dims 16 db .. 16 db + 15, gathered from the [dim][slot] block
-    const int s = t / (D / 16), db = t % (D / 16);
+    // V of slot s, dims 16 db .. 16 db + 15, gathered from the [dim][slot] block; consecutive
+    // threads take consecutive slots, so a warp's byte reads of one dim share a word (the other
+    // order put the 16 dims' reads of a warp in one bank)
+    const int s = t % KVQ_BLOCK_SIZE, db = t / KVQ_BLOCK_SIZE;
     uint32_t w[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
