@@ -7,7 +7,7 @@
 // scale = amax / 127, q = clamp(round(x / scale), -127, 127)) and §2.3 (K in 16-element
 // head-dimension chunks with the tokens of a chunk adjacent, V token-contiguous per dimension).
 // Scales are IEEE fp32 quotients (__fdiv_rn), codes the nearest-even rounding of the IEEE
-// quotient x / scale (computed through the reciprocal where that provably gives the same code).
+// quotient x / scale (computed through a reciprocal where that provably gives the same code).
 #pragma once
 
 #include <cstdint>
@@ -49,28 +49,29 @@ __device__ __forceinline__ float quant_rule_warp(const float (&x)[P], int8_t (&q
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   const float scale = __fdiv_rn(amax, 127.0f);
-  // code = rint(RN(x / scale)), taken as rint(y) with y = RN(x * RN(1 / scale)).  y lies within
-  // |x / scale| * 2^-23 (< 1.6e-5, since |x / scale| <= 127 (1 + 2^-23)) of the exact quotient and
-  // RN(x / scale) within 2^-18 of it, so the two round to the same integer unless y is within 2^-15
-  // of a half-integer; there (and where 1 / scale overflows) the IEEE division decides.
-  const float r = __fdiv_rn(1.0f, scale);
+  // code = rint(RN(x / scale)), taken as c = rint(y) with y = RN(x * r) and r the hardware
+  // reciprocal of scale (at most 1 ulp from 1 / scale).  y then lies within |x / scale| * 1.5 *
+  // 2^-23 (< 2.3e-5, since |x / scale| <= 127 (1 + 2^-23)) of the exact quotient and RN(x / scale)
+  // within 7.6e-6 of it, so c is the rule's code unless y is within 3.1e-5 of a half-integer.
+  // t = y - c is exact (c is the integer nearest y), and |t| > 1/2 - 2^-14 marks those elements
+  // with room to spare (it would still hold for an r 3 ulp off), and non-finite y (where r
+  // overflows or the input is not finite); there the IEEE division decides.
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(scale));
   float c[P];
   bool exact_needed = false;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
     const float y = __fmul_rn(x[i], r);
-    // y's signed distance to the half-integer above floor(y), within 2^-24 of the exact value
-    const float h = __fsub_rn(__fsub_rn(y, floorf(y)), 0.5f);
-    const bool fast = fabsf(h) >= 3.0517578125e-05f;           // false for NaN / inf
-    exact_needed |= !fast;
     c[i] = rintf(y);
+    const bool fast = fabsf(__fsub_rn(y, c[i])) <= 0.49993896484375f;  // 1/2 - 2^-14; false for NaN
+    exact_needed |= !fast;
   }
   if (__any_sync(0xffffffffu, exact_needed && amax != 0.0f)) {
 #pragma unroll
     for (int i = 0; i < P; ++i) {
       const float y = __fmul_rn(x[i], r);
-      const float h = __fsub_rn(__fsub_rn(y, floorf(y)), 0.5f);
-      if (!(fabsf(h) >= 3.0517578125e-05f)) c[i] = rintf(__fdiv_rn(x[i], scale));
+      if (!(fabsf(__fsub_rn(y, rintf(y))) <= 0.49993896484375f)) c[i] = rintf(__fdiv_rn(x[i], scale));
     }
   }
 #pragma unroll

@@ -144,8 +144,9 @@ __device__ __forceinline__ void rope_lane(float (&x)[P], const RopeQuantArgs& a,
   for (int e = 0; e < P; ++e) {
     const float other = __shfl_sync(0xffffffffu, x[e], partner);
     if (rotated) {
-      const float c = __ldg(cs + fi + e), sn = __ldg(cs + half + fi + e);
-      x[e] = first ? __fmaf_rn(x[e], c, -__fmul_rn(other, sn)) : __fmaf_rn(x[e], c, __fmul_rn(other, sn));
+      // -(o * s) == o * (-s) exactly, so the sign goes onto the table value
+      const float c = __ldg(cs + fi + e), sn = first ? -__ldg(cs + half + fi + e) : __ldg(cs + half + fi + e);
+      x[e] = __fmaf_rn(x[e], c, __fmul_rn(other, sn));
     }
   }
 }
@@ -164,13 +165,15 @@ __device__ __forceinline__ void rope_q_rows(const RopeQuantArgs& a, int tok, int
   const int d0 = lane * P;
   const bool first = d0 < half, rotated = d0 < a.rotary_dim;
   const int partner = rotated ? (first ? lane + shift : lane - shift) : lane;
+  // cos and sin of this lane's dims; the sin carries the rotation's sign for the first half
+  // (-(o * s) == o * (-s) exactly)
   float cf[P], sf[P];
   if (pos_ok && rotated) {
     const float* cs = a.cos_sin + static_cast<long long>(p) * a.rotary_dim + (first ? d0 : d0 - half);
 #pragma unroll
     for (int e = 0; e < P; ++e) {
       cf[e] = __ldg(cs + e);
-      sf[e] = __ldg(cs + half + e);
+      sf[e] = first ? -__ldg(cs + half + e) : __ldg(cs + half + e);
     }
   }
   using Raw = typename std::conditional<P == 8, uint4, uint2>::type;
@@ -180,25 +183,27 @@ __device__ __forceinline__ void rope_q_rows(const RopeQuantArgs& a, int tok, int
     const Raw raw = nxt;
     if (h + 1 < h1) nxt = __ldg(reinterpret_cast<const Raw*>(qrow + (h + 1) * D));
     float x[P];
-    {
-      uint32_t w[P / 2];
-      if constexpr (P == 8) {
-        w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
-      } else {
-        w[0] = raw.x; w[1] = raw.y;
-      }
+    uint32_t w[P / 2];
+    if constexpr (P == 8) {
+      w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
+    } else {
+      w[0] = raw.x; w[1] = raw.y;
+    }
 #pragma unroll
-      for (int i = 0; i < P / 2; ++i) {
-        x[2 * i] = __uint_as_float(w[i] << 16);
-        x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
+    for (int i = 0; i < P / 2; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
     // ---- rotate, quantise, codes + scale + rotated bf16 row
     if (pos_ok) {
+      // the partner's element e is element e of lane `partner`: its bf16 pairs move as they are
 #pragma unroll
-      for (int e = 0; e < P; ++e) {
-        const float other = __shfl_sync(0xffffffffu, x[e], partner);
-        if (rotated) x[e] = first ? __fmaf_rn(x[e], cf[e], -__fmul_rn(other, sf[e])) : __fmaf_rn(x[e], cf[e], __fmul_rn(other, sf[e]));
+      for (int i = 0; i < P / 2; ++i) {
+        const uint32_t ow = __shfl_sync(0xffffffffu, w[i], partner);
+        if (rotated) {
+          x[2 * i] = __fmaf_rn(x[2 * i], cf[2 * i], __fmul_rn(__uint_as_float(ow << 16), sf[2 * i]));
+          x[2 * i + 1] = __fmaf_rn(x[2 * i + 1], cf[2 * i + 1], __fmul_rn(__uint_as_float(ow & 0xFFFF0000u), sf[2 * i + 1]));
+        }
       }
     } else {
 #pragma unroll
