@@ -110,16 +110,14 @@ __device__ __forceinline__ void write_new_tokens(const DecodeArgs& a, int b, int
     const long long row = ((static_cast<long long>(b) * nq + (t - first_new)) * a.n_kv_heads + kvh) * D + lane * P;
     const int slot = t % KVQ_BLOCK_SIZE;
     float xk[P], xv[P];
-    int8_t qc[P];
     uint32_t packed[P / 4];
     // both rows before any store (the stores could alias the inputs as far as the compiler knows)
     load_bf16_lane(static_cast<const uint16_t*>(a.k_new) + row, xk);
     load_bf16_lane(static_cast<const uint16_t*>(a.v_new) + row, xv);
-    const float sk = quant_rule_warp(xk, qc);
-    pack_codes(qc, packed);
+    const float sk = quant_rule_warp_packed(xk, packed);
     store_k_codes<D>(a.k, ph, slot, lane, packed);
-    const float sv = quant_rule_warp(xv, qc);
-    store_v_codes<D>(a.v, ph, slot, lane, qc);
+    const float sv = quant_rule_warp_packed(xv, packed);
+    store_v_codes<D>(a.v, ph, slot, lane, packed);
     if (lane == 0) {
       a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = sk;
       a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = sv;
@@ -412,11 +410,8 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
           xv[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
         }
       }
-      int8_t qc[PER];
-      w_sk = quant_rule_warp(xk, qc);
-      pack_codes(qc, kpk);
-      w_sv = quant_rule_warp(xv, qc);
-      pack_codes(qc, vpk);
+      w_sk = quant_rule_warp_packed(xk, kpk);
+      w_sv = quant_rule_warp_packed(xv, vpk);
       // the page: from the issuing window (page k <-> lane k) when it holds it
       const int page = (k_w < 32) ? __shfl_sync(0xffffffffu, pg, k_w) : __ldg(bt + pr_w);
       w_ok = page >= 0 && page < a.num_blocks;
@@ -424,7 +419,7 @@ __global__ void __launch_bounds__(NT * NTEAM * 32, (D == 128 && NT * NTEAM == 8)
         const long long ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
         const int slot = (ctx - 1) % KVQ_BLOCK_SIZE;
         store_k_codes<D>(a.k, ph, slot, lane, kpk);
-        store_v_codes<D>(a.v, ph, slot, lane, qc);
+        store_v_codes<D>(a.v, ph, slot, lane, vpk);
         if (lane == 0) {
           a.k_scale[ph * KVQ_BLOCK_SIZE + slot] = w_sk;
           a.v_scale[ph * KVQ_BLOCK_SIZE + slot] = w_sv;

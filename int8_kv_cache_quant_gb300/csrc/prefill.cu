@@ -52,10 +52,8 @@ __global__ void __launch_bounds__(256) q_quant_kernel(PrefillArgs a) {
   if (row >= static_cast<long long>(a.n_tokens) * a.n_q_heads) return;
   float x[kPerLane];
   load_bf16_lane(static_cast<const uint16_t*>(a.q) + row * D + lane * kPerLane, x);
-  int8_t qc[kPerLane];
   uint32_t packed[kPerLane / 4];
-  const float scale = quant_rule_warp(x, qc);
-  pack_codes(qc, packed);
+  const float scale = quant_rule_warp_packed(x, packed);
   int8_t* dst = a.q_codes + row * D + lane * kPerLane;
   if constexpr (kPerLane == 8) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
@@ -354,13 +352,10 @@ __global__ void __launch_bounds__(kPackGroup * 32) first_pack_kernel(PrefillArgs
       if (page >= 0 && page < a.num_blocks) {
         ph = static_cast<long long>(page) * a.n_kv_heads + kvh;
         slot = t % KVQ_BLOCK_SIZE;
-        int8_t qc[P];
         uint32_t packed[P / 4];
-        const float ck = quant_rule_warp(xk, qc);
-        pack_codes(qc, packed);
+        const float ck = quant_rule_warp_packed(xk, packed);
         store_k_codes<D>(a.k, ph, slot, lane, packed);
-        const float cv = quant_rule_warp(xv, qc);
-        pack_codes(qc, packed);
+        const float cv = quant_rule_warp_packed(xv, packed);
         if constexpr (P == 8) *reinterpret_cast<uint2*>(&vq[k][lane * P]) = make_uint2(packed[0], packed[1]);
         else *reinterpret_cast<uint32_t*>(&vq[k][lane * P]) = packed[0];
         if (lane == 0) {

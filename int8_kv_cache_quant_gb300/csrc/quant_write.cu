@@ -71,13 +71,10 @@ __global__ void __launch_bounds__(kGroup * 32) quant_write_kernel(QuantWriteArgs
       float xk[P], xv[P];
       load_bf16_lane(static_cast<const uint16_t*>(a.k_new) + row, xk);
       load_bf16_lane(static_cast<const uint16_t*>(a.v_new) + row, xv);
-      int8_t q[P];
       uint32_t packed[P / 4];
-      const float sk = quant_rule_warp(xk, q);
-      pack_codes(q, packed);
+      const float sk = quant_rule_warp_packed(xk, packed);
       store_k_codes<D>(a.k, ph, slot, lane, packed);
-      const float sv = quant_rule_warp(xv, q);
-      pack_codes(q, packed);
+      const float sv = quant_rule_warp_packed(xv, packed);
       if constexpr (P == 8) *reinterpret_cast<uint2*>(&vs[k][lane * P]) = make_uint2(packed[0], packed[1]);
       else *reinterpret_cast<uint32_t*>(&vs[k][lane * P]) = packed[0];
       if (lane == 0) {
@@ -209,10 +206,8 @@ __device__ __forceinline__ void rope_q_rows(const RopeQuantArgs& a, int tok, int
 #pragma unroll
       for (int e = 0; e < P; ++e) x[e] = 0.0f;
     }
-    int8_t qc[P];
     uint32_t packed[P / 4];
-    const float scale = quant_rule_warp(x, qc);
-    pack_codes(qc, packed);
+    const float scale = quant_rule_warp_packed(x, packed);
     const long long u = static_cast<long long>(tok) * Hq + h;
     if (a.q_codes) {
       int8_t* dst = a.q_codes + u * D + d0;
@@ -239,7 +234,7 @@ __device__ __forceinline__ void rope_q_rows(const RopeQuantArgs& a, int tok, int
 // slot, the V row staged in shared memory and written page-wise as in quant_write_kernel).  Warp w
 // takes token w.
 template <int D>
-__global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuantArgs a) {
+__global__ void __launch_bounds__(kGroup * 32, 2) rope_quant_write_kernel(RopeQuantArgs a) {
   constexpr int P = D / 32;
   __shared__ __align__(16) int8_t vs[kGroup][D];
   __shared__ long long tok_ph[kGroup];
@@ -286,13 +281,10 @@ __global__ void __launch_bounds__(kGroup * 32) rope_quant_write_kernel(RopeQuant
           load_bf16_lane(static_cast<const uint16_t*>(a.kv.k_new) + row, xk);
           load_bf16_lane(static_cast<const uint16_t*>(a.kv.v_new) + row, xv);
           rope_lane(xk, a, p, lane);
-          int8_t qc[P];
           uint32_t packed[P / 4];
-          const float sk = quant_rule_warp(xk, qc);
-          pack_codes(qc, packed);
+          const float sk = quant_rule_warp_packed(xk, packed);
           store_k_codes<D>(a.kv.k, ph, slot, lane, packed);
-          const float sv = quant_rule_warp(xv, qc);
-          pack_codes(qc, packed);
+          const float sv = quant_rule_warp_packed(xv, packed);
           if constexpr (P == 8) *reinterpret_cast<uint2*>(&vs[k][lane * P]) = make_uint2(packed[0], packed[1]);
           else *reinterpret_cast<uint32_t*>(&vs[k][lane * P]) = packed[0];
           if (lane == 0) {
