@@ -137,13 +137,22 @@ __device__ __forceinline__ void rope_lane(float (&x)[P], const RopeQuantArgs& a,
   const int partner = rotated ? (first ? lane + shift : lane - shift) : lane;
   const float* cs = a.cos_sin + static_cast<long long>(p) * a.rotary_dim;
   const int fi = first ? d0 : d0 - half;  // frequency index of this lane's first dim
+  // the table row is 16-byte aligned at every lane's first frequency (cos_sin is 16-byte aligned
+  // and rotary_dim / 2 is a multiple of P, hence of 4)
 #pragma unroll
-  for (int e = 0; e < P; ++e) {
-    const float other = __shfl_sync(0xffffffffu, x[e], partner);
+  for (int i = 0; i < P / 4; ++i) {
+    float o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = __shfl_sync(0xffffffffu, x[4 * i + j], partner);
     if (rotated) {
       // -(o * s) == o * (-s) exactly, so the sign goes onto the table value
-      const float c = __ldg(cs + fi + e), sn = first ? -__ldg(cs + half + fi + e) : __ldg(cs + half + fi + e);
-      x[e] = __fmaf_rn(x[e], c, __fmul_rn(other, sn));
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs + fi) + i);
+      float4 s4 = __ldg(reinterpret_cast<const float4*>(cs + half + fi) + i);
+      if (first) s4 = make_float4(-s4.x, -s4.y, -s4.z, -s4.w);
+      x[4 * i] = __fmaf_rn(x[4 * i], c4.x, __fmul_rn(o[0], s4.x));
+      x[4 * i + 1] = __fmaf_rn(x[4 * i + 1], c4.y, __fmul_rn(o[1], s4.y));
+      x[4 * i + 2] = __fmaf_rn(x[4 * i + 2], c4.z, __fmul_rn(o[2], s4.z));
+      x[4 * i + 3] = __fmaf_rn(x[4 * i + 3], c4.w, __fmul_rn(o[3], s4.w));
     }
   }
 }
@@ -168,9 +177,17 @@ __device__ __forceinline__ void rope_q_rows(const RopeQuantArgs& a, int tok, int
   if (pos_ok && rotated) {
     const float* cs = a.cos_sin + static_cast<long long>(p) * a.rotary_dim + (first ? d0 : d0 - half);
 #pragma unroll
-    for (int e = 0; e < P; ++e) {
-      cf[e] = __ldg(cs + e);
-      sf[e] = first ? -__ldg(cs + half + e) : __ldg(cs + half + e);
+    for (int i = 0; i < P / 4; ++i) {
+      const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs) + i);
+      const float4 s4 = __ldg(reinterpret_cast<const float4*>(cs + half) + i);
+      cf[4 * i] = c4.x;
+      cf[4 * i + 1] = c4.y;
+      cf[4 * i + 2] = c4.z;
+      cf[4 * i + 3] = c4.w;
+      sf[4 * i] = first ? -s4.x : s4.x;
+      sf[4 * i + 1] = first ? -s4.y : s4.y;
+      sf[4 * i + 2] = first ? -s4.z : s4.z;
+      sf[4 * i + 3] = first ? -s4.w : s4.w;
     }
   }
   using Raw = typename std::conditional<P == 8, uint4, uint2>::type;
