@@ -57,6 +57,52 @@ def test_rope_quant_write_bit_exact(kvq, oracle, d, hq, hkv, rot):
     assert np.array_equal(qr.cpu().view(torch.int16).numpy().view(np.uint16), rqr)
 
 
+@pytest.mark.parametrize("d,c", [(256, 0.70710677), (128, 0.3), (256, 0.9)])
+def test_rope_quant_near_half_integer_quotients(kvq, oracle, d, c):
+    """Rotated fp32 rows whose quotients x / scale sit a hair away from half-integers: rows of
+    integer values in [-254, 254] with amax 254 (so x / scale would be x / 2 exactly), rotated by a
+    table whose cosine is the constant c and whose sine is 0, so that every element becomes
+    RN(x * c) and the scale RN(RN(254 c) / 127).  Most odd x then land within a few 1e-6 of a
+    half-integer, where the rule's fast path must hand the code to the IEEE division.  Gate: codes,
+    scales and rotated rows bit-exact against the oracle's producer."""
+    import torch
+    rng = np.random.default_rng(int(d + 1000 * c))
+    T, hq, hkv, max_pos = 48, 8, 2, 64
+
+    def rows(shape):
+        x = rng.integers(-254, 255, size=shape).astype(np.float32)
+        x[..., 0] = np.where(rng.random(shape[:-1]) < 0.5, 254.0, -254.0)
+        return W.f32_to_bf16_bits(x)  # integers up to 256 are exact in bf16
+
+    q, k, v = rows((T, hq, d)), rows((T, hkv, d)), rows((T, hkv, d))
+    cs = np.zeros((max_pos, d), np.float32)
+    cs[:, : d // 2] = np.float32(c)
+    pos = np.arange(T, dtype=np.int32)
+    seq = np.zeros(T, np.int32)
+    table = np.arange(max_pos // 16, dtype=np.int32)[None, :]
+    # how many quotients the fast path must leave to the division (the test's reason to exist)
+    xr = W.bf16_bits_to_f32(q) * np.float32(c)
+    scale = (np.abs(xr).max(axis=-1, keepdims=True) / np.float32(127.0)).astype(np.float32)
+    quo = xr.astype(np.float64) / scale.astype(np.float64)
+    near = np.abs(np.abs(quo - np.floor(quo)) - 0.5) < 3.0e-5
+    assert near.sum() > 1000, near.sum()
+
+    cache = kvq.KVCache(max_pos // 16, hkv, d)
+    qc, qs, qr = kvq.kvq_rope_quant_write(cache, to_bf16_tensor(q), to_bf16_tensor(k), to_bf16_tensor(v),
+                                          to_i32(seq), to_i32(pos), to_i32(table), torch.from_numpy(cs).cuda(), d)
+    assert kvq.kvq_device_status() == 0
+    hc = oracle.HostCache(max_pos // 16, hkv, d)
+    skipped, rqc, rqs, rqr = oracle.rope_quant_write(hc, q, k, v, seq, pos, table, cs, d)
+    assert skipped == 0
+    assert np.array_equal(cache.k.cpu().numpy(), hc.k)
+    assert np.array_equal(cache.v.cpu().numpy(), hc.v)
+    assert np.array_equal(cache.k_scale.cpu().numpy().view(np.uint32), hc.k_scale.view(np.uint32))
+    assert np.array_equal(cache.v_scale.cpu().numpy().view(np.uint32), hc.v_scale.view(np.uint32))
+    assert np.array_equal(qc.cpu().numpy(), rqc)
+    assert np.array_equal(qs.cpu().numpy().view(np.uint32), rqs.view(np.uint32))
+    assert np.array_equal(qr.cpu().view(torch.int16).numpy().view(np.uint16), rqr)
+
+
 def test_rope_quant_write_without_q(kvq, oracle):
     import torch
     rng = np.random.default_rng(950)
