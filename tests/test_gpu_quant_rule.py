@@ -55,3 +55,31 @@ def test_rule_bit_exact_over_all_bf16(kvq, oracle, d):
     got = codes.cpu().numpy()
     bad = np.argwhere(got != ref_codes)
     assert len(bad) == 0, (len(bad), bad[:5])
+
+
+@pytest.mark.parametrize("d", [256, 128])
+def test_rule_non_finite_rows(kvq, oracle, d):
+    """Rows holding inf, -inf or NaN beside finite values, and a NaN in an otherwise zero row.
+    The rule as written decides them: amax ignores NaN, an infinite amax gives an infinite scale,
+    so finite values quantise to 0 and inf / inf = NaN clamps to -127; a zero amax gives zeros.
+    Gate: codes and scales bit-identical to the oracle."""
+    import torch
+    rng = np.random.default_rng(4242 + d)
+    inf, nan = np.float32(np.inf), np.float32(np.nan)
+    rows = []
+    for special in ([inf], [-inf], [nan], [inf, nan], [inf, -inf], [nan, nan]):
+        x = rng.normal(size=d).astype(np.float32) * 3
+        pos = rng.choice(d, size=len(special), replace=False)
+        x[pos] = special
+        rows.append(x)
+    z = np.zeros(d, np.float32)
+    z[7] = nan
+    rows.append(z)
+    bits = W.f32_to_bf16_bits(np.stack(rows))
+    bits[np.isnan(np.stack(rows))] = 0x7FC0  # a quiet NaN pattern in bf16
+    q = bits[:, None, :]
+    qt = torch.from_numpy(q.view(np.int16)).cuda().view(torch.bfloat16)
+    codes, scales = kvq.kvq_debug_prefill_q_codes(qt)
+    ref_codes, ref_scales = oracle.quant_rows(q)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), ref_scales.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
