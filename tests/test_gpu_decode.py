@@ -92,10 +92,13 @@ def test_bad_block_is_flagged_not_faulted(kvq):
     assert np.isfinite(out.cpu().numpy()).all()
 
 
-def test_decode_1k_full(kvq, oracle):
-    """Workload decode_1k: ctx 1024, contiguous cache, single-CTA route (default)."""
+@pytest.mark.parametrize("route", [None, 1])
+def test_decode_1k_full(kvq, oracle, route):
+    """Workload decode_1k: ctx 1024, contiguous cache, on the automatic route (split-K with the
+    GPU-sized split: 64-key splits on 152 SMs, then the merge) and forced onto the single-CTA
+    route: every output against FP64."""
     w = W.make("decode_1k")
-    got, _, _ = _run(kvq, w)
+    got, _, _ = _run(kvq, w) if route is None else _run(kvq, w, force_route=route)
     hc = host_cache_from(w, oracle)
     ref = oracle.decode_f64(hc, w["q"], w["block_table"], w["ctx_lens"], w["softmax_scale"])
     err = norm_max_err(got, ref)
